@@ -1,0 +1,41 @@
+"""Seeded workload generator: shapes, determinism, padding lengths, FLOP counts."""
+
+import torch
+
+import workloads
+
+
+def test_tiny_is_deterministic_and_bf16():
+    w = workloads.WORKLOADS["tiny"]
+    a = workloads.make_inputs(w)
+    b = workloads.make_inputs(w)
+    for key in ("q", "k", "v", "do"):
+        assert a[key].dtype == torch.bfloat16 and a[key].shape == (1, 1, 128, 64)
+        assert torch.equal(a[key], b[key])
+    assert a["kv_len"] is None
+    # bf16 values are the round-to-nearest of the fp32 draws
+    assert torch.equal(a["q"], a["q_f32"].to(torch.bfloat16))
+
+
+def test_padding_lengths_in_range():
+    w = workloads.WORKLOADS["bert"]
+    x = workloads.draw(w.B, w.H, 8, 8, len_range=(w.len_lo, w.len_hi))
+    kv = x["kv_len"]
+    assert kv.dtype == torch.int32 and kv.shape == (w.B,)
+    assert int(kv.min()) >= 128 and int(kv.max()) <= 512
+
+
+def test_qk_scale_applies_to_q_and_k_only():
+    a = workloads.draw(1, 1, 16, 8, qk_scale=0.5)
+    b = workloads.draw(1, 1, 16, 8)
+    assert torch.equal(a["q_f32"], 0.5 * b["q_f32"])
+    assert torch.equal(a["k_f32"], 0.5 * b["k_f32"])
+    assert torch.equal(a["v_f32"], b["v_f32"])
+
+
+def test_flop_counts():
+    w = workloads.WORKLOADS["gpt2"]
+    f = workloads.flop_counts(w)
+    # 8*12 heads, 0.5 * 1024^2 * 64 per unit
+    unit = 8 * 12 * 0.5 * 1024 * 1024 * 64
+    assert f["fwd"] == 4 * unit and f["fwd_bwd_nominal"] == 12 * unit and f["fwd_bwd_executed"] == 14 * unit

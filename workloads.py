@@ -1,0 +1,121 @@
+"""Seeded synthetic attention workloads (shapes, value distributions, draw order).
+
+This module holds no attention arithmetic: it only names the workloads and
+draws their random inputs, so that the fp64 oracle and the CUDA path can be
+fed the very same bf16 tensors.
+
+Workload shapes follow the end-to-end settings that the FlashAttention
+practice record cites (GPT-2, BERT-large; "Why recomputation is cheaper here
+than storing") and the GPT-2 memory-table configuration (d_model 768, 12
+heads) of "FlashAttention Algorithm > Recomputation Strategy", In[17]/Out[18].
+No dataset or trained weight is involved: every tensor is i.i.d. Gaussian.
+
+Draw recipe (one CPU ``torch.Generator`` seeded with ``seed``):
+  1. q, k, v, dO drawn in that order as fp32 ``[B, H, N, d]`` standard normals;
+  2. q and k multiplied by ``qk_scale`` (0.5 for the head-dim-128 workload);
+  3. for key-padded workloads, per-sequence valid key counts drawn from the
+     same generator as integers uniform in ``[len_lo, len_hi]`` inclusive;
+  4. q, k, v, dO rounded to bf16 (round to nearest even).
+"""
+
+from __future__ import annotations
+
+import dataclasses
+import math
+from typing import Dict, Optional
+
+import torch
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    name: str
+    B: int
+    H: int
+    N: int
+    d: int
+    causal: bool
+    qk_scale: float = 1.0
+    len_lo: Optional[int] = None  # key padding: valid lengths uniform in [len_lo, len_hi]
+    len_hi: Optional[int] = None
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.d)
+
+    @property
+    def padded(self) -> bool:
+        return self.len_lo is not None
+
+    def describe(self) -> str:
+        s = f"{self.name}: B={self.B} H={self.H} N={self.N} d={self.d} " + (
+            "causal" if self.causal else "non-causal")
+        if self.padded:
+            s += f", key padding len~U[{self.len_lo},{self.len_hi}]"
+        if self.qk_scale != 1.0:
+            s += f", q,k x{self.qk_scale}"
+        return s
+
+
+WORKLOADS: Dict[str, Workload] = {
+    w.name: w
+    for w in [
+        Workload("tiny", 1, 1, 128, 64, False),
+        Workload("gpt2", 8, 12, 1024, 64, True),
+        Workload("bert", 16, 16, 512, 64, False, len_lo=128, len_hi=512),
+        Workload("d128", 2, 16, 4096, 128, True, qk_scale=0.5),
+        Workload("long2048", 1, 12, 2048, 64, True),
+        Workload("long8192", 1, 12, 8192, 64, True),
+        Workload("long16384", 1, 12, 16384, 64, True),
+        Workload("long32768", 1, 12, 32768, 64, True),
+    ]
+}
+
+
+def draw(B: int, H: int, N: int, d: int, *, seed: int = 0, qk_scale: float = 1.0,
+         len_range: Optional[tuple] = None) -> Dict[str, Optional[torch.Tensor]]:
+    """Draw q, k, v, dO (bf16, CPU, ``[B,H,N,d]``) and optional kv_len (int32 ``[B]``)."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    shape = (B, H, N, d)
+    q = torch.randn(shape, generator=g, dtype=torch.float32)
+    k = torch.randn(shape, generator=g, dtype=torch.float32)
+    v = torch.randn(shape, generator=g, dtype=torch.float32)
+    do = torch.randn(shape, generator=g, dtype=torch.float32)
+    if qk_scale != 1.0:
+        q = q * qk_scale
+        k = k * qk_scale
+    kv_len = None
+    if len_range is not None:
+        lo, hi = len_range
+        kv_len = torch.randint(lo, hi + 1, (B,), generator=g, dtype=torch.int64).to(torch.int32)
+    return {
+        "q": q.to(torch.bfloat16),
+        "k": k.to(torch.bfloat16),
+        "v": v.to(torch.bfloat16),
+        "do": do.to(torch.bfloat16),
+        "kv_len": kv_len,
+        "q_f32": q, "k_f32": k, "v_f32": v, "do_f32": do,
+    }
+
+
+def make_inputs(w: Workload, seed: int = 0) -> Dict[str, Optional[torch.Tensor]]:
+    rng = (w.len_lo, w.len_hi) if w.padded else None
+    return draw(w.B, w.H, w.N, w.d, seed=seed, qk_scale=w.qk_scale, len_range=rng)
+
+
+def flop_counts(w: Workload, kv_len: Optional[torch.Tensor] = None) -> Dict[str, float]:
+    """Matmul FLOPs of one fwd+bwd over the workload.
+
+    Per head: fwd 4*c*N*Nk*d (QK^T and PV), bwd nominal 8*c*N*Nk*d (dV, dP, dK,
+    dQ) and recompute 2*c*N*Nk*d (QK^T again), with c = 1/2 for causal masks
+    (diagonal counted half, the usual convention) and Nk the valid key count.
+    """
+    c = 0.5 if w.causal else 1.0
+    if kv_len is not None:
+        nk_total = float(kv_len.to(torch.float64).sum().item()) * w.H
+    else:
+        nk_total = float(w.N) * w.B * w.H
+    base = c * w.N * nk_total * w.d
+    return {"fwd": 4 * base, "bwd_nominal": 8 * base, "bwd_recompute": 2 * base,
+            "fwd_bwd_nominal": 12 * base, "fwd_bwd_executed": 14 * base}
