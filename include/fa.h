@@ -1,0 +1,116 @@
+/*
+ * Exact IO-aware softmax attention for NVIDIA GB300 (sm_103a): C ABI.
+ *
+ * What is computed (per batch b and head h, with s = `scale`):
+ *   S = s Q K^T, masked;  P = softmax_rows(S);  O = P V;  LSE = logsumexp_rows(S)
+ * and, for an upstream gradient dO of O,
+ *   D = rowsum(dO * O), dV = P^T dO, dP = dO V^T, dS = P * (dP - D),
+ *   dQ = s dS K, dK = s dS^T Q.
+ *
+ * How it is computed follows the FlashAttention practice record ("Why
+ * recomputation is cheaper here than storing", Anthology of the SOTA): score
+ * tiles live only in on-chip memory and are consumed at once with a running
+ * row maximum and normaliser, the N x N matrix is never written to HBM, and the
+ * backward pass rebuilds every S/P tile from Q, K, V and the saved per-row
+ * statistics. Those statistics are the running maximum m and normaliser l of
+ * "FlashAttention Algorithm > Recomputation Strategy" (section "What Gets
+ * Stored vs Recomputed"), folded here into one value LSE = m + ln l.
+ *
+ * Conventions shared by every entry point:
+ *  - Tensors Q, K, V, O, dO, dQ, dK, dV are contiguous [B, H, N, d] bf16 in
+ *    device memory, d innermost; every base pointer 16-byte aligned.
+ *    LSE is contiguous [B, H, N] fp32 (natural log). kv_len, when given, is
+ *    a device int32 [B]: key j of batch b is valid iff j < kv_len[b].
+ *  - d must be 64 or 128. N >= 0 (any value; N = 0 is a no-op). B, H >= 1.
+ *    causal = 1 keeps key j for query i iff j <= i.
+ *  - All memory is owned by the caller. The library allocates nothing and
+ *    frees nothing; outputs are fully overwritten.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
+ *    stream). A non-OK return means nothing was launched, except FA_ERR_CUDA
+ *    after a failed launch.
+ *  - Inside the kernels every wait is bounded; a wait that runs out records
+ *    FA_ERR_TIMEOUT in a per-device status word that
+ *    fa_get_last_device_status() reads.
+ *  - Entry points are reentrant; calls that share output buffers race.
+ */
+#ifndef IO_AWARE_EXACT_FA_H
+#define IO_AWARE_EXACT_FA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define FA_API __attribute__((visibility("default")))
+#else
+#define FA_API
+#endif
+
+typedef struct CUstream_st* fa_stream_t; /* identical to cudaStream_t */
+
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = 1,  /* null pointer, negative size, bad flag, too-small workspace */
+  FA_ERR_UNSUPPORTED = 2,  /* d not in {64, 128}, or sizes beyond 32-bit indexing */
+  FA_ERR_MISALIGNED = 3,   /* a tensor base pointer not 16-byte aligned */
+  FA_ERR_CUDA = 4,         /* a CUDA runtime/driver call failed */
+  FA_ERR_TIMEOUT = 5,      /* (device status) a bounded wait inside a kernel ran out */
+  FA_ERR_DEVICE_CHECK = 6  /* (device status) an in-kernel consistency check failed */
+} fa_status;
+
+/* Forward pass: O and LSE from Q, K, V.
+ * Defined by the practice record's account of the tiled kernel (scores kept on
+ * chip and consumed immediately, blockwise running-maximum softmax) and by the
+ * handbook's list of what is stored for the backward pass (O plus the per-row
+ * running statistics). Returns an fa_status. */
+FA_API int fa_forward(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+               float scale, int causal, fa_stream_t stream);
+
+/* As fa_forward, with optional key padding: kv_len is NULL or a device int32
+ * [B] of valid key counts (values are clamped to [0, N]). A query row with no
+ * valid key gets O = 0 and LSE = -inf. */
+FA_API int fa_forward_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+                  float scale, int causal, const int32_t* kv_len, fa_stream_t stream);
+
+/* Bytes of device workspace fa_backward needs: per (b, h), D and a base-2
+ * copy of LSE for every query row and an fp32 dQ accumulator, each padded to
+ * a multiple of 128 rows. Linear in N. Returns 0 for unsupported d. */
+FA_API size_t fa_backward_workspace_size(int B, int H, int N, int d);
+
+/* Backward pass: dQ, dK, dV from Q, K, V, O, dO and the LSE saved by the
+ * forward pass. No N x N input exists: every S and P tile is recomputed from
+ * Q, K and LSE, as the practice record and the handbook ("What Gets Stored vs
+ * Recomputed", and the closing paragraph of that section: tiles rebuilt with
+ * the forward's tiling, gradients computed per block and accumulated) describe.
+ * `workspace` is caller-owned device memory of at least
+ * fa_backward_workspace_size(B, H, N, d) bytes, 256-byte aligned; its
+ * contents on entry do not matter. `scale` and `causal` must equal the
+ * forward call's. */
+FA_API int fa_backward(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
+                void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale, int causal, void* workspace,
+                size_t workspace_bytes, fa_stream_t stream);
+
+/* As fa_backward, with the same optional key padding as fa_forward_ex. */
+FA_API int fa_backward_ex(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
+                   void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale, int causal,
+                   const int32_t* kv_len, void* workspace, size_t workspace_bytes, fa_stream_t stream);
+
+/* Static text for an fa_status value. */
+FA_API const char* fa_status_string(int status);
+
+/* Synchronises `stream`, then returns and clears the current device's status
+ * word (FA_OK if no kernel recorded an error). If detail is non-NULL it
+ * receives 4 ints: code, wait site, blockIdx.x, blockIdx.y of the first error. */
+FA_API int fa_get_last_device_status(fa_stream_t stream, int* detail);
+
+/* Library version as major*10000 + minor*100 + patch. */
+FA_API int fa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* IO_AWARE_EXACT_FA_H */

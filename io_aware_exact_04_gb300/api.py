@@ -1,0 +1,126 @@
+"""PyTorch-facing wrappers of the C ABI: argument checks and marshalling only.
+
+PyTorch provides device memory and the current CUDA stream; every step of the
+attention computation runs in the library's kernels.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import math
+from typing import Optional, Tuple
+
+import torch
+
+from . import _lib
+
+
+def _lib_fa():
+    return _lib.load("libfa.so")
+
+
+def _p(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device: torch.device):
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _check_bhnd(name: str, t: torch.Tensor, shape=None):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != torch.bfloat16:
+        raise ValueError(f"{name} must be bfloat16")
+    if t.dim() != 4 or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous [B, H, N, d] tensor")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def _kv(kv_len: Optional[torch.Tensor], B: int, device) -> Optional[torch.Tensor]:
+    if kv_len is None:
+        return None
+    if kv_len.dtype != torch.int32 or kv_len.shape != (B,) or not kv_len.is_contiguous():
+        raise ValueError("kv_len must be a contiguous int32 tensor of shape [B]")
+    if kv_len.device != device:
+        raise ValueError("kv_len must live on the same device as q")
+    return kv_len
+
+
+def forward(q, k, v, causal: bool = False, scale: Optional[float] = None, kv_len=None, out=None,
+            lse=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """O, LSE of exact softmax attention (see include/fa.h: fa_forward_ex)."""
+    _check_bhnd("q", q)
+    B, H, N, d = q.shape
+    _check_bhnd("k", k, q.shape)
+    _check_bhnd("v", v, q.shape)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    o = torch.empty_like(q) if out is None else out
+    _check_bhnd("out", o, q.shape)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
+    kv = _kv(kv_len, B, q.device)
+    with torch.cuda.device(q.device):
+        rc = _lib_fa().fa_forward_ex(_p(q), _p(k), _p(v), _p(o), _p(lse), B, H, N, d, scale, int(bool(causal)),
+                                     _p(kv), _stream(q.device))
+    _lib.check(rc, "fa_forward_ex")
+    return o, lse
+
+
+def workspace_bytes(B: int, H: int, N: int, d: int) -> int:
+    return int(_lib_fa().fa_backward_workspace_size(B, H, N, d))
+
+
+def backward(q, k, v, o, do, lse, causal: bool = False, scale: Optional[float] = None, kv_len=None,
+             dq=None, dk=None, dv=None, workspace=None):
+    """dQ, dK, dV by recomputation from Q, K, V, O, dO and LSE (fa_backward_ex)."""
+    _check_bhnd("q", q)
+    B, H, N, d = q.shape
+    for name, t in (("k", k), ("v", v), ("o", o), ("do", do)):
+        _check_bhnd(name, t, q.shape)
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, N) or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous float32 [B, H, N] tensor")
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(q) if dk is None else dk
+    dv = torch.empty_like(q) if dv is None else dv
+    need = workspace_bytes(B, H, N, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    kv = _kv(kv_len, B, q.device)
+    with torch.cuda.device(q.device):
+        rc = _lib_fa().fa_backward_ex(_p(q), _p(k), _p(v), _p(o), _p(do), _p(lse), _p(dq), _p(dk), _p(dv),
+                                      B, H, N, d, scale, int(bool(causal)), _p(kv), _p(workspace),
+                                      workspace.numel(), _stream(q.device))
+    _lib.check(rc, "fa_backward_ex")
+    return dq, dk, dv
+
+
+def device_status(device=None):
+    """(code, [code, site, blockIdx.x, blockIdx.y]) of the device status word; clears it."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    detail = (ctypes.c_int * 4)()
+    with torch.cuda.device(dev):
+        rc = _lib_fa().fa_get_last_device_status(_stream(dev), detail)
+    return rc, list(detail)
+
+
+class _Attention(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, q, k, v, causal, scale, kv_len):
+        o, lse = forward(q, k, v, causal=causal, scale=scale, kv_len=kv_len)
+        ctx.save_for_backward(q, k, v, o, lse, kv_len if kv_len is not None else torch.empty(0))
+        ctx.causal, ctx.scale, ctx.has_kv = causal, scale, kv_len is not None
+        return o
+
+    @staticmethod
+    def backward(ctx, do):
+        q, k, v, o, lse, kv = ctx.saved_tensors
+        dq, dk, dv = backward(q, k, v, o, do.contiguous(), lse, causal=ctx.causal, scale=ctx.scale,
+                              kv_len=kv if ctx.has_kv else None)
+        return dq, dk, dv, None, None, None
+
+
+def attention(q, k, v, causal: bool = False, scale: Optional[float] = None, kv_len=None) -> torch.Tensor:
+    """Differentiable exact attention: O only; only the LSE is kept for backward."""
+    return _Attention.apply(q, k, v, causal, scale, kv_len)

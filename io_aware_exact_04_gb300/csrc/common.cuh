@@ -1,0 +1,71 @@
+// Device-side helpers shared by the attention kernels: bounded mbarrier waits
+// that record a status instead of hanging, and 128-byte-swizzled smem address
+// arithmetic matching what TMA writes with CU_TENSOR_MAP_SWIZZLE_128B.
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "fa.h"
+#include "ptx.cuh"
+
+namespace fa {
+
+// Upper bound for any single wait inside a kernel. Every wait in these kernels
+// normally completes within microseconds; after this long the CTA gives up,
+// records FA_ERR_TIMEOUT in the status word and exits cleanly.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+// status[0]: first error code, status[1]: wait site, status[2..3]: block index.
+struct DevStatus {
+  int* word;        // global, 4 ints
+  int* abort_smem;  // this CTA's abort flag
+};
+
+__device__ __forceinline__ void record_error(const DevStatus& st, int code, int site) {
+  if (atomicCAS(st.word, 0, code) == 0) {
+    st.word[1] = site;
+    st.word[2] = blockIdx.x;
+    st.word[3] = blockIdx.y;
+  }
+  *(volatile int*)st.abort_smem = 1;
+}
+
+// Single-thread bounded wait. Returns false if the CTA must abort.
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, DevStatus st, int site,
+                                             uint64_t limit_ns = kWaitLimitNs) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t spins = 1;; ++spins) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((spins & 63u) == 0) {
+      if (*(volatile int*)st.abort_smem) return false;
+      if (*(volatile int*)st.word != 0) {
+        *(volatile int*)st.abort_smem = 1;
+        return false;
+      }
+      if (globaltimer_ns() - t0 > limit_ns) {
+        record_error(st, FA_ERR_TIMEOUT, site);
+        return false;
+      }
+    }
+  }
+}
+
+// Whole-warp bounded wait; the result is warp-uniform so that the .sync.aligned
+// tcgen05 instructions that follow stay converged.
+__device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, DevStatus st, int site) {
+  bool ok = wait_bounded(bar, parity, st, site);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// Byte offset of 16-byte chunk `chunk` (0..7) of row `row` inside a tile whose
+// rows are 128 bytes and which TMA fills with 128-byte swizzling (1024-byte atoms).
+__device__ __forceinline__ uint32_t sw128_offset(uint32_t row, uint32_t chunk) {
+  return row * 128u + ((chunk ^ (row & 7u)) << 4);
+}
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+}  // namespace fa

@@ -1,0 +1,184 @@
+// C-ABI entry points: argument validation, workspace carving, tensor-map
+// construction (in the launchers) and the per-device status word.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "fa.h"
+#include "fa_internal.h"
+
+namespace {
+
+// Per-device word the kernels write when a bounded wait runs out or an
+// in-kernel check fails: code, wait site, blockIdx.x, blockIdx.y.
+__device__ int g_status[4];
+
+constexpr int kMaxDevices = 64;
+int* g_status_ptr[kMaxDevices] = {};
+std::mutex g_status_mu;
+
+int* device_status(int* err) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    *err = FA_ERR_CUDA;
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lk(g_status_mu);
+  if (!g_status_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess) {
+      *err = FA_ERR_CUDA;
+      return nullptr;
+    }
+    g_status_ptr[dev] = static_cast<int*>(p);
+  }
+  return g_status_ptr[dev];
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_common(int B, int H, int N, int d, float scale, int causal) {
+  if (B < 0 || H < 0 || N < 0) return FA_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  const long long BH = (long long)B * H;
+  if (BH > 65535) return FA_ERR_UNSUPPORTED;  // one grid row per head
+  if ((long long)N + 255 > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+  return FA_OK;
+}
+
+long long round_up(long long x, long long m) { return (x + m - 1) / m * m; }
+
+struct WsLayout {
+  size_t lse2, dvec, dqacc, total;
+};
+
+WsLayout ws_layout(int B, int H, int N, int d) {
+  const long long BH = (long long)B * H;
+  const long long Npad = round_up(N, 128);
+  WsLayout w;
+  w.lse2 = 0;
+  w.dvec = (size_t)round_up(w.lse2 + BH * Npad * 4, 256);
+  w.dqacc = (size_t)round_up(w.dvec + BH * Npad * 4, 256);
+  w.total = (size_t)round_up(w.dqacc + BH * Npad * d * 4, 256);
+  return w;
+}
+
+}  // namespace
+
+extern "C" {
+
+int fa_version(void) { return 100; }
+
+const char* fa_status_string(int s) {
+  switch (s) {
+    case FA_OK: return "ok";
+    case FA_ERR_INVALID_ARG: return "invalid argument";
+    case FA_ERR_UNSUPPORTED: return "unsupported shape (d must be 64 or 128, B*H <= 65535)";
+    case FA_ERR_MISALIGNED: return "tensor pointer not 16-byte aligned";
+    case FA_ERR_CUDA: return "CUDA call failed";
+    case FA_ERR_TIMEOUT: return "bounded wait inside a kernel ran out";
+    case FA_ERR_DEVICE_CHECK: return "in-kernel consistency check failed";
+    default: return "unknown status";
+  }
+}
+
+int fa_forward_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+                  float scale, int causal, const int32_t* kv_len, fa_stream_t stream) {
+  int rc = check_common(B, H, N, d, scale, causal);
+  if (rc != FA_OK) return rc;
+  if ((long long)B * H * N == 0) return FA_OK;
+  if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return FA_ERR_MISALIGNED;
+  int err = FA_OK;
+  int* status = device_status(&err);
+  if (!status) return err;
+  fa::FwdArgs a;
+  a.H = H;
+  a.N = N;
+  a.n_pairs = (N + 255) / 256;
+  a.causal = causal;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.kv_len = kv_len;
+  a.lse = lse;
+  a.o = static_cast<uint16_t*>(o);
+  a.status = status;
+  return fa::launch_fwd(q, k, v, o, a, B * H, d, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int fa_forward(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+               float scale, int causal, fa_stream_t stream) {
+  return fa_forward_ex(q, k, v, o, lse, B, H, N, d, scale, causal, nullptr, stream);
+}
+
+size_t fa_backward_workspace_size(int B, int H, int N, int d) {
+  if (B < 0 || H < 0 || N < 0 || (d != 64 && d != 128)) return 0;
+  return ws_layout(B, H, N, d).total;
+}
+
+int fa_backward_ex(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
+                   void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale, int causal,
+                   const int32_t* kv_len, void* workspace, size_t workspace_bytes, fa_stream_t stream) {
+  int rc = check_common(B, H, N, d, scale, causal);
+  if (rc != FA_OK) return rc;
+  if ((long long)B * H * N == 0) return FA_OK;
+  if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv || !workspace) return FA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dO) || !aligned16(lse) ||
+      !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+    return FA_ERR_MISALIGNED;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return FA_ERR_MISALIGNED;
+  const WsLayout w = ws_layout(B, H, N, d);
+  if (workspace_bytes < w.total) return FA_ERR_INVALID_ARG;
+  int err = FA_OK;
+  int* status = device_status(&err);
+  if (!status) return err;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  fa::BwdArgs a;
+  a.H = H;
+  a.N = N;
+  a.Npad = (int)round_up(N, 128);
+  a.causal = causal;
+  a.scale = scale;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.kv_len = kv_len;
+  a.o = static_cast<const uint16_t*>(o);
+  a.dO = static_cast<const uint16_t*>(dO);
+  a.lse = lse;
+  a.lse2 = reinterpret_cast<float*>(ws + w.lse2);
+  a.dvec = reinterpret_cast<float*>(ws + w.dvec);
+  a.dq_acc = reinterpret_cast<float*>(ws + w.dqacc);
+  a.dq = static_cast<uint16_t*>(dq);
+  a.dk = static_cast<uint16_t*>(dk);
+  a.dv = static_cast<uint16_t*>(dv);
+  a.status = status;
+  return fa::launch_bwd(q, k, v, a, B * H, d, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int fa_backward(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
+                void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale, int causal, void* workspace,
+                size_t workspace_bytes, fa_stream_t stream) {
+  return fa_backward_ex(q, k, v, o, dO, lse, dq, dk, dv, B, H, N, d, scale, causal, nullptr, workspace,
+                        workspace_bytes, stream);
+}
+
+int fa_get_last_device_status(fa_stream_t stream, int* detail) {
+  int err = FA_OK;
+  int* status = device_status(&err);
+  if (!status) return err;
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return FA_ERR_CUDA;
+  int h[4] = {0, 0, 0, 0};
+  if (cudaMemcpy(h, status, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return FA_ERR_CUDA;
+  if (h[0] != 0) {
+    const int zero[4] = {0, 0, 0, 0};
+    if (cudaMemcpy(status, zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return FA_ERR_CUDA;
+  }
+  if (detail)
+    for (int i = 0; i < 4; ++i) detail[i] = h[i];
+  return h[0];
+}
+
+}  // extern "C"

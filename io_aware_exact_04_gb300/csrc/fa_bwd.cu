@@ -1,0 +1,541 @@
+// Backward pass of exact tiled attention on sm_103a, by recomputation.
+//
+// Method (practice record "Why recomputation is cheaper here than storing";
+// handbook "FlashAttention Algorithm > Recomputation Strategy", section "What
+// Gets Stored vs Recomputed"): no attention matrix is read; each block of S
+// and P is rebuilt from Q, K and the saved per-row statistic, with the same
+// tiling as the forward pass, and the gradients of each block are formed at
+// once and accumulated. Gradient formulas (softmax-attention Jacobian):
+//   D = rowsum(dO * O); P = exp(s Q K^T - LSE); dV += P^T dO; dP = dO V^T;
+//   dS = P * (dP - D); dK += s dS^T Q; dQ += s dS K.
+//
+// Three kernels:
+//   bwd_pre_kernel     D per query row, LSE in base 2, zeroed fp32 dQ accumulator
+//   bwd_kernel<D>      one CTA per 128-key tile of one head, looping over
+//                      query tiles of BR rows (BR = 128 for d = 64, 64 for d = 128):
+//     warp 12     TMA producer (K, V once; Q_i, dO_i, LSE_i, D_i per step, 2 stages)
+//     warp 13     TMEM allocator + tcgen05.mma issuer. Keys are the M dimension:
+//                   S^T = K Q_i^T, dP^T = V dO_i^T          (smem x smem)
+//                   dV += P^T dO_i, dK += dS^T Q_i           (P^T, dS^T from TMEM)
+//                   d=64:  dQ_i  = dS K      (M = 128 query rows)
+//                   d=128: dQ_i^T = K^T dS^T (M = 128 head dims)
+//     warps 0-7   two warpgroups, each half of the BR query columns; thread r
+//                 owns key r (TMEM lane r): P^T and dS^T formed in registers,
+//                 written back to TMEM as bf16; dS also to smem for the dQ MMA.
+//     warps 8-11  dQ epilogue: TMEM -> scaled fp32 -> swizzled smem -> TMA
+//                 reduce-add into the fp32 accumulator (two staging buffers).
+//   dq_convert_kernel  fp32 accumulator -> bf16 dQ
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+#include "fa_internal.h"
+#include "tmap.h"
+
+namespace fa {
+
+// ---------------------------------------------------------------------------------------------
+// D_i = sum_k dO_ik O_ik; lse2_i = LSE_i * log2(e) (+inf where no row or LSE = -inf, so that
+// recomputed P is 0 there); dq_acc row zeroed. One group of D/8 lanes per row, 16 B each.
+template <int D>
+__global__ void __launch_bounds__(256) bwd_pre_kernel(BwdArgs a, int BH) {
+  constexpr int LPR = D / 8;          // lanes per row
+  constexpr int RPW = 32 / LPR;       // rows per warp
+  const int lane = threadIdx.x & 31;
+  const long long gw = (long long)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+  const long long total_rows = (long long)BH * a.Npad;
+  const long long r = gw * RPW + lane / LPR;
+  const int part = lane % LPR;
+  if (r >= total_rows) return;
+  const int bh = (int)(r / a.Npad);
+  const int n = (int)(r % a.Npad);
+  float acc = 0.f;
+  if (n < a.N) {
+    const size_t off = ((size_t)bh * a.N + n) * D + part * 8;
+    const uint4 ov = *reinterpret_cast<const uint4*>(a.o + off);
+    const uint4 gv = *reinterpret_cast<const uint4*>(a.dO + off);
+    const uint32_t ow[4] = {ov.x, ov.y, ov.z, ov.w};
+    const uint32_t gw4[4] = {gv.x, gv.y, gv.z, gv.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      acc = fmaf(__uint_as_float(ow[i] << 16), __uint_as_float(gw4[i] << 16), acc);
+      acc = fmaf(__uint_as_float(ow[i] & 0xFFFF0000u), __uint_as_float(gw4[i] & 0xFFFF0000u), acc);
+    }
+  }
+#pragma unroll
+  for (int m = LPR / 2; m > 0; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
+  float4* dq = reinterpret_cast<float4*>(a.dq_acc + (size_t)r * D + part * 8);
+  dq[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+  dq[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (part == 0) {
+    a.dvec[r] = acc;
+    float l2 = INFINITY;
+    if (n < a.N) {
+      const float l = a.lse[(size_t)bh * a.N + n];
+      if (l != -INFINITY) l2 = l * 1.4426950408889634f;
+    }
+    a.lse2[r] = l2;
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(256) dq_convert_kernel(BwdArgs a, int BH) {
+  const long long total = (long long)BH * a.N * (D / 8);
+  for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+       idx += (long long)gridDim.x * blockDim.x) {
+    const long long row = idx / (D / 8);
+    const int part = (int)(idx % (D / 8));
+    const int bh = (int)(row / a.N), n = (int)(row % a.N);
+    const float4* src = reinterpret_cast<const float4*>(a.dq_acc + ((size_t)bh * a.Npad + n) * D + part * 8);
+    const float4 x = src[0], y = src[1];
+    uint4 o;
+    o.x = pack_bf16x2(x.x, x.y);
+    o.y = pack_bf16x2(x.z, x.w);
+    o.z = pack_bf16x2(y.x, y.y);
+    o.w = pack_bf16x2(y.z, y.w);
+    *reinterpret_cast<uint4*>(a.dq + (size_t)row * D + part * 8) = o;
+  }
+}
+
+// ---------------------------------------------------------------------------------------------
+template <int D>
+struct BwdCfg {
+  static constexpr int BR = (D == 64) ? 128 : 64;  // query rows per step
+  static constexpr int NSUB = D / 64;
+  static constexpr int KSUB = 128 * 128;           // [128 keys][64] bf16 block
+  static constexpr int KTILE = NSUB * KSUB;        // K or V tile
+  static constexpr int QSUB = BR * 128;            // [BR rows][64] bf16 block
+  static constexpr int QTILE = NSUB * QSUB;        // Q_i or dO_i tile
+  static constexpr int NSTQ = 2;
+  static constexpr int DS_BYTES = 128 * BR * 2;    // dS: [128 keys][BR queries] bf16, 64-query blocks
+  static constexpr int DQ_STAGE = BR * D * 4;      // fp32 dQ staging tile
+  static constexpr int OFF_K = 0;
+  static constexpr int OFF_V = OFF_K + KTILE;
+  static constexpr int OFF_Q = OFF_V + KTILE;                 // NSTQ stages, contiguous
+  static constexpr int OFF_DO = OFF_Q + NSTQ * QTILE;         // NSTQ stages, contiguous
+  static constexpr int OFF_DS = OFF_DO + NSTQ * QTILE;
+  static constexpr int OFF_DQ = OFF_DS + DS_BYTES;            // 2 staging buffers
+  static constexpr int OFF_LSE = OFF_DQ + 2 * DQ_STAGE;       // NSTQ x BR floats
+  static constexpr int OFF_DV = OFF_LSE + NSTQ * BR * 4;      // NSTQ x BR floats
+  static constexpr int OFF_BAR = OFF_DV + NSTQ * BR * 4;
+  static constexpr int SMEM_BYTES = OFF_BAR + 256 + 1024;
+  // TMEM columns
+  static constexpr uint32_t TM_ST = 0, TM_DPT = BR, TM_DV = 2 * BR, TM_DK = 2 * BR + D, TM_DQ = 2 * BR + 2 * D;
+  static constexpr uint32_t DQ_COLS = 64;  // d=64: 64 head dims; d=128: BR = 64 query columns
+  static constexpr uint32_t TM_COLS = 512;
+  static constexpr int THREADS = 448;
+  // Each warpgroup owns BR/2 query columns of S^T (and dP^T) in TMEM and packs
+  // its bf16 P^T (dS^T) pairs into the first half of its own range, so neither
+  // warpgroup overwrites fp32 values the other has not read yet.
+  static constexpr int HC = BR / 2;
+  __host__ __device__ static constexpr uint32_t pcol(int qc) { return (qc / HC) * HC + (qc % HC) / 2; }
+};
+
+enum { SITE_B_KV_FULL = 20, SITE_B_QDO_EMPTY, SITE_B_QDO_FULL, SITE_B_S_FULL, SITE_B_DP_FULL, SITE_B_P_READY,
+       SITE_B_DS_READY, SITE_B_DQ_EMPTY, SITE_B_DQ_FULL, SITE_B_FINAL };
+
+template <int D>
+__global__ void __launch_bounds__(448, 1)
+    bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+               const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
+               const __grid_constant__ CUtensorMap tm_dqacc, BwdArgs a) {
+  using C = BwdCfg<D>;
+  constexpr int BR = C::BR;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = align1024(smem_raw);
+  const uint32_t sbase = smem_u32(sm);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::OFF_BAR);
+  const uint32_t b0 = smem_u32(bars);
+  auto BAR = [&](int i) { return b0 + 8u * i; };
+  const uint32_t kv_full = BAR(0);
+  auto qdo_full = [&](int s) { return BAR(1 + s); };
+  auto qdo_empty = [&](int s) { return BAR(3 + s); };
+  const uint32_t s_full = BAR(5), dp_full = BAR(6), p_ready = BAR(7), ds_ready = BAR(8);
+  auto dq_full = [&](int s) { return BAR(9 + s); };
+  auto dq_empty = [&](int s) { return BAR(11 + s); };
+  const uint32_t final_bar = BAR(13);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C::OFF_BAR + 8 * 16);
+  int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+  DevStatus st{a.status, abort_flag};
+
+  const int j = blockIdx.x;  // key tile
+  const int bh = blockIdx.y;
+  const int b = bh / a.H;
+  int kv = a.N;
+  if (a.kv_len) kv = min(max(a.kv_len[b], 0), a.N);
+  const int k0 = j * 128;
+  const int n_qt = (a.N + BR - 1) / BR;
+  const int i_start = a.causal ? (k0 / BR) : 0;
+  const int n_it = (k0 >= kv) ? 0 : (n_qt - i_start);
+
+  if (n_it == 0) {
+    // no valid key in this tile: its dK and dV rows are zero
+    const int rows = min(128, a.N - k0);
+    for (int idx = threadIdx.x; idx < rows * (D / 8); idx += blockDim.x) {
+      const size_t off = ((size_t)bh * a.N + k0 + idx / (D / 8)) * D + (idx % (D / 8)) * 8;
+      *reinterpret_cast<uint4*>(a.dk + off) = make_uint4(0, 0, 0, 0);
+      *reinterpret_cast<uint4*>(a.dv + off) = make_uint4(0, 0, 0, 0);
+    }
+    return;
+  }
+
+  if (threadIdx.x == 0) {
+    mbar_init(kv_full, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(qdo_full(s), 1);
+      mbar_init(qdo_empty(s), 1);
+      mbar_init(dq_full(s), 1);
+      mbar_init(dq_empty(s), 4);
+    }
+    mbar_init(s_full, 1);
+    mbar_init(dp_full, 1);
+    mbar_init(p_ready, 8);
+    mbar_init(ds_ready, 8);
+    mbar_init(final_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 13) {
+    tmem_alloc(smem_u32(tmem_slot), C::TM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const float* lse2_h = a.lse2 + (size_t)bh * a.Npad;
+  const float* dvec_h = a.dvec + (size_t)bh * a.Npad;
+
+  if (warp == 12) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      prefetch_tmap(&tm_q);
+      prefetch_tmap(&tm_do);
+      mbar_arrive_expect_tx(kv_full, 2 * C::KTILE);
+      for (int c = 0; c < C::NSUB; ++c) {
+        tma_load_3d(sbase + C::OFF_K + c * C::KSUB, &tm_k, c * 64, k0, bh, kv_full);
+        tma_load_3d(sbase + C::OFF_V + c * C::KSUB, &tm_v, c * 64, k0, bh, kv_full);
+      }
+      int issued = 0;
+      for (int it = 0; it < n_it; ++it) {
+        const int s = it & 1;
+        const int i = i_start + it;
+        if (!wait_bounded(qdo_empty(s), ((it >> 1) & 1) ^ 1, st, SITE_B_QDO_EMPTY)) break;
+        mbar_arrive_expect_tx(qdo_full(s), 2 * C::QTILE + 2 * BR * 4);
+        for (int c = 0; c < C::NSUB; ++c) {
+          tma_load_3d(sbase + C::OFF_Q + s * C::QTILE + c * C::QSUB, &tm_q, c * 64, i * BR, bh, qdo_full(s));
+          tma_load_3d(sbase + C::OFF_DO + s * C::QTILE + c * C::QSUB, &tm_do, c * 64, i * BR, bh, qdo_full(s));
+        }
+        bulk_load(sbase + C::OFF_LSE + s * BR * 4, lse2_h + (size_t)i * BR, BR * 4, qdo_full(s));
+        bulk_load(sbase + C::OFF_DV + s * BR * 4, dvec_h + (size_t)i * BR, BR * 4, qdo_full(s));
+        issued = it + 1;
+      }
+      if (*(volatile int*)abort_flag) {
+        // let copies already in flight land before the CTA's smem is released
+        const uint64_t t0 = globaltimer_ns();
+        while (!mbar_try_wait(kv_full, 0) && globaltimer_ns() - t0 < 100000000ull) {
+        }
+        for (int it = max(0, issued - 2); it < issued; ++it)
+          while (!mbar_try_wait(qdo_full(it & 1), (it >> 1) & 1) && globaltimer_ns() - t0 < 100000000ull) {
+          }
+      }
+    }
+  } else if (warp == 13) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t IDESC_S = idesc_bf16_f32(128, BR, 0, 0);  // K (or V) x Q_i (or dO_i), K-major
+      constexpr uint32_t IDESC_G = idesc_bf16_f32(128, D, 0, 1);   // TMEM A x MN-major B
+      constexpr uint32_t IDESC_Q = idesc_bf16_f32(128, 64, 1, 1);  // both operands MN-major
+      auto issue_kmajor = [&](uint32_t dst, uint32_t a_base, uint32_t b_base) {
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t oa = (k >> 2) * C::KSUB + (k & 3) * 32;
+          const uint32_t ob = (k >> 2) * C::QSUB + (k & 3) * 32;
+          mma_ss(tmem + dst, sdesc_sw128(a_base + oa, 16, 1024), sdesc_sw128(b_base + ob, 16, 1024), IDESC_S,
+                 k > 0);
+        }
+      };
+      auto issue_grad = [&](uint32_t dst, uint32_t a_tm, uint32_t b_base, uint32_t acc) {
+#pragma unroll
+        for (int k = 0; k < BR / 16; ++k)
+          mma_ts(tmem + dst, tmem + a_tm + C::pcol(16 * k), sdesc_sw128(b_base + k * 2048, C::QSUB, 1024),
+                 IDESC_G, (acc | k) != 0);
+      };
+      auto issue_dq = [&](uint32_t dst) {
+        const uint32_t ds = sbase + C::OFF_DS, kk = sbase + C::OFF_K;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {  // 128 keys
+          if (D == 64)  // dQ = dS K: A = dS (M = queries), B = K (N = head dims)
+            mma_ss(tmem + dst, sdesc_sw128(ds + k * 2048, 128 * 128, 1024),
+                   sdesc_sw128(kk + k * 2048, C::KSUB, 1024), IDESC_Q, k > 0);
+          else  // dQ^T = K^T dS^T: A = K^T (M = head dims), B = dS^T (N = queries)
+            mma_ss(tmem + dst, sdesc_sw128(kk + k * 2048, C::KSUB, 1024),
+                   sdesc_sw128(ds + k * 2048, 128 * 128, 1024), IDESC_Q, k > 0);
+        }
+      };
+      bool ok = wait_bounded(kv_full, 0, st, SITE_B_KV_FULL);
+      for (int it = 0; ok && it < n_it; ++it) {
+        const int s = it & 1;
+        const uint32_t qa = sbase + C::OFF_Q + s * C::QTILE, da = sbase + C::OFF_DO + s * C::QTILE;
+        if (!(ok = wait_bounded(qdo_full(s), (it >> 1) & 1, st, SITE_B_QDO_FULL))) break;
+        tc_fence_after();
+        issue_kmajor(C::TM_ST, sbase + C::OFF_K, qa);
+        mma_commit(s_full);
+        issue_kmajor(C::TM_DPT, sbase + C::OFF_V, da);
+        mma_commit(dp_full);
+        if (!(ok = wait_bounded(p_ready, it & 1, st, SITE_B_P_READY))) break;
+        tc_fence_after();
+        issue_grad(C::TM_DV, C::TM_ST, da, it > 0);
+        if (!(ok = wait_bounded(ds_ready, it & 1, st, SITE_B_DS_READY))) break;
+        tc_fence_after();
+        issue_grad(C::TM_DK, C::TM_DPT, qa, it > 0);
+        const int qb = it & 1;
+        if (!(ok = wait_bounded(dq_empty(qb), ((it >> 1) & 1) ^ 1, st, SITE_B_DQ_EMPTY))) break;
+        tc_fence_after();
+        issue_dq(C::TM_DQ + qb * C::DQ_COLS);
+        mma_commit(dq_full(qb));
+        mma_commit(qdo_empty(s));
+      }
+      mma_commit(final_bar);  // also the drain: completes after every MMA issued above
+      const uint64_t t0 = globaltimer_ns();
+      while (!mbar_try_wait(final_bar, 0) && globaltimer_ns() - t0 < kWaitLimitNs) {
+      }
+    }
+  } else if (warp >= 8) {
+    // ------------------------------------------------------------ dQ epilogue
+    const int wq = warp & 3;
+    const int r = wq * 32 + lane;  // TMEM lane: query row (d=64) or head dim (d=128)
+    const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+    const int tid = threadIdx.x - 256;
+    for (int it = 0; it < n_it; ++it) {
+      const int qb = it & 1;
+      const int i = i_start + it;
+      // the four warps leave the loop together, so the named barriers below never wait on a missing warp
+      if (!named_bar_and(3, 128, wait_warp(dq_full(qb), (it >> 1) & 1, st, SITE_B_DQ_FULL))) break;
+      tc_fence_after();
+      uint32_t v[2][32];
+      tmem_ld32(tmem + lane_off + C::TM_DQ + qb * C::DQ_COLS, v[0]);
+      tmem_ld32(tmem + lane_off + C::TM_DQ + qb * C::DQ_COLS + 32, v[1]);
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(dq_empty(qb));
+      // the reduce issued two steps ago from this staging buffer has finished reading it
+      if (tid == 0) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+      named_bar_sync(3, 128);
+      uint8_t* stg = sm + C::OFF_DQ + qb * C::DQ_STAGE;
+      const float sc = a.scale;
+      if (D == 64) {
+        // row r of a [128 queries][64 dims] fp32 tile, two 32-column swizzled boxes
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            float4 x = make_float4(__uint_as_float(v[h][4 * c]) * sc, __uint_as_float(v[h][4 * c + 1]) * sc,
+                                   __uint_as_float(v[h][4 * c + 2]) * sc, __uint_as_float(v[h][4 * c + 3]) * sc);
+            *reinterpret_cast<float4*>(stg + h * (128 * 128) + sw128_offset(r, c)) = x;
+          }
+      } else {
+        // column r of a [64 queries][128 dims] fp32 tile, four 32-column swizzled boxes
+        const int box = r >> 5, within = r & 31;
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const int q = h * 32 + c;
+            *reinterpret_cast<float*>(stg + box * (BR * 128) + sw128_offset(q, within >> 2) + (within & 3) * 4) =
+                __uint_as_float(v[h][c]) * sc;
+          }
+      }
+      fence_proxy_async_smem();
+      named_bar_sync(3, 128);
+      if (tid == 0) {
+        constexpr int NBOX = D / 32;
+        constexpr int BOX_BYTES = BR * 128;
+        for (int x = 0; x < NBOX; ++x)
+          tma_reduce_add_3d(&tm_dqacc, smem_u32(stg + x * BOX_BYTES), x * 32, i * BR, bh);
+        bulk_commit();
+      }
+    }
+    if (tid == 0) bulk_wait0();
+  } else {
+    // ------------------------------------------------------------ P^T / dS^T warpgroups
+    const int wg = warp >> 2;  // which half of the BR query columns
+    const int wq = warp & 3;
+    const int r = wq * 32 + lane;  // key within the tile (TMEM lane)
+    const int key = k0 + r;
+    const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+    constexpr int HC = C::HC;      // query columns per warpgroup (64 or 32)
+    constexpr int NCH = HC / 32;   // 32-column chunks per warpgroup
+    const int c0 = wg * HC;        // first query column of this warpgroup
+    const float sl2 = a.scale_log2;
+    bool ok = true;
+    for (int it = 0; it < n_it; ++it) {
+      const int s = it & 1;
+      const int i = i_start + it;
+      const int q0 = i * BR;
+      const float* lse_s = reinterpret_cast<const float*>(sm + C::OFF_LSE + s * BR * 4);
+      const float* dv_s = reinterpret_cast<const float*>(sm + C::OFF_DV + s * BR * 4);
+      if (!(ok = wait_warp(qdo_full(s), (it >> 1) & 1, st, SITE_B_QDO_FULL))) break;
+      if (!(ok = wait_warp(s_full, it & 1, st, SITE_B_S_FULL))) break;
+      tc_fence_after();
+      const bool need_mask = (k0 + 127 >= kv) || (a.causal && k0 + 127 > q0);
+      // ---- P^T = exp2(S^T s log2e - LSE2), bf16 into the S^T columns
+#pragma unroll
+      for (int ch = 0; ch < NCH; ++ch) {
+        const int cb = c0 + ch * 32;  // query column base within the tile
+        uint32_t sv[32];
+        tmem_ld32(tmem + lane_off + C::TM_ST + cb, sv);
+        tmem_wait_ld();
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          float p[2];
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int qc = cb + 2 * e + u;
+            float x = ex2_approx(fmaf(__uint_as_float(sv[2 * e + u]), sl2, -lse_s[qc]));
+            if (need_mask && (key >= kv || (a.causal && key > q0 + qc))) x = 0.f;
+            p[u] = x;
+          }
+          pk[e] = pack_bf16x2(p[0], p[1]);
+        }
+        tmem_st16(tmem + lane_off + C::TM_ST + C::pcol(cb), pk);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(p_ready);
+      // ---- dS^T = P^T * (dP^T - D), bf16 into the dP^T columns and into smem
+      if (!(ok = wait_warp(dp_full, it & 1, st, SITE_B_DP_FULL))) break;
+      tc_fence_after();
+#pragma unroll
+      for (int ch = 0; ch < NCH; ++ch) {
+        const int cb = c0 + ch * 32;
+        uint32_t dp[32], pp[16];
+        tmem_ld32(tmem + lane_off + C::TM_DPT + cb, dp);
+        tmem_ld16(tmem + lane_off + C::TM_ST + C::pcol(cb), pp);
+        tmem_wait_ld();
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const float p0 = __uint_as_float(pp[e] << 16), p1 = __uint_as_float(pp[e] & 0xFFFF0000u);
+          const float d0 = p0 * (__uint_as_float(dp[2 * e]) - dv_s[cb + 2 * e]);
+          const float d1 = p1 * (__uint_as_float(dp[2 * e + 1]) - dv_s[cb + 2 * e + 1]);
+          pk[e] = pack_bf16x2(d0, d1);
+        }
+        tmem_st16(tmem + lane_off + C::TM_DPT + C::pcol(cb), pk);
+        // smem dS: row = key r, 64-query blocks of 128 B, 16-byte chunks of 8 queries
+        uint8_t* dsb = sm + C::OFF_DS + (cb >> 6) * (128 * 128);
+        const int chunk0 = (cb & 63) >> 3;
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          *reinterpret_cast<uint4*>(dsb + sw128_offset(r, chunk0 + q)) =
+              make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+      }
+      tmem_wait_st();
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(ds_ready);
+    }
+    // ---- epilogue: warpgroup 0 writes dV, warpgroup 1 writes s * dK
+    if (ok) ok = wait_warp(final_bar, 0, st, SITE_B_FINAL);
+    ok = named_bar_and(1 + wg, 128, ok);  // reached by every warp of the warpgroup
+    if (ok) {
+      tc_fence_after();
+      const uint32_t src = wg == 0 ? C::TM_DV : C::TM_DK;
+      const float mul = wg == 0 ? 1.f : a.scale;
+      uint8_t* stage = sm + (wg == 0 ? C::OFF_Q : C::OFF_DO);  // both free once every MMA is done
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t x[32];
+        tmem_ld32(tmem + lane_off + src + c * 32, x);
+        tmem_wait_ld();
+        const int blk = (c * 32) >> 6;
+        const int chunk0 = ((c * 32) & 63) >> 3;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint4 v;
+          v.x = pack_bf16x2(__uint_as_float(x[q * 8 + 0]) * mul, __uint_as_float(x[q * 8 + 1]) * mul);
+          v.y = pack_bf16x2(__uint_as_float(x[q * 8 + 2]) * mul, __uint_as_float(x[q * 8 + 3]) * mul);
+          v.z = pack_bf16x2(__uint_as_float(x[q * 8 + 4]) * mul, __uint_as_float(x[q * 8 + 5]) * mul);
+          v.w = pack_bf16x2(__uint_as_float(x[q * 8 + 6]) * mul, __uint_as_float(x[q * 8 + 7]) * mul);
+          *reinterpret_cast<uint4*>(stage + blk * C::KSUB + sw128_offset(r, chunk0 + q)) = v;
+        }
+      }
+      fence_proxy_async_smem();
+      named_bar_sync(1 + wg, 128);
+      if (wq == 0 && lane == 0) {
+        for (int c = 0; c < C::NSUB; ++c)
+          tma_store_3d(wg == 0 ? &tm_dv : &tm_dk, smem_u32(stage + c * C::KSUB), c * 64, k0, bh);
+        bulk_commit();
+        bulk_wait0();
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 13) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TM_COLS);
+  }
+}
+
+template <int D>
+static int launch_bwd_d(const void* q, const void* k, const void* v, const BwdArgs& a, int BH,
+                        cudaStream_t stream) {
+  using C = BwdCfg<D>;
+  const uint64_t N = (uint64_t)a.N;
+  const auto BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const auto SW = CU_TENSOR_MAP_SWIZZLE_128B;
+  CUtensorMap mq, mk, mv, mdo, mdk, mdv, mdq;
+  if (!make_tmap_3d(&mq, q, BF, 2, D, N, BH, 64, C::BR, SW) ||
+      !make_tmap_3d(&mdo, a.dO, BF, 2, D, N, BH, 64, C::BR, SW) ||
+      !make_tmap_3d(&mk, k, BF, 2, D, N, BH, 64, 128, SW) || !make_tmap_3d(&mv, v, BF, 2, D, N, BH, 64, 128, SW) ||
+      !make_tmap_3d(&mdk, a.dk, BF, 2, D, N, BH, 64, 128, SW) ||
+      !make_tmap_3d(&mdv, a.dv, BF, 2, D, N, BH, 64, 128, SW) ||
+      !make_tmap_3d(&mdq, a.dq_acc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, D, (uint64_t)a.Npad, BH, 32, C::BR, SW))
+    return FA_ERR_CUDA;
+  static bool attr_set = false;
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) !=
+        cudaSuccess)
+      return FA_ERR_CUDA;
+    attr_set = true;
+  }
+  // 1. D, base-2 LSE, zeroed dQ accumulator
+  {
+    const long long rows = (long long)BH * a.Npad;
+    const int rpw = 32 / (D / 8);
+    const long long warps = (rows + rpw - 1) / rpw;
+    const int blocks = (int)((warps + 7) / 8);
+    bwd_pre_kernel<D><<<blocks, 256, 0, stream>>>(a, BH);
+  }
+  // 2. main kernel: one CTA per (key tile, head)
+  {
+    dim3 grid((a.N + 127) / 128, BH);
+    bwd_kernel<D><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(mq, mk, mv, mdo, mdk, mdv, mdq, a);
+  }
+  // 3. dQ to bf16
+  {
+    const long long total = (long long)BH * a.N * (D / 8);
+    long long blocks = (total + 255) / 256;
+    if (blocks > 148 * 16) blocks = 148 * 16;
+    dq_convert_kernel<D><<<(int)blocks, 256, 0, stream>>>(a, BH);
+  }
+  return cudaPeekAtLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+int launch_bwd(const void* q, const void* k, const void* v, const BwdArgs& args, int BH, int d,
+               cudaStream_t stream) {
+  if (d == 64) return launch_bwd_d<64>(q, k, v, args, BH, stream);
+  if (d == 128) return launch_bwd_d<128>(q, k, v, args, BH, stream);
+  return FA_ERR_UNSUPPORTED;
+}
+
+}  // namespace fa

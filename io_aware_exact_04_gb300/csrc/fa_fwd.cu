@@ -1,0 +1,400 @@
+// Forward pass of exact tiled attention on sm_103a.
+//
+// Method (practice record "Why recomputation is cheaper here than storing"):
+// each block of scores is formed in on-chip memory, consumed at once by a
+// blockwise softmax with a running row maximum and normaliser, and never
+// written to HBM; only O and the per-row statistics leave the chip
+// (handbook "FlashAttention Algorithm > Recomputation Strategy", section
+// "What Gets Stored vs Recomputed"; here m and l are folded into LSE).
+//
+// GB300 mapping (one CTA = two 128-row query tiles of one head):
+//   warp 8      TMA producer: Q tiles once, then K_j / V_j 128-key tiles
+//               through an NST-stage ring of 128-byte-swizzled smem tiles.
+//   warp 9      TMEM allocator and single-thread tcgen05.mma issuer:
+//               S_t = Q_t K_j^T (smem x smem -> TMEM fp32, M=128, N=128),
+//               O_t += P_t V_j (P from TMEM as bf16, V from smem, N=d).
+//   warps 0-3   softmax for query tile 0, warps 4-7 for tile 1; thread r of a
+//               warpgroup owns row r (TMEM lane r): running max/normaliser in
+//               registers, P written back over S in TMEM, O rescaled in TMEM
+//               only when the row maximum grows by more than 2^8 (exact: O and
+//               l always share the same reference maximum).
+// The issuer alternates the two tiles (PV_0, S_0 next, PV_1, S_1 next) so one
+// warpgroup's softmax overlaps the other's tensor-core work.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+#include "fa_internal.h"
+#include "tmap.h"
+
+namespace fa {
+
+template <int D>
+struct FwdCfg {
+  static constexpr int NSUB = D / 64;              // 128-byte column blocks per row
+  static constexpr int SUB_BYTES = 128 * 128;      // one [128 rows][64 bf16] block
+  static constexpr int TILE_BYTES = NSUB * SUB_BYTES;
+  static constexpr int NST = (D == 64) ? 3 : 2;    // K/V ring depth
+  static constexpr int OFF_Q = 0;                  // two query tiles
+  static constexpr int OFF_K = OFF_Q + 2 * TILE_BYTES;
+  static constexpr int OFF_V = OFF_K + NST * TILE_BYTES;
+  static constexpr int OFF_BAR = OFF_V + NST * TILE_BYTES;
+  static constexpr int SMEM_BYTES = OFF_BAR + 256 + 1024;  // barriers + alignment slack
+  // TMEM columns: S_t at 128 t (P_t over its first 64 columns), O_t at 256 + d t
+  __device__ static constexpr uint32_t tm_s(int t) { return 128u * t; }
+  __device__ static constexpr uint32_t tm_o(int t) { return 256u + (uint32_t)D * t; }
+  static constexpr uint32_t TM_COLS = 512;
+  static constexpr int THREADS = 320;
+};
+
+// Wait-site identifiers recorded with FA_ERR_TIMEOUT.
+enum { SITE_F_KV_EMPTY = 1, SITE_F_Q_FULL, SITE_F_K_FULL, SITE_F_V_FULL, SITE_F_P_READY, SITE_F_S_FULL,
+       SITE_F_O_DONE, SITE_F_DRAIN };
+
+template <int D>
+__global__ void __launch_bounds__(320, 1)
+    fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o, FwdArgs a) {
+  using C = FwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = align1024(smem_raw);
+  const uint32_t sbase = smem_u32(sm);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  // barriers
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::OFF_BAR);
+  const uint32_t b0 = smem_u32(bars);
+  auto BAR = [&](int i) { return b0 + 8u * i; };
+  const uint32_t q_full = BAR(0);
+  auto k_full = [&](int s) { return BAR(1 + s); };
+  auto v_full = [&](int s) { return BAR(1 + C::NST + s); };
+  auto kv_empty = [&](int s) { return BAR(1 + 2 * C::NST + s); };
+  const int nb = 1 + 3 * C::NST;
+  auto s_full = [&](int t) { return BAR(nb + t); };
+  auto p_ready = [&](int t) { return BAR(nb + 2 + t); };
+  auto o_done = [&](int t) { return BAR(nb + 4 + t); };
+  const uint32_t drain = BAR(nb + 6);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C::OFF_BAR + 8 * (nb + 7));
+  int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+  DevStatus st{a.status, abort_flag};
+
+  // work description
+  const int pair = a.n_pairs - 1 - (int)blockIdx.x;  // longest causal rows first
+  const int bh = blockIdx.y;
+  const int b = bh / a.H;
+  int kv = a.N;
+  if (a.kv_len) kv = min(max(a.kv_len[b], 0), a.N);
+  const int nkt = (kv + 127) >> 7;
+  const int q0 = pair * 256;
+  int n_t[2];
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    const int qs = q0 + t * 128;
+    n_t[t] = (qs >= a.N) ? 0 : (a.causal ? min(nkt, (qs >> 7) + 1) : nkt);
+  }
+  const int nmax = max(n_t[0], n_t[1]);
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int s = 0; s < C::NST; ++s) {
+      mbar_init(k_full(s), 1);
+      mbar_init(v_full(s), 1);
+      mbar_init(kv_empty(s), 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(s_full(t), 1);
+      mbar_init(p_ready(t), 4);
+      mbar_init(o_done(t), 1);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(smem_u32(tmem_slot), C::TM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0 && nmax > 0) {
+      prefetch_tmap(&tm_q);
+      prefetch_tmap(&tm_k);
+      prefetch_tmap(&tm_v);
+      const int nq = (n_t[1] > 0) ? 2 : 1;
+      mbar_arrive_expect_tx(q_full, nq * C::TILE_BYTES);
+      for (int t = 0; t < nq; ++t)
+        for (int s = 0; s < C::NSUB; ++s)
+          tma_load_3d(sbase + C::OFF_Q + t * C::TILE_BYTES + s * C::SUB_BYTES, &tm_q, s * 64, q0 + t * 128, bh,
+                      q_full);
+      int issued = 0;
+      for (int j = 0; j < nmax; ++j) {
+        const int s = j % C::NST;
+        if (!wait_bounded(kv_empty(s), ((j / C::NST) & 1) ^ 1, st, SITE_F_KV_EMPTY)) break;
+        mbar_arrive_expect_tx(k_full(s), C::TILE_BYTES);
+        for (int c = 0; c < C::NSUB; ++c)
+          tma_load_3d(sbase + C::OFF_K + s * C::TILE_BYTES + c * C::SUB_BYTES, &tm_k, c * 64, j * 128, bh,
+                      k_full(s));
+        mbar_arrive_expect_tx(v_full(s), C::TILE_BYTES);
+        for (int c = 0; c < C::NSUB; ++c)
+          tma_load_3d(sbase + C::OFF_V + s * C::TILE_BYTES + c * C::SUB_BYTES, &tm_v, c * 64, j * 128, bh,
+                      v_full(s));
+        issued = j + 1;
+      }
+      if (*(volatile int*)abort_flag) {
+        // let copies already in flight land before the CTA's smem is released
+        for (int j = max(0, issued - C::NST); j < issued; ++j) {
+          const int s = j % C::NST;
+          const uint32_t par = (j / C::NST) & 1;
+          const uint64_t t0 = globaltimer_ns();
+          while (!(mbar_try_wait(k_full(s), par) && mbar_try_wait(v_full(s), par)) &&
+                 globaltimer_ns() - t0 < 100000000ull) {
+          }
+        }
+      }
+    }
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0 && nmax > 0) {
+      constexpr uint32_t IDESC_S = idesc_bf16_f32(128, 128, 0, 0);  // Q, K both K-major
+      constexpr uint32_t IDESC_O = idesc_bf16_f32(128, D, 0, 1);    // P from TMEM, V MN-major
+      auto issue_s = [&](int t, int kst) {
+        const uint32_t qa = sbase + C::OFF_Q + t * C::TILE_BYTES;
+        const uint32_t ka = sbase + C::OFF_K + kst * C::TILE_BYTES;
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t off = (k >> 2) * C::SUB_BYTES + (k & 3) * 32;
+          mma_ss(tmem + C::tm_s(t), sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024), IDESC_S,
+                 k > 0);
+        }
+      };
+      auto issue_pv = [&](int t, int vst, uint32_t acc) {
+        const uint32_t va = sbase + C::OFF_V + vst * C::TILE_BYTES;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {  // 128 keys, 16 per MMA
+          mma_ts(tmem + C::tm_o(t), tmem + C::tm_s(t) + k * 8, sdesc_sw128(va + k * 2048, C::SUB_BYTES, 1024),
+                 IDESC_O, (acc | k) != 0);
+        }
+      };
+      bool ok = wait_bounded(q_full, 0, st, SITE_F_Q_FULL) && wait_bounded(k_full(0), 0, st, SITE_F_K_FULL);
+      if (ok) {
+        tc_fence_after();
+        for (int t = 0; t < 2; ++t)
+          if (n_t[t] > 0) {
+            issue_s(t, 0);
+            mma_commit(s_full(t));
+          }
+      }
+      for (int j = 0; ok && j < nmax; ++j) {
+        const int s = j % C::NST;
+        ok = wait_bounded(v_full(s), (j / C::NST) & 1, st, SITE_F_V_FULL);
+        if (!ok) break;
+        bool next_k_ready = false;
+        for (int t = 0; t < 2 && ok; ++t) {
+          if (j >= n_t[t]) continue;
+          ok = wait_bounded(p_ready(t), j & 1, st, SITE_F_P_READY);
+          if (!ok) break;
+          tc_fence_after();
+          issue_pv(t, s, j > 0);
+          mma_commit(o_done(t));
+          if (j + 1 < n_t[t]) {
+            const int s2 = (j + 1) % C::NST;
+            if (!next_k_ready) {
+              ok = wait_bounded(k_full(s2), ((j + 1) / C::NST) & 1, st, SITE_F_K_FULL);
+              if (!ok) break;
+              next_k_ready = true;
+            }
+            issue_s(t, s2);
+            mma_commit(s_full(t));
+          }
+        }
+        mma_commit(kv_empty(s));
+      }
+      // every MMA issued by this thread has completed before TMEM is released
+      mma_commit(drain);
+      const uint64_t t0 = globaltimer_ns();
+      while (!mbar_try_wait(drain, 0) && globaltimer_ns() - t0 < kWaitLimitNs) {
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ softmax warpgroups
+    const int t = warp >> 2;
+    const int wq = warp & 3;
+    const int row = wq * 32 + lane;  // TMEM lane == row within the query tile
+    const int qs = q0 + t * 128;
+    const int grow = qs + row;
+    const int n = n_t[t];
+    const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+    const uint32_t tS = tmem + lane_off + C::tm_s(t);
+    const uint32_t tO = tmem + lane_off + C::tm_o(t);
+    const float sl2 = a.scale_log2;
+    float* lse_row = a.lse + (size_t)bh * a.N;
+    if (qs < a.N && n == 0) {
+      // no valid key for any row of this tile: O = 0, LSE = -inf
+      if (grow < a.N) {
+        uint4* orow = reinterpret_cast<uint4*>(a.o + ((size_t)bh * a.N + grow) * D);
+        for (int c = 0; c < D / 8; ++c) orow[c] = make_uint4(0, 0, 0, 0);
+        lse_row[grow] = -INFINITY;
+      }
+    } else if (n > 0) {
+      float m_run = -INFINITY;  // running maximum of s*S*log2(e)
+      float l_run = 0.f;        // running normaliser
+      bool ok = true;
+      for (int j = 0; j < n; ++j) {
+        ok = wait_warp(s_full(t), j & 1, st, SITE_F_S_FULL);
+        if (!ok) break;
+        tc_fence_after();
+        float sv[128];
+        {
+          uint32_t r[4][32];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, r[c]);
+          tmem_wait_ld();
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int i = 0; i < 32; ++i) sv[c * 32 + i] = __uint_as_float(r[c][i]);
+        }
+        const int k0 = j * 128;
+        const bool need_mask = (k0 + 127 >= kv) || (a.causal && k0 + 127 > qs);
+        if (need_mask) {
+          const int lim = a.causal ? min(kv, grow + 1) : kv;  // keys [0, lim) are valid
+#pragma unroll
+          for (int c = 0; c < 128; ++c)
+            if (k0 + c >= lim) sv[c] = -INFINITY;
+        }
+        float mx = sv[0];
+#pragma unroll
+        for (int c = 1; c < 128; ++c) mx = fmaxf(mx, sv[c]);
+        const float m_tile = mx * sl2;
+        // lazy rescale: move the reference maximum only when it grows by > 2^8
+        float f = 1.f;
+        bool rescale_warp = false;
+        if (j == 0) {
+          m_run = m_tile;
+        } else {
+          const bool grow_m = m_tile > m_run + 8.0f;
+          rescale_warp = __any_sync(0xffffffffu, grow_m);
+          if (grow_m) {
+            f = ex2_approx(m_run - m_tile);
+            m_run = m_tile;
+          }
+        }
+        const float base = (m_run == -INFINITY) ? 0.f : m_run;
+        float lsum = 0.f;
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {  // 32 columns -> 16 packed bf16x2 words per store
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float p0 = ex2_approx(fmaf(sv[h * 32 + 2 * i], sl2, -base));
+            const float p1 = ex2_approx(fmaf(sv[h * 32 + 2 * i + 1], sl2, -base));
+            lsum += p0 + p1;
+            pk[i] = pack_bf16x2(p0, p1);
+          }
+          tmem_st16(tS + h * 16, pk);
+        }
+        l_run = l_run * f + lsum;
+        if (rescale_warp) {
+          // PV_{j-1} must have landed in O before it is rescaled
+          ok = wait_warp(o_done(t), (j - 1) & 1, st, SITE_F_O_DONE);
+          if (!ok) break;
+          tc_fence_after();
+          uint32_t r[32];
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            tmem_ld32(tO + c * 32, r);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * f);
+            tmem_st32(tO + c * 32, r);
+          }
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(p_ready(t));
+      }
+      if (ok) ok = wait_warp(o_done(t), (n - 1) & 1, st, SITE_F_O_DONE);
+      // every warp of the warpgroup reaches this vote, aborted or not, so the
+      // named barrier of the epilogue below is entered by all four or by none
+      ok = named_bar_and(1 + t, 128, ok);
+      if (ok) {
+        tc_fence_after();
+        // epilogue: O / l -> bf16 -> swizzled smem (this tile's Q buffer) -> TMA store
+        const float inv = (l_run > 0.f) ? 1.f / l_run : 0.f;
+        uint8_t* stage = sm + C::OFF_Q + t * C::TILE_BYTES;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld32(tO + c * 32, r);
+          tmem_wait_ld();
+          // columns c*32 .. c*32+31 = 4 chunks of 8 bf16 in column block (c*32)/64
+          const int blk = (c * 32) >> 6;
+          const int chunk0 = ((c * 32) & 63) >> 3;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint4 v;
+            v.x = pack_bf16x2(__uint_as_float(r[q * 8 + 0]) * inv, __uint_as_float(r[q * 8 + 1]) * inv);
+            v.y = pack_bf16x2(__uint_as_float(r[q * 8 + 2]) * inv, __uint_as_float(r[q * 8 + 3]) * inv);
+            v.z = pack_bf16x2(__uint_as_float(r[q * 8 + 4]) * inv, __uint_as_float(r[q * 8 + 5]) * inv);
+            v.w = pack_bf16x2(__uint_as_float(r[q * 8 + 6]) * inv, __uint_as_float(r[q * 8 + 7]) * inv);
+            *reinterpret_cast<uint4*>(stage + blk * C::SUB_BYTES + sw128_offset(row, chunk0 + q)) = v;
+          }
+        }
+        if (grow < a.N) lse_row[grow] = (l_run > 0.f) ? (m_run + lg2_approx(l_run)) * 0.6931471805599453f : -INFINITY;
+        fence_proxy_async_smem();
+        named_bar_sync(1 + t, 128);
+        if (wq == 0 && lane == 0) {
+          for (int c = 0; c < C::NSUB; ++c)
+            tma_store_3d(&tm_o, smem_u32(stage + c * C::SUB_BYTES), c * 64, qs, bh);
+          bulk_commit();
+          bulk_wait0();
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TM_COLS);
+  }
+}
+
+template <int D>
+static int launch_fwd_d(const void* q, const void* k, const void* v, void* o, const FwdArgs& args, int BH,
+                        cudaStream_t stream) {
+  using C = FwdCfg<D>;
+  CUtensorMap mq, mk, mv, mo;
+  const uint64_t N = (uint64_t)args.N;
+  const auto BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const auto SW = CU_TENSOR_MAP_SWIZZLE_128B;
+  if (!make_tmap_3d(&mq, q, BF, 2, D, N, BH, 64, 128, SW) || !make_tmap_3d(&mk, k, BF, 2, D, N, BH, 64, 128, SW) ||
+      !make_tmap_3d(&mv, v, BF, 2, D, N, BH, 64, 128, SW) || !make_tmap_3d(&mo, o, BF, 2, D, N, BH, 64, 128, SW))
+    return FA_ERR_CUDA;
+  static bool attr_set = false;  // benign race: idempotent
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) !=
+        cudaSuccess)
+      return FA_ERR_CUDA;
+    attr_set = true;
+  }
+  dim3 grid(args.n_pairs, BH);
+  fwd_kernel<D><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(mq, mk, mv, mo, args);
+  return cudaPeekAtLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+int launch_fwd(const void* q, const void* k, const void* v, void* o, const FwdArgs& args, int BH, int d,
+               cudaStream_t stream) {
+  if (d == 64) return launch_fwd_d<64>(q, k, v, o, args, BH, stream);
+  if (d == 128) return launch_fwd_d<128>(q, k, v, o, args, BH, stream);
+  return FA_ERR_UNSUPPORTED;
+}
+
+}  // namespace fa

@@ -1,0 +1,43 @@
+// Launch descriptions shared between the entry points and the kernels.
+#pragma once
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+namespace fa {
+
+struct FwdArgs {
+  int H, N;            // heads per batch, sequence length
+  int n_pairs;         // ceil(N / 256): CTAs per head (two 128-row query tiles each)
+  int causal;
+  float scale_log2;    // scale * log2(e)
+  const int* kv_len;   // [B] device, or null
+  float* lse;          // [B*H, N]
+  uint16_t* o;         // [B*H, N, d] bf16 (also written through the tensor map)
+  int* status;         // device status word (4 ints)
+};
+
+struct BwdArgs {
+  int H, N, Npad;      // Npad = N rounded up to a multiple of 128
+  int causal;
+  float scale;         // softmax scale s
+  float scale_log2;    // s * log2(e)
+  const int* kv_len;   // [B] device, or null
+  const uint16_t* o;   // [B*H, N, d]
+  const uint16_t* dO;  // [B*H, N, d]
+  const float* lse;    // [B*H, N]
+  float* lse2;         // workspace [B*H, Npad]: LSE * log2(e), +inf on padding rows
+  float* dvec;         // workspace [B*H, Npad]: D = rowsum(dO * O), 0 on padding rows
+  float* dq_acc;       // workspace [B*H, Npad, d] fp32
+  uint16_t* dq;        // [B*H, N, d] bf16
+  uint16_t* dk;        // [B*H, N, d] bf16
+  uint16_t* dv;        // [B*H, N, d] bf16
+  int* status;
+};
+
+int launch_fwd(const void* q, const void* k, const void* v, void* o, const FwdArgs& args, int BH, int d,
+               cudaStream_t stream);
+int launch_bwd(const void* q, const void* k, const void* v, const BwdArgs& args, int BH, int d,
+               cudaStream_t stream);
+
+}  // namespace fa

@@ -1,0 +1,96 @@
+"""The C-ABI library loads, exports what the headers declare, and rejects bad
+arguments on the host, before any CUDA call (so these run without a GPU)."""
+
+import ctypes
+
+import pytest
+
+from io_aware_exact_04_gb300 import _lib
+
+
+@pytest.fixture(scope="module")
+def lib(built):
+    return _lib.load("libfa.so")
+
+
+@pytest.mark.parametrize("header,so", [("fa.h", "libfa.so"), ("fa_selftest.h", "libfa_selftest.so")])
+def test_exports_every_declared_function(built, header, so):
+    names = _lib.declared_functions(header)
+    assert len(names) >= 2
+    lib = _lib.load(so)
+    for name in names:
+        assert hasattr(lib, name), name
+    assert set(names) == set(_lib.SIGNATURES[so]), "binding signatures and header disagree"
+
+
+def test_status_strings(lib):
+    for code in range(7):
+        assert lib.fa_status_string(code)
+    assert b"unknown" in lib.fa_status_string(99)
+    assert lib.fa_version() >= 100
+
+
+def test_workspace_size_is_linear_in_n(lib):
+    def ws(n, d=64):
+        return lib.fa_backward_workspace_size(8, 12, n, d)
+    assert ws(1024) == 96 * 1024 * (8 + 4 * 64)
+    assert ws(2048) == 2 * ws(1024)
+    assert ws(1000) == ws(1024)  # padded to 128 rows
+    assert lib.fa_backward_workspace_size(2, 16, 4096, 128) == 32 * 4096 * (8 + 4 * 128)
+    assert lib.fa_backward_workspace_size(1, 1, 128, 96) == 0
+
+
+A = ctypes.c_void_p(0x1000)  # 16-byte aligned fake device addresses: never dereferenced
+M = ctypes.c_void_p(0x1008)
+
+
+def fwd(lib, q=A, k=A, v=A, o=A, lse=A, B=1, H=1, N=128, d=64, scale=0.125, causal=0, kv=None):
+    return lib.fa_forward_ex(q, k, v, o, lse, B, H, N, d, scale, causal, kv, None)
+
+
+def bwd(lib, ptrs=None, B=1, H=1, N=128, d=64, scale=0.125, causal=0, ws=A, nbytes=1 << 30):
+    p = ptrs or [A] * 9
+    return lib.fa_backward_ex(*p, B, H, N, d, scale, causal, None, ws, nbytes, None)
+
+
+def test_forward_argument_errors(lib):
+    assert fwd(lib, d=96) == 2
+    assert fwd(lib, d=32) == 2
+    assert fwd(lib, causal=2) == 1
+    assert fwd(lib, scale=0.0) == 1
+    assert fwd(lib, scale=-1.0) == 1
+    assert fwd(lib, scale=float("inf")) == 1
+    assert fwd(lib, N=-1) == 1
+    assert fwd(lib, B=300, H=300) == 2
+    assert fwd(lib, q=None) == 1
+    assert fwd(lib, lse=None) == 1
+    assert fwd(lib, k=M) == 3
+    assert fwd(lib, o=M) == 3
+    # empty problems are a successful no-op, pointers unused
+    assert fwd(lib, q=None, k=None, v=None, o=None, lse=None, N=0) == 0
+    assert fwd(lib, q=None, k=None, v=None, o=None, lse=None, B=0) == 0
+
+
+def test_backward_argument_errors(lib):
+    assert bwd(lib, d=96) == 2
+    assert bwd(lib, causal=-1) == 1
+    assert bwd(lib, ws=None) == 1
+    for i in range(9):
+        p = [A] * 9
+        p[i] = None
+        assert bwd(lib, ptrs=p) == 1, i
+        p[i] = M
+        assert bwd(lib, ptrs=p) == 3, i
+    assert bwd(lib, ws=ctypes.c_void_p(0x1010)) == 3  # workspace wants 256-byte alignment
+    need = lib.fa_backward_workspace_size(1, 1, 128, 64)
+    assert bwd(lib, nbytes=need - 1) == 1
+    assert bwd(lib, ptrs=[None] * 9, ws=None, N=0) == 0
+
+
+def test_selftest_argument_errors(built):
+    st = _lib.load("libfa_selftest.so")
+    assert st.fa_selftest_mma(A, A, A, 96, 64, 0, A, None) == 2
+    assert st.fa_selftest_mma(A, A, A, 64, 64, 5, A, None) == 2
+    assert st.fa_selftest_mma(None, A, A, 64, 64, 0, A, None) == 1
+    assert st.fa_selftest_wait_timeout(None, 10, None) == 1
+    assert st.fa_selftest_wait_timeout(A, 0, None) == 1
