@@ -1,0 +1,417 @@
+"""Benchmark: exact attention forward + backward on one GB300 (or N replicas).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+A step is one forward and one backward pass of the whole workload through the
+C ABI on inputs already resident in HBM; L2 is flushed (a 256 MiB write)
+before every timed step and the flush is outside the timed events. The JSON
+line reports nominal fwd+bwd TFLOP/s (12 c N^2 d per head, recompute FLOPs
+excluded and reported separately), the roofline of the dominant kernel, the
+end-to-end number through host buffers, the oracle on host cores, peak
+activation memory and the SM clocks seen while timing.
+
+--impl reference times the fp64 CPU oracle instead (the only reference this
+method has): each step is a bounded sample of heads of the same workload.
+Under torchrun each rank runs the workload on its own GPU (heads are
+independent: weak scaling, no collective on the data path).
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "attention fwd+bwd TFLOP/s (bf16, 1×GB300) and % of tensor-core peak; peak mem"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while it runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.t_start = self.t_stop = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=timestamp," + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self, which):
+        setattr(self, which, time.time())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for ts, line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            rows.append((ts, parts))
+        inside = [r for ts, r in rows if self.t_start and self.t_stop and self.t_start <= ts <= self.t_stop + 0.1]
+        use = inside or rows
+        sm = [float(r[1]) for r in use if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in use if r[2].replace(".", "").isdigit()]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in use:
+            for name, val in zip(names, r[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(inside), "samples_total": len(rows)}
+
+
+# ------------------------------------------------------------------ oracle on host cores
+def oracle_sample(w, x, budget_s: float, max_heads=None):
+    """Time the fp64 oracle on as many heads of the workload as fit in budget_s."""
+    import numpy as np
+
+    from oracle import ref
+
+    B, H = w.B, w.H
+    f64 = lambda t: t.to(dtype=__import__("torch").float64).numpy()  # noqa: E731
+    kv = None if x["kv_len"] is None else x["kv_len"].numpy()
+    heads = [(b, h) for b in range(B) for h in range(H)]
+    done, flops = 0, 0.0
+    c = 0.5 if w.causal else 1.0
+    t0 = time.perf_counter()
+    for b, h in heads:
+        q, k, v, do = (f64(x[n][b, h]) for n in ("q", "k", "v", "do"))
+        kl = None if kv is None else int(kv[b])
+        ref.head_backward(q, k, v, do, w.scale, w.causal, kl, row_block=2048 if w.N > 4096 else None)
+        nk = w.N if kl is None else kl
+        flops += 12 * c * w.N * nk * w.d
+        done += 1
+        if time.perf_counter() - t0 > budget_s or (max_heads and done >= max_heads):
+            break
+    dt = time.perf_counter() - t0
+    cores = len(os.sched_getaffinity(0))
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": f"{done} of {B * H} heads of {w.name} (fp64 numpy, fwd+bwd, S and P materialised), "
+                      f"{dt:.1f} s", "seconds": dt, "heads": done}
+
+
+# ------------------------------------------------------------------ traffic record
+def traffic_record(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if its source hash still matches."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}_traffic.txt")
+    try:
+        with open(path) as f:
+            kv = dict(line.split(":", 1) for line in f if ":" in line and not line.startswith("#"))
+    except OSError:
+        return None
+    src = kv.get("source_sha256", "").strip()
+    files = [s.strip() for s in kv.get("source_files", "").split(",") if s.strip()]
+    h = hashlib.sha256()
+    for fn in files:
+        with open(os.path.join(ROOT, fn), "rb") as f:
+            h.update(f.read())
+    if not files or h.hexdigest() != src:
+        return None
+    try:
+        return float(kv["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+def source_hash(files):
+    h = hashlib.sha256()
+    for fn in files:
+        with open(os.path.join(ROOT, fn), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+# ------------------------------------------------------------------ main arms
+def run_reference(args, w):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    x = workloads.make_inputs(w)
+    budget = min(20.0, 150.0 / max(1, args.steps + args.warmup))  # whole run within a few minutes
+    for _ in range(args.warmup):
+        oracle_sample(w, x, budget, max_heads=1)
+    vals, secs, heads = [], 0.0, 0
+    for _ in range(args.steps):
+        r = oracle_sample(w, x, budget)
+        vals.append(r["value"])
+        secs += r["seconds"]
+        heads += r["heads"]
+    value = statistics.median(vals)
+    cores = len(os.sched_getaffinity(0))
+    sample = f"each step: the fp64 oracle on as many heads of {w.name} as fit in {budget:.1f} s ({heads} heads over {args.steps} steps)"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / max(1, args.steps),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded N(0,1), bf16-rounded, upcast to fp64)",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_gpu(args, w):
+    import ctypes
+
+    import torch
+
+    from io_aware_exact_04_gb300 import _lib, memmodel
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    lib = _lib.load("libfa.so")
+    peaks, peak_src = load_peaks()
+
+    x = workloads.make_inputs(w, seed=0)
+    B, H, N, d = w.B, w.H, w.N, w.d
+    q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "do"))
+    kv = None if x["kv_len"] is None else x["kv_len"].to(dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+    wsb = int(lib.fa_backward_workspace_size(B, H, N, d))
+    work = torch.empty(wsb, dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sp = ctypes.c_void_p(stream.cuda_stream)
+    P = lambda t: ctypes.c_void_p(t.data_ptr()) if t is not None else None  # noqa: E731
+    causal = int(w.causal)
+
+    def fwd():
+        _lib.check(lib.fa_forward_ex(P(q), P(k), P(v), P(o), P(lse), B, H, N, d, w.scale, causal, P(kv), sp), "fwd")
+
+    def bwd_stage(s):
+        _lib.check(lib.fa_backward_stage(s, P(q), P(k), P(v), P(o), P(do), P(lse), P(dq), P(dk), P(dv), B, H, N,
+                                         d, w.scale, causal, P(kv), P(work), wsb, sp), "bwd")
+
+    kernels = ["fwd_kernel", "bwd_pre_kernel", "bwd_kernel", "dq_convert_kernel"]
+
+    def step(ev=None):
+        if ev is None:
+            fwd()
+            for s in range(3):
+                bwd_stage(s)
+            return
+        ev[0].record(stream)
+        fwd()
+        ev[1].record(stream)
+        for s in range(3):
+            bwd_stage(s)
+            ev[2 + s].record(stream)
+
+    for _ in range(max(3, args.warmup)):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(dev)
+    code, detail = ctypes.c_int(0), (ctypes.c_int * 4)()
+    if lib.fa_get_last_device_status(sp, detail) != 0:
+        raise RuntimeError(f"device status after warm-up: {list(detail)}")
+
+    # peak activation memory: what fwd+bwd holds besides inputs and gradients
+    act_bytes = o.numel() * 2 + lse.numel() * 4 + wsb
+
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    sampler = ClockSampler(local if "CUDA_VISIBLE_DEVICES" not in os.environ else 0)
+    if rank == 0:
+        sampler.start()
+        time.sleep(0.3)
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    sampler.mark("t_start")
+    for i in range(args.steps):
+        flush.zero_()
+        step(events[i])
+    torch.cuda.synchronize(dev)
+    sampler.mark("t_stop")
+    if ws > 1:
+        torch.distributed.barrier()
+    per_kernel = {kname: 0.0 for kname in kernels}
+    total_ms = 0.0
+    for ev in events:
+        t = [ev[0].elapsed_time(ev[j]) for j in range(1, 5)]
+        per_kernel["fwd_kernel"] += t[0]
+        per_kernel["bwd_pre_kernel"] += t[1] - t[0]
+        per_kernel["bwd_kernel"] += t[2] - t[1]
+        per_kernel["dq_convert_kernel"] += t[3] - t[2]
+        total_ms += t[3]
+    if lib.fa_get_last_device_status(sp, detail) != 0:
+        raise RuntimeError(f"device status after timing: {list(detail)}")
+    ms_step = total_ms / args.steps
+    if ws > 1:
+        tt = torch.tensor([ms_step], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        ms_step = float(tt.item())
+
+    fl = workloads.flop_counts(w, x["kv_len"])
+    value = ws * fl["fwd_bwd_nominal"] / (ms_step * 1e-3) / 1e12
+    executed = ws * fl["fwd_bwd_executed"] / (ms_step * 1e-3) / 1e12
+
+    # dominant kernel and its roofline (tensor-bound: algorithmic flops per launch / event time)
+    avg = {kname: t / args.steps for kname, t in per_kernel.items()}
+    dom = max(avg, key=avg.get)
+    c = 0.5 if w.causal else 1.0
+    alg_flops = {"fwd_kernel": fl["fwd"], "bwd_kernel": fl["bwd_nominal"] + fl["bwd_recompute"]}
+    if dom in alg_flops:
+        achieved = alg_flops[dom] / (avg[dom] * 1e-3) / 1e12
+        peak = float(peaks["bf16_tflops"])
+        traffic = traffic_record(dom, w.name)
+        roof = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": traffic,
+                "peak_source": f"{peak_src} bf16 dense (burst)", "avg_launch_ms": avg[dom]}
+    else:  # a memory-bound helper dominating would be reported against HBM
+        nbytes = {"bwd_pre_kernel": B * H * N * d * 2 * 2 + B * H * (N + 127) // 128 * 128 * (8 + 4 * d),
+                  "dq_convert_kernel": B * H * N * d * (4 + 2)}[dom]
+        achieved = nbytes / (avg[dom] * 1e-3) / 1e9
+        peak = float(peaks["hbm_gbs"])
+        roof = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "traffic": traffic_record(dom, w.name), "peak_source": peak_src,
+                "avg_launch_ms": avg[dom]}
+
+    # end to end through host buffers: H2D inputs, fwd+bwd, D2H outputs, every step
+    hq, hk, hv, hdo = (x[n].pin_memory() for n in ("q", "k", "v", "do"))
+    ho, hdq, hdk, hdv = (torch.empty_like(hq).pin_memory() for _ in range(4))
+    hlse = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
+    h2d = 4 * hq.numel() * 2
+    d2h = 4 * hq.numel() * 2 + hlse.numel() * 4
+    e2e_steps = max(3, min(args.steps, 50))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_ms = 0.0
+    for i in range(e2e_steps + 2):
+        flush.zero_()
+        torch.cuda.synchronize(dev)
+        e0.record(stream)
+        q.copy_(hq, non_blocking=True)
+        k.copy_(hk, non_blocking=True)
+        v.copy_(hv, non_blocking=True)
+        do.copy_(hdo, non_blocking=True)
+        step()
+        ho.copy_(o, non_blocking=True)
+        hlse.copy_(lse, non_blocking=True)
+        hdq.copy_(dq, non_blocking=True)
+        hdk.copy_(dk, non_blocking=True)
+        hdv.copy_(dv, non_blocking=True)
+        e1.record(stream)
+        e1.synchronize()
+        if i >= 2:
+            e2e_ms += e0.elapsed_time(e1)
+    e2e_ms /= e2e_steps
+    e2e_val = ws * fl["fwd_bwd_nominal"] / (e2e_ms * 1e-3) / 1e12
+
+    clocks = sampler.stop() if rank == 0 else None
+    if ws > 1:
+        torch.distributed.barrier()
+    if rank != 0:
+        return
+    cpu = oracle_sample(w, x, budget_s=args.cpu_budget) if not args.no_cpu_baseline else None
+    std = memmodel.training_memory(N, d_model=H * d, heads=H, layers=1)
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) inputs, bf16)",
+        "config": {"workload": w.name, "B": B, "H": H, "N": N, "d": d, "causal": w.causal,
+                   "key_padding": w.padded, "l2": "flushed before every step (256 MiB write, untimed)",
+                   "flops": "nominal fwd+bwd 12*c*N*Nk*d per head (c = 1/2 causal), recompute excluded",
+                   "parallelism": f"replicas x{ws} (heads independent)"},
+        "tflops_executed": executed,
+        "pct_of_peak": 100.0 * value / float(peaks["bf16_tflops"]),
+        "pct_of_peak_executed": 100.0 * executed / float(peaks["bf16_tflops"]),
+        "peak_source": f"{peak_src} MEASURED_PEAKS bf16_tflops" if peak_src == "measured" else "fallback 1900 TFLOP/s",
+        "fwd_ms": avg["fwd_kernel"], "bwd_ms": avg["bwd_pre_kernel"] + avg["bwd_kernel"] + avg["dq_convert_kernel"],
+        "fwd_tflops": fl["fwd"] / (avg["fwd_kernel"] * 1e-3) / 1e12,
+        "bwd_tflops_nominal": fl["bwd_nominal"] / ((avg["bwd_pre_kernel"] + avg["bwd_kernel"] + avg["dq_convert_kernel"]) * 1e-3) / 1e12,
+        "kernel_ms": avg,
+        "peak_act_mem_bytes": act_bytes,
+        "act_bytes_per_head_row": act_bytes / (B * H * N),
+        "std_attention_matrix_bytes_bf16": B * 2 * N * N * H * 2,
+        "std_attention_memmodel_gb_per_layer_B1": std["standard_gb"],
+        "roofline": roof,
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_ms, "steps": e2e_steps},
+        "gpu_launches": 4 * args.steps,
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default="gpt2", choices=sorted(workloads.WORKLOADS))
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    w = workloads.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_gpu(args, w)
+
+
+if __name__ == "__main__":
+    main()

@@ -98,6 +98,19 @@ FA_API int fa_backward_ex(const void* q, const void* k, const void* v, const voi
                    void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale, int causal,
                    const int32_t* kv_len, void* workspace, size_t workspace_bytes, fa_stream_t stream);
 
+/* One stage of fa_backward_ex, same arguments; running stages 0, 1, 2 in
+ * order on one stream is exactly fa_backward_ex. Exposed so that each kernel
+ * can be timed on its own.
+ *   0: D = rowsum(dO * O) and LSE in base 2 per query row, into the workspace;
+ *      zeroes the fp32 dQ accumulator.
+ *   1: the recomputing kernel: dK and dV written, dQ accumulated in fp32.
+ *   2: the fp32 dQ accumulator rounded to bf16 into dq.
+ * Any other stage value returns FA_ERR_INVALID_ARG. */
+FA_API int fa_backward_stage(int stage, const void* q, const void* k, const void* v, const void* o, const void* dO,
+                             const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+                             float scale, int causal, const int32_t* kv_len, void* workspace,
+                             size_t workspace_bytes, fa_stream_t stream);
+
 /* Static text for an fa_status value. */
 FA_API const char* fa_status_string(int status);
 
@@ -105,6 +118,10 @@ FA_API const char* fa_status_string(int status);
  * word (FA_OK if no kernel recorded an error). If detail is non-NULL it
  * receives 4 ints: code, wait site, blockIdx.x, blockIdx.y of the first error. */
 FA_API int fa_get_last_device_status(fa_stream_t stream, int* detail);
+
+/* For the calling host thread: text naming the CUDA call that made the last
+ * FA_ERR_CUDA return and its error, or "" if none has. Static storage. */
+FA_API const char* fa_last_error_detail(void);
 
 /* Library version as major*10000 + minor*100 + patch. */
 FA_API int fa_version(void);

@@ -29,9 +29,11 @@ SIGNATURES = {
         "fa_backward_workspace_size": (_sz, [_i, _i, _i, _i]),
         "fa_backward": (_i, [_vp] * 9 + [_i, _i, _i, _i, _f, _i, _vp, _sz, _vp]),
         "fa_backward_ex": (_i, [_vp] * 9 + [_i, _i, _i, _i, _f, _i, _vp, _vp, _sz, _vp]),
+        "fa_backward_stage": (_i, [_i] + [_vp] * 9 + [_i, _i, _i, _i, _f, _i, _vp, _vp, _sz, _vp]),
         "fa_status_string": (ctypes.c_char_p, [_i]),
         "fa_get_last_device_status": (_i, [_vp, _vp]),
         "fa_version": (_i, []),
+        "fa_last_error_detail": (ctypes.c_char_p, []),
     },
     "libfa_selftest.so": {
         "fa_selftest_mma": (_i, [_vp, _vp, _vp, _i, _i, _i, _vp, _vp]),
@@ -73,8 +75,10 @@ def declared_functions(header: str):
 class FaError(RuntimeError):
     def __init__(self, code: int, where: str):
         self.code = code
-        msg = load().fa_status_string(code).decode()
-        super().__init__(f"{where}: {STATUS_NAMES.get(code, code)} ({msg})")
+        lib = load()
+        msg = lib.fa_status_string(code).decode()
+        detail = lib.fa_last_error_detail().decode() if code == 4 else ""
+        super().__init__(f"{where}: {STATUS_NAMES.get(code, code)} ({msg}){' ' + detail if detail else ''}")
 
 
 def check(code: int, where: str) -> None:

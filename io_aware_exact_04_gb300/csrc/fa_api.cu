@@ -4,6 +4,7 @@
 
 #include <cmath>
 #include <cstdint>
+#include <cstdio>
 #include <mutex>
 
 #include "fa.h"
@@ -21,15 +22,17 @@ std::mutex g_status_mu;
 
 int* device_status(int* err) {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
-    *err = FA_ERR_CUDA;
+  const cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    *err = fa::cuda_fail("cudaGetDevice", (int)e, cudaGetErrorName(e));
     return nullptr;
   }
   std::lock_guard<std::mutex> lk(g_status_mu);
   if (!g_status_ptr[dev]) {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess) {
-      *err = FA_ERR_CUDA;
+    const cudaError_t e2 = cudaGetSymbolAddress(&p, g_status);
+    if (e2 != cudaSuccess) {
+      *err = fa::cuda_fail("cudaGetSymbolAddress", (int)e2, cudaGetErrorName(e2));
       return nullptr;
     }
     g_status_ptr[dev] = static_cast<int*>(p);
@@ -67,9 +70,25 @@ WsLayout ws_layout(int B, int H, int N, int d) {
   return w;
 }
 
+thread_local char g_last_error[256] = "";
+
 }  // namespace
 
+namespace fa {
+int cuda_fail(const char* where, int code, const char* what) {
+  std::snprintf(g_last_error, sizeof(g_last_error), "%s failed: %s (code %d)", where, what ? what : "", code);
+  return FA_ERR_CUDA;
+}
+int check_launch(const char* kernel) {
+  const cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) return FA_OK;
+  return cuda_fail(kernel, (int)e, cudaGetErrorName(e));
+}
+}  // namespace fa
+
 extern "C" {
+
+const char* fa_last_error_detail(void) { return g_last_error; }
 
 int fa_version(void) { return 100; }
 
@@ -120,9 +139,11 @@ size_t fa_backward_workspace_size(int B, int H, int N, int d) {
   return ws_layout(B, H, N, d).total;
 }
 
-int fa_backward_ex(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
-                   void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale, int causal,
-                   const int32_t* kv_len, void* workspace, size_t workspace_bytes, fa_stream_t stream) {
+int fa_backward_stage(int stage, const void* q, const void* k, const void* v, const void* o, const void* dO,
+                      const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale,
+                      int causal, const int32_t* kv_len, void* workspace, size_t workspace_bytes,
+                      fa_stream_t stream) {
+  if (stage < 0 || stage > 2) return FA_ERR_INVALID_ARG;
   int rc = check_common(B, H, N, d, scale, causal);
   if (rc != FA_OK) return rc;
   if ((long long)B * H * N == 0) return FA_OK;
@@ -155,7 +176,18 @@ int fa_backward_ex(const void* q, const void* k, const void* v, const void* o, c
   a.dk = static_cast<uint16_t*>(dk);
   a.dv = static_cast<uint16_t*>(dv);
   a.status = status;
-  return fa::launch_bwd(q, k, v, a, B * H, d, reinterpret_cast<cudaStream_t>(stream));
+  return fa::launch_bwd_stage(stage, q, k, v, a, B * H, d, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int fa_backward_ex(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
+                   void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale, int causal,
+                   const int32_t* kv_len, void* workspace, size_t workspace_bytes, fa_stream_t stream) {
+  for (int stage = 0; stage < 3; ++stage) {
+    const int rc = fa_backward_stage(stage, q, k, v, o, dO, lse, dq, dk, dv, B, H, N, d, scale, causal, kv_len,
+                                     workspace, workspace_bytes, stream);
+    if (rc != FA_OK) return rc;
+  }
+  return FA_OK;
 }
 
 int fa_backward(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,

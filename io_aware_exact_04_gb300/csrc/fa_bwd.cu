@@ -487,8 +487,18 @@ __global__ void __launch_bounds__(448, 1)
 }
 
 template <int D>
-static int launch_bwd_d(const void* q, const void* k, const void* v, const BwdArgs& a, int BH,
-                        cudaStream_t stream) {
+static int launch_bwd_pre_d(const BwdArgs& a, int BH, cudaStream_t stream) {
+  const long long rows = (long long)BH * a.Npad;
+  const int rpw = 32 / (D / 8);
+  const long long warps = (rows + rpw - 1) / rpw;
+  const int blocks = (int)((warps + 7) / 8);
+  bwd_pre_kernel<D><<<blocks, 256, 0, stream>>>(a, BH);
+  return check_launch(__func__);
+}
+
+template <int D>
+static int launch_bwd_main_d(const void* q, const void* k, const void* v, const BwdArgs& a, int BH,
+                             cudaStream_t stream) {
   using C = BwdCfg<D>;
   const uint64_t N = (uint64_t)a.N;
   const auto BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
@@ -500,42 +510,38 @@ static int launch_bwd_d(const void* q, const void* k, const void* v, const BwdAr
       !make_tmap_3d(&mdk, a.dk, BF, 2, D, N, BH, 64, 128, SW) ||
       !make_tmap_3d(&mdv, a.dv, BF, 2, D, N, BH, 64, 128, SW) ||
       !make_tmap_3d(&mdq, a.dq_acc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, D, (uint64_t)a.Npad, BH, 32, C::BR, SW))
-    return FA_ERR_CUDA;
-  static bool attr_set = false;
+    return cuda_fail("cuTensorMapEncodeTiled", 0, "tensor map rejected");
+  static bool attr_set = false;  // benign race: idempotent
   if (!attr_set) {
-    if (cudaFuncSetAttribute(bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) !=
-        cudaSuccess)
-      return FA_ERR_CUDA;
+    const cudaError_t e =
+        cudaFuncSetAttribute(bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    if (e != cudaSuccess) return cuda_fail("cudaFuncSetAttribute", (int)e, cudaGetErrorName(e));
     attr_set = true;
   }
-  // 1. D, base-2 LSE, zeroed dQ accumulator
-  {
-    const long long rows = (long long)BH * a.Npad;
-    const int rpw = 32 / (D / 8);
-    const long long warps = (rows + rpw - 1) / rpw;
-    const int blocks = (int)((warps + 7) / 8);
-    bwd_pre_kernel<D><<<blocks, 256, 0, stream>>>(a, BH);
-  }
-  // 2. main kernel: one CTA per (key tile, head)
-  {
-    dim3 grid((a.N + 127) / 128, BH);
-    bwd_kernel<D><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(mq, mk, mv, mdo, mdk, mdv, mdq, a);
-  }
-  // 3. dQ to bf16
-  {
-    const long long total = (long long)BH * a.N * (D / 8);
-    long long blocks = (total + 255) / 256;
-    if (blocks > 148 * 16) blocks = 148 * 16;
-    dq_convert_kernel<D><<<(int)blocks, 256, 0, stream>>>(a, BH);
-  }
-  return cudaPeekAtLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+  dim3 grid((a.N + 127) / 128, BH);
+  bwd_kernel<D><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(mq, mk, mv, mdo, mdk, mdv, mdq, a);
+  return check_launch(__func__);
 }
 
-int launch_bwd(const void* q, const void* k, const void* v, const BwdArgs& args, int BH, int d,
-               cudaStream_t stream) {
-  if (d == 64) return launch_bwd_d<64>(q, k, v, args, BH, stream);
-  if (d == 128) return launch_bwd_d<128>(q, k, v, args, BH, stream);
-  return FA_ERR_UNSUPPORTED;
+template <int D>
+static int launch_bwd_convert_d(const BwdArgs& a, int BH, cudaStream_t stream) {
+  const long long total = (long long)BH * a.N * (D / 8);
+  long long blocks = (total + 255) / 256;
+  if (blocks > 152 * 16) blocks = 152 * 16;
+  dq_convert_kernel<D><<<(int)blocks, 256, 0, stream>>>(a, BH);
+  return check_launch(__func__);
+}
+
+int launch_bwd_stage(int stage, const void* q, const void* k, const void* v, const BwdArgs& a, int BH, int d,
+                     cudaStream_t stream) {
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  switch (stage) {
+    case 0: return d == 64 ? launch_bwd_pre_d<64>(a, BH, stream) : launch_bwd_pre_d<128>(a, BH, stream);
+    case 1:
+      return d == 64 ? launch_bwd_main_d<64>(q, k, v, a, BH, stream) : launch_bwd_main_d<128>(q, k, v, a, BH, stream);
+    case 2: return d == 64 ? launch_bwd_convert_d<64>(a, BH, stream) : launch_bwd_convert_d<128>(a, BH, stream);
+    default: return FA_ERR_INVALID_ARG;
+  }
 }
 
 }  // namespace fa

@@ -377,17 +377,17 @@ static int launch_fwd_d(const void* q, const void* k, const void* v, void* o, co
   const auto SW = CU_TENSOR_MAP_SWIZZLE_128B;
   if (!make_tmap_3d(&mq, q, BF, 2, D, N, BH, 64, 128, SW) || !make_tmap_3d(&mk, k, BF, 2, D, N, BH, 64, 128, SW) ||
       !make_tmap_3d(&mv, v, BF, 2, D, N, BH, 64, 128, SW) || !make_tmap_3d(&mo, o, BF, 2, D, N, BH, 64, 128, SW))
-    return FA_ERR_CUDA;
+    return cuda_fail("cuTensorMapEncodeTiled", 0, "tensor map rejected");
   static bool attr_set = false;  // benign race: idempotent
   if (!attr_set) {
-    if (cudaFuncSetAttribute(fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) !=
-        cudaSuccess)
-      return FA_ERR_CUDA;
+    const cudaError_t e =
+        cudaFuncSetAttribute(fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    if (e != cudaSuccess) return cuda_fail("cudaFuncSetAttribute", (int)e, cudaGetErrorName(e));
     attr_set = true;
   }
   dim3 grid(args.n_pairs, BH);
   fwd_kernel<D><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(mq, mk, mv, mo, args);
-  return cudaPeekAtLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+  return check_launch(__func__);
 }
 
 int launch_fwd(const void* q, const void* k, const void* v, void* o, const FwdArgs& args, int BH, int d,

@@ -35,9 +35,17 @@ struct BwdArgs {
   int* status;
 };
 
+// Records, for this host thread, which CUDA call failed and why (read back by
+// fa_last_error_detail). Returns FA_ERR_CUDA for convenience.
+int cuda_fail(const char* where, int code, const char* what);
+// After a launch: FA_OK, or FA_ERR_CUDA with the launch error recorded.
+int check_launch(const char* kernel);
+
 int launch_fwd(const void* q, const void* k, const void* v, void* o, const FwdArgs& args, int BH, int d,
                cudaStream_t stream);
-int launch_bwd(const void* q, const void* k, const void* v, const BwdArgs& args, int BH, int d,
-               cudaStream_t stream);
+// stage 0: D, base-2 LSE, zeroed dQ accumulator; 1: main kernel (dK, dV, dQ accumulator);
+// 2: dQ accumulator -> bf16 dQ
+int launch_bwd_stage(int stage, const void* q, const void* k, const void* v, const BwdArgs& args, int BH, int d,
+                     cudaStream_t stream);
 
 }  // namespace fa

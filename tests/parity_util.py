@@ -13,6 +13,7 @@ from oracle import ref
 # <= 2e-2 * max |reference tensor| (bf16 inputs, fp32 accumulation).
 LSE_ATOL = 1e-3
 REL_TOL = 2e-2
+ABS_FLOOR = 1e-4
 
 
 def run_gpu(x, causal, device, scale=None):
@@ -42,7 +43,10 @@ def compare(name, got, want):
         return err, LSE_ATOL
     err = float(np.abs(got - want).max()) if got.size else 0.0
     bound = REL_TOL * float(np.abs(want).max()) if want.size else 0.0
-    return err, max(bound, 1e-6)
+    # Where the mathematics makes the reference tensor identically zero (one
+    # valid key: dS = 0, so dQ = dK = 0), the relative bound is 0; fp32
+    # accumulation of O(1) bf16 inputs leaves rounding noise of order 1e-6 there.
+    return err, max(bound, ABS_FLOOR)
 
 
 def check_all_heads(B, H, N, d, causal, kv_len=None, seed=0, device=None, qk_scale=1.0):

@@ -85,6 +85,9 @@ def test_backward_argument_errors(lib):
     need = lib.fa_backward_workspace_size(1, 1, 128, 64)
     assert bwd(lib, nbytes=need - 1) == 1
     assert bwd(lib, ptrs=[None] * 9, ws=None, N=0) == 0
+    for stage in (-1, 3):
+        assert lib.fa_backward_stage(stage, *[A] * 9, 1, 1, 128, 64, 0.125, 0, None, A, 1 << 30, None) == 1
+    assert lib.fa_backward_stage(1, *[A] * 9, 1, 1, 128, 96, 0.125, 0, None, A, 1 << 30, None) == 2
 
 
 def test_selftest_argument_errors(built):

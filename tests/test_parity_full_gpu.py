@@ -1,0 +1,72 @@
+"""Parity at the workloads' full sizes, in the launch configuration the
+benchmark times: selected heads compared with the fp64 oracle (whole heads up
+to N = 4096, sampled query rows and keys beyond), and on every head the
+invariants that hold at any size:
+  sum_j dK_j = 0            (each row of dS sums to zero)
+  sum_j dV_j = sum_i dO_i   (each row of P sums to one; rows with a valid key)
+  dK_j = dV_j = 0           for keys beyond the valid length
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from oracle import ref
+from tests.parity_util import assert_within, compare, f64, run_gpu
+
+pytestmark = pytest.mark.gpu
+
+FULL = ["gpt2", "bert", "d128", "long2048", "long8192", "long16384", "long32768"]
+
+
+def _heads(w):
+    return [(0, 0), (w.B - 1, w.H - 1)]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_sampled_parity_and_invariants(gpu, name):
+    w = workloads.WORKLOADS[name]
+    x = workloads.make_inputs(w)
+    g = run_gpu(x, w.causal, gpu)
+    kv = None if x["kv_len"] is None else x["kv_len"].numpy()
+
+    # ---- oracle on selected heads
+    rng = np.random.default_rng(0)
+    for b, h in _heads(w):
+        q, k, v, do = (f64(x[n][b, h]) for n in ("q", "k", "v", "do"))
+        kl = None if kv is None else int(kv[b])
+        if w.N <= 4096:
+            r = ref.head_backward(q, k, v, do, w.scale, w.causal, kl)
+            rows = keys = np.arange(w.N)
+        else:
+            rows = np.unique(np.concatenate([[0, 1, 127, 128, w.N // 2, w.N - 1], rng.integers(0, w.N, 10)]))
+            keys = np.unique(np.concatenate([[0, 1, 127, 128, w.N // 2, w.N - 1], rng.integers(0, w.N, 10)]))
+            smp = ref.head_sampled(q, k, v, do, w.scale, w.causal, kl, rows, keys)
+            r = {"o": smp["o"], "lse": smp["lse"], "dq": smp["dq"], "dk": smp["dk"], "dv": smp["dv"]}
+        errs = {}
+        for nm, idx in (("o", rows), ("lse", rows), ("dq", rows), ("dk", keys), ("dv", keys)):
+            got = f64(g[nm][b, h])[idx]
+            want = r[nm] if w.N > 4096 else r[nm][idx]
+            errs[nm] = compare(nm, got, want)
+        assert_within(errs)
+
+    # ---- invariants on every head (fp64 sums of the bf16 outputs)
+    dk = g["dk"].double()
+    dv = g["dv"].double()
+    dO = x["do"].to(gpu).double()
+    sum_dk = dk.sum(dim=2).abs().amax(dim=-1)            # [B, H]
+    abs_dk = dk.abs().sum(dim=2).amax(dim=-1)
+    assert float((sum_dk / abs_dk).max()) < 2e-3
+    if kv is None:
+        diff = (dv.sum(dim=2) - dO.sum(dim=2)).abs().amax(dim=-1)
+        scale_ = dO.abs().sum(dim=2).amax(dim=-1)
+        assert float((diff / scale_).max()) < 2e-3
+    else:
+        for b in range(w.B):
+            n_valid = int(kv[b])
+            assert torch.all(g["dk"][b, :, n_valid:] == 0) and torch.all(g["dv"][b, :, n_valid:] == 0)
+            diff = (dv[b].sum(dim=1) - dO[b].sum(dim=1)).abs().amax(dim=-1)
+            assert float((diff / dO[b].abs().sum(dim=1).amax(dim=-1)).max()) < 2e-3
+    lse = g["lse"]
+    assert torch.isfinite(lse).all()
