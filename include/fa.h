@@ -111,6 +111,31 @@ FA_API int fa_backward_stage(int stage, const void* q, const void* k, const void
                              float scale, int causal, const int32_t* kv_len, void* workspace,
                              size_t workspace_bytes, fa_stream_t stream);
 
+/* Backward pass for callers that cannot allocate device memory: no workspace
+ * argument. The pages have no counterpart of this entry point; it exists for
+ * callers that are handed only their input and output buffers and may not
+ * call cudaMalloc (for example a runtime that reserves all device memory up
+ * front and gives a plugin nothing else). Instead of a caller's workspace it
+ * uses one fixed scratch array compiled into the library, of
+ * fa_backward_noalloc_max_bytes() bytes (32 MiB) on every GPU that loads the
+ * library, held until the process exits.
+ *  - Same arguments and results as fa_backward_ex without the workspace.
+ *  - A shape whose workspace (fa_backward_workspace_size) exceeds the array
+ *    returns FA_ERR_UNSUPPORTED before anything runs; fa_last_error_detail()
+ *    then says how many bytes it needed.
+ *  - Allocates nothing. The first call on each device looks up the array's
+ *    device address (cudaGetSymbolAddress) with that device current; make that
+ *    first call before any stream capture.
+ *  - All calls on a device share the one array: calls whose kernels overlap on
+ *    the GPU (other streams, other host threads) race and corrupt each other's
+ *    gradients. Serialise them. Each call re-initialises what it needs. */
+FA_API int fa_backward_noalloc(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                               const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+                               float scale, int causal, const int32_t* kv_len, fa_stream_t stream);
+
+/* Size in bytes of the scratch array fa_backward_noalloc uses. */
+FA_API size_t fa_backward_noalloc_max_bytes(void);
+
 /* Static text for an fa_status value. */
 FA_API const char* fa_status_string(int status);
 
@@ -120,7 +145,8 @@ FA_API const char* fa_status_string(int status);
 FA_API int fa_get_last_device_status(fa_stream_t stream, int* detail);
 
 /* For the calling host thread: text naming the CUDA call that made the last
- * FA_ERR_CUDA return and its error, or "" if none has. Static storage. */
+ * FA_ERR_CUDA return and its error (or the reason for a size rejection by
+ * fa_backward_noalloc), or "" if none has. Static storage. */
 FA_API const char* fa_last_error_detail(void);
 
 /* Library version as major*10000 + minor*100 + patch. */

@@ -30,6 +30,8 @@ SIGNATURES = {
         "fa_backward": (_i, [_vp] * 9 + [_i, _i, _i, _i, _f, _i, _vp, _sz, _vp]),
         "fa_backward_ex": (_i, [_vp] * 9 + [_i, _i, _i, _i, _f, _i, _vp, _vp, _sz, _vp]),
         "fa_backward_stage": (_i, [_i] + [_vp] * 9 + [_i, _i, _i, _i, _f, _i, _vp, _vp, _sz, _vp]),
+        "fa_backward_noalloc": (_i, [_vp] * 9 + [_i, _i, _i, _i, _f, _i, _vp, _vp]),
+        "fa_backward_noalloc_max_bytes": (_sz, []),
         "fa_status_string": (ctypes.c_char_p, [_i]),
         "fa_get_last_device_status": (_i, [_vp, _vp]),
         "fa_version": (_i, []),

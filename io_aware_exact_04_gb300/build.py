@@ -27,7 +27,7 @@ FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", 
          "-I" + INCLUDE, "-I" + CSRC]
 
 LIBS = {
-    "libfa.so": ["fa_api.cu", "fa_fwd.cu", "fa_bwd.cu"],
+    "libfa.so": ["fa_api.cu", "fa_fwd.cu", "fa_bwd.cu", "fa_noalloc.cu"],
     "libfa_selftest.so": ["selftest.cu"],
 }
 

@@ -79,6 +79,7 @@ int cuda_fail(const char* where, int code, const char* what) {
   std::snprintf(g_last_error, sizeof(g_last_error), "%s failed: %s (code %d)", where, what ? what : "", code);
   return FA_ERR_CUDA;
 }
+void set_error_detail(const char* text) { std::snprintf(g_last_error, sizeof(g_last_error), "%s", text); }
 int check_launch(const char* kernel) {
   const cudaError_t e = cudaGetLastError();
   if (e == cudaSuccess) return FA_OK;

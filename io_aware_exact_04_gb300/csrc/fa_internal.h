@@ -38,6 +38,8 @@ struct BwdArgs {
 // Records, for this host thread, which CUDA call failed and why (read back by
 // fa_last_error_detail). Returns FA_ERR_CUDA for convenience.
 int cuda_fail(const char* where, int code, const char* what);
+// Records a free-form reason for this host thread (read back by fa_last_error_detail).
+void set_error_detail(const char* text);
 // After a launch: FA_OK, or FA_ERR_CUDA with the launch error recorded.
 int check_launch(const char* kernel);
 
