@@ -249,49 +249,54 @@ __global__ void __launch_bounds__(448, 1)
       constexpr uint32_t IDESC_S = idesc_bf16_f32(128, BR, 0, 0);  // K (or V) x Q_i (or dO_i), K-major
       constexpr uint32_t IDESC_G = idesc_bf16_f32(128, D, 0, 1);   // TMEM A x MN-major B
       constexpr uint32_t IDESC_Q = idesc_bf16_f32(128, 64, 1, 1);  // both operands MN-major
-      auto issue_kmajor = [&](uint32_t dst, uint32_t a_base, uint32_t b_base) {
+      // Descriptors are formed once; each MMA only adds a constant to the low word.
+      constexpr uint32_t HI = sdesc_hi(1024);
+      constexpr uint32_t QT16 = C::QTILE >> 4;
+      const uint32_t k_lo = sdesc_lo(sbase + C::OFF_K, 16), v_lo = sdesc_lo(sbase + C::OFF_V, 16);
+      const uint32_t q_lo = sdesc_lo(sbase + C::OFF_Q, 16), do_lo = sdesc_lo(sbase + C::OFF_DO, 16);
+      const uint32_t qmn_lo = sdesc_lo(sbase + C::OFF_Q, C::QSUB), domn_lo = sdesc_lo(sbase + C::OFF_DO, C::QSUB);
+      const uint32_t ds_lo = sdesc_lo(sbase + C::OFF_DS, 128 * 128), kmn_lo = sdesc_lo(sbase + C::OFF_K, C::KSUB);
+      auto issue_kmajor = [&](uint32_t dst, uint32_t a_lo, uint32_t b_lo) {
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
-          const uint32_t oa = (k >> 2) * C::KSUB + (k & 3) * 32;
-          const uint32_t ob = (k >> 2) * C::QSUB + (k & 3) * 32;
-          mma_ss(tmem + dst, sdesc_sw128(a_base + oa, 16, 1024), sdesc_sw128(b_base + ob, 16, 1024), IDESC_S,
-                 k > 0);
+          const uint32_t oa = ((k >> 2) * C::KSUB + (k & 3) * 32) >> 4;
+          const uint32_t ob = ((k >> 2) * C::QSUB + (k & 3) * 32) >> 4;
+          mma_ss(tmem + dst, sdesc_join(a_lo + oa, HI), sdesc_join(b_lo + ob, HI), IDESC_S, k > 0);
         }
       };
-      auto issue_grad = [&](uint32_t dst, uint32_t a_tm, uint32_t b_base, uint32_t acc) {
+      auto issue_grad = [&](uint32_t dst, uint32_t a_tm, uint32_t b_lo, uint32_t acc) {
 #pragma unroll
         for (int k = 0; k < BR / 16; ++k)
-          mma_ts(tmem + dst, tmem + a_tm + C::pcol(16 * k), sdesc_sw128(b_base + k * 2048, C::QSUB, 1024),
-                 IDESC_G, (acc | k) != 0);
+          mma_ts(tmem + dst, tmem + a_tm + C::pcol(16 * k), sdesc_join(b_lo + k * (2048 >> 4), HI), IDESC_G,
+                 (acc | k) != 0);
       };
       auto issue_dq = [&](uint32_t dst) {
-        const uint32_t ds = sbase + C::OFF_DS, kk = sbase + C::OFF_K;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {  // 128 keys
           if (D == 64)  // dQ = dS K: A = dS (M = queries), B = K (N = head dims)
-            mma_ss(tmem + dst, sdesc_sw128(ds + k * 2048, 128 * 128, 1024),
-                   sdesc_sw128(kk + k * 2048, C::KSUB, 1024), IDESC_Q, k > 0);
+            mma_ss(tmem + dst, sdesc_join(ds_lo + k * (2048 >> 4), HI), sdesc_join(kmn_lo + k * (2048 >> 4), HI),
+                   IDESC_Q, k > 0);
           else  // dQ^T = K^T dS^T: A = K^T (M = head dims), B = dS^T (N = queries)
-            mma_ss(tmem + dst, sdesc_sw128(kk + k * 2048, C::KSUB, 1024),
-                   sdesc_sw128(ds + k * 2048, 128 * 128, 1024), IDESC_Q, k > 0);
+            mma_ss(tmem + dst, sdesc_join(kmn_lo + k * (2048 >> 4), HI), sdesc_join(ds_lo + k * (2048 >> 4), HI),
+                   IDESC_Q, k > 0);
         }
       };
       bool ok = wait_bounded(kv_full, 0, st, SITE_B_KV_FULL);
       for (int it = 0; ok && it < n_it; ++it) {
         const int s = it & 1;
-        const uint32_t qa = sbase + C::OFF_Q + s * C::QTILE, da = sbase + C::OFF_DO + s * C::QTILE;
+        const uint32_t so = s * QT16;
         if (!(ok = wait_bounded(qdo_full(s), (it >> 1) & 1, st, SITE_B_QDO_FULL))) break;
         tc_fence_after();
-        issue_kmajor(C::TM_ST, sbase + C::OFF_K, qa);
+        issue_kmajor(C::TM_ST, k_lo, q_lo + so);
         mma_commit(s_full);
-        issue_kmajor(C::TM_DPT, sbase + C::OFF_V, da);
+        issue_kmajor(C::TM_DPT, v_lo, do_lo + so);
         mma_commit(dp_full);
         if (!(ok = wait_bounded(p_ready, it & 1, st, SITE_B_P_READY))) break;
         tc_fence_after();
-        issue_grad(C::TM_DV, C::TM_ST, da, it > 0);
+        issue_grad(C::TM_DV, C::TM_ST, domn_lo + so, it > 0);
         if (!(ok = wait_bounded(ds_ready, it & 1, st, SITE_B_DS_READY))) break;
         tc_fence_after();
-        issue_grad(C::TM_DK, C::TM_DPT, qa, it > 0);
+        issue_grad(C::TM_DK, C::TM_DPT, qmn_lo + so, it > 0);
         const int qb = it & 1;
         if (!(ok = wait_bounded(dq_empty(qb), ((it >> 1) & 1) ^ 1, st, SITE_B_DQ_EMPTY))) break;
         tc_fence_after();
@@ -389,17 +394,27 @@ __global__ void __launch_bounds__(448, 1)
         const int cb = c0 + ch * 32;  // query column base within the tile
         uint32_t sv[32];
         tmem_ld32(tmem + lane_off + C::TM_ST + cb, sv);
+        float lz[32];  // LSE of the 32 queries, broadcast loads
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float4 t4 = reinterpret_cast<const float4*>(lse_s + cb)[e];
+          lz[4 * e] = t4.x, lz[4 * e + 1] = t4.y, lz[4 * e + 2] = t4.z, lz[4 * e + 3] = t4.w;
+        }
         tmem_wait_ld();
         uint32_t pk[16];
+        const uint64_t sl2x2 = f2_pack(sl2, sl2);
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
+          float x[2];
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[2 * e]), __uint_as_float(sv[2 * e + 1])), sl2x2,
+                           f2_pack(-lz[2 * e], -lz[2 * e + 1])),
+                    x[0], x[1]);
           float p[2];
 #pragma unroll
           for (int u = 0; u < 2; ++u) {
             const int qc = cb + 2 * e + u;
-            float x = ex2_approx(fmaf(__uint_as_float(sv[2 * e + u]), sl2, -lse_s[qc]));
-            if (need_mask && (key >= kv || (a.causal && key > q0 + qc))) x = 0.f;
-            p[u] = x;
+            p[u] = ex2_approx(x[u]);
+            if (need_mask && (key >= kv || (a.causal && key > q0 + qc))) p[u] = 0.f;
           }
           pk[e] = pack_bf16x2(p[0], p[1]);
         }
@@ -418,13 +433,22 @@ __global__ void __launch_bounds__(448, 1)
         uint32_t dp[32], pp[16];
         tmem_ld32(tmem + lane_off + C::TM_DPT + cb, dp);
         tmem_ld16(tmem + lane_off + C::TM_ST + C::pcol(cb), pp);
+        float dz[32];  // D of the 32 queries, broadcast loads
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float4 t4 = reinterpret_cast<const float4*>(dv_s + cb)[e];
+          dz[4 * e] = t4.x, dz[4 * e + 1] = t4.y, dz[4 * e + 2] = t4.z, dz[4 * e + 3] = t4.w;
+        }
         tmem_wait_ld();
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
           const float p0 = __uint_as_float(pp[e] << 16), p1 = __uint_as_float(pp[e] & 0xFFFF0000u);
-          const float d0 = p0 * (__uint_as_float(dp[2 * e]) - dv_s[cb + 2 * e]);
-          const float d1 = p1 * (__uint_as_float(dp[2 * e + 1]) - dv_s[cb + 2 * e + 1]);
+          // dS = P (dP - D), two columns per paired instruction
+          const uint64_t t2 = f2_add(f2_pack(__uint_as_float(dp[2 * e]), __uint_as_float(dp[2 * e + 1])),
+                                     f2_pack(-dz[2 * e], -dz[2 * e + 1]));
+          float d0, d1;
+          f2_unpack(f2_mul(t2, f2_pack(p0, p1)), d0, d1);
           pk[e] = pack_bf16x2(d0, d1);
         }
         tmem_st16(tmem + lane_off + C::TM_DPT + C::pcol(cb), pk);

@@ -40,16 +40,20 @@ struct FwdCfg {
   static constexpr int OFF_V = OFF_K + NST * TILE_BYTES;
   static constexpr int OFF_BAR = OFF_V + NST * TILE_BYTES;
   static constexpr int SMEM_BYTES = OFF_BAR + 256 + 1024;  // barriers + alignment slack
-  // TMEM columns: S_t at 128 t (P_t over its first 64 columns), O_t at 256 + d t
+  // TMEM columns. d = 64: S_t at 128 t, P_t (bf16 pairs) at 256 + 64 t, O_t at 384 + 64 t,
+  // so S_t is free again as soon as its values are in registers. d = 128: S_t at
+  // 128 t with P_t written over its first 64 columns, O_t at 256 + 128 t.
+  static constexpr bool SEP_P = (D == 64);
   __device__ static constexpr uint32_t tm_s(int t) { return 128u * t; }
-  __device__ static constexpr uint32_t tm_o(int t) { return 256u + (uint32_t)D * t; }
+  __device__ static constexpr uint32_t tm_p(int t) { return SEP_P ? 256u + 64u * t : 128u * t; }
+  __device__ static constexpr uint32_t tm_o(int t) { return SEP_P ? 384u + 64u * t : 256u + (uint32_t)D * t; }
   static constexpr uint32_t TM_COLS = 512;
   static constexpr int THREADS = 320;
 };
 
 // Wait-site identifiers recorded with FA_ERR_TIMEOUT.
 enum { SITE_F_KV_EMPTY = 1, SITE_F_Q_FULL, SITE_F_K_FULL, SITE_F_V_FULL, SITE_F_P_READY, SITE_F_S_FULL,
-       SITE_F_O_DONE, SITE_F_DRAIN };
+       SITE_F_O_DONE, SITE_F_DRAIN, SITE_F_S_FREE };
 
 template <int D>
 __global__ void __launch_bounds__(320, 1)
@@ -73,8 +77,9 @@ __global__ void __launch_bounds__(320, 1)
   auto s_full = [&](int t) { return BAR(nb + t); };
   auto p_ready = [&](int t) { return BAR(nb + 2 + t); };
   auto o_done = [&](int t) { return BAR(nb + 4 + t); };
-  const uint32_t drain = BAR(nb + 6);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C::OFF_BAR + 8 * (nb + 7));
+  auto s_free = [&](int t) { return BAR(nb + 6 + t); };
+  const uint32_t drain = BAR(nb + 8);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C::OFF_BAR + 8 * (nb + 9));
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
   DevStatus st{a.status, abort_flag};
 
@@ -105,6 +110,7 @@ __global__ void __launch_bounds__(320, 1)
       mbar_init(s_full(t), 1);
       mbar_init(p_ready(t), 4);
       mbar_init(o_done(t), 1);
+      mbar_init(s_free(t), 4);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -162,23 +168,25 @@ __global__ void __launch_bounds__(320, 1)
     if (lane == 0 && nmax > 0) {
       constexpr uint32_t IDESC_S = idesc_bf16_f32(128, 128, 0, 0);  // Q, K both K-major
       constexpr uint32_t IDESC_O = idesc_bf16_f32(128, D, 0, 1);    // P from TMEM, V MN-major
-      auto issue_s = [&](int t, int kst) {
-        const uint32_t qa = sbase + C::OFF_Q + t * C::TILE_BYTES;
-        const uint32_t ka = sbase + C::OFF_K + kst * C::TILE_BYTES;
+      // Descriptors are formed once; each MMA only adds a constant to the low word.
+      constexpr uint32_t HI = sdesc_hi(1024);
+      const uint32_t q_lo = sdesc_lo(sbase + C::OFF_Q, 16);
+      const uint32_t k_lo = sdesc_lo(sbase + C::OFF_K, 16);
+      const uint32_t v_lo = sdesc_lo(sbase + C::OFF_V, C::SUB_BYTES);
+      constexpr uint32_t TILE16 = C::TILE_BYTES >> 4;
+      auto issue_s = [&](int t, int kst) {  // S_t = Q_t K^T (K from stage kst)
+        const uint32_t qa = q_lo + t * TILE16, ka = k_lo + kst * TILE16, d = tmem + C::tm_s(t);
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
-          const uint32_t off = (k >> 2) * C::SUB_BYTES + (k & 3) * 32;
-          mma_ss(tmem + C::tm_s(t), sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024), IDESC_S,
-                 k > 0);
+          const uint32_t off = ((k >> 2) * C::SUB_BYTES + (k & 3) * 32) >> 4;
+          mma_ss(d, sdesc_join(qa + off, HI), sdesc_join(ka + off, HI), IDESC_S, k > 0);
         }
       };
-      auto issue_pv = [&](int t, int vst, uint32_t acc) {
-        const uint32_t va = sbase + C::OFF_V + vst * C::TILE_BYTES;
+      auto issue_pv = [&](int t, int vst, uint32_t acc) {  // O_t += P_t V (V from stage vst)
+        const uint32_t va = v_lo + vst * TILE16, d = tmem + C::tm_o(t), pa = tmem + C::tm_p(t);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {  // 128 keys, 16 per MMA
-          mma_ts(tmem + C::tm_o(t), tmem + C::tm_s(t) + k * 8, sdesc_sw128(va + k * 2048, C::SUB_BYTES, 1024),
-                 IDESC_O, (acc | k) != 0);
-        }
+        for (int k = 0; k < 8; ++k)  // 128 keys, 16 per MMA
+          mma_ts(d, pa + k * 8, sdesc_join(va + k * (2048 >> 4), HI), IDESC_O, (acc | k) != 0);
       };
       bool ok = wait_bounded(q_full, 0, st, SITE_F_Q_FULL) && wait_bounded(k_full(0), 0, st, SITE_F_K_FULL);
       if (ok) {
@@ -189,30 +197,54 @@ __global__ void __launch_bounds__(320, 1)
             mma_commit(s_full(t));
           }
       }
+      int s = 0, ph = 0;  // ring stage and phase of tile j
       for (int j = 0; ok && j < nmax; ++j) {
-        const int s = j % C::NST;
-        ok = wait_bounded(v_full(s), (j / C::NST) & 1, st, SITE_F_V_FULL);
-        if (!ok) break;
+        const int s2 = (s + 1 == C::NST) ? 0 : s + 1;
+        const int ph2 = (s + 1 == C::NST) ? ph ^ 1 : ph;
         bool next_k_ready = false;
-        for (int t = 0; t < 2 && ok; ++t) {
-          if (j >= n_t[t]) continue;
-          ok = wait_bounded(p_ready(t), j & 1, st, SITE_F_P_READY);
-          if (!ok) break;
-          tc_fence_after();
-          issue_pv(t, s, j > 0);
-          mma_commit(o_done(t));
-          if (j + 1 < n_t[t]) {
-            const int s2 = (j + 1) % C::NST;
+        if (C::SEP_P) {
+          // S_t(j+1) as soon as warpgroup t has S_t(j) in registers, then PV_t(j) once P_t(j) is written
+          for (int t = 0; t < 2 && ok; ++t) {
+            if (j + 1 >= n_t[t]) continue;
             if (!next_k_ready) {
-              ok = wait_bounded(k_full(s2), ((j + 1) / C::NST) & 1, st, SITE_F_K_FULL);
-              if (!ok) break;
+              if (!(ok = wait_bounded(k_full(s2), ph2, st, SITE_F_K_FULL))) break;
               next_k_ready = true;
             }
+            if (!(ok = wait_bounded(s_free(t), j & 1, st, SITE_F_S_FREE))) break;
+            tc_fence_after();
             issue_s(t, s2);
             mma_commit(s_full(t));
           }
+          if (ok) ok = wait_bounded(v_full(s), ph, st, SITE_F_V_FULL);
+          for (int t = 0; t < 2 && ok; ++t) {
+            if (j >= n_t[t]) continue;
+            if (!(ok = wait_bounded(p_ready(t), j & 1, st, SITE_F_P_READY))) break;
+            tc_fence_after();
+            issue_pv(t, s, j > 0);
+            mma_commit(o_done(t));
+          }
+        } else {
+          // P_t(j) lives over S_t(j): S_t(j+1) may only follow PV_t(j)
+          ok = wait_bounded(v_full(s), ph, st, SITE_F_V_FULL);
+          for (int t = 0; t < 2 && ok; ++t) {
+            if (j >= n_t[t]) continue;
+            if (!(ok = wait_bounded(p_ready(t), j & 1, st, SITE_F_P_READY))) break;
+            tc_fence_after();
+            issue_pv(t, s, j > 0);
+            mma_commit(o_done(t));
+            if (j + 1 < n_t[t]) {
+              if (!next_k_ready) {
+                if (!(ok = wait_bounded(k_full(s2), ph2, st, SITE_F_K_FULL))) break;
+                next_k_ready = true;
+              }
+              issue_s(t, s2);
+              mma_commit(s_full(t));
+            }
+          }
         }
         mma_commit(kv_empty(s));
+        s = s2;
+        ph = ph2;
       }
       // every MMA issued by this thread has completed before TMEM is released
       mma_commit(drain);
@@ -230,6 +262,7 @@ __global__ void __launch_bounds__(320, 1)
     const int n = n_t[t];
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
     const uint32_t tS = tmem + lane_off + C::tm_s(t);
+    const uint32_t tP = tmem + lane_off + C::tm_p(t);
     const uint32_t tO = tmem + lane_off + C::tm_o(t);
     const float sl2 = a.scale_log2;
     float* lse_row = a.lse + (size_t)bh * a.N;
@@ -259,6 +292,11 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
             for (int i = 0; i < 32; ++i) sv[c * 32 + i] = __uint_as_float(r[c][i]);
         }
+        if (C::SEP_P) {  // S_t is in registers: the MMA may overwrite it with S_t(j+1)
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(s_free(t));
+        }
         const int k0 = j * 128;
         const bool need_mask = (k0 + 127 >= kv) || (a.causal && k0 + 127 > qs);
         if (need_mask) {
@@ -267,9 +305,15 @@ __global__ void __launch_bounds__(320, 1)
           for (int c = 0; c < 128; ++c)
             if (k0 + c >= lim) sv[c] = -INFINITY;
         }
-        float mx = sv[0];
+        // row maximum: four independent partial maxima (three-input max), then a short tree
+        float pm[4];
 #pragma unroll
-        for (int c = 1; c < 128; ++c) mx = fmaxf(mx, sv[c]);
+        for (int u = 0; u < 4; ++u) pm[u] = sv[u];
+#pragma unroll
+        for (int c = 4; c < 124; c += 8)
+#pragma unroll
+          for (int u = 0; u < 4; ++u) pm[u] = fmax3(pm[u], sv[c + 2 * u], sv[c + 2 * u + 1]);
+        const float mx = fmax3(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3]), fmax3(sv[124], sv[125], fmaxf(sv[126], sv[127])));
         const float m_tile = mx * sl2;
         // lazy rescale: move the reference maximum only when it grows by > 2^8
         float f = 1.f;
@@ -284,26 +328,39 @@ __global__ void __launch_bounds__(320, 1)
             m_run = m_tile;
           }
         }
+        if (C::SEP_P && j > 0) {
+          // PV_t(j-1) has finished reading P_t(j-1) (and updating O_t) before both are touched
+          if (!(ok = wait_warp(o_done(t), (j - 1) & 1, st, SITE_F_O_DONE))) break;
+          tc_fence_after();
+        }
         const float base = (m_run == -INFINITY) ? 0.f : m_run;
-        float lsum = 0.f;
+        // P = exp2(S s log2e - base): the argument of two columns per fma.f32x2,
+        // the row sum in two paired partial sums
+        const uint64_t sl2x2 = f2_pack(sl2, sl2), nbase2 = f2_pack(-base, -base);
+        uint64_t ps2[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
 #pragma unroll
         for (int h = 0; h < 4; ++h) {  // 32 columns -> 16 packed bf16x2 words per store
           uint32_t pk[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            const float p0 = ex2_approx(fmaf(sv[h * 32 + 2 * i], sl2, -base));
-            const float p1 = ex2_approx(fmaf(sv[h * 32 + 2 * i + 1], sl2, -base));
-            lsum += p0 + p1;
+            float x0, x1;
+            f2_unpack(f2_fma(f2_pack(sv[h * 32 + 2 * i], sv[h * 32 + 2 * i + 1]), sl2x2, nbase2), x0, x1);
+            const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+            ps2[i & 1] = f2_add(ps2[i & 1], f2_pack(p0, p1));
             pk[i] = pack_bf16x2(p0, p1);
           }
-          tmem_st16(tS + h * 16, pk);
+          tmem_st16(tP + h * 16, pk);
         }
+        float ps[4];
+        f2_unpack(ps2[0], ps[0], ps[1]);
+        f2_unpack(ps2[1], ps[2], ps[3]);
+        const float lsum = (ps[0] + ps[1]) + (ps[2] + ps[3]);
         l_run = l_run * f + lsum;
         if (rescale_warp) {
-          // PV_{j-1} must have landed in O before it is rescaled
-          ok = wait_warp(o_done(t), (j - 1) & 1, st, SITE_F_O_DONE);
-          if (!ok) break;
-          tc_fence_after();
+          if (!C::SEP_P) {  // PV_{j-1} must have landed in O before it is rescaled
+            if (!(ok = wait_warp(o_done(t), (j - 1) & 1, st, SITE_F_O_DONE))) break;
+            tc_fence_after();
+          }
           uint32_t r[32];
 #pragma unroll
           for (int c = 0; c < D / 32; ++c) {
