@@ -116,6 +116,28 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(inside), "samples_total": len(rows)}
 
 
+# ------------------------------------------------------------------ multi-rank aggregation
+def job_throughput(ms_local: float, units_local: float, device=None):
+    """Whole-job rate over all ranks: every rank processes its own copy of the
+    workload (heads are independent, no collective on the data path), so the
+    job takes the slowest rank's time and does world_size times the units.
+    Returns (ms_max, total_units_per_s). Single process: the local values."""
+    import torch
+    ws = 1
+    if torch.distributed.is_available() and torch.distributed.is_initialized():
+        ws = torch.distributed.get_world_size()
+    ms = float(ms_local)
+    units = float(units_local)
+    if ws > 1:
+        t = torch.tensor([ms, units], dtype=torch.float64, device=device)
+        tmax = t.clone()
+        torch.distributed.all_reduce(tmax, op=torch.distributed.ReduceOp.MAX)
+        tsum = t.clone()
+        torch.distributed.all_reduce(tsum, op=torch.distributed.ReduceOp.SUM)
+        ms, units = float(tmax[0]), float(tsum[1])
+    return ms, units / (ms * 1e-3)
+
+
 # ------------------------------------------------------------------ oracle on host cores
 def oracle_sample(w, x, budget_s: float, max_heads=None):
     """Time the fp64 oracle on as many heads of the workload as fit in budget_s."""
@@ -298,15 +320,10 @@ def run_gpu(args, w):
         total_ms += t[3]
     if lib.fa_get_last_device_status(sp, detail) != 0:
         raise RuntimeError(f"device status after timing: {list(detail)}")
-    ms_step = total_ms / args.steps
-    if ws > 1:
-        tt = torch.tensor([ms_step], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        ms_step = float(tt.item())
-
     fl = workloads.flop_counts(w, x["kv_len"])
-    value = ws * fl["fwd_bwd_nominal"] / (ms_step * 1e-3) / 1e12
-    executed = ws * fl["fwd_bwd_executed"] / (ms_step * 1e-3) / 1e12
+    ms_step, nominal_rate = job_throughput(total_ms / args.steps, fl["fwd_bwd_nominal"], device=dev)
+    value = nominal_rate / 1e12
+    executed = value * fl["fwd_bwd_executed"] / fl["fwd_bwd_nominal"]
 
     # dominant kernel and its roofline (tensor-bound: algorithmic flops per launch / event time)
     avg = {kname: t / args.steps for kname, t in per_kernel.items()}
@@ -357,7 +374,8 @@ def run_gpu(args, w):
         if i >= 2:
             e2e_ms += e0.elapsed_time(e1)
     e2e_ms /= e2e_steps
-    e2e_val = ws * fl["fwd_bwd_nominal"] / (e2e_ms * 1e-3) / 1e12
+    e2e_ms, e2e_rate = job_throughput(e2e_ms, fl["fwd_bwd_nominal"], device=dev)
+    e2e_val = e2e_rate / 1e12
 
     clocks = sampler.stop() if rank == 0 else None
     if ws > 1:
