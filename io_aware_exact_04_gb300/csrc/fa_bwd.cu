@@ -535,11 +535,11 @@ struct Bwd64 {
   // 128 + 64 w (dS^T packed likewise), dV 256, dK 320, dQ buffer c at 384 + 64 c.
   static constexpr uint32_t TM_ST = 0, TM_DPT = 128, TM_DV = 256, TM_DK = 320, TM_DQ = 384;
   static constexpr uint32_t TM_COLS = 512;
-  static constexpr int THREADS = 448;
+  static constexpr int THREADS = 480;
 };
 
 template <int DUMMY>
-__global__ void __launch_bounds__(448, 1)
+__global__ void __launch_bounds__(480, 1)
     bwd_kernel_d64(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                    const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
@@ -564,9 +564,12 @@ __global__ void __launch_bounds__(448, 1)
   auto ds_ready = [&](int w) { return BAR(nb + 6 + w); };
   auto dq_full = [&](int c) { return BAR(nb + 8 + c); };
   auto dq_empty = [&](int c) { return BAR(nb + 10 + c); };
-  const uint32_t final_bar = BAR(nb + 12);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C::OFF_BAR + 8 * (nb + 13));
+  auto dq_done = [&](int c) { return BAR(nb + 12 + c); };
+  const uint32_t final_bar = BAR(nb + 14);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C::OFF_BAR + 8 * (nb + 15));
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+  // number of dS^T steps warpgroup 0 has finished, times 4 (one add per warp)
+  const uint32_t ds0_count = smem_u32(tmem_slot + 2);
   DevStatus st{a.status, abort_flag};
 
   const int j = blockIdx.x;  // key tile
@@ -603,9 +606,11 @@ __global__ void __launch_bounds__(448, 1)
       mbar_init(ds_ready(w), 4);
       mbar_init(dq_full(w), 1);
       mbar_init(dq_empty(w), 4);
+      mbar_init(dq_done(w), 1);
     }
-    mbar_init(final_bar, 1);
+    mbar_init(final_bar, 2);  // one commit per MMA-issuing thread
     *abort_flag = 0;
+    tmem_slot[2] = 0;
     fence_mbar_init();
   }
   if (warp == 13) {
@@ -616,6 +621,20 @@ __global__ void __launch_bounds__(448, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  if (warp < 8) {
+    // dV (warpgroup 0) and dK (warpgroup 1) start at zero: the two MMA-issuing
+    // threads then always accumulate, whichever of them reaches a tile first
+    uint32_t z[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) z[i] = 0;
+    const uint32_t base = tmem + ((uint32_t)((warp & 3) * 32) << 16) + (warp < 4 ? C::TM_DV : C::TM_DK);
+    tmem_st32(base, z);
+    tmem_st32(base + 32, z);
+    tmem_wait_st();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
   const float* lse2_h = a.lse2 + (size_t)bh * a.Npad;
   const float* dvec_h = a.dvec + (size_t)bh * a.Npad;
 
@@ -648,9 +667,11 @@ __global__ void __launch_bounds__(448, 1)
           }
       }
     }
-  } else if (warp == 13) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == 13 || warp == 14) {
+    // ------------------------------------------------------------ MMA issuers: warp 13 serves
+    // warpgroup 0 (even steps), warp 14 warpgroup 1 (odd steps) and forms dQ
     if (lane == 0) {
+      const int w = warp - 13;
       constexpr uint32_t IDESC_S = idesc_bf16_f32(128, BR, 0, 0);  // K (V) x Q_i (dO_i), K-major
       constexpr uint32_t IDESC_G = idesc_bf16_f32(128, 64, 0, 1);  // TMEM A x MN-major B
       constexpr uint32_t IDESC_Q = idesc_bf16_f32(128, 64, 1, 1);  // dS x K, both MN-major
@@ -682,24 +703,22 @@ __global__ void __launch_bounds__(448, 1)
         for (int k = 0; k < 4; ++k)
           mma_ts(tmem + dst, tmem + a_tm + 8 * k, sdesc_join(b_lo + k * (2048 >> 4), HI), IDESC_G, (acc | k) != 0);
       };
-      // Steps 0 and 1 start both buffers. Afterwards S^T(i+2) follows dV(i) as soon as
-      // warpgroup i%2 has P^T(i) (it keeps P in registers for dS, so S^T's columns
-      // are free), and dP^T(i+2) follows dK(i) once dS^T(i) is written.
-      bool ok = wait_bounded(kv_full, 0, st, SITE_B_KV_FULL);
-      for (int it = 0; ok && it < 2 && it < n_it; ++it) {
-        if (!(ok = wait_bounded(qdo_full(it), 0, st, SITE_B_QDO_FULL))) break;
+      // This thread's first step starts its buffers. Afterwards S^T(i+2) follows dV(i) as
+      // soon as the warpgroup has P^T(i) (it keeps P in registers for dS, so S^T's
+      // columns are free), and dP^T(i+2) follows dK(i) once dS^T(i) is written.
+      bool ok = wait_bounded(kv_full, 0, st, SITE_B_KV_FULL) && wait_bounded(qdo_full(w), 0, st, SITE_B_QDO_FULL);
+      if (ok) {
         tc_fence_after();
-        issue_s(it);
-        issue_dp(it);
+        issue_s(w);
+        issue_dp(w);
       }
-      for (int it = 0; ok && it < n_it; ++it) {
-        const int w = it & 1;
+      for (int it = w; ok && it < n_it; it += 2) {
         const uint32_t par = (it >> 1) & 1;
         const uint32_t so = (it % NQS) * QT16;
         const bool more = it + 2 < n_it;
         if (!(ok = wait_bounded(p_ready(w), par, st, SITE_B_P_READY))) break;
         tc_fence_after();
-        issue_grad(C::TM_DV, C::TM_ST + 64 * w, domn_lo + so, it > 0);
+        issue_grad(C::TM_DV, C::TM_ST + 64 * w, domn_lo + so, 1);
         if (more) {
           if (!(ok = wait_bounded(qdo_full((it + 2) % NQS), ((it + 2) / NQS) & 1, st, SITE_B_QDO_FULL))) break;
           tc_fence_after();
@@ -707,11 +726,26 @@ __global__ void __launch_bounds__(448, 1)
         }
         if (!(ok = wait_bounded(ds_ready(w), par, st, SITE_B_DS_READY))) break;
         tc_fence_after();
-        issue_grad(C::TM_DK, C::TM_DPT + 64 * w, qmn_lo + so, it > 0);
+        issue_grad(C::TM_DK, C::TM_DPT + 64 * w, qmn_lo + so, 1);
         mma_commit(qdo_empty(it % NQS));  // last readers of Q_i and dO_i issued
         if (more) issue_dp(it + 2);
-        if (w == 1) {                     // the pair (it-1, it) is complete: dQ of its 128 queries
+        if (w == 1) {  // the pair (it-1, it) is complete once warpgroup 0's dS of step it-1 is in smem
           const int p = it >> 1, c = p & 1;
+          const uint32_t need = 4u * (uint32_t)(p + 1);
+          const uint64_t t0 = globaltimer_ns();
+          while (smem_ld_acquire(ds0_count) < need) {
+            if (*(volatile int*)abort_flag || *(volatile int*)a.status != 0) {
+              *(volatile int*)abort_flag = 1;
+              ok = false;
+              break;
+            }
+            if (globaltimer_ns() - t0 > kWaitLimitNs) {
+              record_error(st, FA_ERR_TIMEOUT, SITE_B_DS_READY);
+              ok = false;
+              break;
+            }
+          }
+          if (!ok) break;
           if (!(ok = wait_bounded(dq_empty(c), ((p >> 1) & 1) ^ 1, st, SITE_B_DQ_EMPTY))) break;
           tc_fence_after();
           const uint32_t dsb = ds_lo + c * (C::DS_BYTES >> 4);
@@ -720,6 +754,7 @@ __global__ void __launch_bounds__(448, 1)
             mma_ss(tmem + C::TM_DQ + 64 * c, sdesc_join(dsb + k * (2048 >> 4), HI),
                    sdesc_join(kmn_lo + k * (2048 >> 4), HI), IDESC_Q, k > 0);
           mma_commit(dq_full(c));
+          mma_commit(dq_done(c));
         }
       }
       mma_commit(final_bar);  // also the drain: completes after every MMA issued above
@@ -827,6 +862,10 @@ __global__ void __launch_bounds__(448, 1)
       if (!(ok = wait_warp(dp_full(w), par, st, SITE_B_DP_FULL))) break;
       tc_fence_after();
       uint8_t* dsb = sm + C::OFF_DS + ((it >> 1) & 1) * C::DS_BYTES + w * (128 * 128);
+      if (w == 0 && it >= 4) {  // dQ of the pair that last used this dS tile has read it
+        const int pp2 = (it >> 1) - 2;
+        if (!(ok = wait_warp(dq_done(pp2 & 1), (pp2 >> 1) & 1, st, SITE_B_DQ_EMPTY))) break;
+      }
 #pragma unroll
       for (int ch = 0; ch < 2; ++ch) {
         uint32_t dp[32];
@@ -859,7 +898,10 @@ __global__ void __launch_bounds__(448, 1)
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(ds_ready(w));
+      if (lane == 0) {
+        mbar_arrive(ds_ready(w));
+        if (w == 0) smem_add_release(ds0_count, 1);
+      }
     }
     // ---- epilogue: warpgroup 0 writes dV, warpgroup 1 writes s * dK
     if (ok) ok = wait_warp(final_bar, 0, st, SITE_B_FINAL);

@@ -75,6 +75,17 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parit
   return ok != 0;
 }
 
+// Release-add / acquire-load on a shared-memory counter (a monotonic progress
+// count that one thread can wait on without the phase aliasing of a barrier).
+__device__ __forceinline__ void smem_add_release(uint32_t addr, uint32_t v) {
+  asm volatile("red.release.cta.shared::cta.add.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t smem_ld_acquire(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+
 // ---------------------------------------------------------------- proxies / fences
 // Generic-proxy writes to shared memory become visible to the async proxy
 // (TMA stores, tcgen05.mma operand reads).
