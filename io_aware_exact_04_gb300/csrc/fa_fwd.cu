@@ -48,7 +48,10 @@ struct FwdCfg {
   __device__ static constexpr uint32_t tm_p(int t) { return SEP_P ? 256u + 64u * t : 128u * t; }
   __device__ static constexpr uint32_t tm_o(int t) { return SEP_P ? 384u + 64u * t : 256u + (uint32_t)D * t; }
   static constexpr uint32_t TM_COLS = 512;
-  static constexpr int THREADS = 320;
+  static constexpr int THREADS = 352;
+  // MMA-issuing threads: d = 64 one per query tile (warps 9, 10); d = 128 one
+  // (warp 9) for both tiles, P_t over S_t forcing S_t(j+1) behind PV_t(j) anyway.
+  static constexpr int NMMA = SEP_P ? 2 : 1;
 };
 
 // Wait-site identifiers recorded with FA_ERR_TIMEOUT.
@@ -56,7 +59,7 @@ enum { SITE_F_KV_EMPTY = 1, SITE_F_Q_FULL, SITE_F_K_FULL, SITE_F_V_FULL, SITE_F_
        SITE_F_O_DONE, SITE_F_DRAIN, SITE_F_S_FREE };
 
 template <int D>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(352, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o, FwdArgs a) {
   using C = FwdCfg<D>;
@@ -104,7 +107,7 @@ __global__ void __launch_bounds__(320, 1)
     for (int s = 0; s < C::NST; ++s) {
       mbar_init(k_full(s), 1);
       mbar_init(v_full(s), 1);
-      mbar_init(kv_empty(s), 1);
+      mbar_init(kv_empty(s), C::NMMA);  // one arrival per MMA-issuing thread
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(s_full(t), 1);
@@ -112,7 +115,7 @@ __global__ void __launch_bounds__(320, 1)
       mbar_init(o_done(t), 1);
       mbar_init(s_free(t), 4);
     }
-    mbar_init(drain, 1);
+    mbar_init(drain, C::NMMA);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -163,9 +166,11 @@ __global__ void __launch_bounds__(320, 1)
         }
       }
     }
-  } else if (warp == 9) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0 && nmax > 0) {
+  } else if (warp == 9 || warp == 10) {
+    // ------------------------------------------------------------ MMA issuers: for d = 64 warp 9
+    // serves query tile 0 and warp 10 query tile 1, each in its own order; for d = 128
+    // warp 9 serves both, alternating
+    if (lane == 0 && nmax > 0 && warp - 9 < C::NMMA) {
       constexpr uint32_t IDESC_S = idesc_bf16_f32(128, 128, 0, 0);  // Q, K both K-major
       constexpr uint32_t IDESC_O = idesc_bf16_f32(128, D, 0, 1);    // P from TMEM, V MN-major
       // Descriptors are formed once; each MMA only adds a constant to the low word.
@@ -189,9 +194,10 @@ __global__ void __launch_bounds__(320, 1)
           mma_ts(d, pa + k * 8, sdesc_join(va + k * (2048 >> 4), HI), IDESC_O, (acc | k) != 0);
       };
       bool ok = wait_bounded(q_full, 0, st, SITE_F_Q_FULL) && wait_bounded(k_full(0), 0, st, SITE_F_K_FULL);
+      const int t_lo = C::SEP_P ? warp - 9 : 0, t_hi = C::SEP_P ? warp - 9 : 1;  // query tiles served
       if (ok) {
         tc_fence_after();
-        for (int t = 0; t < 2; ++t)
+        for (int t = t_lo; t <= t_hi; ++t)
           if (n_t[t] > 0) {
             issue_s(t, 0);
             mma_commit(s_full(t));
@@ -201,52 +207,43 @@ __global__ void __launch_bounds__(320, 1)
       for (int j = 0; ok && j < nmax; ++j) {
         const int s2 = (s + 1 == C::NST) ? 0 : s + 1;
         const int ph2 = (s + 1 == C::NST) ? ph ^ 1 : ph;
-        bool next_k_ready = false;
-        if (C::SEP_P) {
-          // S_t(j+1) as soon as warpgroup t has S_t(j) in registers, then PV_t(j) once P_t(j) is written
-          for (int t = 0; t < 2 && ok; ++t) {
-            if (j + 1 >= n_t[t]) continue;
-            if (!next_k_ready) {
-              if (!(ok = wait_bounded(k_full(s2), ph2, st, SITE_F_K_FULL))) break;
-              next_k_ready = true;
-            }
+        bool used = false;
+        for (int t = t_lo; t <= t_hi && ok; ++t) {
+          const int n = n_t[t];
+          if (j >= n) continue;
+          used = true;
+          if (C::SEP_P && j + 1 < n) {
+            // S_t(j+1) as soon as the warpgroup has S_t(j) in registers
+            if (!(ok = wait_bounded(k_full(s2), ph2, st, SITE_F_K_FULL))) break;
             if (!(ok = wait_bounded(s_free(t), j & 1, st, SITE_F_S_FREE))) break;
             tc_fence_after();
             issue_s(t, s2);
             mma_commit(s_full(t));
           }
-          if (ok) ok = wait_bounded(v_full(s), ph, st, SITE_F_V_FULL);
-          for (int t = 0; t < 2 && ok; ++t) {
-            if (j >= n_t[t]) continue;
-            if (!(ok = wait_bounded(p_ready(t), j & 1, st, SITE_F_P_READY))) break;
-            tc_fence_after();
-            issue_pv(t, s, j > 0);
-            mma_commit(o_done(t));
-          }
-        } else {
-          // P_t(j) lives over S_t(j): S_t(j+1) may only follow PV_t(j)
-          ok = wait_bounded(v_full(s), ph, st, SITE_F_V_FULL);
-          for (int t = 0; t < 2 && ok; ++t) {
-            if (j >= n_t[t]) continue;
-            if (!(ok = wait_bounded(p_ready(t), j & 1, st, SITE_F_P_READY))) break;
-            tc_fence_after();
-            issue_pv(t, s, j > 0);
-            mma_commit(o_done(t));
-            if (j + 1 < n_t[t]) {
-              if (!next_k_ready) {
-                if (!(ok = wait_bounded(k_full(s2), ph2, st, SITE_F_K_FULL))) break;
-                next_k_ready = true;
-              }
-              issue_s(t, s2);
-              mma_commit(s_full(t));
-            }
+          if (!(ok = wait_bounded(v_full(s), ph, st, SITE_F_V_FULL))) break;
+          if (!(ok = wait_bounded(p_ready(t), j & 1, st, SITE_F_P_READY))) break;
+          tc_fence_after();
+          issue_pv(t, s, j > 0);
+          mma_commit(o_done(t));
+          if (!C::SEP_P && j + 1 < n) {  // P_t(j) lives over S_t(j): S_t(j+1) follows PV_t(j)
+            if (!(ok = wait_bounded(k_full(s2), ph2, st, SITE_F_K_FULL))) break;
+            issue_s(t, s2);
+            mma_commit(s_full(t));
           }
         }
-        mma_commit(kv_empty(s));
+        if (!ok) break;
+        if (used) {
+          mma_commit(kv_empty(s));  // this thread's readers of K_j, V_j are issued
+        } else {
+          // tile j is not this thread's: once it has landed (so its stage's previous use
+          // is released), add this thread's arrival without waiting for anything else
+          if (!(ok = wait_bounded(v_full(s), ph, st, SITE_F_V_FULL))) break;
+          mbar_arrive(kv_empty(s));
+        }
         s = s2;
         ph = ph2;
       }
-      // every MMA issued by this thread has completed before TMEM is released
+      // every MMA issued by either thread has completed before TMEM is released
       mma_commit(drain);
       const uint64_t t0 = globaltimer_ns();
       while (!mbar_try_wait(drain, 0) && globaltimer_ns() - t0 < kWaitLimitNs) {
