@@ -54,7 +54,7 @@ typedef struct CUstream_st* fa_stream_t; /* identical to cudaStream_t */
 typedef enum {
   FA_OK = 0,
   FA_ERR_INVALID_ARG = 1,  /* null pointer, negative size, bad flag, too-small workspace */
-  FA_ERR_UNSUPPORTED = 2,  /* d not in {64, 128}, or sizes beyond 32-bit indexing */
+  FA_ERR_UNSUPPORTED = 2,  /* d not in {64, 128}, B*H > 65535, or N beyond 32-bit indexing */
   FA_ERR_MISALIGNED = 3,   /* a tensor base pointer not 16-byte aligned */
   FA_ERR_CUDA = 4,         /* a CUDA runtime/driver call failed */
   FA_ERR_TIMEOUT = 5,      /* (device status) a bounded wait inside a kernel ran out */

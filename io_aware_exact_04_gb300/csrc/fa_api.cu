@@ -48,8 +48,9 @@ int check_common(int B, int H, int N, int d, float scale, int causal) {
   if (!(scale > 0.f) || !std::isfinite(scale)) return FA_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
   const long long BH = (long long)B * H;
-  if (BH > 65535) return FA_ERR_UNSUPPORTED;  // one grid row per head
+  if (BH > 65535) return FA_ERR_UNSUPPORTED;  // documented limit on B*H
   if ((long long)N + 255 > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+  if ((N + 127) / 128 > 65535) return FA_ERR_UNSUPPORTED;  // key tiles / query pairs on the grid's y axis
   return FA_OK;
 }
 

@@ -161,8 +161,9 @@ __global__ void __launch_bounds__(448, 1)
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
   DevStatus st{a.status, abort_flag};
 
-  const int j = blockIdx.x;  // key tile
-  const int bh = blockIdx.y;
+  // blocks launch x-fastest: every head's longest causal key tile (j = 0) goes first
+  const int j = blockIdx.y;  // key tile
+  const int bh = blockIdx.x;
   const int b = bh / a.H;
   int kv = a.N;
   if (a.kv_len) kv = min(max(a.kv_len[b], 0), a.N);
@@ -572,8 +573,9 @@ __global__ void __launch_bounds__(480, 1)
   const uint32_t ds0_count = smem_u32(tmem_slot + 2);
   DevStatus st{a.status, abort_flag};
 
-  const int j = blockIdx.x;  // key tile
-  const int bh = blockIdx.y;
+  // blocks launch x-fastest: every head's longest causal key tile (j = 0) goes first
+  const int j = blockIdx.y;  // key tile
+  const int bh = blockIdx.x;
   const int b = bh / a.H;
   int kv = a.N;
   if (a.kv_len) kv = min(max(a.kv_len[b], 0), a.N);
@@ -981,7 +983,7 @@ static int launch_bwd_main_d(const void* q, const void* k, const void* v, const 
       if (e != cudaSuccess) return cuda_fail("cudaFuncSetAttribute", (int)e, cudaGetErrorName(e));
       attr_set = true;
     }
-    dim3 grid((a.N + 127) / 128, BH);
+    dim3 grid(BH, (a.N + 127) / 128);
     bwd_kernel_d64<0><<<grid, Bwd64::THREADS, Bwd64::SMEM_BYTES, stream>>>(mq64, mk, mv, mdo64, mdk, mdv, mdq, a);
     return check_launch(__func__);
   }
@@ -991,7 +993,7 @@ static int launch_bwd_main_d(const void* q, const void* k, const void* v, const 
     if (e != cudaSuccess) return cuda_fail("cudaFuncSetAttribute", (int)e, cudaGetErrorName(e));
     attr_set = true;
   }
-  dim3 grid((a.N + 127) / 128, BH);
+  dim3 grid(BH, (a.N + 127) / 128);
   bwd_kernel<D><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(mq, mk, mv, mdo, mdk, mdv, mdq, a);
   return check_launch(__func__);
 }

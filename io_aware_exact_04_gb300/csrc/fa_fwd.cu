@@ -87,8 +87,9 @@ __global__ void __launch_bounds__(352, 1)
   DevStatus st{a.status, abort_flag};
 
   // work description
-  const int pair = a.n_pairs - 1 - (int)blockIdx.x;  // longest causal rows first
-  const int bh = blockIdx.y;
+  // blocks launch x-fastest: every head's longest causal query pair goes first
+  const int pair = a.n_pairs - 1 - (int)blockIdx.y;
+  const int bh = blockIdx.x;
   const int b = bh / a.H;
   int kv = a.N;
   if (a.kv_len) kv = min(max(a.kv_len[b], 0), a.N);
@@ -439,7 +440,7 @@ static int launch_fwd_d(const void* q, const void* k, const void* v, void* o, co
     if (e != cudaSuccess) return cuda_fail("cudaFuncSetAttribute", (int)e, cudaGetErrorName(e));
     attr_set = true;
   }
-  dim3 grid(args.n_pairs, BH);
+  dim3 grid(BH, args.n_pairs);
   fwd_kernel<D><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(mq, mk, mv, mo, args);
   return check_launch(__func__);
 }
