@@ -101,7 +101,7 @@ FA_API int fa_backward_ex(const void* q, const void* k, const void* v, const voi
 /* One stage of fa_backward_ex, same arguments; running stages 0, 1, 2 in
  * order on one stream is exactly fa_backward_ex. Exposed so that each kernel
  * can be timed on its own.
- *   0: D = rowsum(dO * O) and LSE in base 2 per query row, into the workspace;
+ *   0: -D = -rowsum(dO * O) and -LSE in base 2 per query row, into the workspace;
  *      zeroes the fp32 dQ accumulator.
  *   1: the recomputing kernel: dK and dV written, dQ accumulated in fp32.
  *   2: the fp32 dQ accumulator rounded to bf16 into dq.

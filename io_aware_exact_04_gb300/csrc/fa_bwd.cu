@@ -10,20 +10,18 @@
 //   dS = P * (dP - D); dK += s dS^T Q; dQ += s dS K.
 //
 // Three kernels:
-//   bwd_pre_kernel     D per query row, LSE in base 2, zeroed fp32 dQ accumulator
-//   bwd_kernel<D>      one CTA per 128-key tile of one head, looping over
-//                      query tiles of BR rows (BR = 128 for d = 64, 64 for d = 128):
-//     warp 12     TMA producer (K, V once; Q_i, dO_i, LSE_i, D_i per step, 2 stages)
-//     warp 13     TMEM allocator + tcgen05.mma issuer. Keys are the M dimension:
-//                   S^T = K Q_i^T, dP^T = V dO_i^T          (smem x smem)
-//                   dV += P^T dO_i, dK += dS^T Q_i           (P^T, dS^T from TMEM)
-//                   d=64:  dQ_i  = dS K      (M = 128 query rows)
-//                   d=128: dQ_i^T = K^T dS^T (M = 128 head dims)
-//     warps 0-7   two warpgroups, each half of the BR query columns; thread r
-//                 owns key r (TMEM lane r): P^T and dS^T formed in registers,
-//                 written back to TMEM as bf16; dS also to smem for the dQ MMA.
-//     warps 8-11  dQ epilogue: TMEM -> scaled fp32 -> swizzled smem -> TMA
-//                 reduce-add into the fp32 accumulator (two staging buffers).
+//   bwd_pre_kernel     -D and -LSE (base 2) per query row, zeroed fp32 dQ accumulator
+//   main kernel        one CTA per 128-key tile of one head, looping over query steps
+//                      (bwd_kernel_d64 for d = 64, bwd_kernel<128> for d = 128). Keys are
+//                      the M dimension of every MMA but dQ's:
+//                        S^T = K Q_i^T, dP^T = V dO_i^T          (smem x smem)
+//                        dV += P^T dO_i, dK += dS^T Q_i           (P^T, dS^T from TMEM)
+//                        d=64:  dQ = dS K per pair of steps       (M = 128 query rows)
+//                        d=128: dQ_i^T = K^T dS^T                 (M = 128 head dims)
+//                      One TMA producer warp, MMA-issuing warp(s), two warpgroups whose
+//                      thread r owns key r (TMEM lane r) and forms P^T and dS^T in
+//                      registers, and a dQ epilogue warpgroup (TMEM -> scaled fp32 ->
+//                      swizzled smem -> TMA reduce-add into the fp32 accumulator).
 //   dq_convert_kernel  fp32 accumulator -> bf16 dQ
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -35,8 +33,10 @@
 namespace fa {
 
 // ---------------------------------------------------------------------------------------------
-// D_i = sum_k dO_ik O_ik; lse2_i = LSE_i * log2(e) (+inf where no row or LSE = -inf, so that
-// recomputed P is 0 there); dq_acc row zeroed. One group of D/8 lanes per row, 16 B each.
+// Stored negated, so that the main kernels add them with no extra instruction:
+// dvec_i = -D_i = -sum_k dO_ik O_ik; lse2_i = -LSE_i * log2(e) (-inf where no row or
+// LSE = -inf, so that recomputed P is 0 there); dq_acc row zeroed. One group of D/8 lanes
+// per row, 16 B each.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(BwdArgs a, int BH) {
   constexpr int LPR = D / 8;          // lanes per row
@@ -68,11 +68,11 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(BwdArgs a, int BH) {
   dq[0] = make_float4(0.f, 0.f, 0.f, 0.f);
   dq[1] = make_float4(0.f, 0.f, 0.f, 0.f);
   if (part == 0) {
-    a.dvec[r] = acc;
-    float l2 = INFINITY;
+    a.dvec[r] = -acc;
+    float l2 = -INFINITY;
     if (n < a.N) {
       const float l = a.lse[(size_t)bh * a.N + n];
-      if (l != -INFINITY) l2 = l * 1.4426950408889634f;
+      if (l != -INFINITY) l2 = l * -1.4426950408889634f;
     }
     a.lse2[r] = l2;
   }
@@ -389,7 +389,7 @@ __global__ void __launch_bounds__(448, 1)
       if (!(ok = wait_warp(s_full, it & 1, st, SITE_B_S_FULL))) break;
       tc_fence_after();
       const bool need_mask = (k0 + 127 >= kv) || (a.causal && k0 + 127 > q0);
-      // ---- P^T = exp2(S^T s log2e - LSE2), bf16 into the S^T columns
+      // ---- P^T = exp2(S^T s log2e + lse2), bf16 into the S^T columns (lse2 = -LSE log2e)
 #pragma unroll
       for (int ch = 0; ch < NCH; ++ch) {
         const int cb = c0 + ch * 32;  // query column base within the tile
@@ -402,22 +402,21 @@ __global__ void __launch_bounds__(448, 1)
           lz[4 * e] = t4.x, lz[4 * e + 1] = t4.y, lz[4 * e + 2] = t4.z, lz[4 * e + 3] = t4.w;
         }
         tmem_wait_ld();
+        if (need_mask) {  // only steps on the diagonal or past kv_len: masked S -> -inf, so P = 0
+          const int lim = key >= kv ? 32 : (a.causal ? key - q0 - cb : 0);  // columns [0, lim)
+#pragma unroll
+          for (int c = 0; c < 32; ++c)
+            if (c < lim) sv[c] = 0xff800000u;
+        }
         uint32_t pk[16];
         const uint64_t sl2x2 = f2_pack(sl2, sl2);
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
           float x[2];
           f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[2 * e]), __uint_as_float(sv[2 * e + 1])), sl2x2,
-                           f2_pack(-lz[2 * e], -lz[2 * e + 1])),
+                           f2_pack(lz[2 * e], lz[2 * e + 1])),
                     x[0], x[1]);
-          float p[2];
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int qc = cb + 2 * e + u;
-            p[u] = ex2_approx(x[u]);
-            if (need_mask && (key >= kv || (a.causal && key > q0 + qc))) p[u] = 0.f;
-          }
-          pk[e] = pack_bf16x2(p[0], p[1]);
+          pk[e] = pack_bf16x2(ex2_approx(x[0]), ex2_approx(x[1]));
         }
         tmem_st16(tmem + lane_off + C::TM_ST + C::pcol(cb), pk);
       }
@@ -425,7 +424,7 @@ __global__ void __launch_bounds__(448, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(p_ready);
-      // ---- dS^T = P^T * (dP^T - D), bf16 into the dP^T columns and into smem
+      // ---- dS^T = P^T * (dP^T + dvec), bf16 into the dP^T columns and into smem (dvec = -D)
       if (!(ok = wait_warp(dp_full, it & 1, st, SITE_B_DP_FULL))) break;
       tc_fence_after();
 #pragma unroll
@@ -445,9 +444,9 @@ __global__ void __launch_bounds__(448, 1)
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
           const float p0 = __uint_as_float(pp[e] << 16), p1 = __uint_as_float(pp[e] & 0xFFFF0000u);
-          // dS = P (dP - D), two columns per paired instruction
+          // dS = P (dP - D), two columns per paired instruction (dz holds -D)
           const uint64_t t2 = f2_add(f2_pack(__uint_as_float(dp[2 * e]), __uint_as_float(dp[2 * e + 1])),
-                                     f2_pack(-dz[2 * e], -dz[2 * e + 1]));
+                                     f2_pack(dz[2 * e], dz[2 * e + 1]));
           float d0, d1;
           f2_unpack(f2_mul(t2, f2_pack(p0, p1)), d0, d1);
           pk[e] = pack_bf16x2(d0, d1);
@@ -824,8 +823,9 @@ __global__ void __launch_bounds__(480, 1)
       if (!(ok = wait_warp(s_full(w), par, st, SITE_B_S_FULL))) break;
       tc_fence_after();
       const bool need_mask = (k0 + 127 >= kv) || (a.causal && k0 + 127 > q0);
-      // ---- P^T = exp2(S^T s log2e - LSE2) -> bf16 pairs in the first 32 columns of this buffer,
-      //      kept in registers too: S^T's columns are overwritten by the next step once P^T is out
+      // ---- P^T = exp2(S^T s log2e + lse2) (lse2 = -LSE log2e) -> bf16 pairs in the first 32
+      //      columns of this buffer, kept in registers too: S^T's columns are overwritten by
+      //      the next step once P^T is out
       uint32_t pkeep[2][16];
 #pragma unroll
       for (int ch = 0; ch < 2; ++ch) {
@@ -838,20 +838,20 @@ __global__ void __launch_bounds__(480, 1)
           lz[4 * e] = t4.x, lz[4 * e + 1] = t4.y, lz[4 * e + 2] = t4.z, lz[4 * e + 3] = t4.w;
         }
         tmem_wait_ld();
+        if (need_mask) {  // only steps on the diagonal or past kv_len: masked S -> -inf, so P = 0
+          const int lim = key >= kv ? 32 : (a.causal ? key - q0 - 32 * ch : 0);  // columns [0, lim)
+#pragma unroll
+          for (int c = 0; c < 32; ++c)
+            if (c < lim) sv[c] = 0xff800000u;
+        }
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
           float x[2];
           f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[2 * e]), __uint_as_float(sv[2 * e + 1])), sl2x2,
-                           f2_pack(-lz[2 * e], -lz[2 * e + 1])),
+                           f2_pack(lz[2 * e], lz[2 * e + 1])),
                     x[0], x[1]);
-          float pp[2];
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            pp[u] = ex2_approx(x[u]);
-            if (need_mask && (key >= kv || (a.causal && key > q0 + 32 * ch + 2 * e + u))) pp[u] = 0.f;
-          }
-          pk[e] = pack_bf16x2(pp[0], pp[1]);
+          pk[e] = pack_bf16x2(ex2_approx(x[0]), ex2_approx(x[1]));
           pkeep[ch][e] = pk[e];
         }
         tmem_st16(tST + 16 * ch, pk);
@@ -860,7 +860,7 @@ __global__ void __launch_bounds__(480, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(p_ready(w));
-      // ---- dS^T = P^T * (dP^T - D) -> bf16 pairs in this dP^T buffer and into the pair's dS tile
+      // ---- dS^T = P^T * (dP^T + dvec) -> bf16 pairs in this dP^T buffer and into the pair's dS tile
       if (!(ok = wait_warp(dp_full(w), par, st, SITE_B_DP_FULL))) break;
       tc_fence_after();
       uint8_t* dsb = sm + C::OFF_DS + ((it >> 1) & 1) * C::DS_BYTES + w * (128 * 128);
@@ -885,7 +885,7 @@ __global__ void __launch_bounds__(480, 1)
         for (int e = 0; e < 16; ++e) {
           const float p0 = __uint_as_float(pp[e] << 16), p1 = __uint_as_float(pp[e] & 0xFFFF0000u);
           const uint64_t t2 = f2_add(f2_pack(__uint_as_float(dp[2 * e]), __uint_as_float(dp[2 * e + 1])),
-                                     f2_pack(-dz[2 * e], -dz[2 * e + 1]));
+                                     f2_pack(dz[2 * e], dz[2 * e + 1]));
           float d0, d1;
           f2_unpack(f2_mul(t2, f2_pack(p0, p1)), d0, d1);
           pk[e] = pack_bf16x2(d0, d1);
@@ -959,42 +959,38 @@ static int launch_bwd_pre_d(const BwdArgs& a, int BH, cudaStream_t stream) {
 template <int D>
 static int launch_bwd_main_d(const void* q, const void* k, const void* v, const BwdArgs& a, int BH,
                              cudaStream_t stream) {
-  using C = BwdCfg<D>;
+  constexpr int BR = (D == 64) ? Bwd64::BR : BwdCfg<D>::BR;  // query rows per step
   const uint64_t N = (uint64_t)a.N;
   const auto BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const auto SW = CU_TENSOR_MAP_SWIZZLE_128B;
   CUtensorMap mq, mk, mv, mdo, mdk, mdv, mdq;
-  if (!make_tmap_3d(&mq, q, BF, 2, D, N, BH, 64, C::BR, SW) ||
-      !make_tmap_3d(&mdo, a.dO, BF, 2, D, N, BH, 64, C::BR, SW) ||
+  if (!make_tmap_3d(&mq, q, BF, 2, D, N, BH, 64, BR, SW) || !make_tmap_3d(&mdo, a.dO, BF, 2, D, N, BH, 64, BR, SW) ||
       !make_tmap_3d(&mk, k, BF, 2, D, N, BH, 64, 128, SW) || !make_tmap_3d(&mv, v, BF, 2, D, N, BH, 64, 128, SW) ||
       !make_tmap_3d(&mdk, a.dk, BF, 2, D, N, BH, 64, 128, SW) ||
       !make_tmap_3d(&mdv, a.dv, BF, 2, D, N, BH, 64, 128, SW) ||
-      !make_tmap_3d(&mdq, a.dq_acc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, D, (uint64_t)a.Npad, BH, 32, C::BR, SW))
+      !make_tmap_3d(&mdq, a.dq_acc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, D, (uint64_t)a.Npad, BH, 32,
+                    (D == 64) ? 128 : BR, SW))
     return cuda_fail("cuTensorMapEncodeTiled", 0, "tensor map rejected");
   static bool attr_set = false;  // benign race: idempotent
-  if (D == 64) {
-    CUtensorMap mq64, mdo64;  // 64-row query steps
-    if (!make_tmap_3d(&mq64, q, BF, 2, D, N, BH, 64, Bwd64::BR, SW) ||
-        !make_tmap_3d(&mdo64, a.dO, BF, 2, D, N, BH, 64, Bwd64::BR, SW))
-      return cuda_fail("cuTensorMapEncodeTiled", 0, "tensor map rejected");
+  dim3 grid(BH, (a.N + 127) / 128);
+  if constexpr (D == 64) {
     if (!attr_set) {
       const cudaError_t e = cudaFuncSetAttribute(bwd_kernel_d64<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                  Bwd64::SMEM_BYTES);
       if (e != cudaSuccess) return cuda_fail("cudaFuncSetAttribute", (int)e, cudaGetErrorName(e));
       attr_set = true;
     }
-    dim3 grid(BH, (a.N + 127) / 128);
-    bwd_kernel_d64<0><<<grid, Bwd64::THREADS, Bwd64::SMEM_BYTES, stream>>>(mq64, mk, mv, mdo64, mdk, mdv, mdq, a);
-    return check_launch(__func__);
+    bwd_kernel_d64<0><<<grid, Bwd64::THREADS, Bwd64::SMEM_BYTES, stream>>>(mq, mk, mv, mdo, mdk, mdv, mdq, a);
+  } else {
+    using C = BwdCfg<D>;
+    if (!attr_set) {
+      const cudaError_t e =
+          cudaFuncSetAttribute(bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+      if (e != cudaSuccess) return cuda_fail("cudaFuncSetAttribute", (int)e, cudaGetErrorName(e));
+      attr_set = true;
+    }
+    bwd_kernel<D><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(mq, mk, mv, mdo, mdk, mdv, mdq, a);
   }
-  if (!attr_set) {
-    const cudaError_t e =
-        cudaFuncSetAttribute(bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
-    if (e != cudaSuccess) return cuda_fail("cudaFuncSetAttribute", (int)e, cudaGetErrorName(e));
-    attr_set = true;
-  }
-  dim3 grid(BH, (a.N + 127) / 128);
-  bwd_kernel<D><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(mq, mk, mv, mdo, mdk, mdv, mdq, a);
   return check_launch(__func__);
 }
 

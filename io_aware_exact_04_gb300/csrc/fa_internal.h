@@ -26,8 +26,8 @@ struct BwdArgs {
   const uint16_t* o;   // [B*H, N, d]
   const uint16_t* dO;  // [B*H, N, d]
   const float* lse;    // [B*H, N]
-  float* lse2;         // workspace [B*H, Npad]: LSE * log2(e), +inf on padding rows
-  float* dvec;         // workspace [B*H, Npad]: D = rowsum(dO * O), 0 on padding rows
+  float* lse2;         // workspace [B*H, Npad]: -LSE * log2(e), -inf on padding rows
+  float* dvec;         // workspace [B*H, Npad]: -D = -rowsum(dO * O), 0 on padding rows
   float* dq_acc;       // workspace [B*H, Npad, d] fp32
   uint16_t* dq;        // [B*H, N, d] bf16
   uint16_t* dk;        // [B*H, N, d] bf16
