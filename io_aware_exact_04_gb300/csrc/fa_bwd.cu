@@ -245,8 +245,9 @@ __global__ void __launch_bounds__(448, 1)
       }
     }
   } else if (warp == 13) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // ------------------------------------------------------------ MMA issuer (whole warp runs
+    // the loop; one elected lane issues each MMA and commit)
+    {
       constexpr uint32_t IDESC_S = idesc_bf16_f32(128, BR, 0, 0);  // K (or V) x Q_i (or dO_i), K-major
       constexpr uint32_t IDESC_G = idesc_bf16_f32(128, D, 0, 1);   // TMEM A x MN-major B
       constexpr uint32_t IDESC_Q = idesc_bf16_f32(128, 64, 1, 1);  // both operands MN-major
@@ -262,18 +263,24 @@ __global__ void __launch_bounds__(448, 1)
         for (int k = 0; k < D / 16; ++k) {
           const uint32_t oa = ((k >> 2) * C::KSUB + (k & 3) * 32) >> 4;
           const uint32_t ob = ((k >> 2) * C::QSUB + (k & 3) * 32) >> 4;
-          mma_ss(tmem + dst, sdesc_join(a_lo + oa, HI), sdesc_join(b_lo + ob, HI), IDESC_S, k > 0);
+          if (elect_one()) mma_ss(tmem + dst, sdesc_join(a_lo + oa, HI), sdesc_join(b_lo + ob, HI), IDESC_S, k > 0);
         }
       };
       auto issue_grad = [&](uint32_t dst, uint32_t a_tm, uint32_t b_lo, uint32_t acc) {
 #pragma unroll
         for (int k = 0; k < BR / 16; ++k)
-          mma_ts(tmem + dst, tmem + a_tm + C::pcol(16 * k), sdesc_join(b_lo + k * (2048 >> 4), HI), IDESC_G,
-                 (acc | k) != 0);
+          if (elect_one())
+            mma_ts(tmem + dst, tmem + a_tm + C::pcol(16 * k), sdesc_join(b_lo + k * (2048 >> 4), HI), IDESC_G,
+                   (acc | k) != 0);
+      };
+      auto commit = [&](uint32_t bar) {
+        if (elect_one()) mma_commit(bar);
+        __syncwarp();
       };
       auto issue_dq = [&](uint32_t dst) {
 #pragma unroll
         for (int k = 0; k < 8; ++k) {  // 128 keys
+          if (!elect_one()) continue;
           if (D == 64)  // dQ = dS K: A = dS (M = queries), B = K (N = head dims)
             mma_ss(tmem + dst, sdesc_join(ds_lo + k * (2048 >> 4), HI), sdesc_join(kmn_lo + k * (2048 >> 4), HI),
                    IDESC_Q, k > 0);
@@ -282,30 +289,30 @@ __global__ void __launch_bounds__(448, 1)
                    IDESC_Q, k > 0);
         }
       };
-      bool ok = wait_bounded(kv_full, 0, st, SITE_B_KV_FULL);
+      bool ok = wait_warp(kv_full, 0, st, SITE_B_KV_FULL);
       for (int it = 0; ok && it < n_it; ++it) {
         const int s = it & 1;
         const uint32_t so = s * QT16;
-        if (!(ok = wait_bounded(qdo_full(s), (it >> 1) & 1, st, SITE_B_QDO_FULL))) break;
+        if (!(ok = wait_warp(qdo_full(s), (it >> 1) & 1, st, SITE_B_QDO_FULL))) break;
         tc_fence_after();
         issue_kmajor(C::TM_ST, k_lo, q_lo + so);
-        mma_commit(s_full);
+        commit(s_full);
         issue_kmajor(C::TM_DPT, v_lo, do_lo + so);
-        mma_commit(dp_full);
-        if (!(ok = wait_bounded(p_ready, it & 1, st, SITE_B_P_READY))) break;
+        commit(dp_full);
+        if (!(ok = wait_warp(p_ready, it & 1, st, SITE_B_P_READY))) break;
         tc_fence_after();
         issue_grad(C::TM_DV, C::TM_ST, domn_lo + so, it > 0);
-        if (!(ok = wait_bounded(ds_ready, it & 1, st, SITE_B_DS_READY))) break;
+        if (!(ok = wait_warp(ds_ready, it & 1, st, SITE_B_DS_READY))) break;
         tc_fence_after();
         issue_grad(C::TM_DK, C::TM_DPT, qmn_lo + so, it > 0);
         const int qb = it & 1;
-        if (!(ok = wait_bounded(dq_empty(qb), ((it >> 1) & 1) ^ 1, st, SITE_B_DQ_EMPTY))) break;
+        if (!(ok = wait_warp(dq_empty(qb), ((it >> 1) & 1) ^ 1, st, SITE_B_DQ_EMPTY))) break;
         tc_fence_after();
         issue_dq(C::TM_DQ + qb * C::DQ_COLS);
-        mma_commit(dq_full(qb));
-        mma_commit(qdo_empty(s));
+        commit(dq_full(qb));
+        commit(qdo_empty(s));
       }
-      mma_commit(final_bar);  // also the drain: completes after every MMA issued above
+      commit(final_bar);  // also the drain: completes after every MMA issued above
       const uint64_t t0 = globaltimer_ns();
       while (!mbar_try_wait(final_bar, 0) && globaltimer_ns() - t0 < kWaitLimitNs) {
       }
@@ -670,8 +677,9 @@ __global__ void __launch_bounds__(480, 1)
     }
   } else if (warp == 13 || warp == 14) {
     // ------------------------------------------------------------ MMA issuers: warp 13 serves
-    // warpgroup 0 (even steps), warp 14 warpgroup 1 (odd steps) and forms dQ
-    if (lane == 0) {
+    // warpgroup 0 (even steps), warp 14 warpgroup 1 (odd steps) and forms dQ. The whole warp
+    // runs the loop; one elected lane issues each MMA and commit.
+    {
       const int w = warp - 13;
       constexpr uint32_t IDESC_S = idesc_bf16_f32(128, BR, 0, 0);  // K (V) x Q_i (dO_i), K-major
       constexpr uint32_t IDESC_G = idesc_bf16_f32(128, 64, 0, 1);  // TMEM A x MN-major B
@@ -682,32 +690,39 @@ __global__ void __launch_bounds__(480, 1)
       const uint32_t q_lo = sdesc_lo(sbase + C::OFF_Q, 16), do_lo = sdesc_lo(sbase + C::OFF_DO, 16);
       const uint32_t qmn_lo = sdesc_lo(sbase + C::OFF_Q, C::QTILE), domn_lo = sdesc_lo(sbase + C::OFF_DO, C::QTILE);
       const uint32_t ds_lo = sdesc_lo(sbase + C::OFF_DS, 128 * 128), kmn_lo = sdesc_lo(sbase + C::OFF_K, C::KTILE);
+      auto commit = [&](uint32_t bar) {
+        if (elect_one()) mma_commit(bar);
+        __syncwarp();
+      };
       auto issue_s = [&](int it) {  // S^T of step it into buffer it % 2
         const uint32_t so = (it % NQS) * QT16;
 #pragma unroll
         for (int k = 0; k < 4; ++k)
-          mma_ss(tmem + C::TM_ST + 64 * (it & 1), sdesc_join(k_lo + 2 * k, HI), sdesc_join(q_lo + so + 2 * k, HI),
-                 IDESC_S, k > 0);
-        mma_commit(s_full(it & 1));
+          if (elect_one())
+            mma_ss(tmem + C::TM_ST + 64 * (it & 1), sdesc_join(k_lo + 2 * k, HI), sdesc_join(q_lo + so + 2 * k, HI),
+                   IDESC_S, k > 0);
+        commit(s_full(it & 1));
       };
       auto issue_dp = [&](int it) {  // dP^T of step it into buffer it % 2
         const uint32_t so = (it % NQS) * QT16;
 #pragma unroll
         for (int k = 0; k < 4; ++k)
-          mma_ss(tmem + C::TM_DPT + 64 * (it & 1), sdesc_join(v_lo + 2 * k, HI), sdesc_join(do_lo + so + 2 * k, HI),
-                 IDESC_S, k > 0);
-        mma_commit(dp_full(it & 1));
+          if (elect_one())
+            mma_ss(tmem + C::TM_DPT + 64 * (it & 1), sdesc_join(v_lo + 2 * k, HI),
+                   sdesc_join(do_lo + so + 2 * k, HI), IDESC_S, k > 0);
+        commit(dp_full(it & 1));
       };
       // dV (dK) += P^T (dS^T) [128 keys x 64 queries, TMEM] x dO_i (Q_i) [64 queries x 64 dims]
       auto issue_grad = [&](uint32_t dst, uint32_t a_tm, uint32_t b_lo, uint32_t acc) {
 #pragma unroll
         for (int k = 0; k < 4; ++k)
-          mma_ts(tmem + dst, tmem + a_tm + 8 * k, sdesc_join(b_lo + k * (2048 >> 4), HI), IDESC_G, (acc | k) != 0);
+          if (elect_one())
+            mma_ts(tmem + dst, tmem + a_tm + 8 * k, sdesc_join(b_lo + k * (2048 >> 4), HI), IDESC_G, (acc | k) != 0);
       };
       // This thread's first step starts its buffers. Afterwards S^T(i+2) follows dV(i) as
       // soon as the warpgroup has P^T(i) (it keeps P in registers for dS, so S^T's
       // columns are free), and dP^T(i+2) follows dK(i) once dS^T(i) is written.
-      bool ok = wait_bounded(kv_full, 0, st, SITE_B_KV_FULL) && wait_bounded(qdo_full(w), 0, st, SITE_B_QDO_FULL);
+      bool ok = wait_warp(kv_full, 0, st, SITE_B_KV_FULL) && wait_warp(qdo_full(w), 0, st, SITE_B_QDO_FULL);
       if (ok) {
         tc_fence_after();
         issue_s(w);
@@ -717,48 +732,51 @@ __global__ void __launch_bounds__(480, 1)
         const uint32_t par = (it >> 1) & 1;
         const uint32_t so = (it % NQS) * QT16;
         const bool more = it + 2 < n_it;
-        if (!(ok = wait_bounded(p_ready(w), par, st, SITE_B_P_READY))) break;
+        if (!(ok = wait_warp(p_ready(w), par, st, SITE_B_P_READY))) break;
         tc_fence_after();
         issue_grad(C::TM_DV, C::TM_ST + 64 * w, domn_lo + so, 1);
         if (more) {
-          if (!(ok = wait_bounded(qdo_full((it + 2) % NQS), ((it + 2) / NQS) & 1, st, SITE_B_QDO_FULL))) break;
+          if (!(ok = wait_warp(qdo_full((it + 2) % NQS), ((it + 2) / NQS) & 1, st, SITE_B_QDO_FULL))) break;
           tc_fence_after();
           issue_s(it + 2);
         }
-        if (!(ok = wait_bounded(ds_ready(w), par, st, SITE_B_DS_READY))) break;
+        if (!(ok = wait_warp(ds_ready(w), par, st, SITE_B_DS_READY))) break;
         tc_fence_after();
         issue_grad(C::TM_DK, C::TM_DPT + 64 * w, qmn_lo + so, 1);
-        mma_commit(qdo_empty(it % NQS));  // last readers of Q_i and dO_i issued
+        commit(qdo_empty(it % NQS));  // last readers of Q_i and dO_i issued
         if (more) issue_dp(it + 2);
         if (w == 1) {  // the pair (it-1, it) is complete once warpgroup 0's dS of step it-1 is in smem
           const int p = it >> 1, c = p & 1;
           const uint32_t need = 4u * (uint32_t)(p + 1);
-          const uint64_t t0 = globaltimer_ns();
-          while (smem_ld_acquire(ds0_count) < need) {
-            if (*(volatile int*)abort_flag || *(volatile int*)a.status != 0) {
-              *(volatile int*)abort_flag = 1;
-              ok = false;
-              break;
-            }
-            if (globaltimer_ns() - t0 > kWaitLimitNs) {
-              record_error(st, FA_ERR_TIMEOUT, SITE_B_DS_READY);
-              ok = false;
-              break;
+          if (lane == 0) {
+            const uint64_t t0 = globaltimer_ns();
+            while (smem_ld_acquire(ds0_count) < need) {
+              if (*(volatile int*)abort_flag || *(volatile int*)a.status != 0) {
+                *(volatile int*)abort_flag = 1;
+                ok = false;
+                break;
+              }
+              if (globaltimer_ns() - t0 > kWaitLimitNs) {
+                record_error(st, FA_ERR_TIMEOUT, SITE_B_DS_READY);
+                ok = false;
+                break;
+              }
             }
           }
-          if (!ok) break;
-          if (!(ok = wait_bounded(dq_empty(c), ((p >> 1) & 1) ^ 1, st, SITE_B_DQ_EMPTY))) break;
+          if (!(ok = __all_sync(0xffffffffu, ok))) break;
+          if (!(ok = wait_warp(dq_empty(c), ((p >> 1) & 1) ^ 1, st, SITE_B_DQ_EMPTY))) break;
           tc_fence_after();
           const uint32_t dsb = ds_lo + c * (C::DS_BYTES >> 4);
 #pragma unroll
           for (int k = 0; k < 8; ++k)  // 128 keys
-            mma_ss(tmem + C::TM_DQ + 64 * c, sdesc_join(dsb + k * (2048 >> 4), HI),
-                   sdesc_join(kmn_lo + k * (2048 >> 4), HI), IDESC_Q, k > 0);
-          mma_commit(dq_full(c));
-          mma_commit(dq_done(c));
+            if (elect_one())
+              mma_ss(tmem + C::TM_DQ + 64 * c, sdesc_join(dsb + k * (2048 >> 4), HI),
+                     sdesc_join(kmn_lo + k * (2048 >> 4), HI), IDESC_Q, k > 0);
+          commit(dq_full(c));
+          commit(dq_done(c));
         }
       }
-      mma_commit(final_bar);  // also the drain: completes after every MMA issued above
+      commit(final_bar);  // also the drain: completes after every MMA issued above
       const uint64_t t0 = globaltimer_ns();
       while (!mbar_try_wait(final_bar, 0) && globaltimer_ns() - t0 < kWaitLimitNs) {
       }
@@ -826,35 +844,29 @@ __global__ void __launch_bounds__(480, 1)
       // ---- P^T = exp2(S^T s log2e + lse2) (lse2 = -LSE log2e) -> bf16 pairs in the first 32
       //      columns of this buffer, kept in registers too: S^T's columns are overwritten by
       //      the next step once P^T is out
-      uint32_t pkeep[2][16];
-#pragma unroll
-      for (int ch = 0; ch < 2; ++ch) {
-        uint32_t sv[32];
-        tmem_ld32(tST + 32 * ch, sv);
-        float lz[32];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const float4 t4 = reinterpret_cast<const float4*>(lse_s + 32 * ch)[e];
-          lz[4 * e] = t4.x, lz[4 * e + 1] = t4.y, lz[4 * e + 2] = t4.z, lz[4 * e + 3] = t4.w;
-        }
+      // Both 32-column halves are loaded before one wait, so the TMEM load latency is paid once.
+      uint32_t pkeep[32];
+      {
+        uint32_t sv[2][32];
+        tmem_ld32(tST, sv[0]);
+        tmem_ld32(tST + 32, sv[1]);
         tmem_wait_ld();
         if (need_mask) {  // only steps on the diagonal or past kv_len: masked S -> -inf, so P = 0
-          const int lim = key >= kv ? 32 : (a.causal ? key - q0 - 32 * ch : 0);  // columns [0, lim)
+          const int lim = key >= kv ? 64 : (a.causal ? key - q0 : 0);  // columns [0, lim)
 #pragma unroll
-          for (int c = 0; c < 32; ++c)
-            if (c < lim) sv[c] = 0xff800000u;
+          for (int c = 0; c < 64; ++c)
+            if (c < lim) sv[c >> 5][c & 31] = 0xff800000u;
         }
-        uint32_t pk[16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          float x[2];
-          f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[2 * e]), __uint_as_float(sv[2 * e + 1])), sl2x2,
-                           f2_pack(lz[2 * e], lz[2 * e + 1])),
-                    x[0], x[1]);
-          pk[e] = pack_bf16x2(ex2_approx(x[0]), ex2_approx(x[1]));
-          pkeep[ch][e] = pk[e];
+        for (int e = 0; e < 32; ++e) {
+          const float2 l2 = reinterpret_cast<const float2*>(lse_s)[e];
+          float x0, x1;
+          const uint32_t* se = &sv[e >> 4][(2 * e) & 31];
+          const uint64_t s2 = f2_pack(__uint_as_float(se[0]), __uint_as_float(se[1]));
+          f2_unpack(f2_fma(s2, sl2x2, f2_pack(l2.x, l2.y)), x0, x1);
+          pkeep[e] = pack_bf16x2(ex2_approx(x0), ex2_approx(x1));
         }
-        tmem_st16(tST + 16 * ch, pk);
+        tmem_st32(tST, pkeep);
       }
       tmem_wait_st();
       tc_fence_before();
@@ -868,33 +880,31 @@ __global__ void __launch_bounds__(480, 1)
         const int pp2 = (it >> 1) - 2;
         if (!(ok = wait_warp(dq_done(pp2 & 1), (pp2 >> 1) & 1, st, SITE_B_DQ_EMPTY))) break;
       }
-#pragma unroll
-      for (int ch = 0; ch < 2; ++ch) {
-        uint32_t dp[32];
-        tmem_ld32(tDPT + 32 * ch, dp);
-        const uint32_t* pp = pkeep[ch];
-        float dz[32];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const float4 t4 = reinterpret_cast<const float4*>(dv_s + 32 * ch)[e];
-          dz[4 * e] = t4.x, dz[4 * e + 1] = t4.y, dz[4 * e + 2] = t4.z, dz[4 * e + 3] = t4.w;
-        }
+      {
+        uint32_t dp[2][32];
+        tmem_ld32(tDPT, dp[0]);
+        tmem_ld32(tDPT + 32, dp[1]);
         tmem_wait_ld();
-        uint32_t pk[16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const float p0 = __uint_as_float(pp[e] << 16), p1 = __uint_as_float(pp[e] & 0xFFFF0000u);
-          const uint64_t t2 = f2_add(f2_pack(__uint_as_float(dp[2 * e]), __uint_as_float(dp[2 * e + 1])),
-                                     f2_pack(dz[2 * e], dz[2 * e + 1]));
-          float d0, d1;
-          f2_unpack(f2_mul(t2, f2_pack(p0, p1)), d0, d1);
-          pk[e] = pack_bf16x2(d0, d1);
+        for (int h = 0; h < 2; ++h) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int g = 16 * h + e;
+            const float2 d2 = reinterpret_cast<const float2*>(dv_s)[g];
+            const float p0 = __uint_as_float(pkeep[g] << 16), p1 = __uint_as_float(pkeep[g] & 0xFFFF0000u);
+            const uint64_t t2 =
+                f2_add(f2_pack(__uint_as_float(dp[h][2 * e]), __uint_as_float(dp[h][2 * e + 1])), f2_pack(d2.x, d2.y));
+            float d0, d1;
+            f2_unpack(f2_mul(t2, f2_pack(p0, p1)), d0, d1);
+            pk[e] = pack_bf16x2(d0, d1);
+          }
+          tmem_st16(tDPT + 16 * h, pk);
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            *reinterpret_cast<uint4*>(dsb + sw128_offset(r, 4 * h + q)) =
+                make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
         }
-        tmem_st16(tDPT + 16 * ch, pk);
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-          *reinterpret_cast<uint4*>(dsb + sw128_offset(r, 4 * ch + q)) =
-              make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
       }
       tmem_wait_st();
       fence_proxy_async_smem();

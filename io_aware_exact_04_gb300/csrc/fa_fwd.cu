@@ -108,7 +108,7 @@ __global__ void __launch_bounds__(352, 1)
     for (int s = 0; s < C::NST; ++s) {
       mbar_init(k_full(s), 1);
       mbar_init(v_full(s), 1);
-      mbar_init(kv_empty(s), C::NMMA);  // one arrival per MMA-issuing thread
+      mbar_init(kv_empty(s), C::NMMA);  // one arrival per MMA-issuing warp
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(s_full(t), 1);
@@ -170,8 +170,8 @@ __global__ void __launch_bounds__(352, 1)
   } else if (warp == 9 || warp == 10) {
     // ------------------------------------------------------------ MMA issuers: for d = 64 warp 9
     // serves query tile 0 and warp 10 query tile 1, each in its own order; for d = 128
-    // warp 9 serves both, alternating
-    if (lane == 0 && nmax > 0 && warp - 9 < C::NMMA) {
+    // warp 9 serves both, alternating. The whole warp runs the loop; one elected lane issues.
+    if (nmax > 0 && warp - 9 < C::NMMA) {
       constexpr uint32_t IDESC_S = idesc_bf16_f32(128, 128, 0, 0);  // Q, K both K-major
       constexpr uint32_t IDESC_O = idesc_bf16_f32(128, D, 0, 1);    // P from TMEM, V MN-major
       // Descriptors are formed once; each MMA only adds a constant to the low word.
@@ -185,23 +185,27 @@ __global__ void __launch_bounds__(352, 1)
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
           const uint32_t off = ((k >> 2) * C::SUB_BYTES + (k & 3) * 32) >> 4;
-          mma_ss(d, sdesc_join(qa + off, HI), sdesc_join(ka + off, HI), IDESC_S, k > 0);
+          if (elect_one()) mma_ss(d, sdesc_join(qa + off, HI), sdesc_join(ka + off, HI), IDESC_S, k > 0);
         }
       };
       auto issue_pv = [&](int t, int vst, uint32_t acc) {  // O_t += P_t V (V from stage vst)
         const uint32_t va = v_lo + vst * TILE16, d = tmem + C::tm_o(t), pa = tmem + C::tm_p(t);
 #pragma unroll
         for (int k = 0; k < 8; ++k)  // 128 keys, 16 per MMA
-          mma_ts(d, pa + k * 8, sdesc_join(va + k * (2048 >> 4), HI), IDESC_O, (acc | k) != 0);
+          if (elect_one()) mma_ts(d, pa + k * 8, sdesc_join(va + k * (2048 >> 4), HI), IDESC_O, (acc | k) != 0);
       };
-      bool ok = wait_bounded(q_full, 0, st, SITE_F_Q_FULL) && wait_bounded(k_full(0), 0, st, SITE_F_K_FULL);
+      auto commit = [&](uint32_t bar) {
+        if (elect_one()) mma_commit(bar);
+        __syncwarp();
+      };
+      bool ok = wait_warp(q_full, 0, st, SITE_F_Q_FULL) && wait_warp(k_full(0), 0, st, SITE_F_K_FULL);
       const int t_lo = C::SEP_P ? warp - 9 : 0, t_hi = C::SEP_P ? warp - 9 : 1;  // query tiles served
       if (ok) {
         tc_fence_after();
         for (int t = t_lo; t <= t_hi; ++t)
           if (n_t[t] > 0) {
             issue_s(t, 0);
-            mma_commit(s_full(t));
+            commit(s_full(t));
           }
       }
       int s = 0, ph = 0;  // ring stage and phase of tile j
@@ -215,37 +219,38 @@ __global__ void __launch_bounds__(352, 1)
           used = true;
           if (C::SEP_P && j + 1 < n) {
             // S_t(j+1) as soon as the warpgroup has S_t(j) in registers
-            if (!(ok = wait_bounded(k_full(s2), ph2, st, SITE_F_K_FULL))) break;
-            if (!(ok = wait_bounded(s_free(t), j & 1, st, SITE_F_S_FREE))) break;
+            if (!(ok = wait_warp(k_full(s2), ph2, st, SITE_F_K_FULL))) break;
+            if (!(ok = wait_warp(s_free(t), j & 1, st, SITE_F_S_FREE))) break;
             tc_fence_after();
             issue_s(t, s2);
-            mma_commit(s_full(t));
+            commit(s_full(t));
           }
-          if (!(ok = wait_bounded(v_full(s), ph, st, SITE_F_V_FULL))) break;
-          if (!(ok = wait_bounded(p_ready(t), j & 1, st, SITE_F_P_READY))) break;
+          if (!(ok = wait_warp(v_full(s), ph, st, SITE_F_V_FULL))) break;
+          if (!(ok = wait_warp(p_ready(t), j & 1, st, SITE_F_P_READY))) break;
           tc_fence_after();
           issue_pv(t, s, j > 0);
-          mma_commit(o_done(t));
+          commit(o_done(t));
           if (!C::SEP_P && j + 1 < n) {  // P_t(j) lives over S_t(j): S_t(j+1) follows PV_t(j)
-            if (!(ok = wait_bounded(k_full(s2), ph2, st, SITE_F_K_FULL))) break;
+            if (!(ok = wait_warp(k_full(s2), ph2, st, SITE_F_K_FULL))) break;
             issue_s(t, s2);
-            mma_commit(s_full(t));
+            commit(s_full(t));
           }
         }
         if (!ok) break;
         if (used) {
-          mma_commit(kv_empty(s));  // this thread's readers of K_j, V_j are issued
+          commit(kv_empty(s));  // this warp's readers of K_j, V_j are issued
         } else {
-          // tile j is not this thread's: once it has landed (so its stage's previous use
-          // is released), add this thread's arrival without waiting for anything else
-          if (!(ok = wait_bounded(v_full(s), ph, st, SITE_F_V_FULL))) break;
-          mbar_arrive(kv_empty(s));
+          // tile j is not this warp's: once it has landed (so its stage's previous use
+          // is released), add this warp's arrival without waiting for anything else
+          if (!(ok = wait_warp(v_full(s), ph, st, SITE_F_V_FULL))) break;
+          if (elect_one()) mbar_arrive(kv_empty(s));
+          __syncwarp();
         }
         s = s2;
         ph = ph2;
       }
-      // every MMA issued by either thread has completed before TMEM is released
-      mma_commit(drain);
+      // every MMA issued by either warp has completed before TMEM is released
+      commit(drain);
       const uint64_t t0 = globaltimer_ns();
       while (!mbar_try_wait(drain, 0) && globaltimer_ns() - t0 < kWaitLimitNs) {
       }

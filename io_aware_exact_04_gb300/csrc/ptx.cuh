@@ -306,6 +306,18 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
   return r;
 }
+// One lane of a converged warp (elect.sync). Issuing warps run their loops with the whole
+// warp, so that descriptors and TMEM addresses stay warp-uniform, and let one elected lane
+// execute each single-thread tcgen05 instruction: on sm_103a this issues MMAs faster than a
+// loop run by lane 0 alone.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n .reg .pred P;\n elect.sync _|P, 0xffffffff;\n selp.u32 %0, 1, 0, P;\n}"
+      : "=r"(pred));
+  return pred != 0;
+}
+
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
