@@ -183,21 +183,54 @@ __global__ void __launch_bounds__(448, 1)
     return;
   }
 
-  if (threadIdx.x == 0) {
-    mbar_init(kv_full, 1);
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(qdo_full(s), 1);
-      mbar_init(qdo_empty(s), 1);
-      mbar_init(dq_full(s), 1);
-      mbar_init(dq_empty(s), 4);
+  const float* lse2_h = a.lse2 + (size_t)bh * a.Npad;
+  const float* dvec_h = a.dvec + (size_t)bh * a.Npad;
+  // The producer warp initialises the barriers and starts the first copies (K, V and the first
+  // two query steps, whose slots are free) before the CTA-wide setup, hiding their latency. It
+  // runs its code with the whole warp and lets one elected lane issue each copy.
+  const int n_pre = min(2, n_it);
+  auto load_qdo = [&](int it) {  // whole warp
+    const int s = it & 1, i = i_start + it;
+    const uint32_t bar = qdo_full(s);
+    const float* lsrc = lse2_h + (size_t)i * BR;
+    const float* dsrc = dvec_h + (size_t)i * BR;
+    if (elect_one()) mbar_arrive_expect_tx(bar, 2 * C::QTILE + 2 * BR * 4);
+    for (int c = 0; c < C::NSUB; ++c) {
+      if (elect_one()) tma_load_3d(sbase + C::OFF_Q + s * C::QTILE + c * C::QSUB, &tm_q, c * 64, i * BR, bh, bar);
+      if (elect_one()) tma_load_3d(sbase + C::OFF_DO + s * C::QTILE + c * C::QSUB, &tm_do, c * 64, i * BR, bh, bar);
     }
-    mbar_init(s_full, 1);
-    mbar_init(dp_full, 1);
-    mbar_init(p_ready, 8);
-    mbar_init(ds_ready, 8);
-    mbar_init(final_bar, 1);
-    *abort_flag = 0;
-    fence_mbar_init();
+    if (elect_one()) bulk_load(sbase + C::OFF_LSE + s * BR * 4, lsrc, BR * 4, bar);
+    if (elect_one()) bulk_load(sbase + C::OFF_DV + s * BR * 4, dsrc, BR * 4, bar);
+    __syncwarp();
+  };
+  if (warp == 12) {
+    if (lane == 0) {
+      mbar_init(kv_full, 1);
+      for (int s = 0; s < 2; ++s) {
+        mbar_init(qdo_full(s), 1);
+        mbar_init(qdo_empty(s), 1);
+        mbar_init(dq_full(s), 1);
+        mbar_init(dq_empty(s), 4);
+      }
+      mbar_init(s_full, 1);
+      mbar_init(dp_full, 1);
+      mbar_init(p_ready, 8);
+      mbar_init(ds_ready, 8);
+      mbar_init(final_bar, 1);
+      *abort_flag = 0;
+      fence_mbar_init();
+    }
+    __syncwarp();
+    if (elect_one()) {
+      prefetch_tmap(&tm_q);
+      prefetch_tmap(&tm_do);
+    }
+    if (elect_one()) mbar_arrive_expect_tx(kv_full, 2 * C::KTILE);
+    for (int c = 0; c < C::NSUB; ++c) {
+      if (elect_one()) tma_load_3d(sbase + C::OFF_K + c * C::KSUB, &tm_k, c * 64, k0, bh, kv_full);
+      if (elect_one()) tma_load_3d(sbase + C::OFF_V + c * C::KSUB, &tm_v, c * 64, k0, bh, kv_full);
+    }
+    for (int it = 0; it < n_pre; ++it) load_qdo(it);
   }
   if (warp == 13) {
     tmem_alloc(smem_u32(tmem_slot), C::TM_COLS);
@@ -207,31 +240,14 @@ __global__ void __launch_bounds__(448, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const float* lse2_h = a.lse2 + (size_t)bh * a.Npad;
-  const float* dvec_h = a.dvec + (size_t)bh * a.Npad;
 
   if (warp == 12) {
     // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      prefetch_tmap(&tm_q);
-      prefetch_tmap(&tm_do);
-      mbar_arrive_expect_tx(kv_full, 2 * C::KTILE);
-      for (int c = 0; c < C::NSUB; ++c) {
-        tma_load_3d(sbase + C::OFF_K + c * C::KSUB, &tm_k, c * 64, k0, bh, kv_full);
-        tma_load_3d(sbase + C::OFF_V + c * C::KSUB, &tm_v, c * 64, k0, bh, kv_full);
-      }
-      int issued = 0;
-      for (int it = 0; it < n_it; ++it) {
-        const int s = it & 1;
-        const int i = i_start + it;
-        if (!wait_bounded(qdo_empty(s), ((it >> 1) & 1) ^ 1, st, SITE_B_QDO_EMPTY)) break;
-        mbar_arrive_expect_tx(qdo_full(s), 2 * C::QTILE + 2 * BR * 4);
-        for (int c = 0; c < C::NSUB; ++c) {
-          tma_load_3d(sbase + C::OFF_Q + s * C::QTILE + c * C::QSUB, &tm_q, c * 64, i * BR, bh, qdo_full(s));
-          tma_load_3d(sbase + C::OFF_DO + s * C::QTILE + c * C::QSUB, &tm_do, c * 64, i * BR, bh, qdo_full(s));
-        }
-        bulk_load(sbase + C::OFF_LSE + s * BR * 4, lse2_h + (size_t)i * BR, BR * 4, qdo_full(s));
-        bulk_load(sbase + C::OFF_DV + s * BR * 4, dvec_h + (size_t)i * BR, BR * 4, qdo_full(s));
+    {
+      int issued = n_pre;
+      for (int it = n_pre; it < n_it; ++it) {
+        if (!wait_warp(qdo_empty(it & 1), ((it >> 1) & 1) ^ 1, st, SITE_B_QDO_EMPTY)) break;
+        load_qdo(it);
         issued = it + 1;
       }
       if (*(volatile int*)abort_flag) {
@@ -373,7 +389,7 @@ __global__ void __launch_bounds__(448, 1)
         bulk_commit();
       }
     }
-    if (tid == 0) bulk_wait0();
+    if (tid == 0) bulk_wait_read0();
   } else {
     // ------------------------------------------------------------ P^T / dS^T warpgroups
     const int wg = warp >> 2;  // which half of the BR query columns
@@ -504,7 +520,7 @@ __global__ void __launch_bounds__(448, 1)
         for (int c = 0; c < C::NSUB; ++c)
           tma_store_3d(wg == 0 ? &tm_dv : &tm_dk, smem_u32(stage + c * C::KSUB), c * 64, k0, bh);
         bulk_commit();
-        bulk_wait0();
+        bulk_wait_read0();  // the staging tile must outlive the copy's reads
       }
     }
   }
@@ -601,25 +617,54 @@ __global__ void __launch_bounds__(480, 1)
     return;
   }
 
-  if (threadIdx.x == 0) {
-    mbar_init(kv_full, 1);
-    for (int s = 0; s < NQS; ++s) {
-      mbar_init(qdo_full(s), 1);
-      mbar_init(qdo_empty(s), 1);
+  const float* lse2_h = a.lse2 + (size_t)bh * a.Npad;
+  const float* dvec_h = a.dvec + (size_t)bh * a.Npad;
+  // The producer warp initialises the barriers and starts the first copies (K, V and the first
+  // NQS query steps, whose slots are free) before the CTA-wide setup, hiding their latency. It
+  // runs its code with the whole warp and lets one elected lane issue each copy.
+  const int n_pre = min(NQS, n_it);
+  auto load_qdo = [&](int it) {  // whole warp
+    const int s = it % NQS, i = i_start + it;
+    const uint32_t bar = qdo_full(s);
+    const float* lsrc = lse2_h + (size_t)i * BR;
+    const float* dsrc = dvec_h + (size_t)i * BR;
+    if (elect_one()) mbar_arrive_expect_tx(bar, 2 * C::QTILE + 2 * BR * 4);
+    if (elect_one()) tma_load_3d(sbase + C::OFF_Q + s * C::QTILE, &tm_q, 0, i * BR, bh, bar);
+    if (elect_one()) tma_load_3d(sbase + C::OFF_DO + s * C::QTILE, &tm_do, 0, i * BR, bh, bar);
+    if (elect_one()) bulk_load(sbase + C::OFF_LSE + s * BR * 4, lsrc, BR * 4, bar);
+    if (elect_one()) bulk_load(sbase + C::OFF_DV + s * BR * 4, dsrc, BR * 4, bar);
+    __syncwarp();
+  };
+  if (warp == 12) {
+    if (lane == 0) {
+      mbar_init(kv_full, 1);
+      for (int s = 0; s < NQS; ++s) {
+        mbar_init(qdo_full(s), 1);
+        mbar_init(qdo_empty(s), 1);
+      }
+      for (int w = 0; w < 2; ++w) {
+        mbar_init(s_full(w), 1);
+        mbar_init(dp_full(w), 1);
+        mbar_init(p_ready(w), 4);
+        mbar_init(ds_ready(w), 4);
+        mbar_init(dq_full(w), 1);
+        mbar_init(dq_empty(w), 4);
+        mbar_init(dq_done(w), 1);
+      }
+      mbar_init(final_bar, 2);  // one commit per MMA-issuing warp
+      *abort_flag = 0;
+      tmem_slot[2] = 0;
+      fence_mbar_init();
     }
-    for (int w = 0; w < 2; ++w) {
-      mbar_init(s_full(w), 1);
-      mbar_init(dp_full(w), 1);
-      mbar_init(p_ready(w), 4);
-      mbar_init(ds_ready(w), 4);
-      mbar_init(dq_full(w), 1);
-      mbar_init(dq_empty(w), 4);
-      mbar_init(dq_done(w), 1);
+    __syncwarp();
+    if (elect_one()) {
+      prefetch_tmap(&tm_q);
+      prefetch_tmap(&tm_do);
     }
-    mbar_init(final_bar, 2);  // one commit per MMA-issuing thread
-    *abort_flag = 0;
-    tmem_slot[2] = 0;
-    fence_mbar_init();
+    if (elect_one()) mbar_arrive_expect_tx(kv_full, 2 * C::KTILE);
+    if (elect_one()) tma_load_3d(sbase + C::OFF_K, &tm_k, 0, k0, bh, kv_full);
+    if (elect_one()) tma_load_3d(sbase + C::OFF_V, &tm_v, 0, k0, bh, kv_full);
+    for (int it = 0; it < n_pre; ++it) load_qdo(it);
   }
   if (warp == 13) {
     tmem_alloc(smem_u32(tmem_slot), C::TM_COLS);
@@ -643,27 +688,14 @@ __global__ void __launch_bounds__(480, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const float* lse2_h = a.lse2 + (size_t)bh * a.Npad;
-  const float* dvec_h = a.dvec + (size_t)bh * a.Npad;
 
   if (warp == 12) {
     // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      prefetch_tmap(&tm_q);
-      prefetch_tmap(&tm_do);
-      mbar_arrive_expect_tx(kv_full, 2 * C::KTILE);
-      tma_load_3d(sbase + C::OFF_K, &tm_k, 0, k0, bh, kv_full);
-      tma_load_3d(sbase + C::OFF_V, &tm_v, 0, k0, bh, kv_full);
-      int issued = 0;
-      for (int it = 0; it < n_it; ++it) {
-        const int s = it % NQS;
-        const int i = i_start + it;
-        if (!wait_bounded(qdo_empty(s), ((it / NQS) & 1) ^ 1, st, SITE_B_QDO_EMPTY)) break;
-        mbar_arrive_expect_tx(qdo_full(s), 2 * C::QTILE + 2 * BR * 4);
-        tma_load_3d(sbase + C::OFF_Q + s * C::QTILE, &tm_q, 0, i * BR, bh, qdo_full(s));
-        tma_load_3d(sbase + C::OFF_DO + s * C::QTILE, &tm_do, 0, i * BR, bh, qdo_full(s));
-        bulk_load(sbase + C::OFF_LSE + s * BR * 4, lse2_h + (size_t)i * BR, BR * 4, qdo_full(s));
-        bulk_load(sbase + C::OFF_DV + s * BR * 4, dvec_h + (size_t)i * BR, BR * 4, qdo_full(s));
+    {
+      int issued = n_pre;
+      for (int it = n_pre; it < n_it; ++it) {
+        if (!wait_warp(qdo_empty(it % NQS), ((it / NQS) & 1) ^ 1, st, SITE_B_QDO_EMPTY)) break;
+        load_qdo(it);
         issued = it + 1;
       }
       if (*(volatile int*)abort_flag) {
@@ -819,7 +851,7 @@ __global__ void __launch_bounds__(480, 1)
         }
       }
     }
-    if (tid == 0) bulk_wait0();
+    if (tid == 0) bulk_wait_read0();
   } else {
     // ------------------------------------------------------------ P^T / dS^T warpgroups
     const int w = warp >> 2;       // this warpgroup's steps: it % 2 == w
@@ -859,11 +891,12 @@ __global__ void __launch_bounds__(480, 1)
         }
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
-          const float2 l2 = reinterpret_cast<const float2*>(lse_s)[e];
+          // lse2 of the 64 queries: 16-byte broadcast loads (one shared-memory wavefront each)
+          const float4 l4 = reinterpret_cast<const float4*>(lse_s)[e >> 1];
           float x0, x1;
           const uint32_t* se = &sv[e >> 4][(2 * e) & 31];
           const uint64_t s2 = f2_pack(__uint_as_float(se[0]), __uint_as_float(se[1]));
-          f2_unpack(f2_fma(s2, sl2x2, f2_pack(l2.x, l2.y)), x0, x1);
+          f2_unpack(f2_fma(s2, sl2x2, (e & 1) ? f2_pack(l4.z, l4.w) : f2_pack(l4.x, l4.y)), x0, x1);
           pkeep[e] = pack_bf16x2(ex2_approx(x0), ex2_approx(x1));
         }
         tmem_st32(tST, pkeep);
@@ -891,7 +924,8 @@ __global__ void __launch_bounds__(480, 1)
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
             const int g = 16 * h + e;
-            const float2 d2 = reinterpret_cast<const float2*>(dv_s)[g];
+            const float4 d4 = reinterpret_cast<const float4*>(dv_s)[g >> 1];
+            const float2 d2 = (g & 1) ? make_float2(d4.z, d4.w) : make_float2(d4.x, d4.y);
             const float p0 = __uint_as_float(pkeep[g] << 16), p1 = __uint_as_float(pkeep[g] & 0xFFFF0000u);
             const uint64_t t2 =
                 f2_add(f2_pack(__uint_as_float(dp[h][2 * e]), __uint_as_float(dp[h][2 * e + 1])), f2_pack(d2.x, d2.y));
@@ -943,7 +977,7 @@ __global__ void __launch_bounds__(480, 1)
       if (wq == 0 && lane == 0) {
         tma_store_3d(w == 0 ? &tm_dv : &tm_dk, smem_u32(stage), 0, k0, bh);
         bulk_commit();
-        bulk_wait0();
+        bulk_wait_read0();  // the staging tile must outlive the copy's reads
       }
     }
   }

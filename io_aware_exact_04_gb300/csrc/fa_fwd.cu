@@ -103,22 +103,56 @@ __global__ void __launch_bounds__(352, 1)
   }
   const int nmax = max(n_t[0], n_t[1]);
 
-  if (threadIdx.x == 0) {
-    mbar_init(q_full, 1);
-    for (int s = 0; s < C::NST; ++s) {
-      mbar_init(k_full(s), 1);
-      mbar_init(v_full(s), 1);
-      mbar_init(kv_empty(s), C::NMMA);  // one arrival per MMA-issuing warp
+  // The producer warp initialises the barriers and starts the first copies (Q and the first
+  // NST K/V stages, whose slots are free) before the CTA-wide setup, hiding their latency. It
+  // runs its code with the whole warp and lets one elected lane issue each copy.
+  const int n_pre = min(C::NST, nmax);
+  auto load_kv = [&](int j) {  // whole warp
+    const int s = j % C::NST;
+    const uint32_t kf = k_full(s), vf = v_full(s);
+    const uint32_t kd = sbase + C::OFF_K + s * C::TILE_BYTES, vd = sbase + C::OFF_V + s * C::TILE_BYTES;
+    if (elect_one()) mbar_arrive_expect_tx(kf, C::TILE_BYTES);
+    for (int c = 0; c < C::NSUB; ++c)
+      if (elect_one()) tma_load_3d(kd + c * C::SUB_BYTES, &tm_k, c * 64, j * 128, bh, kf);
+    if (elect_one()) mbar_arrive_expect_tx(vf, C::TILE_BYTES);
+    for (int c = 0; c < C::NSUB; ++c)
+      if (elect_one()) tma_load_3d(vd + c * C::SUB_BYTES, &tm_v, c * 64, j * 128, bh, vf);
+    __syncwarp();
+  };
+  if (warp == 8) {
+    if (lane == 0) {
+      mbar_init(q_full, 1);
+      for (int s = 0; s < C::NST; ++s) {
+        mbar_init(k_full(s), 1);
+        mbar_init(v_full(s), 1);
+        mbar_init(kv_empty(s), C::NMMA);  // one arrival per MMA-issuing warp
+      }
+      for (int t = 0; t < 2; ++t) {
+        mbar_init(s_full(t), 1);
+        mbar_init(p_ready(t), 4);
+        mbar_init(o_done(t), 1);
+        mbar_init(s_free(t), 4);
+      }
+      mbar_init(drain, C::NMMA);
+      *abort_flag = 0;
+      fence_mbar_init();
     }
-    for (int t = 0; t < 2; ++t) {
-      mbar_init(s_full(t), 1);
-      mbar_init(p_ready(t), 4);
-      mbar_init(o_done(t), 1);
-      mbar_init(s_free(t), 4);
+    __syncwarp();
+    if (nmax > 0) {
+      if (elect_one()) {
+        prefetch_tmap(&tm_q);
+        prefetch_tmap(&tm_k);
+        prefetch_tmap(&tm_v);
+      }
+      const int nq = (n_t[1] > 0) ? 2 : 1;
+      if (elect_one()) mbar_arrive_expect_tx(q_full, nq * C::TILE_BYTES);
+      for (int t = 0; t < nq; ++t)
+        for (int s = 0; s < C::NSUB; ++s)
+          if (elect_one())
+            tma_load_3d(sbase + C::OFF_Q + t * C::TILE_BYTES + s * C::SUB_BYTES, &tm_q, s * 64, q0 + t * 128, bh,
+                        q_full);
+      for (int j = 0; j < n_pre; ++j) load_kv(j);
     }
-    mbar_init(drain, C::NMMA);
-    *abort_flag = 0;
-    fence_mbar_init();
   }
   if (warp == 9) {
     tmem_alloc(smem_u32(tmem_slot), C::TM_COLS);
@@ -131,28 +165,11 @@ __global__ void __launch_bounds__(352, 1)
 
   if (warp == 8) {
     // ------------------------------------------------------------ TMA producer
-    if (lane == 0 && nmax > 0) {
-      prefetch_tmap(&tm_q);
-      prefetch_tmap(&tm_k);
-      prefetch_tmap(&tm_v);
-      const int nq = (n_t[1] > 0) ? 2 : 1;
-      mbar_arrive_expect_tx(q_full, nq * C::TILE_BYTES);
-      for (int t = 0; t < nq; ++t)
-        for (int s = 0; s < C::NSUB; ++s)
-          tma_load_3d(sbase + C::OFF_Q + t * C::TILE_BYTES + s * C::SUB_BYTES, &tm_q, s * 64, q0 + t * 128, bh,
-                      q_full);
-      int issued = 0;
-      for (int j = 0; j < nmax; ++j) {
-        const int s = j % C::NST;
-        if (!wait_bounded(kv_empty(s), ((j / C::NST) & 1) ^ 1, st, SITE_F_KV_EMPTY)) break;
-        mbar_arrive_expect_tx(k_full(s), C::TILE_BYTES);
-        for (int c = 0; c < C::NSUB; ++c)
-          tma_load_3d(sbase + C::OFF_K + s * C::TILE_BYTES + c * C::SUB_BYTES, &tm_k, c * 64, j * 128, bh,
-                      k_full(s));
-        mbar_arrive_expect_tx(v_full(s), C::TILE_BYTES);
-        for (int c = 0; c < C::NSUB; ++c)
-          tma_load_3d(sbase + C::OFF_V + s * C::TILE_BYTES + c * C::SUB_BYTES, &tm_v, c * 64, j * 128, bh,
-                      v_full(s));
+    if (nmax > 0) {
+      int issued = n_pre;
+      for (int j = n_pre; j < nmax; ++j) {
+        if (!wait_warp(kv_empty(j % C::NST), ((j / C::NST) & 1) ^ 1, st, SITE_F_KV_EMPTY)) break;
+        load_kv(j);
         issued = j + 1;
       }
       if (*(volatile int*)abort_flag) {
@@ -413,7 +430,7 @@ __global__ void __launch_bounds__(352, 1)
           for (int c = 0; c < C::NSUB; ++c)
             tma_store_3d(&tm_o, smem_u32(stage + c * C::SUB_BYTES), c * 64, qs, bh);
           bulk_commit();
-          bulk_wait0();
+          bulk_wait_read0();  // the staging tile must outlive the copy's reads
         }
       }
     }
