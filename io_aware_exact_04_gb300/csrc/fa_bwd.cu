@@ -39,6 +39,8 @@ namespace fa {
 // per row, 16 B each.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(BwdArgs a, int BH) {
+  griddep_wait();
+  griddep_launch_dependents();
   constexpr int LPR = D / 8;          // lanes per row
   constexpr int RPW = 32 / LPR;       // rows per warp
   const int lane = threadIdx.x & 31;
@@ -80,6 +82,8 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(BwdArgs a, int BH) {
 
 template <int D>
 __global__ void __launch_bounds__(256) dq_convert_kernel(BwdArgs a, int BH) {
+  griddep_wait();
+  griddep_launch_dependents();
   const long long total = (long long)BH * a.N * (D / 8);
   for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
        idx += (long long)gridDim.x * blockDim.x) {
@@ -140,6 +144,8 @@ __global__ void __launch_bounds__(448, 1)
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
                const __grid_constant__ CUtensorMap tm_dqacc, BwdArgs a) {
+  griddep_wait();  // before any access to global memory
+  griddep_launch_dependents();
   using C = BwdCfg<D>;
   constexpr int BR = C::BR;
   extern __shared__ uint8_t smem_raw[];
@@ -567,6 +573,8 @@ __global__ void __launch_bounds__(480, 1)
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                    const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
                    const __grid_constant__ CUtensorMap tm_dqacc, BwdArgs a) {
+  griddep_wait();  // before any access to global memory
+  griddep_launch_dependents();
   using C = Bwd64;
   constexpr int BR = C::BR, NQS = C::NQS;
   extern __shared__ uint8_t smem_raw[];
@@ -996,8 +1004,7 @@ static int launch_bwd_pre_d(const BwdArgs& a, int BH, cudaStream_t stream) {
   const int rpw = 32 / (D / 8);
   const long long warps = (rows + rpw - 1) / rpw;
   const int blocks = (int)((warps + 7) / 8);
-  bwd_pre_kernel<D><<<blocks, 256, 0, stream>>>(a, BH);
-  return check_launch(__func__);
+  return launch_pdl(__func__, bwd_pre_kernel<D>, dim3(blocks), dim3(256), 0, stream, a, BH);
 }
 
 template <int D>
@@ -1024,7 +1031,8 @@ static int launch_bwd_main_d(const void* q, const void* k, const void* v, const 
       if (e != cudaSuccess) return cuda_fail("cudaFuncSetAttribute", (int)e, cudaGetErrorName(e));
       attr_set = true;
     }
-    bwd_kernel_d64<0><<<grid, Bwd64::THREADS, Bwd64::SMEM_BYTES, stream>>>(mq, mk, mv, mdo, mdk, mdv, mdq, a);
+    return launch_pdl(__func__, bwd_kernel_d64<0>, grid, dim3(Bwd64::THREADS), Bwd64::SMEM_BYTES, stream, mq, mk, mv,
+                      mdo, mdk, mdv, mdq, a);
   } else {
     using C = BwdCfg<D>;
     if (!attr_set) {
@@ -1033,9 +1041,9 @@ static int launch_bwd_main_d(const void* q, const void* k, const void* v, const 
       if (e != cudaSuccess) return cuda_fail("cudaFuncSetAttribute", (int)e, cudaGetErrorName(e));
       attr_set = true;
     }
-    bwd_kernel<D><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(mq, mk, mv, mdo, mdk, mdv, mdq, a);
+    return launch_pdl(__func__, bwd_kernel<D>, grid, dim3(C::THREADS), C::SMEM_BYTES, stream, mq, mk, mv, mdo, mdk,
+                      mdv, mdq, a);
   }
-  return check_launch(__func__);
 }
 
 template <int D>
@@ -1043,8 +1051,7 @@ static int launch_bwd_convert_d(const BwdArgs& a, int BH, cudaStream_t stream) {
   const long long total = (long long)BH * a.N * (D / 8);
   long long blocks = (total + 255) / 256;
   if (blocks > 152 * 16) blocks = 152 * 16;
-  dq_convert_kernel<D><<<(int)blocks, 256, 0, stream>>>(a, BH);
-  return check_launch(__func__);
+  return launch_pdl(__func__, dq_convert_kernel<D>, dim3((int)blocks), dim3(256), 0, stream, a, BH);
 }
 
 int launch_bwd_stage(int stage, const void* q, const void* k, const void* v, const BwdArgs& a, int BH, int d,

@@ -62,6 +62,8 @@ template <int D>
 __global__ void __launch_bounds__(352, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o, FwdArgs a) {
+  griddep_wait();  // before any access to global memory
+  griddep_launch_dependents();
   using C = FwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1024(smem_raw);
@@ -463,8 +465,7 @@ static int launch_fwd_d(const void* q, const void* k, const void* v, void* o, co
     attr_set = true;
   }
   dim3 grid(BH, args.n_pairs);
-  fwd_kernel<D><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(mq, mk, mv, mo, args);
-  return check_launch(__func__);
+  return launch_pdl(__func__, fwd_kernel<D>, grid, dim3(C::THREADS), C::SMEM_BYTES, stream, mq, mk, mv, mo, args);
 }
 
 int launch_fwd(const void* q, const void* k, const void* v, void* o, const FwdArgs& args, int BH, int d,

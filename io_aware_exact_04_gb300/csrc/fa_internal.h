@@ -43,6 +43,27 @@ void set_error_detail(const char* text);
 // After a launch: FA_OK, or FA_ERR_CUDA with the launch error recorded.
 int check_launch(const char* kernel);
 
+// Launches `kernel` with programmatic stream serialization (programmatic dependent launch): its
+// CTAs may start while the previous grid in the stream finishes, and wait for it in
+// griddep_wait() before touching global memory. Returns FA_OK or FA_ERR_CUDA.
+template <typename... Params, typename... Args>
+int launch_pdl(const char* name, void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+               Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+  if (e != cudaSuccess) return cuda_fail(name, (int)e, cudaGetErrorName(e));
+  return check_launch(name);
+}
+
 int launch_fwd(const void* q, const void* k, const void* v, void* o, const FwdArgs& args, int BH, int d,
                cudaStream_t stream);
 // stage 0: D, base-2 LSE, zeroed dQ accumulator; 1: main kernel (dK, dV, dQ accumulator);

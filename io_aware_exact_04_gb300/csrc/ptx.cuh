@@ -309,6 +309,16 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
   return r;
 }
+// Programmatic dependent launch. Every kernel of this library is launched with programmatic
+// stream serialization, so its CTAs may start while the previous grid in the stream is still
+// finishing; each thread calls griddep_wait() before its first access to global memory (it
+// returns once that grid has completed and its writes are visible, at once for a launch without
+// the attribute), and griddep_launch_dependents() lets the next grid begin launching.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // One lane of a converged warp (elect.sync). Issuing warps run their loops with the whole
 // warp, so that descriptors and TMEM addresses stay warp-uniform, and let one elected lane
 // execute each single-thread tcgen05 instruction: on sm_103a this issues MMAs faster than a
