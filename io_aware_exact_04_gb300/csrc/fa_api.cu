@@ -81,6 +81,26 @@ int cuda_fail(const char* where, int code, const char* what) {
   return FA_ERR_CUDA;
 }
 void set_error_detail(const char* text) { std::snprintf(g_last_error, sizeof(g_last_error), "%s", text); }
+bool sm_count(int* out) {
+  static int cache[64] = {0};  // benign race: every writer stores the same value
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail("cudaGetDevice", (int)e, cudaGetErrorName(e)) == FA_OK;
+  if (dev >= 0 && dev < 64 && cache[dev] > 0) {
+    *out = cache[dev];
+    return true;
+  }
+  int n = 0;
+  e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess || n <= 0) {
+    cuda_fail("cudaDeviceGetAttribute(MultiProcessorCount)", (int)e, cudaGetErrorName(e));
+    return false;
+  }
+  if (dev >= 0 && dev < 64) cache[dev] = n;
+  *out = n;
+  return true;
+}
+
 int check_launch(const char* kernel) {
   const cudaError_t e = cudaGetLastError();
   if (e == cudaSuccess) return FA_OK;

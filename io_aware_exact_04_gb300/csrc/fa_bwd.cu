@@ -540,32 +540,77 @@ __global__ void __launch_bounds__(448, 1)
 }
 
 // ---------------------------------------------------------------------------------------------
-// d = 64 backward with double-buffered S^T / dP^T: one CTA per 128-key tile, 64-query steps.
-// Warpgroup w (w = 0, 1) owns TMEM buffer w of S^T and dP^T and every step i with i % 2 == w,
-// so the tensor core forms S^T, dP^T of step i+1 while warpgroup (i % 2) turns step i into P^T
-// and dS^T. dQ is formed once per pair of steps (128 queries, M = 128) from a double-buffered
-// dS tile in shared memory.
+// d = 64 backward, persistent: G CTAs (one per SM) loop over the 128-key tiles of every head.
+// Tile t is key tile j = t / BH of head t % BH, so for causal attention the longest tiles come
+// first; CTA c takes tile r G + c in even rounds r and r G + G - 1 - c in odd ones. Within a
+// tile the 64-query steps are double-buffered: warpgroup w (w = 0, 1) owns TMEM buffer w of
+// S^T and dP^T and the steps of global index parity w, so the tensor core forms S^T, dP^T of
+// the next step while a warpgroup turns the current one into P^T and dS^T; dQ is formed per pair
+// of steps (128 queries, M = 128) from a double-buffered dS tile in shared memory. The global
+// step index runs on across tiles, so MMA issue flows from one tile into the next; K and V are
+// double-buffered, and the dV / dK epilogue (TMEM -> bf16 -> TMA store, then the accumulators
+// zeroed for the next tile) runs on the dQ epilogue warps while the warpgroups move on.
 struct Bwd64 {
-  static constexpr int D = 64, BR = 64, NQS = 4;   // queries per step, Q/dO ring depth
+  static constexpr int D = 64, BR = 64;           // queries per step
+  // Q/dO ring depth: four stages keep the copy of step g+2 clear of the readers of step g-1
+  // (three measured 40 % slower); the epilogue warps need one staging buffer.
+  static constexpr int NQS = 4;
+  static constexpr int NSTG = 1;
   static constexpr int KTILE = 128 * 128;          // K or V tile: [128 keys][64] bf16
   static constexpr int QTILE = BR * 128;           // Q_i or dO_i: [64 rows][64] bf16
   static constexpr int DS_BYTES = 128 * 128 * 2;   // dS of a pair: [128 keys][2 blocks of 64 queries]
-  static constexpr int DQ_CHUNK = 16384;           // [128 queries][32 dims] fp32
-  static constexpr int OFF_K = 0, OFF_V = KTILE;
-  static constexpr int OFF_Q = 2 * KTILE;                    // NQS stages
+  static constexpr int STG_BYTES = 16384;          // staging: [128][32] fp32 dQ, or [128][64] bf16 dV / dK
+  static constexpr int OFF_KV = 0;                           // 2 buffers, each K then V
+  static constexpr int OFF_Q = 4 * KTILE;                    // NQS stages
   static constexpr int OFF_DO = OFF_Q + NQS * QTILE;         // NQS stages
   static constexpr int OFF_DS = OFF_DO + NQS * QTILE;        // 2 buffers (even / odd pairs)
-  static constexpr int OFF_DQ = OFF_DS + 2 * DS_BYTES;       // 2 chunks
-  static constexpr int OFF_LSE = OFF_DQ + 2 * DQ_CHUNK;      // NQS x BR floats
+  static constexpr int OFF_STG = OFF_DS + 2 * DS_BYTES;
+  static constexpr int OFF_LSE = OFF_STG + NSTG * STG_BYTES; // NQS x BR floats
   static constexpr int OFF_DV = OFF_LSE + NQS * BR * 4;      // NQS x BR floats
   static constexpr int OFF_BAR = OFF_DV + NQS * BR * 4;
   static constexpr int SMEM_BYTES = OFF_BAR + 256 + 1024;
+  __host__ __device__ static constexpr int off_k(int b) { return OFF_KV + b * 2 * KTILE; }
+  __host__ __device__ static constexpr int off_v(int b) { return OFF_KV + b * 2 * KTILE + KTILE; }
   // TMEM: S^T buffer w at 64 w (P^T packed in its first 32 columns), dP^T buffer w at
   // 128 + 64 w (dS^T packed likewise), dV 256, dK 320, dQ buffer c at 384 + 64 c.
   static constexpr uint32_t TM_ST = 0, TM_DPT = 128, TM_DV = 256, TM_DK = 320, TM_DQ = 384;
   static constexpr uint32_t TM_COLS = 512;
   static constexpr int THREADS = 480;
 };
+static_assert(Bwd64::SMEM_BYTES <= 232448, "d = 64 backward: shared memory above the 227 KB per-CTA limit");
+static_assert(8 * (4 + 2 * Bwd64::NQS + 17) + 12 <= 256, "d = 64 backward: barrier area");
+
+// One key tile of the persistent schedule.
+struct TileD64 {
+  int bh, k0, kv, n_it, i_start;
+};
+__device__ __forceinline__ TileD64 tile_d64(int t, const BwdArgs& a) {
+  TileD64 r;
+  const int j = t / a.BH;
+  r.bh = t - j * a.BH;
+  r.kv = a.N;
+  if (a.kv_len) r.kv = min(max(a.kv_len[r.bh / a.H], 0), a.N);
+  r.k0 = j * 128;
+  const int n_qt = (a.N + Bwd64::BR - 1) / Bwd64::BR;
+  r.i_start = a.causal ? (r.k0 / Bwd64::BR) : 0;  // even: k0 is a multiple of 128
+  const int n = (r.k0 >= r.kv) ? 0 : (n_qt - r.i_start);
+  r.n_it = n + (n & 1);  // whole pairs: a trailing step past N reads zero Q/dO and -inf lse2, so adds nothing
+  return r;
+}
+// Tile of round r for CTA c of G, or -1 past the end (later rounds are past it too).
+__device__ __forceinline__ int sched_d64(int r, int c, int G, int T) {
+  const int t = r * G + ((r & 1) ? (G - 1 - c) : c);
+  return t < T ? t : -1;
+}
+// First tile with work at or after round r; returns its round, or -1.
+__device__ __forceinline__ int next_work_d64(int r, int c, int G, int T, const BwdArgs& a, TileD64& out) {
+  for (;; ++r) {
+    const int t = sched_d64(r, c, G, T);
+    if (t < 0) return -1;
+    out = tile_d64(t, a);
+    if (out.n_it > 0) return r;
+  }
+}
 
 template <int DUMMY>
 __global__ void __launch_bounds__(480, 1)
@@ -585,10 +630,11 @@ __global__ void __launch_bounds__(480, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::OFF_BAR);
   const uint32_t b0 = smem_u32(bars);
   auto BAR = [&](int i) { return b0 + 8u * i; };
-  const uint32_t kv_full = BAR(0);
-  auto qdo_full = [&](int s) { return BAR(1 + s); };
-  auto qdo_empty = [&](int s) { return BAR(1 + NQS + s); };
-  constexpr int nb = 1 + 2 * NQS;
+  auto kv_full = [&](int b) { return BAR(b); };
+  auto kv_empty = [&](int b) { return BAR(2 + b); };
+  auto qdo_full = [&](int s) { return BAR(4 + s); };
+  auto qdo_empty = [&](int s) { return BAR(4 + NQS + s); };
+  constexpr int nb = 4 + 2 * NQS;
   auto s_full = [&](int w) { return BAR(nb + w); };
   auto dp_full = [&](int w) { return BAR(nb + 2 + w); };
   auto p_ready = [&](int w) { return BAR(nb + 4 + w); };
@@ -596,56 +642,46 @@ __global__ void __launch_bounds__(480, 1)
   auto dq_full = [&](int c) { return BAR(nb + 8 + c); };
   auto dq_empty = [&](int c) { return BAR(nb + 10 + c); };
   auto dq_done = [&](int c) { return BAR(nb + 12 + c); };
-  const uint32_t final_bar = BAR(nb + 14);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C::OFF_BAR + 8 * (nb + 15));
+  const uint32_t tile_done = BAR(nb + 14);  // every MMA of a tile complete (one commit per issuing warp)
+  const uint32_t acc_free = BAR(nb + 15);   // dV / dK read out and zeroed (one arrival per epilogue warp)
+  const uint32_t final_bar = BAR(nb + 16);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C::OFF_BAR + 8 * (nb + 17));
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
   // number of dS^T steps warpgroup 0 has finished, times 4 (one add per warp)
   const uint32_t ds0_count = smem_u32(tmem_slot + 2);
   DevStatus st{a.status, abort_flag};
 
-  // blocks launch x-fastest: every head's longest causal key tile (j = 0) goes first
-  const int j = blockIdx.y;  // key tile
-  const int bh = blockIdx.x;
-  const int b = bh / a.H;
-  int kv = a.N;
-  if (a.kv_len) kv = min(max(a.kv_len[b], 0), a.N);
-  const int k0 = j * 128;
-  const int n_qt = (a.N + BR - 1) / BR;
-  const int i_start = a.causal ? (k0 / BR) : 0;  // even: k0 is a multiple of 128
-  int n_it = (k0 >= kv) ? 0 : (n_qt - i_start);
-  n_it += n_it & 1;  // whole pairs: a trailing step past N reads zero Q/dO and +inf LSE, so adds nothing
+  const int T = a.BH * ((a.N + 127) >> 7);
+  const int G = gridDim.x, cta = blockIdx.x;
 
-  if (n_it == 0) {
-    const int rows = min(128, a.N - k0);
-    for (int idx = threadIdx.x; idx < rows * (C::D / 8); idx += blockDim.x) {
-      const size_t off = ((size_t)bh * a.N + k0 + idx / (C::D / 8)) * C::D + (idx % (C::D / 8)) * 8;
-      *reinterpret_cast<uint4*>(a.dk + off) = make_uint4(0, 0, 0, 0);
-      *reinterpret_cast<uint4*>(a.dv + off) = make_uint4(0, 0, 0, 0);
-    }
-    return;
-  }
-
-  const float* lse2_h = a.lse2 + (size_t)bh * a.Npad;
-  const float* dvec_h = a.dvec + (size_t)bh * a.Npad;
   // The producer warp initialises the barriers and starts the first copies (K, V and the first
-  // NQS query steps, whose slots are free) before the CTA-wide setup, hiding their latency. It
-  // runs its code with the whole warp and lets one elected lane issue each copy.
-  const int n_pre = min(NQS, n_it);
-  auto load_qdo = [&](int it) {  // whole warp
-    const int s = it % NQS, i = i_start + it;
+  // NQS steps of this CTA's first tile, whose slots are free) before the CTA-wide setup, hiding
+  // their latency. It runs its code with the whole warp and lets one elected lane issue each copy.
+  auto load_kv = [&](int b, const TileD64& tl) {  // whole warp
+    if (elect_one()) mbar_arrive_expect_tx(kv_full(b), 2 * C::KTILE);
+    if (elect_one()) tma_load_3d(sbase + C::off_k(b), &tm_k, 0, tl.k0, tl.bh, kv_full(b));
+    if (elect_one()) tma_load_3d(sbase + C::off_v(b), &tm_v, 0, tl.k0, tl.bh, kv_full(b));
+    __syncwarp();
+  };
+  auto load_qdo = [&](int gs, const TileD64& tl, int it) {  // whole warp
+    const int s = gs % NQS, i = tl.i_start + it;
     const uint32_t bar = qdo_full(s);
-    const float* lsrc = lse2_h + (size_t)i * BR;
-    const float* dsrc = dvec_h + (size_t)i * BR;
+    const float* lsrc = a.lse2 + (size_t)tl.bh * a.Npad + (size_t)i * BR;
+    const float* dsrc = a.dvec + (size_t)tl.bh * a.Npad + (size_t)i * BR;
     if (elect_one()) mbar_arrive_expect_tx(bar, 2 * C::QTILE + 2 * BR * 4);
-    if (elect_one()) tma_load_3d(sbase + C::OFF_Q + s * C::QTILE, &tm_q, 0, i * BR, bh, bar);
-    if (elect_one()) tma_load_3d(sbase + C::OFF_DO + s * C::QTILE, &tm_do, 0, i * BR, bh, bar);
+    if (elect_one()) tma_load_3d(sbase + C::OFF_Q + s * C::QTILE, &tm_q, 0, i * BR, tl.bh, bar);
+    if (elect_one()) tma_load_3d(sbase + C::OFF_DO + s * C::QTILE, &tm_do, 0, i * BR, tl.bh, bar);
     if (elect_one()) bulk_load(sbase + C::OFF_LSE + s * BR * 4, lsrc, BR * 4, bar);
     if (elect_one()) bulk_load(sbase + C::OFF_DV + s * BR * 4, dsrc, BR * 4, bar);
     __syncwarp();
   };
+  int pre_steps = 0;  // steps of the first tile issued before the setup
   if (warp == 12) {
     if (lane == 0) {
-      mbar_init(kv_full, 1);
+      for (int b = 0; b < 2; ++b) {
+        mbar_init(kv_full(b), 1);
+        mbar_init(kv_empty(b), 2);  // one commit per MMA-issuing warp
+      }
       for (int s = 0; s < NQS; ++s) {
         mbar_init(qdo_full(s), 1);
         mbar_init(qdo_empty(s), 1);
@@ -659,20 +695,24 @@ __global__ void __launch_bounds__(480, 1)
         mbar_init(dq_empty(w), 4);
         mbar_init(dq_done(w), 1);
       }
-      mbar_init(final_bar, 2);  // one commit per MMA-issuing warp
+      mbar_init(tile_done, 2);
+      mbar_init(acc_free, 4);
+      mbar_init(final_bar, 2);
       *abort_flag = 0;
       tmem_slot[2] = 0;
       fence_mbar_init();
     }
     __syncwarp();
-    if (elect_one()) {
-      prefetch_tmap(&tm_q);
-      prefetch_tmap(&tm_do);
+    TileD64 tl;
+    if (next_work_d64(0, cta, G, T, a, tl) >= 0) {
+      if (elect_one()) {
+        prefetch_tmap(&tm_q);
+        prefetch_tmap(&tm_do);
+      }
+      load_kv(0, tl);
+      pre_steps = min(NQS, tl.n_it);
+      for (int it = 0; it < pre_steps; ++it) load_qdo(it, tl, it);
     }
-    if (elect_one()) mbar_arrive_expect_tx(kv_full, 2 * C::KTILE);
-    if (elect_one()) tma_load_3d(sbase + C::OFF_K, &tm_k, 0, k0, bh, kv_full);
-    if (elect_one()) tma_load_3d(sbase + C::OFF_V, &tm_v, 0, k0, bh, kv_full);
-    for (int it = 0; it < n_pre; ++it) load_qdo(it);
   }
   if (warp == 13) {
     tmem_alloc(smem_u32(tmem_slot), C::TM_COLS);
@@ -683,8 +723,8 @@ __global__ void __launch_bounds__(480, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   if (warp < 8) {
-    // dV (warpgroup 0) and dK (warpgroup 1) start at zero: the two MMA-issuing
-    // threads then always accumulate, whichever of them reaches a tile first
+    // dV (warpgroup 0) and dK (warpgroup 1) start at zero: the two MMA-issuing warps then
+    // always accumulate, whichever reaches a tile first (the epilogue zeroes them per tile)
     uint32_t z[32];
 #pragma unroll
     for (int i = 0; i < 32; ++i) z[i] = 0;
@@ -699,95 +739,125 @@ __global__ void __launch_bounds__(480, 1)
 
   if (warp == 12) {
     // ------------------------------------------------------------ TMA producer
-    {
-      int issued = n_pre;
-      for (int it = n_pre; it < n_it; ++it) {
-        if (!wait_warp(qdo_empty(it % NQS), ((it / NQS) & 1) ^ 1, st, SITE_B_QDO_EMPTY)) break;
-        load_qdo(it);
-        issued = it + 1;
+    int gs0 = 0, tu = 0, issued = 0, kv_loads = 0;
+    bool ok = true;
+    TileD64 tl;
+    for (int r = next_work_d64(0, cta, G, T, a, tl); ok && r >= 0; r = next_work_d64(r + 1, cta, G, T, a, tl)) {
+      const int b = tu & 1;
+      if (tu > 0) {  // the first tile's K and V went out before the setup
+        if (!(ok = wait_warp(kv_empty(b), ((tu >> 1) & 1) ^ 1, st, SITE_B_QDO_EMPTY))) break;
+        load_kv(b, tl);
       }
-      if (*(volatile int*)abort_flag) {
-        const uint64_t t0 = globaltimer_ns();
-        while (!mbar_try_wait(kv_full, 0) && globaltimer_ns() - t0 < 100000000ull) {
+      ++kv_loads;
+      for (int it = (tu == 0 ? pre_steps : 0); it < tl.n_it; ++it) {
+        const int gs = gs0 + it;
+        if (!(ok = wait_warp(qdo_empty(gs % NQS), ((gs / NQS) & 1) ^ 1, st, SITE_B_QDO_EMPTY))) break;
+        load_qdo(gs, tl, it);
+      }
+      gs0 += tl.n_it;
+      issued = gs0;
+      ++tu;
+    }
+    if (*(volatile int*)abort_flag) {
+      // let copies already in flight land before the CTA's smem is released
+      const uint64_t t0 = globaltimer_ns();
+      for (int u = max(0, kv_loads - 2); u < kv_loads; ++u)
+        while (!mbar_try_wait(kv_full(u & 1), (u >> 1) & 1) && globaltimer_ns() - t0 < 100000000ull) {
         }
-        for (int it = max(0, issued - NQS); it < issued; ++it)
-          while (!mbar_try_wait(qdo_full(it % NQS), (it / NQS) & 1) && globaltimer_ns() - t0 < 100000000ull) {
-          }
-      }
+      for (int gs = max(0, issued - NQS); gs < issued; ++gs)
+        while (!mbar_try_wait(qdo_full(gs % NQS), (gs / NQS) & 1) && globaltimer_ns() - t0 < 100000000ull) {
+        }
     }
   } else if (warp == 13 || warp == 14) {
     // ------------------------------------------------------------ MMA issuers: warp 13 serves
-    // warpgroup 0 (even steps), warp 14 warpgroup 1 (odd steps) and forms dQ. The whole warp
-    // runs the loop; one elected lane issues each MMA and commit.
-    {
-      const int w = warp - 13;
-      constexpr uint32_t IDESC_S = idesc_bf16_f32(128, BR, 0, 0);  // K (V) x Q_i (dO_i), K-major
-      constexpr uint32_t IDESC_G = idesc_bf16_f32(128, 64, 0, 1);  // TMEM A x MN-major B
-      constexpr uint32_t IDESC_Q = idesc_bf16_f32(128, 64, 1, 1);  // dS x K, both MN-major
-      constexpr uint32_t HI = sdesc_hi(1024);
-      constexpr uint32_t QT16 = C::QTILE >> 4;
-      const uint32_t k_lo = sdesc_lo(sbase + C::OFF_K, 16), v_lo = sdesc_lo(sbase + C::OFF_V, 16);
-      const uint32_t q_lo = sdesc_lo(sbase + C::OFF_Q, 16), do_lo = sdesc_lo(sbase + C::OFF_DO, 16);
-      const uint32_t qmn_lo = sdesc_lo(sbase + C::OFF_Q, C::QTILE), domn_lo = sdesc_lo(sbase + C::OFF_DO, C::QTILE);
-      const uint32_t ds_lo = sdesc_lo(sbase + C::OFF_DS, 128 * 128), kmn_lo = sdesc_lo(sbase + C::OFF_K, C::KTILE);
-      auto commit = [&](uint32_t bar) {
-        if (elect_one()) mma_commit(bar);
-        __syncwarp();
-      };
-      auto issue_s = [&](int it) {  // S^T of step it into buffer it % 2
-        const uint32_t so = (it % NQS) * QT16;
+    // warpgroup 0 (even global steps), warp 14 warpgroup 1 (odd steps) and forms dQ. The whole
+    // warp runs the loop; one elected lane issues each MMA and commit.
+    const int w = warp - 13;
+    constexpr uint32_t IDESC_S = idesc_bf16_f32(128, BR, 0, 0);  // K (V) x Q_i (dO_i), K-major
+    constexpr uint32_t IDESC_G = idesc_bf16_f32(128, 64, 0, 1);  // TMEM A x MN-major B
+    constexpr uint32_t IDESC_Q = idesc_bf16_f32(128, 64, 1, 1);  // dS x K, both MN-major
+    constexpr uint32_t HI = sdesc_hi(1024);
+    constexpr uint32_t QT16 = C::QTILE >> 4;
+    const uint32_t q_lo = sdesc_lo(sbase + C::OFF_Q, 16), do_lo = sdesc_lo(sbase + C::OFF_DO, 16);
+    const uint32_t qmn_lo = sdesc_lo(sbase + C::OFF_Q, C::QTILE), domn_lo = sdesc_lo(sbase + C::OFF_DO, C::QTILE);
+    const uint32_t ds_lo = sdesc_lo(sbase + C::OFF_DS, 128 * 128);
+    auto k_lo = [&](int b) { return sdesc_lo(sbase + C::off_k(b), 16); };
+    auto v_lo = [&](int b) { return sdesc_lo(sbase + C::off_v(b), 16); };
+    auto kmn_lo = [&](int b) { return sdesc_lo(sbase + C::off_k(b), C::KTILE); };
+    auto commit = [&](uint32_t bar) {
+      if (elect_one()) mma_commit(bar);
+      __syncwarp();
+    };
+    auto issue_s = [&](int gs, int b) {  // S^T of global step gs into buffer gs % 2
+      const uint32_t so = (gs % NQS) * QT16, kl = k_lo(b);
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-          if (elect_one())
-            mma_ss(tmem + C::TM_ST + 64 * (it & 1), sdesc_join(k_lo + 2 * k, HI), sdesc_join(q_lo + so + 2 * k, HI),
-                   IDESC_S, k > 0);
-        commit(s_full(it & 1));
-      };
-      auto issue_dp = [&](int it) {  // dP^T of step it into buffer it % 2
-        const uint32_t so = (it % NQS) * QT16;
+      for (int k = 0; k < 4; ++k)
+        if (elect_one())
+          mma_ss(tmem + C::TM_ST + 64 * (gs & 1), sdesc_join(kl + 2 * k, HI), sdesc_join(q_lo + so + 2 * k, HI),
+                 IDESC_S, k > 0);
+      commit(s_full(gs & 1));
+    };
+    auto issue_dp = [&](int gs, int b) {  // dP^T of global step gs into buffer gs % 2
+      const uint32_t so = (gs % NQS) * QT16, vl = v_lo(b);
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-          if (elect_one())
-            mma_ss(tmem + C::TM_DPT + 64 * (it & 1), sdesc_join(v_lo + 2 * k, HI),
-                   sdesc_join(do_lo + so + 2 * k, HI), IDESC_S, k > 0);
-        commit(dp_full(it & 1));
-      };
-      // dV (dK) += P^T (dS^T) [128 keys x 64 queries, TMEM] x dO_i (Q_i) [64 queries x 64 dims]
-      auto issue_grad = [&](uint32_t dst, uint32_t a_tm, uint32_t b_lo, uint32_t acc) {
+      for (int k = 0; k < 4; ++k)
+        if (elect_one())
+          mma_ss(tmem + C::TM_DPT + 64 * (gs & 1), sdesc_join(vl + 2 * k, HI), sdesc_join(do_lo + so + 2 * k, HI),
+                 IDESC_S, k > 0);
+      commit(dp_full(gs & 1));
+    };
+    // dV (dK) += P^T (dS^T) [128 keys x 64 queries, TMEM] x dO_i (Q_i) [64 queries x 64 dims]
+    auto issue_grad = [&](uint32_t dst, uint32_t a_tm, uint32_t b_lo) {
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-          if (elect_one())
-            mma_ts(tmem + dst, tmem + a_tm + 8 * k, sdesc_join(b_lo + k * (2048 >> 4), HI), IDESC_G, (acc | k) != 0);
-      };
-      // This thread's first step starts its buffers. Afterwards S^T(i+2) follows dV(i) as
-      // soon as the warpgroup has P^T(i) (it keeps P in registers for dS, so S^T's
-      // columns are free), and dP^T(i+2) follows dK(i) once dS^T(i) is written.
-      bool ok = wait_warp(kv_full, 0, st, SITE_B_KV_FULL) && wait_warp(qdo_full(w), 0, st, SITE_B_QDO_FULL);
+      for (int k = 0; k < 4; ++k)
+        if (elect_one())
+          mma_ts(tmem + dst, tmem + a_tm + 8 * k, sdesc_join(b_lo + k * (2048 >> 4), HI), IDESC_G, 1);
+    };
+    // This warp's first step starts its buffers. Afterwards S^T(g+2) follows dV(g) as soon as the
+    // warpgroup has P^T(g) (it keeps P in registers for dS, so S^T's columns are free), and
+    // dP^T(g+2) follows dK(g) once dS^T(g) is written; step g+2 may belong to the next tile.
+    bool ok = true;
+    int gs0 = 0, tu = 0;
+    TileD64 cur, nxt;
+    int r = next_work_d64(0, cta, G, T, a, cur);
+    if (r >= 0) {
+      ok = wait_warp(kv_full(0), 0, st, SITE_B_KV_FULL) && wait_warp(qdo_full(w), 0, st, SITE_B_QDO_FULL);
       if (ok) {
         tc_fence_after();
-        issue_s(w);
-        issue_dp(w);
+        issue_s(w, 0);
+        issue_dp(w, 0);
       }
-      for (int it = w; ok && it < n_it; it += 2) {
-        const uint32_t par = (it >> 1) & 1;
-        const uint32_t so = (it % NQS) * QT16;
-        const bool more = it + 2 < n_it;
+    }
+    while (ok && r >= 0) {
+      const int b = tu & 1;
+      const int r2 = next_work_d64(r + 1, cta, G, T, a, nxt);
+      for (int it = w; ok && it < cur.n_it; it += 2) {
+        const int gs = gs0 + it;
+        const uint32_t par = (gs >> 1) & 1;
+        const uint32_t so = (gs % NQS) * QT16;
+        const bool in_tile = it + 2 < cur.n_it;
+        const bool succ = in_tile || r2 >= 0;
+        const int b2 = in_tile ? b : (b ^ 1);
         if (!(ok = wait_warp(p_ready(w), par, st, SITE_B_P_READY))) break;
+        if (it == w && tu > 0) {  // the epilogue has read and zeroed the previous tile's dV, dK
+          if (!(ok = wait_warp(acc_free, (tu - 1) & 1, st, SITE_B_FINAL))) break;
+        }
         tc_fence_after();
-        issue_grad(C::TM_DV, C::TM_ST + 64 * w, domn_lo + so, 1);
-        if (more) {
-          if (!(ok = wait_warp(qdo_full((it + 2) % NQS), ((it + 2) / NQS) & 1, st, SITE_B_QDO_FULL))) break;
+        issue_grad(C::TM_DV, C::TM_ST + 64 * w, domn_lo + so);
+        if (succ) {
+          if (!in_tile && !(ok = wait_warp(kv_full(b2), ((tu + 1) >> 1) & 1, st, SITE_B_KV_FULL))) break;
+          if (!(ok = wait_warp(qdo_full((gs + 2) % NQS), ((gs + 2) / NQS) & 1, st, SITE_B_QDO_FULL))) break;
           tc_fence_after();
-          issue_s(it + 2);
+          issue_s(gs + 2, b2);
         }
         if (!(ok = wait_warp(ds_ready(w), par, st, SITE_B_DS_READY))) break;
         tc_fence_after();
-        issue_grad(C::TM_DK, C::TM_DPT + 64 * w, qmn_lo + so, 1);
-        commit(qdo_empty(it % NQS));  // last readers of Q_i and dO_i issued
-        if (more) issue_dp(it + 2);
-        if (w == 1) {  // the pair (it-1, it) is complete once warpgroup 0's dS of step it-1 is in smem
-          const int p = it >> 1, c = p & 1;
-          const uint32_t need = 4u * (uint32_t)(p + 1);
+        issue_grad(C::TM_DK, C::TM_DPT + 64 * w, qmn_lo + so);
+        commit(qdo_empty(gs % NQS));  // last readers of Q_i and dO_i issued
+        if (succ) issue_dp(gs + 2, b2);
+        if (w == 1) {  // the pair (gs-1, gs) is complete once warpgroup 0's dS of step gs-1 is in smem
+          const int pg = gs >> 1, c = pg & 1;
+          const uint32_t need = 4u * (uint32_t)(pg + 1);
           if (lane == 0) {
             const uint64_t t0 = globaltimer_ns();
             while (smem_ld_acquire(ds0_count) < need) {
@@ -804,189 +874,243 @@ __global__ void __launch_bounds__(480, 1)
             }
           }
           if (!(ok = __all_sync(0xffffffffu, ok))) break;
-          if (!(ok = wait_warp(dq_empty(c), ((p >> 1) & 1) ^ 1, st, SITE_B_DQ_EMPTY))) break;
+          if (!(ok = wait_warp(dq_empty(c), ((pg >> 1) & 1) ^ 1, st, SITE_B_DQ_EMPTY))) break;
           tc_fence_after();
-          const uint32_t dsb = ds_lo + c * (C::DS_BYTES >> 4);
+          const uint32_t dsb = ds_lo + c * (C::DS_BYTES >> 4), kb = kmn_lo(b);
 #pragma unroll
           for (int k = 0; k < 8; ++k)  // 128 keys
             if (elect_one())
               mma_ss(tmem + C::TM_DQ + 64 * c, sdesc_join(dsb + k * (2048 >> 4), HI),
-                     sdesc_join(kmn_lo + k * (2048 >> 4), HI), IDESC_Q, k > 0);
+                     sdesc_join(kb + k * (2048 >> 4), HI), IDESC_Q, k > 0);
           commit(dq_full(c));
           commit(dq_done(c));
         }
       }
-      commit(final_bar);  // also the drain: completes after every MMA issued above
-      const uint64_t t0 = globaltimer_ns();
-      while (!mbar_try_wait(final_bar, 0) && globaltimer_ns() - t0 < kWaitLimitNs) {
-      }
+      if (!ok) break;
+      commit(tile_done);    // every MMA of this tile issued by this warp
+      commit(kv_empty(b));  // ... and with them the last readers of this tile's K and V
+      gs0 += cur.n_it;
+      ++tu;
+      cur = nxt;
+      r = r2;
+    }
+    commit(final_bar);  // also the drain: completes after every MMA issued above
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(final_bar, 0) && globaltimer_ns() - t0 < kWaitLimitNs) {
     }
   } else if (warp >= 8) {
-    // ------------------------------------------------------------ dQ epilogue (one pair = 128 queries)
+    // ------------------------------------------------------------ epilogue warps: dQ of each pair
+    // (reduced into the fp32 accumulator), then each tile's dV and dK
     const int wq = warp & 3;
-    const int r = wq * 32 + lane;  // TMEM lane: query row within the pair
+    const int r = wq * 32 + lane;  // TMEM lane
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
     const int tid = threadIdx.x - 256;
     const float sc = a.scale;
-    for (int p = 0; p < n_it / 2; ++p) {
-      const int c = p & 1;
-      if (!named_bar_and(3, 128, wait_warp(dq_full(c), (p >> 1) & 1, st, SITE_B_DQ_FULL))) break;
+    // Staging buffers are used in strict rotation (dQ halves, then a tile's dV and dK); before
+    // writing one, the copy that last read it (NSTG copies back) must have finished reading.
+    int ng = 0;
+    auto stage_acquire = [&]() -> uint8_t* {
+      if (tid == 0) {
+        if (C::NSTG == 1)
+          bulk_wait_read0();
+        else
+          asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+      }
+      named_bar_sync(3, 128);
+      return sm + C::OFF_STG + (ng++ % C::NSTG) * C::STG_BYTES;
+    };
+    bool ok = true;
+    int gs0 = 0, tu = 0;
+    for (int rr = 0; ok; ++rr) {
+      const int t = sched_d64(rr, cta, G, T);
+      if (t < 0) break;
+      const TileD64 tl = tile_d64(t, a);
+      if (tl.n_it == 0) {  // no valid key in this tile: its dK and dV rows are zero
+        const int rows = min(128, a.N - tl.k0);
+        for (int idx = tid; idx < rows * (C::D / 8); idx += 128) {
+          const size_t off = ((size_t)tl.bh * a.N + tl.k0 + idx / (C::D / 8)) * C::D + (idx % (C::D / 8)) * 8;
+          *reinterpret_cast<uint4*>(a.dk + off) = make_uint4(0, 0, 0, 0);
+          *reinterpret_cast<uint4*>(a.dv + off) = make_uint4(0, 0, 0, 0);
+        }
+        continue;
+      }
+      for (int p = 0; p < tl.n_it / 2; ++p) {
+        const int pg = (gs0 >> 1) + p, c = pg & 1;
+        if (!(ok = named_bar_and(3, 128, wait_warp(dq_full(c), (pg >> 1) & 1, st, SITE_B_DQ_FULL)))) break;
+        tc_fence_after();
+        uint32_t v[2][32];
+        tmem_ld32(tmem + lane_off + C::TM_DQ + 64 * c, v[0]);
+        tmem_ld32(tmem + lane_off + C::TM_DQ + 64 * c + 32, v[1]);
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(dq_empty(c));
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint8_t* stg = stage_acquire();
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const float4 x = make_float4(__uint_as_float(v[h][4 * k]) * sc, __uint_as_float(v[h][4 * k + 1]) * sc,
+                                         __uint_as_float(v[h][4 * k + 2]) * sc, __uint_as_float(v[h][4 * k + 3]) * sc);
+            *reinterpret_cast<float4*>(stg + sw128_offset(r, k)) = x;
+          }
+          fence_proxy_async_smem();
+          named_bar_sync(3, 128);
+          if (tid == 0) {
+            tma_reduce_add_3d(&tm_dqacc, smem_u32(stg), h * 32, (tl.i_start + 2 * p) * BR, tl.bh);
+            bulk_commit();
+          }
+        }
+      }
+      if (!ok) break;
+      // ---- this tile's dV and s * dK: TMEM -> bf16 -> staging -> TMA store; then zero both
+      if (!(ok = named_bar_and(3, 128, wait_warp(tile_done, tu & 1, st, SITE_B_FINAL)))) break;
       tc_fence_after();
-      uint32_t v[2][32];
-      tmem_ld32(tmem + lane_off + C::TM_DQ + 64 * c, v[0]);
-      tmem_ld32(tmem + lane_off + C::TM_DQ + 64 * c + 32, v[1]);
-      tmem_wait_ld();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(dq_empty(c));
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        // the reduce issued from this chunk buffer one chunk ago has finished reading it
-        if (tid == 0) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
-        named_bar_sync(3, 128);
-        uint8_t* stg = sm + C::OFF_DQ + h * C::DQ_CHUNK;
+      for (int g = 0; g < 2; ++g) {
+        uint32_t x[2][32];
+        tmem_ld32(tmem + lane_off + (g == 0 ? C::TM_DV : C::TM_DK), x[0]);
+        tmem_ld32(tmem + lane_off + (g == 0 ? C::TM_DV : C::TM_DK) + 32, x[1]);
+        tmem_wait_ld();
+        const float mul = g == 0 ? 1.f : sc;
+        uint8_t* stg = stage_acquire();
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const float4 x = make_float4(__uint_as_float(v[h][4 * k]) * sc, __uint_as_float(v[h][4 * k + 1]) * sc,
-                                       __uint_as_float(v[h][4 * k + 2]) * sc, __uint_as_float(v[h][4 * k + 3]) * sc);
-          *reinterpret_cast<float4*>(stg + sw128_offset(r, k)) = x;
+        for (int q = 0; q < 8; ++q) {
+          const uint32_t* xs = &x[q >> 2][(q & 3) * 8];
+          uint4 vv;
+          vv.x = pack_bf16x2(__uint_as_float(xs[0]) * mul, __uint_as_float(xs[1]) * mul);
+          vv.y = pack_bf16x2(__uint_as_float(xs[2]) * mul, __uint_as_float(xs[3]) * mul);
+          vv.z = pack_bf16x2(__uint_as_float(xs[4]) * mul, __uint_as_float(xs[5]) * mul);
+          vv.w = pack_bf16x2(__uint_as_float(xs[6]) * mul, __uint_as_float(xs[7]) * mul);
+          *reinterpret_cast<uint4*>(stg + sw128_offset(r, q)) = vv;
         }
         fence_proxy_async_smem();
         named_bar_sync(3, 128);
         if (tid == 0) {
-          tma_reduce_add_3d(&tm_dqacc, smem_u32(stg), h * 32, (i_start + 2 * p) * BR, bh);
+          tma_store_3d(g == 0 ? &tm_dv : &tm_dk, smem_u32(stg), 0, tl.k0, tl.bh);
           bulk_commit();
         }
       }
+      {
+        uint32_t z[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) z[i] = 0;
+        tmem_st32(tmem + lane_off + C::TM_DV, z);
+        tmem_st32(tmem + lane_off + C::TM_DV + 32, z);
+        tmem_st32(tmem + lane_off + C::TM_DK, z);
+        tmem_st32(tmem + lane_off + C::TM_DK + 32, z);
+        tmem_wait_st();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acc_free);
+      gs0 += tl.n_it;
+      ++tu;
     }
-    if (tid == 0) bulk_wait_read0();
+    if (tid == 0) bulk_wait_read0();  // the staging buffer must outlive the copies' reads
   } else {
     // ------------------------------------------------------------ P^T / dS^T warpgroups
-    const int w = warp >> 2;       // this warpgroup's steps: it % 2 == w
+    const int w = warp >> 2;       // this warpgroup's steps: global index % 2 == w
     const int wq = warp & 3;
     const int r = wq * 32 + lane;  // key within the tile (TMEM lane)
-    const int key = k0 + r;
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
     const float sl2 = a.scale_log2;
     const uint64_t sl2x2 = f2_pack(sl2, sl2);
     const uint32_t tST = tmem + lane_off + C::TM_ST + 64 * w, tDPT = tmem + lane_off + C::TM_DPT + 64 * w;
     bool ok = true;
-    for (int it = w; it < n_it; it += 2) {
-      const int s = it % NQS;
-      const uint32_t par = (it >> 1) & 1;
-      const int q0 = (i_start + it) * BR;
-      const float* lse_s = reinterpret_cast<const float*>(sm + C::OFF_LSE + s * BR * 4);
-      const float* dv_s = reinterpret_cast<const float*>(sm + C::OFF_DV + s * BR * 4);
-      if (!(ok = wait_warp(qdo_full(s), (it / NQS) & 1, st, SITE_B_QDO_FULL))) break;
-      if (!(ok = wait_warp(s_full(w), par, st, SITE_B_S_FULL))) break;
-      tc_fence_after();
-      const bool need_mask = (k0 + 127 >= kv) || (a.causal && k0 + 127 > q0);
-      // ---- P^T = exp2(S^T s log2e + lse2) (lse2 = -LSE log2e) -> bf16 pairs in the first 32
-      //      columns of this buffer, kept in registers too: S^T's columns are overwritten by
-      //      the next step once P^T is out
-      // Both 32-column halves are loaded before one wait, so the TMEM load latency is paid once.
-      uint32_t pkeep[32];
-      {
-        uint32_t sv[2][32];
-        tmem_ld32(tST, sv[0]);
-        tmem_ld32(tST + 32, sv[1]);
-        tmem_wait_ld();
-        if (need_mask) {  // only steps on the diagonal or past kv_len: masked S -> -inf, so P = 0
-          const int lim = key >= kv ? 64 : (a.causal ? key - q0 : 0);  // columns [0, lim)
+    int gs0 = 0;
+    TileD64 tl;
+    for (int rr = next_work_d64(0, cta, G, T, a, tl); ok && rr >= 0; rr = next_work_d64(rr + 1, cta, G, T, a, tl)) {
+      const int key = tl.k0 + r;
+      for (int it = w; it < tl.n_it; it += 2) {
+        const int gs = gs0 + it;
+        const int s = gs % NQS;
+        const uint32_t par = (gs >> 1) & 1;
+        const int q0 = (tl.i_start + it) * BR;
+        const float* lse_s = reinterpret_cast<const float*>(sm + C::OFF_LSE + s * BR * 4);
+        const float* dv_s = reinterpret_cast<const float*>(sm + C::OFF_DV + s * BR * 4);
+        if (!(ok = wait_warp(qdo_full(s), (gs / NQS) & 1, st, SITE_B_QDO_FULL))) break;
+        if (!(ok = wait_warp(s_full(w), par, st, SITE_B_S_FULL))) break;
+        tc_fence_after();
+        const bool need_mask = (tl.k0 + 127 >= tl.kv) || (a.causal && tl.k0 + 127 > q0);
+        // ---- P^T = exp2(S^T s log2e + lse2) (lse2 = -LSE log2e) -> bf16 pairs in the first 32
+        //      columns of this buffer, kept in registers too: S^T's columns are overwritten by
+        //      the next step once P^T is out
+        // Both 32-column halves are loaded before one wait, so the TMEM load latency is paid once.
+        uint32_t pkeep[32];
+        {
+          uint32_t sv[2][32];
+          tmem_ld32(tST, sv[0]);
+          tmem_ld32(tST + 32, sv[1]);
+          tmem_wait_ld();
+          if (need_mask) {  // only steps on the diagonal or past kv_len: masked S -> -inf, so P = 0
+            const int lim = key >= tl.kv ? 64 : (a.causal ? key - q0 : 0);  // columns [0, lim)
 #pragma unroll
-          for (int c = 0; c < 64; ++c)
-            if (c < lim) sv[c >> 5][c & 31] = 0xff800000u;
-        }
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          // lse2 of the 64 queries: 16-byte broadcast loads (one shared-memory wavefront each)
-          const float4 l4 = reinterpret_cast<const float4*>(lse_s)[e >> 1];
-          float x0, x1;
-          const uint32_t* se = &sv[e >> 4][(2 * e) & 31];
-          const uint64_t s2 = f2_pack(__uint_as_float(se[0]), __uint_as_float(se[1]));
-          f2_unpack(f2_fma(s2, sl2x2, (e & 1) ? f2_pack(l4.z, l4.w) : f2_pack(l4.x, l4.y)), x0, x1);
-          pkeep[e] = pack_bf16x2(ex2_approx(x0), ex2_approx(x1));
-        }
-        tmem_st32(tST, pkeep);
-      }
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(p_ready(w));
-      // ---- dS^T = P^T * (dP^T + dvec) -> bf16 pairs in this dP^T buffer and into the pair's dS tile
-      if (!(ok = wait_warp(dp_full(w), par, st, SITE_B_DP_FULL))) break;
-      tc_fence_after();
-      uint8_t* dsb = sm + C::OFF_DS + ((it >> 1) & 1) * C::DS_BYTES + w * (128 * 128);
-      if (w == 0 && it >= 4) {  // dQ of the pair that last used this dS tile has read it
-        const int pp2 = (it >> 1) - 2;
-        if (!(ok = wait_warp(dq_done(pp2 & 1), (pp2 >> 1) & 1, st, SITE_B_DQ_EMPTY))) break;
-      }
-      {
-        uint32_t dp[2][32];
-        tmem_ld32(tDPT, dp[0]);
-        tmem_ld32(tDPT + 32, dp[1]);
-        tmem_wait_ld();
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          uint32_t pk[16];
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const int g = 16 * h + e;
-            const float4 d4 = reinterpret_cast<const float4*>(dv_s)[g >> 1];
-            const float2 d2 = (g & 1) ? make_float2(d4.z, d4.w) : make_float2(d4.x, d4.y);
-            const float p0 = __uint_as_float(pkeep[g] << 16), p1 = __uint_as_float(pkeep[g] & 0xFFFF0000u);
-            const uint64_t t2 =
-                f2_add(f2_pack(__uint_as_float(dp[h][2 * e]), __uint_as_float(dp[h][2 * e + 1])), f2_pack(d2.x, d2.y));
-            float d0, d1;
-            f2_unpack(f2_mul(t2, f2_pack(p0, p1)), d0, d1);
-            pk[e] = pack_bf16x2(d0, d1);
+            for (int c = 0; c < 64; ++c)
+              if (c < lim) sv[c >> 5][c & 31] = 0xff800000u;
           }
-          tmem_st16(tDPT + 16 * h, pk);
 #pragma unroll
-          for (int q = 0; q < 4; ++q)
-            *reinterpret_cast<uint4*>(dsb + sw128_offset(r, 4 * h + q)) =
-                make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+          for (int e = 0; e < 32; ++e) {
+            // lse2 of the 64 queries: 16-byte broadcast loads (one shared-memory wavefront each)
+            const float4 l4 = reinterpret_cast<const float4*>(lse_s)[e >> 1];
+            float x0, x1;
+            const uint32_t* se = &sv[e >> 4][(2 * e) & 31];
+            const uint64_t s2 = f2_pack(__uint_as_float(se[0]), __uint_as_float(se[1]));
+            f2_unpack(f2_fma(s2, sl2x2, (e & 1) ? f2_pack(l4.z, l4.w) : f2_pack(l4.x, l4.y)), x0, x1);
+            pkeep[e] = pack_bf16x2(ex2_approx(x0), ex2_approx(x1));
+          }
+          tmem_st32(tST, pkeep);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(p_ready(w));
+        // ---- dS^T = P^T * (dP^T + dvec) -> bf16 pairs in this dP^T buffer and into the pair's dS tile
+        if (!(ok = wait_warp(dp_full(w), par, st, SITE_B_DP_FULL))) break;
+        tc_fence_after();
+        const int pg = gs >> 1;
+        uint8_t* dsb = sm + C::OFF_DS + (pg & 1) * C::DS_BYTES + w * (128 * 128);
+        if (w == 0 && pg >= 2) {  // dQ of the pair that last used this dS tile has read it
+          if (!(ok = wait_warp(dq_done(pg & 1), ((pg - 2) >> 1) & 1, st, SITE_B_DQ_EMPTY))) break;
+        }
+        {
+          // dP^T in two halves, each waited for on its own: loading both before one wait needs
+          // 32 more live registers than the 128 this kernel has per thread
+          uint32_t dp[2][32];
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            tmem_ld32(tDPT + 32 * h, dp[h]);
+            tmem_wait_ld();
+            uint32_t pk[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const int g = 16 * h + e;
+              const float4 d4 = reinterpret_cast<const float4*>(dv_s)[g >> 1];
+              const float2 d2 = (g & 1) ? make_float2(d4.z, d4.w) : make_float2(d4.x, d4.y);
+              const float p0 = __uint_as_float(pkeep[g] << 16), p1 = __uint_as_float(pkeep[g] & 0xFFFF0000u);
+              const uint64_t t2 = f2_add(f2_pack(__uint_as_float(dp[h][2 * e]), __uint_as_float(dp[h][2 * e + 1])),
+                                         f2_pack(d2.x, d2.y));
+              float d0, d1;
+              f2_unpack(f2_mul(t2, f2_pack(p0, p1)), d0, d1);
+              pk[e] = pack_bf16x2(d0, d1);
+            }
+            tmem_st16(tDPT + 16 * h, pk);
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              *reinterpret_cast<uint4*>(dsb + sw128_offset(r, 4 * h + q)) =
+                  make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+          }
+        }
+        tmem_wait_st();
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(ds_ready(w));
+          if (w == 0) smem_add_release(ds0_count, 1);
         }
       }
-      tmem_wait_st();
-      fence_proxy_async_smem();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(ds_ready(w));
-        if (w == 0) smem_add_release(ds0_count, 1);
-      }
-    }
-    // ---- epilogue: warpgroup 0 writes dV, warpgroup 1 writes s * dK
-    if (ok) ok = wait_warp(final_bar, 0, st, SITE_B_FINAL);
-    ok = named_bar_and(1 + w, 128, ok);  // reached by every warp of the warpgroup
-    if (ok) {
-      tc_fence_after();
-      const uint32_t src = w == 0 ? C::TM_DV : C::TM_DK;
-      const float mul = w == 0 ? 1.f : a.scale;
-      uint8_t* stage = sm + (w == 0 ? C::OFF_Q : C::OFF_DO);  // both free once every MMA is done
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t x[32];
-        tmem_ld32(tmem + lane_off + src + c * 32, x);
-        tmem_wait_ld();
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          uint4 vv;
-          vv.x = pack_bf16x2(__uint_as_float(x[q * 8 + 0]) * mul, __uint_as_float(x[q * 8 + 1]) * mul);
-          vv.y = pack_bf16x2(__uint_as_float(x[q * 8 + 2]) * mul, __uint_as_float(x[q * 8 + 3]) * mul);
-          vv.z = pack_bf16x2(__uint_as_float(x[q * 8 + 4]) * mul, __uint_as_float(x[q * 8 + 5]) * mul);
-          vv.w = pack_bf16x2(__uint_as_float(x[q * 8 + 6]) * mul, __uint_as_float(x[q * 8 + 7]) * mul);
-          *reinterpret_cast<uint4*>(stage + sw128_offset(r, c * 4 + q)) = vv;
-        }
-      }
-      fence_proxy_async_smem();
-      named_bar_sync(1 + w, 128);
-      if (wq == 0 && lane == 0) {
-        tma_store_3d(w == 0 ? &tm_dv : &tm_dk, smem_u32(stage), 0, k0, bh);
-        bulk_commit();
-        bulk_wait_read0();  // the staging tile must outlive the copy's reads
-      }
+      gs0 += tl.n_it;
     }
   }
 
@@ -1031,8 +1155,14 @@ static int launch_bwd_main_d(const void* q, const void* k, const void* v, const 
       if (e != cudaSuccess) return cuda_fail("cudaFuncSetAttribute", (int)e, cudaGetErrorName(e));
       attr_set = true;
     }
-    return launch_pdl(__func__, bwd_kernel_d64<0>, grid, dim3(Bwd64::THREADS), Bwd64::SMEM_BYTES, stream, mq, mk, mv,
-                      mdo, mdk, mdv, mdq, a);
+    // persistent: one CTA per SM (at most one per key tile)
+    int sms = 0;
+    if (!sm_count(&sms)) return FA_ERR_CUDA;
+    const long long tiles = (long long)BH * ((a.N + 127) / 128);
+    BwdArgs ap = a;
+    ap.BH = BH;
+    return launch_pdl(__func__, bwd_kernel_d64<0>, dim3((unsigned)std::min<long long>(tiles, sms)),
+                      dim3(Bwd64::THREADS), Bwd64::SMEM_BYTES, stream, mq, mk, mv, mdo, mdk, mdv, mdq, ap);
   } else {
     using C = BwdCfg<D>;
     if (!attr_set) {

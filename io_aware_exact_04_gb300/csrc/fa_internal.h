@@ -19,6 +19,7 @@ struct FwdArgs {
 
 struct BwdArgs {
   int H, N, Npad;      // Npad = N rounded up to a multiple of 128
+  int BH;              // B * H (set by the launcher of the persistent d = 64 kernel)
   int causal;
   float scale;         // softmax scale s
   float scale_log2;    // s * log2(e)
@@ -40,6 +41,9 @@ struct BwdArgs {
 int cuda_fail(const char* where, int code, const char* what);
 // Records a free-form reason for this host thread (read back by fa_last_error_detail).
 void set_error_detail(const char* text);
+// Number of SMs of the current device (cached per device); false, with the CUDA error
+// recorded, when it cannot be read.
+bool sm_count(int* out);
 // After a launch: FA_OK, or FA_ERR_CUDA with the launch error recorded.
 int check_launch(const char* kernel);
 

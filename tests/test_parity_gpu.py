@@ -38,6 +38,22 @@ def test_small_cases_match_oracle(gpu, B, H, N, d, causal, kv_len):
     assert_within(check_all_heads(B, H, N, d, causal, kv_len, seed=N + d, device=gpu))
 
 
+# The d = 64 backward kernel is persistent: one CTA per SM loops over the key tiles of all
+# heads. These shapes give every CTA several tiles (more than 152 tiles), mixing causal and
+# full tiles, a ragged last tile, and key padding that leaves whole tiles without a valid key.
+MANY_TILES = [
+    # B, H, N, d, causal, kv_len
+    (8, 24, 256, 64, True, None),                              # 384 tiles
+    (6, 20, 300, 64, False, [0, 50, 300, 129, 257, 1]),        # 360 tiles, empty ones included
+    (4, 30, 384, 64, True, [384, 200, 10, 384]),               # 360 tiles, causal with padding
+]
+
+
+@pytest.mark.parametrize("B,H,N,d,causal,kv_len", MANY_TILES)
+def test_many_tiles_per_cta_match_oracle(gpu, B, H, N, d, causal, kv_len):
+    assert_within(check_all_heads(B, H, N, d, causal, kv_len, seed=7 * N + B, device=gpu))
+
+
 def test_tiny_workload(gpu):
     w = workloads.WORKLOADS["tiny"]
     x = workloads.make_inputs(w)
