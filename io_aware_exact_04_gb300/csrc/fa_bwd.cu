@@ -963,35 +963,43 @@ __global__ void __launch_bounds__(480, 1)
         }
       }
       if (!ok) break;
-      // ---- this tile's dV and s * dK: TMEM -> bf16 -> staging -> TMA store; then zero both
+      // ---- this tile's dV and s * dK -> bf16 -> staging -> TMA store. dV is staged and stored
+      //      first; once dK is in registers both accumulators are zeroed and handed back to
+      //      the issuers (the next tile's first dV / dK MMAs wait for that), before dK waits
+      //      for the staging buffer.
       if (!(ok = named_bar_and(3, 128, wait_warp(tile_done, tu & 1, st, SITE_B_FINAL)))) break;
       tc_fence_after();
-#pragma unroll
-      for (int g = 0; g < 2; ++g) {
+      auto load_packed = [&](uint32_t col, float mul, uint32_t (&out)[32]) {
         uint32_t x[2][32];
-        tmem_ld32(tmem + lane_off + (g == 0 ? C::TM_DV : C::TM_DK), x[0]);
-        tmem_ld32(tmem + lane_off + (g == 0 ? C::TM_DV : C::TM_DK) + 32, x[1]);
+        tmem_ld32(tmem + lane_off + col, x[0]);
+        tmem_ld32(tmem + lane_off + col + 32, x[1]);
         tmem_wait_ld();
-        const float mul = g == 0 ? 1.f : sc;
+#pragma unroll
+        for (int e = 0; e < 32; ++e)
+          out[e] = pack_bf16x2(__uint_as_float(x[e >> 4][(2 * e) & 31]) * mul,
+                               __uint_as_float(x[e >> 4][(2 * e + 1) & 31]) * mul);
+      };
+      auto stage_store = [&](const uint32_t (&pk)[32], const CUtensorMap* map) {
         uint8_t* stg = stage_acquire();
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const uint32_t* xs = &x[q >> 2][(q & 3) * 8];
-          uint4 vv;
-          vv.x = pack_bf16x2(__uint_as_float(xs[0]) * mul, __uint_as_float(xs[1]) * mul);
-          vv.y = pack_bf16x2(__uint_as_float(xs[2]) * mul, __uint_as_float(xs[3]) * mul);
-          vv.z = pack_bf16x2(__uint_as_float(xs[4]) * mul, __uint_as_float(xs[5]) * mul);
-          vv.w = pack_bf16x2(__uint_as_float(xs[6]) * mul, __uint_as_float(xs[7]) * mul);
-          *reinterpret_cast<uint4*>(stg + sw128_offset(r, q)) = vv;
-        }
+        for (int q = 0; q < 8; ++q)
+          *reinterpret_cast<uint4*>(stg + sw128_offset(r, q)) =
+              make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
         fence_proxy_async_smem();
         named_bar_sync(3, 128);
         if (tid == 0) {
-          tma_store_3d(g == 0 ? &tm_dv : &tm_dk, smem_u32(stg), 0, tl.k0, tl.bh);
+          tma_store_3d(map, smem_u32(stg), 0, tl.k0, tl.bh);
           bulk_commit();
         }
+      };
+      {
+        uint32_t pk[32];
+        load_packed(C::TM_DV, 1.f, pk);
+        stage_store(pk, &tm_dv);
       }
       {
+        uint32_t pk[32];
+        load_packed(C::TM_DK, sc, pk);
         uint32_t z[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) z[i] = 0;
@@ -1000,10 +1008,11 @@ __global__ void __launch_bounds__(480, 1)
         tmem_st32(tmem + lane_off + C::TM_DK, z);
         tmem_st32(tmem + lane_off + C::TM_DK + 32, z);
         tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(acc_free);
+        stage_store(pk, &tm_dk);
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(acc_free);
       gs0 += tl.n_it;
       ++tu;
     }
