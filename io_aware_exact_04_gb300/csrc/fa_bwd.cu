@@ -35,22 +35,18 @@ namespace fa {
 // ---------------------------------------------------------------------------------------------
 // Stored negated, so that the main kernels add them with no extra instruction:
 // dvec_i = -D_i = -sum_k dO_ik O_ik; lse2_i = -LSE_i * log2(e) (-inf where no row or
-// LSE = -inf, so that recomputed P is 0 there); dq_acc row zeroed. One group of D/8 lanes
-// per row, 16 B each.
+// LSE = -inf, so that recomputed P is 0 there); dq_acc row zeroed. Grid (row blocks, heads):
+// one group of D/8 lanes per row, 16 B each, so no index needs a division.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(BwdArgs a, int BH) {
   griddep_wait();
   griddep_launch_dependents();
-  constexpr int LPR = D / 8;          // lanes per row
-  constexpr int RPW = 32 / LPR;       // rows per warp
-  const int lane = threadIdx.x & 31;
-  const long long gw = (long long)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
-  const long long total_rows = (long long)BH * a.Npad;
-  const long long r = gw * RPW + lane / LPR;
-  const int part = lane % LPR;
-  if (r >= total_rows) return;
-  const int bh = (int)(r / a.Npad);
-  const int n = (int)(r % a.Npad);
+  constexpr int LPR = D / 8;         // lanes per row
+  constexpr int RPB = 256 / LPR;     // rows per block
+  const int part = threadIdx.x % LPR;
+  const int n = blockIdx.x * RPB + threadIdx.x / LPR;
+  const int bh = blockIdx.y;
+  if (n >= a.Npad) return;  // whole row groups leave together: RPB divides the 128-row padding
   float acc = 0.f;
   if (n < a.N) {
     const size_t off = ((size_t)bh * a.N + n) * D + part * 8;
@@ -66,7 +62,8 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(BwdArgs a, int BH) {
   }
 #pragma unroll
   for (int m = LPR / 2; m > 0; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
-  float4* dq = reinterpret_cast<float4*>(a.dq_acc + (size_t)r * D + part * 8);
+  const size_t r = (size_t)bh * a.Npad + n;
+  float4* dq = reinterpret_cast<float4*>(a.dq_acc + r * D + part * 8);
   dq[0] = make_float4(0.f, 0.f, 0.f, 0.f);
   dq[1] = make_float4(0.f, 0.f, 0.f, 0.f);
   if (part == 0) {
@@ -80,24 +77,38 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(BwdArgs a, int BH) {
   }
 }
 
+// fp32 dQ accumulator -> bf16 dQ. Grid (row blocks, heads), each thread two rows' worth of
+// 16-byte outputs with both rows' loads in flight before the stores.
 template <int D>
 __global__ void __launch_bounds__(256) dq_convert_kernel(BwdArgs a, int BH) {
   griddep_wait();
   griddep_launch_dependents();
-  const long long total = (long long)BH * a.N * (D / 8);
-  for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
-       idx += (long long)gridDim.x * blockDim.x) {
-    const long long row = idx / (D / 8);
-    const int part = (int)(idx % (D / 8));
-    const int bh = (int)(row / a.N), n = (int)(row % a.N);
-    const float4* src = reinterpret_cast<const float4*>(a.dq_acc + ((size_t)bh * a.Npad + n) * D + part * 8);
-    const float4 x = src[0], y = src[1];
-    uint4 o;
-    o.x = pack_bf16x2(x.x, x.y);
-    o.y = pack_bf16x2(x.z, x.w);
-    o.z = pack_bf16x2(y.x, y.y);
-    o.w = pack_bf16x2(y.z, y.w);
-    *reinterpret_cast<uint4*>(a.dq + (size_t)row * D + part * 8) = o;
+  constexpr int LPR = D / 8;         // threads per row (8 outputs each)
+  constexpr int RPB = 256 / LPR;     // rows per block and pass
+  const int part = threadIdx.x % LPR;
+  const int bh = blockIdx.y;
+  const int n0 = blockIdx.x * (2 * RPB) + threadIdx.x / LPR;
+  float4 x[2][2];
+#pragma unroll
+  for (int u = 0; u < 2; ++u) {
+    const int n = n0 + u * RPB;
+    if (n < a.N) {
+      const float4* src = reinterpret_cast<const float4*>(a.dq_acc + ((size_t)bh * a.Npad + n) * D + part * 8);
+      x[u][0] = src[0];
+      x[u][1] = src[1];
+    }
+  }
+#pragma unroll
+  for (int u = 0; u < 2; ++u) {
+    const int n = n0 + u * RPB;
+    if (n < a.N) {
+      uint4 o;
+      o.x = pack_bf16x2(x[u][0].x, x[u][0].y);
+      o.y = pack_bf16x2(x[u][0].z, x[u][0].w);
+      o.z = pack_bf16x2(x[u][1].x, x[u][1].y);
+      o.w = pack_bf16x2(x[u][1].z, x[u][1].w);
+      *reinterpret_cast<uint4*>(a.dq + ((size_t)bh * a.N + n) * D + part * 8) = o;
+    }
   }
 }
 
@@ -1133,11 +1144,9 @@ __global__ void __launch_bounds__(480, 1)
 
 template <int D>
 static int launch_bwd_pre_d(const BwdArgs& a, int BH, cudaStream_t stream) {
-  const long long rows = (long long)BH * a.Npad;
-  const int rpw = 32 / (D / 8);
-  const long long warps = (rows + rpw - 1) / rpw;
-  const int blocks = (int)((warps + 7) / 8);
-  return launch_pdl(__func__, bwd_pre_kernel<D>, dim3(blocks), dim3(256), 0, stream, a, BH);
+  constexpr int RPB = 256 / (D / 8);
+  const dim3 grid((unsigned)((a.Npad + RPB - 1) / RPB), (unsigned)BH);
+  return launch_pdl(__func__, bwd_pre_kernel<D>, grid, dim3(256), 0, stream, a, BH);
 }
 
 template <int D>
@@ -1187,10 +1196,9 @@ static int launch_bwd_main_d(const void* q, const void* k, const void* v, const 
 
 template <int D>
 static int launch_bwd_convert_d(const BwdArgs& a, int BH, cudaStream_t stream) {
-  const long long total = (long long)BH * a.N * (D / 8);
-  long long blocks = (total + 255) / 256;
-  if (blocks > 152 * 16) blocks = 152 * 16;
-  return launch_pdl(__func__, dq_convert_kernel<D>, dim3((int)blocks), dim3(256), 0, stream, a, BH);
+  constexpr int RPB = 256 / (D / 8);
+  const dim3 grid((unsigned)((a.N + 2 * RPB - 1) / (2 * RPB)), (unsigned)BH);
+  return launch_pdl(__func__, dq_convert_kernel<D>, grid, dim3(256), 0, stream, a, BH);
 }
 
 int launch_bwd_stage(int stage, const void* q, const void* k, const void* v, const BwdArgs& a, int BH, int d,
