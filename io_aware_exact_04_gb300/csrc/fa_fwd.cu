@@ -446,6 +446,494 @@ __global__ void __launch_bounds__(352, 1)
   }
 }
 
+// ---------------------------------------------------------------------------------------------
+// d = 64 forward, persistent: G CTAs (one per SM) loop over work items = (pair of 128-row query
+// tiles, head), longest causal pairs first with heads fastest, in the snake order of the
+// backward (CTA c takes item r G + c in even rounds r and r G + G - 1 - c in odd ones). Inside
+// an item the pipeline is that of fwd_kernel<64>; across items the K/V ring, the TMEM buffers
+// and every barrier phase run on, Q is double-buffered by item (the next item's Q loads while
+// this one runs; a set doubles as its item's O staging and is released once the O stores have
+// read it), S_t(0) of the next item is issued as soon as S_t is free, and PV_t(0) of the next
+// item waits until the epilogue has read O_t out of TMEM.
+struct FwdP64 {
+  static constexpr int D = 64, NST = 3;
+  static constexpr int TILE_BYTES = 128 * 128;         // [128 rows][64] bf16
+  static constexpr int OFF_Q = 0;                      // 2 sets x 2 query tiles
+  static constexpr int OFF_K = OFF_Q + 4 * TILE_BYTES;
+  static constexpr int OFF_V = OFF_K + NST * TILE_BYTES;
+  static constexpr int OFF_BAR = OFF_V + NST * TILE_BYTES;
+  static constexpr int SMEM_BYTES = OFF_BAR + 256 + 1024;
+  // TMEM columns as fwd_kernel<64>: S_t 128 t, P_t 256 + 64 t, O_t 384 + 64 t
+  __device__ static constexpr uint32_t tm_s(int t) { return 128u * t; }
+  __device__ static constexpr uint32_t tm_p(int t) { return 256u + 64u * t; }
+  __device__ static constexpr uint32_t tm_o(int t) { return 384u + 64u * t; }
+  static constexpr uint32_t TM_COLS = 512;
+  static constexpr int THREADS = 352;  // 0-7 softmax, 8 TMA, 9-10 MMA (one per query tile)
+  __host__ __device__ static constexpr int off_q(int set, int t) { return OFF_Q + (2 * set + t) * TILE_BYTES; }
+};
+static_assert(8 * (10 + 3 * FwdP64::NST + 1) + 8 <= 256, "persistent forward: barrier area");
+
+struct ItemF64 {
+  int bh, kv, q0, n[2], nmax;
+};
+__device__ __forceinline__ ItemF64 item_f64(int t, const FwdArgs& a, int BH) {
+  ItemF64 it;
+  const int p = t / BH;
+  it.bh = t - p * BH;
+  it.q0 = (a.n_pairs - 1 - p) * 256;
+  it.kv = a.N;
+  if (a.kv_len) it.kv = min(max(a.kv_len[it.bh / a.H], 0), a.N);
+  const int nkt = (it.kv + 127) >> 7;
+#pragma unroll
+  for (int u = 0; u < 2; ++u) {
+    const int qs = it.q0 + u * 128;
+    it.n[u] = (qs >= a.N) ? 0 : (a.causal ? min(nkt, (qs >> 7) + 1) : nkt);
+  }
+  it.nmax = max(it.n[0], it.n[1]);
+  return it;
+}
+__device__ __forceinline__ int sched_f64(int r, int c, int G, int T) {
+  const int t = r * G + ((r & 1) ? (G - 1 - c) : c);
+  return t < T ? t : -1;
+}
+
+// The rows of an item with no valid key (kv_len = 0): O = 0 and LSE = -inf. Kept out of
+// line: inlined into the producer's loop it made the register allocator spill in the
+// softmax warpgroups.
+__device__ __noinline__ void zero_rows_f64(uint16_t* o, float* lse, int N, int bh, int q0, int lane) {
+  constexpr int D = FwdP64::D;
+  for (int idx = lane; idx < 256 * (D / 8); idx += 32) {
+    const int grow = q0 + idx / (D / 8);
+    if (grow < N) {
+      const size_t off = ((size_t)bh * N + grow) * D + (idx % (D / 8)) * 8;
+      *reinterpret_cast<uint4*>(o + off) = make_uint4(0, 0, 0, 0);
+      if (idx % (D / 8) == 0) lse[(size_t)bh * N + grow] = -INFINITY;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(352, 1)
+    fwd_kernel_p64(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o, FwdArgs a,
+                   int BH) {
+  griddep_wait();  // before any access to global memory
+  griddep_launch_dependents();
+  using C = FwdP64;
+  constexpr int D = C::D, NST = C::NST;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = align1024(smem_raw);
+  const uint32_t sbase = smem_u32(sm);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::OFF_BAR);
+  const uint32_t b0 = smem_u32(bars);
+  auto BAR = [&](int i) { return b0 + 8u * i; };
+  auto q_full = [&](int set) { return BAR(set); };
+  auto q_empty = [&](int set) { return BAR(2 + set); };  // one arrival per query tile
+  auto k_full = [&](int s) { return BAR(4 + s); };
+  auto v_full = [&](int s) { return BAR(4 + NST + s); };
+  auto kv_empty = [&](int s) { return BAR(4 + 2 * NST + s); };
+  constexpr int nb = 4 + 3 * NST;
+  auto s_full = [&](int t) { return BAR(nb + t); };
+  auto p_ready = [&](int t) { return BAR(nb + 2 + t); };
+  auto o_done = [&](int t) { return BAR(nb + 4 + t); };
+  auto s_free = [&](int t) { return BAR(nb + 6 + t); };
+  auto o_free = [&](int t) { return BAR(nb + 8 + t); };  // O_t read out by the epilogue
+  const uint32_t drain = BAR(nb + 10);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C::OFF_BAR + 8 * (nb + 11));
+  int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+  DevStatus st{a.status, abort_flag};
+
+  const int T = BH * a.n_pairs;
+  const int G = gridDim.x, cta = blockIdx.x;
+  // the next item with work at or after round r (its round, or -1)
+  auto next_item = [&](int r, ItemF64& out) -> int {
+    for (;; ++r) {
+      const int t = sched_f64(r, cta, G, T);
+      if (t < 0) return -1;
+      out = item_f64(t, a, BH);
+      if (out.nmax > 0) return r;
+    }
+  };
+
+  // Producer warp: barriers, then the first item's Q and first K/V stages before the setup.
+  auto load_kv = [&](int g, int j, int bh) {  // whole warp; ring index g, key tile j
+    const int s = g % NST;
+    const uint32_t kf = k_full(s), vf = v_full(s);
+    if (elect_one()) mbar_arrive_expect_tx(kf, C::TILE_BYTES);
+    if (elect_one()) tma_load_3d(sbase + C::OFF_K + s * C::TILE_BYTES, &tm_k, 0, j * 128, bh, kf);
+    if (elect_one()) mbar_arrive_expect_tx(vf, C::TILE_BYTES);
+    if (elect_one()) tma_load_3d(sbase + C::OFF_V + s * C::TILE_BYTES, &tm_v, 0, j * 128, bh, vf);
+    __syncwarp();
+  };
+  auto load_q = [&](int set, const ItemF64& it) {  // whole warp
+    const int nq = (it.n[1] > 0) ? 2 : 1;
+    if (elect_one()) mbar_arrive_expect_tx(q_full(set), nq * C::TILE_BYTES);
+    for (int u = 0; u < nq; ++u)
+      if (elect_one()) tma_load_3d(sbase + C::off_q(set, u), &tm_q, 0, it.q0 + u * 128, it.bh, q_full(set));
+    __syncwarp();
+  };
+  int n_pre = 0;  // K/V stages of the first item issued before the setup (producer warp)
+  if (warp == 8) {
+    if (lane == 0) {
+      for (int u = 0; u < 2; ++u) {
+        mbar_init(q_full(u), 1);
+        mbar_init(q_empty(u), 2);
+      }
+      for (int s = 0; s < NST; ++s) {
+        mbar_init(k_full(s), 1);
+        mbar_init(v_full(s), 1);
+        mbar_init(kv_empty(s), 2);  // one arrival per MMA-issuing warp
+      }
+      for (int t = 0; t < 2; ++t) {
+        mbar_init(s_full(t), 1);
+        mbar_init(p_ready(t), 4);
+        mbar_init(o_done(t), 1);
+        mbar_init(s_free(t), 4);
+        mbar_init(o_free(t), 4);
+      }
+      mbar_init(drain, 2);
+      *abort_flag = 0;
+      fence_mbar_init();
+    }
+    __syncwarp();
+    ItemF64 it;
+    if (next_item(0, it) >= 0) {
+      if (elect_one()) {
+        prefetch_tmap(&tm_q);
+        prefetch_tmap(&tm_k);
+        prefetch_tmap(&tm_v);
+      }
+      load_q(0, it);
+      n_pre = min(NST, it.nmax);
+      for (int j = 0; j < n_pre; ++j) load_kv(j, j, it.bh);
+    }
+  }
+  if (warp == 9) {
+    tmem_alloc(smem_u32(tmem_slot), C::TM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ TMA producer
+    bool ok = true;
+    int iu = 0, g0 = 0, issued = 0, q_loads = 1;  // the first item's Q went out before the setup
+    for (int r = 0; ok; ++r) {
+      const int tt = sched_f64(r, cta, G, T);
+      if (tt < 0) break;
+      const ItemF64 it = item_f64(tt, a, BH);
+      if (it.nmax == 0) {
+        zero_rows_f64(a.o, a.lse, a.N, it.bh, it.q0, lane);
+        continue;
+      }
+      const int set = iu & 1;
+      if (iu > 0) {
+        if (!(ok = wait_warp(q_empty(set), ((iu >> 1) & 1) ^ 1, st, SITE_F_Q_FULL))) break;
+        load_q(set, it);
+        ++q_loads;
+      }
+      for (int j = (iu == 0 ? n_pre : 0); j < it.nmax; ++j) {
+        const int g = g0 + j;
+        if (!(ok = wait_warp(kv_empty(g % NST), ((g / NST) & 1) ^ 1, st, SITE_F_KV_EMPTY))) break;
+        load_kv(g, j, it.bh);
+        issued = g + 1;
+      }
+      g0 += it.nmax;
+      ++iu;
+    }
+    if (*(volatile int*)abort_flag) {
+      // let copies already in flight land before the CTA's smem is released
+      const uint64_t t0 = globaltimer_ns();
+      for (int g = max(0, issued - NST); g < issued; ++g)
+        while (!(mbar_try_wait(k_full(g % NST), (g / NST) & 1) && mbar_try_wait(v_full(g % NST), (g / NST) & 1)) &&
+               globaltimer_ns() - t0 < 100000000ull) {
+        }
+      for (int u = max(0, q_loads - 2); u < q_loads; ++u)
+        while (!mbar_try_wait(q_full(u & 1), (u >> 1) & 1) && globaltimer_ns() - t0 < 100000000ull) {
+        }
+    }
+  } else if (warp == 9 || warp == 10) {
+    // ------------------------------------------------------------ MMA issuer of query tile t
+    // (whole warp; one elected lane issues)
+    const int t = warp - 9;
+    constexpr uint32_t IDESC_S = idesc_bf16_f32(128, 128, 0, 0);  // Q, K both K-major
+    constexpr uint32_t IDESC_O = idesc_bf16_f32(128, D, 0, 1);    // P from TMEM, V MN-major
+    constexpr uint32_t HI = sdesc_hi(1024);
+    constexpr uint32_t TILE16 = C::TILE_BYTES >> 4;
+    const uint32_t k_lo = sdesc_lo(sbase + C::OFF_K, 16);
+    const uint32_t v_lo = sdesc_lo(sbase + C::OFF_V, C::TILE_BYTES);
+    auto issue_s = [&](int set, int kst) {  // S_t = Q_t K^T (Q from set, K from stage kst)
+      const uint32_t qa = sdesc_lo(sbase + C::off_q(set, t), 16), ka = k_lo + kst * TILE16, d = tmem + C::tm_s(t);
+#pragma unroll
+      for (int k = 0; k < D / 16; ++k)
+        if (elect_one()) mma_ss(d, sdesc_join(qa + 2 * k, HI), sdesc_join(ka + 2 * k, HI), IDESC_S, k > 0);
+    };
+    auto issue_pv = [&](int vst, uint32_t acc) {  // O_t += P_t V (V from stage vst)
+      const uint32_t va = v_lo + vst * TILE16, d = tmem + C::tm_o(t), pa = tmem + C::tm_p(t);
+#pragma unroll
+      for (int k = 0; k < 8; ++k)  // 128 keys, 16 per MMA
+        if (elect_one()) mma_ts(d, pa + k * 8, sdesc_join(va + k * (2048 >> 4), HI), IDESC_O, (acc | k) != 0);
+    };
+    auto commit = [&](uint32_t bar) {
+      if (elect_one()) mma_commit(bar);
+      __syncwarp();
+    };
+    bool ok = true;
+    int iu = 0, g0 = 0, gj = 0, ep = 0;  // items, ring index, S_t count, epilogues of tile t
+    bool s0_issued = false;              // S_t(0) of the current item already issued ahead
+    ItemF64 it, nx;
+    for (int r = next_item(0, it); ok && r >= 0;) {
+      const int set = iu & 1;
+      const int n = (t == 0 ? it.n[0] : it.n[1]);
+      const int r2 = next_item(r + 1, nx);
+      if (n > 0 && !s0_issued) {  // S_t(0) of this item (S_t is free once its last one was read)
+        if (!(ok = wait_warp(q_full(set), (iu >> 1) & 1, st, SITE_F_Q_FULL))) break;
+        if (!(ok = wait_warp(k_full(g0 % NST), (g0 / NST) & 1, st, SITE_F_K_FULL))) break;
+        if (gj > 0 && !(ok = wait_warp(s_free(t), (gj - 1) & 1, st, SITE_F_S_FREE))) break;
+        tc_fence_after();
+        issue_s(set, g0 % NST);
+        commit(s_full(t));
+      }
+      s0_issued = false;
+      for (int j = 0; ok && j < it.nmax; ++j) {
+        const int g = g0 + j, s = g % NST;
+        const uint32_t ph = (g / NST) & 1;
+        if (j < n) {
+          if (j + 1 < n) {  // S_t(j+1) as soon as the warpgroup has S_t(j) in registers
+            if (!(ok = wait_warp(k_full((g + 1) % NST), ((g + 1) / NST) & 1, st, SITE_F_K_FULL))) break;
+            if (!(ok = wait_warp(s_free(t), (gj + j) & 1, st, SITE_F_S_FREE))) break;
+            tc_fence_after();
+            issue_s(set, (g + 1) % NST);
+            commit(s_full(t));
+          } else if (r2 >= 0 && (t == 0 ? nx.n[0] : nx.n[1]) > 0 && it.nmax - n <= NST) {
+            // ... and S_t(0) of the next item. Its Q goes out after this item's last K/V copy,
+            // which waits for this warp's release of ring slot g0 + nmax - 1 - NST: processed
+            // already when nmax - n <= NST (always for causal and full tiles).
+            const int g2 = g0 + it.nmax;
+            if (!(ok = wait_warp(q_full(set ^ 1), ((iu + 1) >> 1) & 1, st, SITE_F_Q_FULL))) break;
+            if (!(ok = wait_warp(k_full(g2 % NST), (g2 / NST) & 1, st, SITE_F_K_FULL))) break;
+            if (!(ok = wait_warp(s_free(t), (gj + j) & 1, st, SITE_F_S_FREE))) break;
+            tc_fence_after();
+            issue_s(set ^ 1, g2 % NST);
+            commit(s_full(t));
+            s0_issued = true;
+          }
+          if (!(ok = wait_warp(v_full(s), ph, st, SITE_F_V_FULL))) break;
+          if (!(ok = wait_warp(p_ready(t), (gj + j) & 1, st, SITE_F_P_READY))) break;
+          if (j == 0 && ep > 0) {  // the epilogue has read O_t of the previous item
+            if (!(ok = wait_warp(o_free(t), (ep - 1) & 1, st, SITE_F_O_DONE))) break;
+          }
+          tc_fence_after();
+          issue_pv(s, j > 0);
+          commit(o_done(t));
+          commit(kv_empty(s));  // this warp's readers of K_j, V_j are issued
+        } else {
+          // tile j is not this warp's: once it has landed (so its stage's previous use is
+          // released), add this warp's arrival without waiting for anything else
+          if (!(ok = wait_warp(v_full(s), ph, st, SITE_F_V_FULL))) break;
+          if (elect_one()) mbar_arrive(kv_empty(s));
+          __syncwarp();
+        }
+      }
+      if (!ok) break;
+      gj += n;
+      if (n > 0) ++ep;
+      g0 += it.nmax;
+      ++iu;
+      it = nx;
+      r = r2;
+    }
+    commit(drain);  // completes after every MMA issued above
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(drain, 0) && globaltimer_ns() - t0 < kWaitLimitNs) {
+    }
+  } else if (warp < 8) {
+    // ------------------------------------------------------------ softmax warpgroup of tile t
+    const int t = warp >> 2;
+    const int wq = warp & 3;
+    const int row = wq * 32 + lane;  // TMEM lane == row within the query tile
+    const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+    const uint32_t tS = tmem + lane_off + C::tm_s(t);
+    const uint32_t tP = tmem + lane_off + C::tm_p(t);
+    const uint32_t tO = tmem + lane_off + C::tm_o(t);
+    const float sl2 = a.scale_log2;
+    bool ok = true;
+    int iu = 0, gj = 0;
+    ItemF64 it;
+    for (int r = next_item(0, it); ok && r >= 0; r = next_item(r + 1, it)) {
+      // only n, qs and kv live through the key loop; the rest of the item is recomputed for
+      // the epilogue (fewer live registers in the softmax)
+      const int n = (t == 0 ? it.n[0] : it.n[1]);
+      const int qs = it.q0 + t * 128;
+      const int kvv = it.kv;
+      const int grow = qs + row;
+      bool stored = false;
+      if (qs < a.N && n == 0) {
+        // no valid key for any row of this tile: O = 0, LSE = -inf
+        if (grow < a.N) {
+          uint4* orow = reinterpret_cast<uint4*>(a.o + ((size_t)it.bh * a.N + grow) * D);
+          for (int c = 0; c < D / 8; ++c) orow[c] = make_uint4(0, 0, 0, 0);
+          a.lse[(size_t)it.bh * a.N + grow] = -INFINITY;
+        }
+      } else if (n > 0) {
+        float m_run = -INFINITY;  // running maximum of s*S*log2(e)
+        float l_run = 0.f;        // running normaliser
+        for (int j = 0; j < n; ++j) {
+          const uint32_t par = (gj + j) & 1;
+          ok = wait_warp(s_full(t), par, st, SITE_F_S_FULL);
+          if (!ok) break;
+          tc_fence_after();
+          float sv[128];
+          {
+            uint32_t rr[4][32];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, rr[c]);
+            tmem_wait_ld();
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+#pragma unroll
+              for (int i = 0; i < 32; ++i) sv[c * 32 + i] = __uint_as_float(rr[c][i]);
+          }
+          // S_t is in registers: the MMA may overwrite it with the next S_t
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(s_free(t));
+          const int k0 = j * 128;
+          const bool need_mask = (k0 + 127 >= kvv) || (a.causal && k0 + 127 > qs);
+          if (need_mask) {
+            const int lim = a.causal ? min(kvv, grow + 1) : kvv;  // keys [0, lim) are valid
+#pragma unroll
+            for (int c = 0; c < 128; ++c)
+              if (k0 + c >= lim) sv[c] = -INFINITY;
+          }
+          // row maximum: four independent partial maxima (three-input max), then a short tree
+          float pm[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) pm[u] = sv[u];
+#pragma unroll
+          for (int c = 4; c < 124; c += 8)
+#pragma unroll
+            for (int u = 0; u < 4; ++u) pm[u] = fmax3(pm[u], sv[c + 2 * u], sv[c + 2 * u + 1]);
+          const float mx =
+              fmax3(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3]), fmax3(sv[124], sv[125], fmaxf(sv[126], sv[127])));
+          const float m_tile = mx * sl2;
+          // lazy rescale: move the reference maximum only when it grows by > 2^8
+          float f = 1.f;
+          bool rescale_warp = false;
+          if (j == 0) {
+            m_run = m_tile;
+          } else {
+            const bool grow_m = m_tile > m_run + 8.0f;
+            rescale_warp = __any_sync(0xffffffffu, grow_m);
+            if (grow_m) {
+              f = ex2_approx(m_run - m_tile);
+              m_run = m_tile;
+            }
+          }
+          if (j > 0) {
+            // PV_t(j-1) has finished reading P_t(j-1) (and updating O_t) before both are touched
+            if (!(ok = wait_warp(o_done(t), par ^ 1, st, SITE_F_O_DONE))) break;
+            tc_fence_after();
+          }
+          const float base = (m_run == -INFINITY) ? 0.f : m_run;
+          // P = exp2(S s log2e - base): the argument of two columns per fma.f32x2,
+          // the row sum in two paired partial sums
+          const uint64_t sl2x2 = f2_pack(sl2, sl2), nbase2 = f2_pack(-base, -base);
+          uint64_t ps2[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
+#pragma unroll
+          for (int h = 0; h < 4; ++h) {  // 32 columns -> 16 packed bf16x2 words per store
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              float x0, x1;
+              f2_unpack(f2_fma(f2_pack(sv[h * 32 + 2 * i], sv[h * 32 + 2 * i + 1]), sl2x2, nbase2), x0, x1);
+              const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+              ps2[i & 1] = f2_add(ps2[i & 1], f2_pack(p0, p1));
+              pk[i] = pack_bf16x2(p0, p1);
+            }
+            tmem_st16(tP + h * 16, pk);
+          }
+          float ps[4];
+          f2_unpack(ps2[0], ps[0], ps[1]);
+          f2_unpack(ps2[1], ps[2], ps[3]);
+          const float lsum = (ps[0] + ps[1]) + (ps[2] + ps[3]);
+          l_run = l_run * f + lsum;
+          if (rescale_warp) {
+            uint32_t rr[32];
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+              tmem_ld32(tO + c * 32, rr);
+              tmem_wait_ld();
+#pragma unroll
+              for (int i = 0; i < 32; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * f);
+              tmem_st32(tO + c * 32, rr);
+            }
+          }
+          tmem_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(p_ready(t));
+        }
+        if (ok) ok = wait_warp(o_done(t), (gj + n - 1) & 1, st, SITE_F_O_DONE);
+        // every warp of the warpgroup reaches this vote, aborted or not, so the
+        // named barrier of the epilogue below is entered by all four or by none
+        ok = named_bar_and(1 + t, 128, ok);
+        if (!ok) break;
+        tc_fence_after();
+        const int bh = item_f64(sched_f64(r, cta, G, T), a, BH).bh;
+        const int set = iu & 1;
+        // epilogue: O_t out of TMEM (then released to the next item's PV), O / l -> bf16 ->
+        // swizzled smem (this item's Q_t buffer, which no MMA reads any more) -> TMA store
+        uint32_t ov[2][32];
+        tmem_ld32(tO, ov[0]);
+        tmem_ld32(tO + 32, ov[1]);
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(o_free(t));
+        const float inv = (l_run > 0.f) ? 1.f / l_run : 0.f;
+        uint8_t* stage = sm + C::off_q(set, t);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const uint32_t* x = &ov[q >> 2][(q & 3) * 8];
+          uint4 v;
+          v.x = pack_bf16x2(__uint_as_float(x[0]) * inv, __uint_as_float(x[1]) * inv);
+          v.y = pack_bf16x2(__uint_as_float(x[2]) * inv, __uint_as_float(x[3]) * inv);
+          v.z = pack_bf16x2(__uint_as_float(x[4]) * inv, __uint_as_float(x[5]) * inv);
+          v.w = pack_bf16x2(__uint_as_float(x[6]) * inv, __uint_as_float(x[7]) * inv);
+          *reinterpret_cast<uint4*>(stage + sw128_offset(row, q)) = v;
+        }
+        if (grow < a.N)
+          a.lse[(size_t)bh * a.N + grow] =
+              (l_run > 0.f) ? (m_run + lg2_approx(l_run)) * 0.6931471805599453f : -INFINITY;
+        fence_proxy_async_smem();
+        named_bar_sync(1 + t, 128);
+        if (wq == 0 && lane == 0) {
+          tma_store_3d(&tm_o, smem_u32(stage), 0, qs, bh);
+          bulk_commit();
+          bulk_wait_read0();  // the Q_t buffer is free again once the store has read it
+          mbar_arrive(q_empty(set));
+        }
+        stored = true;
+      }
+      if (!stored && wq == 0 && lane == 0) mbar_arrive(q_empty(iu & 1));  // nothing staged in Q_t
+      gj += n;
+      ++iu;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TM_COLS);
+  }
+}
+
 template <int D>
 static int launch_fwd_d(const void* q, const void* k, const void* v, void* o, const FwdArgs& args, int BH,
                         cudaStream_t stream) {
@@ -468,8 +956,39 @@ static int launch_fwd_d(const void* q, const void* k, const void* v, void* o, co
   return launch_pdl(__func__, fwd_kernel<D>, grid, dim3(C::THREADS), C::SMEM_BYTES, stream, mq, mk, mv, mo, args);
 }
 
+// d = 64: the persistent kernel, one CTA per SM (at most one per work item)
+static int launch_fwd_p64(const void* q, const void* k, const void* v, void* o, const FwdArgs& args, int BH,
+                          cudaStream_t stream) {
+  using C = FwdP64;
+  CUtensorMap mq, mk, mv, mo;
+  const uint64_t N = (uint64_t)args.N;
+  const auto BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const auto SW = CU_TENSOR_MAP_SWIZZLE_128B;
+  if (!make_tmap_3d(&mq, q, BF, 2, 64, N, BH, 64, 128, SW) || !make_tmap_3d(&mk, k, BF, 2, 64, N, BH, 64, 128, SW) ||
+      !make_tmap_3d(&mv, v, BF, 2, 64, N, BH, 64, 128, SW) || !make_tmap_3d(&mo, o, BF, 2, 64, N, BH, 64, 128, SW))
+    return cuda_fail("cuTensorMapEncodeTiled", 0, "tensor map rejected");
+  static bool attr_set = false;  // benign race: idempotent
+  if (!attr_set) {
+    const cudaError_t e =
+        cudaFuncSetAttribute(fwd_kernel_p64, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    if (e != cudaSuccess) return cuda_fail("cudaFuncSetAttribute", (int)e, cudaGetErrorName(e));
+    attr_set = true;
+  }
+  int sms = 0;
+  if (!sm_count(&sms)) return FA_ERR_CUDA;
+  const long long items = (long long)BH * args.n_pairs;
+  const dim3 grid((unsigned)std::min<long long>(items, sms));
+  return launch_pdl(__func__, fwd_kernel_p64, grid, dim3(C::THREADS), C::SMEM_BYTES, stream, mq, mk, mv, mo, args,
+                    BH);
+}
+
 int launch_fwd(const void* q, const void* k, const void* v, void* o, const FwdArgs& args, int BH, int d,
                cudaStream_t stream) {
+  // Short rows (at most 4 query-tile pairs, N <= 1024): the persistent kernel, whose per-CTA
+  // setup and item epilogues overlap the next item's MMAs. Longer rows: one CTA per item,
+  // where the hardware's block dispatch balances the causal work at least as well as the
+  // static order and the per-item setup is amortised over many key tiles.
+  if (d == 64 && args.n_pairs <= 4) return launch_fwd_p64(q, k, v, o, args, BH, stream);
   if (d == 64) return launch_fwd_d<64>(q, k, v, o, args, BH, stream);
   if (d == 128) return launch_fwd_d<128>(q, k, v, o, args, BH, stream);
   return FA_ERR_UNSUPPORTED;

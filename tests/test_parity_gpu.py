@@ -30,6 +30,8 @@ SMALL = [
     (1, 1, 1, 64, False, None),           # a single row and key
     (1, 1, 1, 128, True, None),
     (1, 1, 17, 64, True, None),
+    (1, 2, 1300, 64, True, None),         # d = 64 rows past 1024: the one-CTA-per-item forward grid
+    (2, 1, 1100, 64, False, [1100, 3]),
 ]
 
 
