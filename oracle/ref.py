@@ -30,9 +30,12 @@ the N x N matrices that the tiled method avoids storing.
       dQ = s * dS K
       dK = s * dS^T Q
 
-Masks: causal keeps key j for query i iff j <= i (square case, diagonal kept);
-key padding keeps key j iff j < kv_len. A row whose keys are all masked has
-O = 0, LSE = -inf and contributes nothing to any gradient.
+Masks: causal keeps key j for query i iff j <= i + (N_k - N_q): the N_q query
+rows stand for the last N_q positions of the N_k keys' sequence, so that for
+N_q = N_k this is j <= i (diagonal kept); key padding keeps key j iff
+j < kv_len. A row whose keys are all masked (kv_len = 0, or a causal row before
+the first key when N_q > N_k) has O = 0, LSE = -inf and contributes nothing to
+any gradient.
 
 Every function takes float64 numpy arrays (callers pass the bf16-rounded
 inputs upcast to float64). Library primitives used as single steps: numpy
@@ -46,13 +49,16 @@ from typing import Dict, Iterable, Optional
 import numpy as np
 
 
-def keep_mask(rows: np.ndarray, cols: np.ndarray, causal: bool, kv_len: Optional[int]) -> np.ndarray:
-    """Boolean [len(rows), len(cols)]: True where query row i may attend to key j."""
+def keep_mask(rows: np.ndarray, cols: np.ndarray, causal: bool, kv_len: Optional[int],
+              offset: int = 0) -> np.ndarray:
+    """Boolean [len(rows), len(cols)]: True where query row i may attend to key j.
+
+    ``offset`` = N_k - N_q aligns the query rows with the last keys (causal only)."""
     i = np.asarray(rows)[:, None]
     j = np.asarray(cols)[None, :]
     keep = np.ones((i.shape[0], j.shape[1]), dtype=bool)
     if causal:
-        keep &= j <= i
+        keep &= j <= i + int(offset)
     if kv_len is not None:
         keep &= j < int(kv_len)
     return keep
@@ -62,7 +68,7 @@ def scores(q: np.ndarray, k: np.ndarray, scale: float, causal: bool,
            kv_len: Optional[int], rows: np.ndarray) -> np.ndarray:
     """S = s * Q[rows] K^T with masked entries at -inf."""
     s_mat = scale * (q[rows] @ k.T)
-    s_mat[~keep_mask(rows, np.arange(k.shape[0]), causal, kv_len)] = -np.inf
+    s_mat[~keep_mask(rows, np.arange(k.shape[0]), causal, kv_len, k.shape[0] - q.shape[0])] = -np.inf
     return s_mat
 
 
@@ -156,7 +162,7 @@ def head_sampled(q, k, v, do, scale: float, causal: bool, kv_len: Optional[int],
     dq_rows = scale * (ds @ k)
     # keys: column j of S, P, dP, dS over all rows
     s_cols = scale * (q @ k[keys].T)                                  # [n, len(keys)]
-    keep = keep_mask(np.arange(n), keys, causal, kv_len)
+    keep = keep_mask(np.arange(n), keys, causal, kv_len, k.shape[0] - n)
     with np.errstate(invalid="ignore"):
         p_cols = np.where(keep & np.isfinite(lse)[:, None], np.exp(s_cols - lse[:, None]), 0.0)
     dp_cols = do @ v[keys].T
@@ -182,7 +188,7 @@ def head_intermediates(q, k, v, do, scale, causal, kv_len=None) -> Dict[str, np.
 def attention(q, k, v, do=None, *, scale: float, causal: bool, kv_len=None,
               heads: Optional[Iterable] = None, row_block: Optional[int] = None,
               backward: bool = True) -> Dict[str, np.ndarray]:
-    """Batched driver over [B, H, N, d] float64 arrays.
+    """Batched driver over float64 arrays: q, do [B, H, N_q, d]; k, v [B, H, N_k, d].
 
     ``kv_len`` is None or a length-B integer array. ``heads`` optionally lists
     (b, h) pairs; outputs are then stacked in that order as [len(heads), N, ...].

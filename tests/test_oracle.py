@@ -274,3 +274,132 @@ def test_pins_catch_planted_mistakes(kind):
         o_loop, _ = _loops_forward(q.tolist(), k.tolist(), v.tolist(), 0.7, True)
         caught = caught or np.abs(o_bad - o_loop).max() > 1e-6
     assert caught, kind
+
+
+# ---- query and key lengths that differ (causal: queries aligned with the last keys) ----
+
+def _rand_qk(nq, nk, d, seed, scale=1.0):
+    r = np.random.default_rng(seed)
+    return (scale * r.standard_normal((nq, d)), scale * r.standard_normal((nk, d)),
+            scale * r.standard_normal((nk, d)), scale * r.standard_normal((nq, d)))
+
+
+QK_CASES = [  # (N_q, N_k, causal, kv_len)
+    (1, 5, True, None), (1, 5, False, None), (5, 2, True, None), (3, 7, False, None),
+    (4, 6, True, 4), (6, 3, True, 2), (2, 8, True, 7),
+]
+
+
+@pytest.mark.parametrize("nq,nk,causal,kv_len", QK_CASES)
+def test_gradients_match_finite_differences_unequal_lengths(nq, nk, causal, kv_len):
+    d = 4
+    q, k, v, do = _rand_qk(nq, nk, d, 12)
+    s = 1.0 / math.sqrt(d)
+    g = ref.head_backward(q, k, v, do, s, causal, kv_len)
+    for name, x in (("dq", q), ("dk", k), ("dv", v)):
+        fd = _fd_grad(lambda: _loss(q, k, v, do, s, causal, kv_len), x)
+        assert np.abs(fd - g[name]).max() / max(np.abs(fd).max(), 1e-3) < 1e-6, name
+
+
+def _loops_forward_qk(q, k, v, s, causal, kv_len):
+    """Scalar loops with the alignment spelled out: query i of N_q is position i + N_k - N_q
+    of the key sequence and sees the keys at or before that position."""
+    nq, nk, d = len(q), len(k), len(q[0])
+    o = [[0.0] * d for _ in range(nq)]
+    lse = [-math.inf] * nq
+    for i in range(nq):
+        pos = i + nk - nq
+        sc = [(j, s * sum(q[i][t] * k[j][t] for t in range(d))) for j in range(nk)
+              if (not causal or j <= pos) and (kv_len is None or j < kv_len)]
+        if not sc:
+            continue
+        mx = max(x for _, x in sc)
+        den = sum(math.exp(x - mx) for _, x in sc)
+        lse[i] = mx + math.log(den)
+        for j, x in sc:
+            for t in range(d):
+                o[i][t] += math.exp(x - mx) / den * v[j][t]
+    return np.array(o), np.array(lse)
+
+
+@pytest.mark.parametrize("nq,nk,causal,kv_len", QK_CASES)
+def test_forward_matches_scalar_loops_unequal_lengths(nq, nk, causal, kv_len):
+    q, k, v, _ = _rand_qk(nq, nk, 3, 13, scale=1.5)
+    o, lse = ref.head_forward(q, k, v, 0.6, causal, kv_len)
+    o2, lse2 = _loops_forward_qk(q.tolist(), k.tolist(), v.tolist(), 0.6, causal, kv_len)
+    np.testing.assert_allclose(o, o2, atol=1e-13)
+    np.testing.assert_array_equal(np.isinf(lse), np.isinf(lse2))
+    fin = np.isfinite(lse2)
+    np.testing.assert_allclose(lse[fin], lse2[fin], atol=1e-13)
+
+
+def test_fewer_queries_are_the_last_rows_of_the_square_causal_problem():
+    # N_q < N_k causal: exactly the last N_q rows of the N_k x N_k causal problem (pinned
+    # above by loops, finite differences and torch); with dO zero on the other rows the
+    # square problem's dK and dV are those of the short one.
+    nq, nk, d = 7, 19, 8
+    r = np.random.default_rng(14)
+    qf, k, v, dof = (r.standard_normal((nk, d)) for _ in range(4))
+    dof[: nk - nq] = 0.0
+    s = 0.35
+    sq = ref.head_backward(qf, k, v, dof, s, True, None)
+    sh = ref.head_backward(qf[nk - nq:], k, v, dof[nk - nq:], s, True, None)
+    for name in ("o", "lse", "dq"):
+        np.testing.assert_allclose(sh[name], sq[name][nk - nq:], rtol=0, atol=1e-12)
+    for name in ("dk", "dv"):
+        np.testing.assert_allclose(sh[name], sq[name], rtol=0, atol=1e-12)
+
+
+def test_more_queries_than_keys_leaves_the_first_rows_empty():
+    nq, nk, d = 9, 4, 5
+    q, k, v, do = _rand_qk(nq, nk, d, 15)
+    g = ref.head_backward(q, k, v, do, 0.4, True, None)
+    lead = nq - nk
+    assert np.all(g["o"][:lead] == 0) and np.all(np.isneginf(g["lse"][:lead])) and np.all(g["dq"][:lead] == 0)
+    sq = ref.head_backward(q[lead:], k, v, do[lead:], 0.4, True, None)  # the square problem
+    for name in ("o", "lse", "dq"):
+        np.testing.assert_allclose(g[name][lead:], sq[name], rtol=0, atol=1e-12)
+    for name in ("dk", "dv"):
+        np.testing.assert_allclose(g[name], sq[name], rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("nq,nk,causal,kv_len", [(20, 45, True, None), (45, 20, True, None),
+                                                 (30, 50, False, 33), (24, 40, True, 35)])
+def test_matches_torch_fp64_autograd_unequal_lengths(nq, nk, causal, kv_len):
+    d = 16
+    q, k, v, do = _rand_qk(nq, nk, d, 16)
+    s = 1 / math.sqrt(d)
+    g = ref.head_backward(q, k, v, do, s, causal, kv_len)
+    tq, tk, tv = (torch.tensor(x, dtype=torch.float64, requires_grad=True) for x in (q, k, v))
+    pos = torch.arange(nq)[:, None] + (nk - nq)  # each query's position in the key sequence
+    j = torch.arange(nk)[None, :]
+    masked = torch.zeros(nq, nk, dtype=torch.bool)
+    if causal:
+        masked |= j > pos
+    if kv_len is not None:
+        masked |= j >= kv_len
+    logits = ((tq @ tk.T) * s).masked_fill(masked, float("-inf"))
+    live = ~masked.all(dim=1)  # rows with at least one key; the others are O = 0, LSE = -inf
+    p = torch.zeros(nq, nk, dtype=torch.float64)
+    p[live] = torch.softmax(logits[live], dim=-1)
+    o = p @ tv
+    o.backward(torch.tensor(do))
+    lse = torch.logsumexp(logits, dim=-1)
+    for name, a, b in (("o", g["o"], o.detach().numpy()), ("lse", g["lse"], lse.detach().numpy()),
+                       ("dq", g["dq"], tq.grad.numpy()), ("dk", g["dk"], tk.grad.numpy()),
+                       ("dv", g["dv"], tv.grad.numpy())):
+        fin = np.isfinite(b)
+        assert np.array_equal(np.isfinite(a), fin), name
+        assert np.abs(a[fin] - b[fin]).max() <= 1e-12 * max(1.0, np.abs(b[fin]).max()), name
+
+
+def test_pins_catch_a_reversed_alignment():
+    # a copy of the mask with the offset's sign flipped (queries aligned with the first keys)
+    nq, nk, d = 3, 7, 4
+    q, k, v, do = _rand_qk(nq, nk, d, 17)
+    sm = 0.5 * (q @ k.T)
+    sm[~ref.keep_mask(np.arange(nq), np.arange(nk), True, None, nq - nk)] = -np.inf
+    p, _, _, _ = ref.softmax_stats(sm)
+    o_bad = p @ v
+    o_loop, _ = _loops_forward_qk(q.tolist(), k.tolist(), v.tolist(), 0.5, True, None)
+    assert np.abs(o_bad - o_loop).max() > 1e-3
