@@ -75,6 +75,18 @@ FA_API int fa_forward(const void* q, const void* k, const void* v, void* o, floa
 FA_API int fa_forward_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
                   float scale, int causal, const int32_t* kv_len, fa_stream_t stream);
 
+/* As fa_forward_ex, with query and key lengths that may differ: q and o are
+ * [B, H, Nq, d], k and v [B, H, Nk, d], lse [B, H, Nq]; kv_len values are
+ * clamped to [0, Nk]. With causal = 1 the queries stand for the last Nq
+ * positions of the keys' sequence: query row i keeps key j iff
+ * j <= i + Nk - Nq (for Nq = Nk the pages' rule j <= i; the pages state only
+ * that case). When Nq > Nk the first Nq - Nk rows keep no key and get O = 0,
+ * LSE = -inf. Nq = 0 with Nk > 0 or the reverse returns FA_ERR_UNSUPPORTED;
+ * both 0 is FA_OK with nothing to do. fa_forward_ex(.., N, ..) is exactly
+ * fa_forward_qk(.., N, N, ..). */
+FA_API int fa_forward_qk(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq,
+                         int Nk, int d, float scale, int causal, const int32_t* kv_len, fa_stream_t stream);
+
 /* Bytes of device workspace fa_backward needs: per (b, h), D and a base-2
  * copy of LSE for every query row and an fp32 dQ accumulator, each padded to
  * a multiple of 128 rows. Linear in N. Returns 0 for unsupported d. */
@@ -98,6 +110,16 @@ FA_API int fa_backward_ex(const void* q, const void* k, const void* v, const voi
                    void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale, int causal,
                    const int32_t* kv_len, void* workspace, size_t workspace_bytes, fa_stream_t stream);
 
+/* Backward of fa_forward_qk: q, o, dO, dq are [B, H, Nq, d], k, v, dk, dv
+ * [B, H, Nk, d], lse [B, H, Nq]; the same masking as the forward call. The
+ * workspace is fa_backward_workspace_size(B, H, Nq, d) bytes (it holds
+ * per-query-row data only). fa_backward_ex(.., N, ..) is exactly
+ * fa_backward_qk(.., N, N, ..). */
+FA_API int fa_backward_qk(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                          const float* lse, void* dq, void* dk, void* dv, int B, int H, int Nq, int Nk, int d,
+                          float scale, int causal, const int32_t* kv_len, void* workspace, size_t workspace_bytes,
+                          fa_stream_t stream);
+
 /* One stage of fa_backward_ex, same arguments; running stages 0, 1, 2 in
  * order on one stream is exactly fa_backward_ex. Exposed so that each kernel
  * can be timed on its own.
@@ -110,6 +132,12 @@ FA_API int fa_backward_stage(int stage, const void* q, const void* k, const void
                              const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d,
                              float scale, int causal, const int32_t* kv_len, void* workspace,
                              size_t workspace_bytes, fa_stream_t stream);
+
+/* One stage of fa_backward_qk (stages as for fa_backward_stage). */
+FA_API int fa_backward_stage_qk(int stage, const void* q, const void* k, const void* v, const void* o,
+                                const void* dO, const float* lse, void* dq, void* dk, void* dv, int B, int H,
+                                int Nq, int Nk, int d, float scale, int causal, const int32_t* kv_len,
+                                void* workspace, size_t workspace_bytes, fa_stream_t stream);
 
 /* Backward pass for callers that cannot allocate device memory: no workspace
  * argument. The pages have no counterpart of this entry point; it exists for

@@ -26,10 +26,13 @@ SIGNATURES = {
     "libfa.so": {
         "fa_forward": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp]),
         "fa_forward_ex": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp, _vp]),
+        "fa_forward_qk": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _vp, _vp]),
         "fa_backward_workspace_size": (_sz, [_i, _i, _i, _i]),
         "fa_backward": (_i, [_vp] * 9 + [_i, _i, _i, _i, _f, _i, _vp, _sz, _vp]),
         "fa_backward_ex": (_i, [_vp] * 9 + [_i, _i, _i, _i, _f, _i, _vp, _vp, _sz, _vp]),
         "fa_backward_stage": (_i, [_i] + [_vp] * 9 + [_i, _i, _i, _i, _f, _i, _vp, _vp, _sz, _vp]),
+        "fa_backward_qk": (_i, [_vp] * 9 + [_i, _i, _i, _i, _i, _f, _i, _vp, _vp, _sz, _vp]),
+        "fa_backward_stage_qk": (_i, [_i] + [_vp] * 9 + [_i, _i, _i, _i, _i, _f, _i, _vp, _vp, _sz, _vp]),
         "fa_backward_noalloc": (_i, [_vp] * 9 + [_i, _i, _i, _i, _f, _i, _vp, _vp]),
         "fa_backward_noalloc_max_bytes": (_sz, []),
         "fa_status_string": (ctypes.c_char_p, [_i]),

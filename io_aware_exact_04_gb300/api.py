@@ -48,22 +48,31 @@ def _kv(kv_len: Optional[torch.Tensor], B: int, device) -> Optional[torch.Tensor
     return kv_len
 
 
+def _kv_shape(q, k):
+    """[B, H, N_k, d] of k: q's batch, heads and head dim with its own length."""
+    _check_bhnd("k", k)
+    if k.shape[0] != q.shape[0] or k.shape[1] != q.shape[1] or k.shape[3] != q.shape[3]:
+        raise ValueError(f"k has shape {tuple(k.shape)}; q is {tuple(q.shape)} (only N may differ)")
+    return tuple(k.shape)
+
+
 def forward(q, k, v, causal: bool = False, scale: Optional[float] = None, kv_len=None, out=None,
             lse=None) -> Tuple[torch.Tensor, torch.Tensor]:
-    """O, LSE of exact softmax attention (see include/fa.h: fa_forward_ex)."""
+    """O, LSE of exact softmax attention (include/fa.h: fa_forward_qk). q is [B, H, N_q, d];
+    k and v are [B, H, N_k, d] (N_k may differ; causal aligns the queries with the last keys)."""
     _check_bhnd("q", q)
     B, H, N, d = q.shape
-    _check_bhnd("k", k, q.shape)
-    _check_bhnd("v", v, q.shape)
+    kshape = _kv_shape(q, k)
+    _check_bhnd("v", v, kshape)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     o = torch.empty_like(q) if out is None else out
     _check_bhnd("out", o, q.shape)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
     kv = _kv(kv_len, B, q.device)
     with torch.cuda.device(q.device):
-        rc = _lib_fa().fa_forward_ex(_p(q), _p(k), _p(v), _p(o), _p(lse), B, H, N, d, scale, int(bool(causal)),
-                                     _p(kv), _stream(q.device))
-    _lib.check(rc, "fa_forward_ex")
+        rc = _lib_fa().fa_forward_qk(_p(q), _p(k), _p(v), _p(o), _p(lse), B, H, N, kshape[2], d, scale,
+                                     int(bool(causal)), _p(kv), _stream(q.device))
+    _lib.check(rc, "fa_forward_qk")
     return o, lse
 
 
@@ -73,26 +82,28 @@ def workspace_bytes(B: int, H: int, N: int, d: int) -> int:
 
 def backward(q, k, v, o, do, lse, causal: bool = False, scale: Optional[float] = None, kv_len=None,
              dq=None, dk=None, dv=None, workspace=None):
-    """dQ, dK, dV by recomputation from Q, K, V, O, dO and LSE (fa_backward_ex)."""
+    """dQ, dK, dV by recomputation from Q, K, V, O, dO and LSE (fa_backward_qk); shapes as
+    for forward."""
     _check_bhnd("q", q)
     B, H, N, d = q.shape
-    for name, t in (("k", k), ("v", v), ("o", o), ("do", do)):
-        _check_bhnd(name, t, q.shape)
+    kshape = _kv_shape(q, k)
+    for name, t, shp in (("v", v, kshape), ("o", o, q.shape), ("do", do, q.shape)):
+        _check_bhnd(name, t, shp)
     if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, N) or not lse.is_contiguous():
         raise ValueError("lse must be a contiguous float32 [B, H, N] tensor")
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     dq = torch.empty_like(q) if dq is None else dq
-    dk = torch.empty_like(q) if dk is None else dk
-    dv = torch.empty_like(q) if dv is None else dv
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(k) if dv is None else dv
     need = workspace_bytes(B, H, N, d)
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
     kv = _kv(kv_len, B, q.device)
     with torch.cuda.device(q.device):
-        rc = _lib_fa().fa_backward_ex(_p(q), _p(k), _p(v), _p(o), _p(do), _p(lse), _p(dq), _p(dk), _p(dv),
-                                      B, H, N, d, scale, int(bool(causal)), _p(kv), _p(workspace),
+        rc = _lib_fa().fa_backward_qk(_p(q), _p(k), _p(v), _p(o), _p(do), _p(lse), _p(dq), _p(dk), _p(dv),
+                                      B, H, N, kshape[2], d, scale, int(bool(causal)), _p(kv), _p(workspace),
                                       workspace.numel(), _stream(q.device))
-    _lib.check(rc, "fa_backward_ex")
+    _lib.check(rc, "fa_backward_qk")
     return dq, dk, dv
 
 

@@ -42,15 +42,18 @@ int* device_status(int* err) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-int check_common(int B, int H, int N, int d, float scale, int causal) {
-  if (B < 0 || H < 0 || N < 0) return FA_ERR_INVALID_ARG;
+int check_common(int B, int H, int Nq, int Nk, int d, float scale, int causal) {
+  if (B < 0 || H < 0 || Nq < 0 || Nk < 0) return FA_ERR_INVALID_ARG;
   if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
   if (!(scale > 0.f) || !std::isfinite(scale)) return FA_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
   const long long BH = (long long)B * H;
   if (BH > 65535) return FA_ERR_UNSUPPORTED;  // documented limit on B*H
-  if ((long long)N + 255 > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
-  if ((N + 127) / 128 > 65535) return FA_ERR_UNSUPPORTED;  // key tiles / query pairs on the grid's y axis
+  for (const int n : {Nq, Nk}) {
+    if ((long long)n + 255 > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+    if ((n + 127) / 128 > 65535) return FA_ERR_UNSUPPORTED;  // key tiles / query pairs on the grid's y axis
+  }
+  if (BH > 0 && (Nq == 0) != (Nk == 0)) return FA_ERR_UNSUPPORTED;  // queries without keys or keys without queries
   return FA_OK;
 }
 
@@ -127,11 +130,11 @@ const char* fa_status_string(int s) {
   }
 }
 
-int fa_forward_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
-                  float scale, int causal, const int32_t* kv_len, fa_stream_t stream) {
-  int rc = check_common(B, H, N, d, scale, causal);
+int fa_forward_qk(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq, int Nk,
+                  int d, float scale, int causal, const int32_t* kv_len, fa_stream_t stream) {
+  int rc = check_common(B, H, Nq, Nk, d, scale, causal);
   if (rc != FA_OK) return rc;
-  if ((long long)B * H * N == 0) return FA_OK;
+  if ((long long)B * H * Nq == 0) return FA_OK;
   if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
     return FA_ERR_MISALIGNED;
@@ -140,8 +143,10 @@ int fa_forward_ex(const void* q, const void* k, const void* v, void* o, float* l
   if (!status) return err;
   fa::FwdArgs a;
   a.H = H;
-  a.N = N;
-  a.n_pairs = (N + 255) / 256;
+  a.N = Nq;
+  a.Nk = Nk;
+  a.coff = Nk - Nq;
+  a.n_pairs = (Nq + 255) / 256;
   a.causal = causal;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.kv_len = kv_len;
@@ -149,6 +154,11 @@ int fa_forward_ex(const void* q, const void* k, const void* v, void* o, float* l
   a.o = static_cast<uint16_t*>(o);
   a.status = status;
   return fa::launch_fwd(q, k, v, o, a, B * H, d, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int fa_forward_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+                  float scale, int causal, const int32_t* kv_len, fa_stream_t stream) {
+  return fa_forward_qk(q, k, v, o, lse, B, H, N, N, d, scale, causal, kv_len, stream);
 }
 
 int fa_forward(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
@@ -161,14 +171,15 @@ size_t fa_backward_workspace_size(int B, int H, int N, int d) {
   return ws_layout(B, H, N, d).total;
 }
 
-int fa_backward_stage(int stage, const void* q, const void* k, const void* v, const void* o, const void* dO,
-                      const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale,
-                      int causal, const int32_t* kv_len, void* workspace, size_t workspace_bytes,
-                      fa_stream_t stream) {
+int fa_backward_stage_qk(int stage, const void* q, const void* k, const void* v, const void* o, const void* dO,
+                         const float* lse, void* dq, void* dk, void* dv, int B, int H, int Nq, int Nk, int d,
+                         float scale, int causal, const int32_t* kv_len, void* workspace, size_t workspace_bytes,
+                         fa_stream_t stream) {
   if (stage < 0 || stage > 2) return FA_ERR_INVALID_ARG;
-  int rc = check_common(B, H, N, d, scale, causal);
+  int rc = check_common(B, H, Nq, Nk, d, scale, causal);
   if (rc != FA_OK) return rc;
-  if ((long long)B * H * N == 0) return FA_OK;
+  if ((long long)B * H * Nq == 0) return FA_OK;
+  const int N = Nq;
   if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv || !workspace) return FA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dO) || !aligned16(lse) ||
       !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
@@ -184,6 +195,8 @@ int fa_backward_stage(int stage, const void* q, const void* k, const void* v, co
   a.H = H;
   a.N = N;
   a.Npad = (int)round_up(N, 128);
+  a.Nk = Nk;
+  a.coff = Nk - Nq;
   a.causal = causal;
   a.scale = scale;
   a.scale_log2 = scale * 1.4426950408889634f;
@@ -201,15 +214,30 @@ int fa_backward_stage(int stage, const void* q, const void* k, const void* v, co
   return fa::launch_bwd_stage(stage, q, k, v, a, B * H, d, reinterpret_cast<cudaStream_t>(stream));
 }
 
-int fa_backward_ex(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
-                   void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale, int causal,
+int fa_backward_stage(int stage, const void* q, const void* k, const void* v, const void* o, const void* dO,
+                      const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale,
+                      int causal, const int32_t* kv_len, void* workspace, size_t workspace_bytes,
+                      fa_stream_t stream) {
+  return fa_backward_stage_qk(stage, q, k, v, o, dO, lse, dq, dk, dv, B, H, N, N, d, scale, causal, kv_len,
+                              workspace, workspace_bytes, stream);
+}
+
+int fa_backward_qk(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
+                   void* dq, void* dk, void* dv, int B, int H, int Nq, int Nk, int d, float scale, int causal,
                    const int32_t* kv_len, void* workspace, size_t workspace_bytes, fa_stream_t stream) {
   for (int stage = 0; stage < 3; ++stage) {
-    const int rc = fa_backward_stage(stage, q, k, v, o, dO, lse, dq, dk, dv, B, H, N, d, scale, causal, kv_len,
-                                     workspace, workspace_bytes, stream);
+    const int rc = fa_backward_stage_qk(stage, q, k, v, o, dO, lse, dq, dk, dv, B, H, Nq, Nk, d, scale, causal,
+                                        kv_len, workspace, workspace_bytes, stream);
     if (rc != FA_OK) return rc;
   }
   return FA_OK;
+}
+
+int fa_backward_ex(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
+                   void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale, int causal,
+                   const int32_t* kv_len, void* workspace, size_t workspace_bytes, fa_stream_t stream) {
+  return fa_backward_qk(q, k, v, o, dO, lse, dq, dk, dv, B, H, N, N, d, scale, causal, kv_len, workspace,
+                        workspace_bytes, stream);
 }
 
 int fa_backward(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,

@@ -182,18 +182,19 @@ __global__ void __launch_bounds__(448, 1)
   const int j = blockIdx.y;  // key tile
   const int bh = blockIdx.x;
   const int b = bh / a.H;
-  int kv = a.N;
-  if (a.kv_len) kv = min(max(a.kv_len[b], 0), a.N);
+  int kv = a.Nk;
+  if (a.kv_len) kv = min(max(a.kv_len[b], 0), a.Nk);
   const int k0 = j * 128;
   const int n_qt = (a.N + BR - 1) / BR;
-  const int i_start = a.causal ? (k0 / BR) : 0;
-  const int n_it = (k0 >= kv) ? 0 : (n_qt - i_start);
+  // causal: the first query row that sees key k0 is k0 - coff
+  const int i_start = a.causal ? max(0, k0 - a.coff) / BR : 0;
+  const int n_it = (k0 >= kv || i_start >= n_qt) ? 0 : (n_qt - i_start);
 
   if (n_it == 0) {
-    // no valid key in this tile: its dK and dV rows are zero
-    const int rows = min(128, a.N - k0);
+    // no valid key in this tile, or no query sees it: its dK and dV rows are zero
+    const int rows = min(128, a.Nk - k0);
     for (int idx = threadIdx.x; idx < rows * (D / 8); idx += blockDim.x) {
-      const size_t off = ((size_t)bh * a.N + k0 + idx / (D / 8)) * D + (idx % (D / 8)) * 8;
+      const size_t off = ((size_t)bh * a.Nk + k0 + idx / (D / 8)) * D + (idx % (D / 8)) * 8;
       *reinterpret_cast<uint4*>(a.dk + off) = make_uint4(0, 0, 0, 0);
       *reinterpret_cast<uint4*>(a.dv + off) = make_uint4(0, 0, 0, 0);
     }
@@ -428,7 +429,7 @@ __global__ void __launch_bounds__(448, 1)
       if (!(ok = wait_warp(qdo_full(s), (it >> 1) & 1, st, SITE_B_QDO_FULL))) break;
       if (!(ok = wait_warp(s_full, it & 1, st, SITE_B_S_FULL))) break;
       tc_fence_after();
-      const bool need_mask = (k0 + 127 >= kv) || (a.causal && k0 + 127 > q0);
+      const bool need_mask = (k0 + 127 >= kv) || (a.causal && k0 + 127 > q0 + a.coff);
       // ---- P^T = exp2(S^T s log2e + lse2), bf16 into the S^T columns (lse2 = -LSE log2e)
 #pragma unroll
       for (int ch = 0; ch < NCH; ++ch) {
@@ -443,7 +444,7 @@ __global__ void __launch_bounds__(448, 1)
         }
         tmem_wait_ld();
         if (need_mask) {  // only steps on the diagonal or past kv_len: masked S -> -inf, so P = 0
-          const int lim = key >= kv ? 32 : (a.causal ? key - q0 - cb : 0);  // columns [0, lim)
+          const int lim = key >= kv ? 32 : (a.causal ? key - a.coff - q0 - cb : 0);  // columns [0, lim)
 #pragma unroll
           for (int c = 0; c < 32; ++c)
             if (c < lim) sv[c] = 0xff800000u;
@@ -599,12 +600,14 @@ __device__ __forceinline__ TileD64 tile_d64(int t, const BwdArgs& a) {
   TileD64 r;
   const int j = t / a.BH;
   r.bh = t - j * a.BH;
-  r.kv = a.N;
-  if (a.kv_len) r.kv = min(max(a.kv_len[r.bh / a.H], 0), a.N);
+  r.kv = a.Nk;
+  if (a.kv_len) r.kv = min(max(a.kv_len[r.bh / a.H], 0), a.Nk);
   r.k0 = j * 128;
   const int n_qt = (a.N + Bwd64::BR - 1) / Bwd64::BR;
-  r.i_start = a.causal ? (r.k0 / Bwd64::BR) : 0;  // even: k0 is a multiple of 128
-  const int n = (r.k0 >= r.kv) ? 0 : (n_qt - r.i_start);
+  // causal: the first query row that sees key k0 is k0 - coff; steps start on a 128-row
+  // boundary (even) so that dQ pairs cover whole 128-row blocks
+  r.i_start = a.causal ? (max(0, r.k0 - a.coff) >> 7) << 1 : 0;
+  const int n = (r.k0 >= r.kv || r.i_start >= n_qt) ? 0 : (n_qt - r.i_start);
   r.n_it = n + (n & 1);  // whole pairs: a trailing step past N reads zero Q/dO and -inf lse2, so adds nothing
   return r;
 }
@@ -662,7 +665,7 @@ __global__ void __launch_bounds__(480, 1)
   const uint32_t ds0_count = smem_u32(tmem_slot + 2);
   DevStatus st{a.status, abort_flag};
 
-  const int T = a.BH * ((a.N + 127) >> 7);
+  const int T = a.BH * ((a.Nk + 127) >> 7);
   const int G = gridDim.x, cta = blockIdx.x;
 
   // The producer warp initialises the barriers and starts the first copies (K, V and the first
@@ -937,9 +940,9 @@ __global__ void __launch_bounds__(480, 1)
       if (t < 0) break;
       const TileD64 tl = tile_d64(t, a);
       if (tl.n_it == 0) {  // no valid key in this tile: its dK and dV rows are zero
-        const int rows = min(128, a.N - tl.k0);
+        const int rows = min(128, a.Nk - tl.k0);
         for (int idx = tid; idx < rows * (C::D / 8); idx += 128) {
-          const size_t off = ((size_t)tl.bh * a.N + tl.k0 + idx / (C::D / 8)) * C::D + (idx % (C::D / 8)) * 8;
+          const size_t off = ((size_t)tl.bh * a.Nk + tl.k0 + idx / (C::D / 8)) * C::D + (idx % (C::D / 8)) * 8;
           *reinterpret_cast<uint4*>(a.dk + off) = make_uint4(0, 0, 0, 0);
           *reinterpret_cast<uint4*>(a.dv + off) = make_uint4(0, 0, 0, 0);
         }
@@ -1052,7 +1055,7 @@ __global__ void __launch_bounds__(480, 1)
         if (!(ok = wait_warp(qdo_full(s), (gs / NQS) & 1, st, SITE_B_QDO_FULL))) break;
         if (!(ok = wait_warp(s_full(w), par, st, SITE_B_S_FULL))) break;
         tc_fence_after();
-        const bool need_mask = (tl.k0 + 127 >= tl.kv) || (a.causal && tl.k0 + 127 > q0);
+        const bool need_mask = (tl.k0 + 127 >= tl.kv) || (a.causal && tl.k0 + 127 > q0 + a.coff);
         // ---- P^T = exp2(S^T s log2e + lse2) (lse2 = -LSE log2e) -> bf16 pairs in the first 32
         //      columns of this buffer, kept in registers too: S^T's columns are overwritten by
         //      the next step once P^T is out
@@ -1064,7 +1067,7 @@ __global__ void __launch_bounds__(480, 1)
           tmem_ld32(tST + 32, sv[1]);
           tmem_wait_ld();
           if (need_mask) {  // only steps on the diagonal or past kv_len: masked S -> -inf, so P = 0
-            const int lim = key >= tl.kv ? 64 : (a.causal ? key - q0 : 0);  // columns [0, lim)
+            const int lim = key >= tl.kv ? 64 : (a.causal ? key - a.coff - q0 : 0);  // columns [0, lim)
 #pragma unroll
             for (int c = 0; c < 64; ++c)
               if (c < lim) sv[c >> 5][c & 31] = 0xff800000u;
@@ -1153,19 +1156,19 @@ template <int D>
 static int launch_bwd_main_d(const void* q, const void* k, const void* v, const BwdArgs& a, int BH,
                              cudaStream_t stream) {
   constexpr int BR = (D == 64) ? Bwd64::BR : BwdCfg<D>::BR;  // query rows per step
-  const uint64_t N = (uint64_t)a.N;
+  const uint64_t N = (uint64_t)a.N, Nk = (uint64_t)a.Nk;
   const auto BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const auto SW = CU_TENSOR_MAP_SWIZZLE_128B;
   CUtensorMap mq, mk, mv, mdo, mdk, mdv, mdq;
   if (!make_tmap_3d(&mq, q, BF, 2, D, N, BH, 64, BR, SW) || !make_tmap_3d(&mdo, a.dO, BF, 2, D, N, BH, 64, BR, SW) ||
-      !make_tmap_3d(&mk, k, BF, 2, D, N, BH, 64, 128, SW) || !make_tmap_3d(&mv, v, BF, 2, D, N, BH, 64, 128, SW) ||
-      !make_tmap_3d(&mdk, a.dk, BF, 2, D, N, BH, 64, 128, SW) ||
-      !make_tmap_3d(&mdv, a.dv, BF, 2, D, N, BH, 64, 128, SW) ||
+      !make_tmap_3d(&mk, k, BF, 2, D, Nk, BH, 64, 128, SW) || !make_tmap_3d(&mv, v, BF, 2, D, Nk, BH, 64, 128, SW) ||
+      !make_tmap_3d(&mdk, a.dk, BF, 2, D, Nk, BH, 64, 128, SW) ||
+      !make_tmap_3d(&mdv, a.dv, BF, 2, D, Nk, BH, 64, 128, SW) ||
       !make_tmap_3d(&mdq, a.dq_acc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, D, (uint64_t)a.Npad, BH, 32,
                     (D == 64) ? 128 : BR, SW))
     return cuda_fail("cuTensorMapEncodeTiled", 0, "tensor map rejected");
   static bool attr_set = false;  // benign race: idempotent
-  dim3 grid(BH, (a.N + 127) / 128);
+  dim3 grid(BH, (a.Nk + 127) / 128);
   if constexpr (D == 64) {
     if (!attr_set) {
       const cudaError_t e = cudaFuncSetAttribute(bwd_kernel_d64<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1176,7 +1179,7 @@ static int launch_bwd_main_d(const void* q, const void* k, const void* v, const 
     // persistent: one CTA per SM (at most one per key tile)
     int sms = 0;
     if (!sm_count(&sms)) return FA_ERR_CUDA;
-    const long long tiles = (long long)BH * ((a.N + 127) / 128);
+    const long long tiles = (long long)BH * ((a.Nk + 127) / 128);
     BwdArgs ap = a;
     ap.BH = BH;
     return launch_pdl(__func__, bwd_kernel_d64<0>, dim3((unsigned)std::min<long long>(tiles, sms)),

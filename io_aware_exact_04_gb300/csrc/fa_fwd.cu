@@ -58,6 +58,15 @@ struct FwdCfg {
 enum { SITE_F_KV_EMPTY = 1, SITE_F_Q_FULL, SITE_F_K_FULL, SITE_F_V_FULL, SITE_F_P_READY, SITE_F_S_FULL,
        SITE_F_O_DONE, SITE_F_DRAIN, SITE_F_S_FREE };
 
+// Key tiles that the query tile of rows [qs, qs + 128) needs: those below kv (the valid keys)
+// that some row of the tile may see. Causal row i sees keys j <= i + coff.
+__device__ __forceinline__ int key_tiles(int qs, int nq, int nkt, int causal, int coff) {
+  if (qs >= nq) return 0;
+  if (!causal) return nkt;
+  const int lim = min(qs + 128, nq) + coff;  // keys [0, lim) are visible to some row
+  return lim <= 0 ? 0 : min(nkt, (lim + 127) >> 7);
+}
+
 template <int D>
 __global__ void __launch_bounds__(352, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -93,16 +102,13 @@ __global__ void __launch_bounds__(352, 1)
   const int pair = a.n_pairs - 1 - (int)blockIdx.y;
   const int bh = blockIdx.x;
   const int b = bh / a.H;
-  int kv = a.N;
-  if (a.kv_len) kv = min(max(a.kv_len[b], 0), a.N);
+  int kv = a.Nk;
+  if (a.kv_len) kv = min(max(a.kv_len[b], 0), a.Nk);
   const int nkt = (kv + 127) >> 7;
   const int q0 = pair * 256;
   int n_t[2];
 #pragma unroll
-  for (int t = 0; t < 2; ++t) {
-    const int qs = q0 + t * 128;
-    n_t[t] = (qs >= a.N) ? 0 : (a.causal ? min(nkt, (qs >> 7) + 1) : nkt);
-  }
+  for (int t = 0; t < 2; ++t) n_t[t] = key_tiles(q0 + t * 128, a.N, nkt, a.causal, a.coff);
   const int nmax = max(n_t[0], n_t[1]);
 
   // The producer warp initialises the barriers and starts the first copies (Q and the first
@@ -320,9 +326,9 @@ __global__ void __launch_bounds__(352, 1)
           if (lane == 0) mbar_arrive(s_free(t));
         }
         const int k0 = j * 128;
-        const bool need_mask = (k0 + 127 >= kv) || (a.causal && k0 + 127 > qs);
+        const bool need_mask = (k0 + 127 >= kv) || (a.causal && k0 + 127 > qs + a.coff);
         if (need_mask) {
-          const int lim = a.causal ? min(kv, grow + 1) : kv;  // keys [0, lim) are valid
+          const int lim = a.causal ? min(kv, grow + 1 + a.coff) : kv;  // keys [0, lim) are valid
 #pragma unroll
           for (int c = 0; c < 128; ++c)
             if (k0 + c >= lim) sv[c] = -INFINITY;
@@ -481,14 +487,11 @@ __device__ __forceinline__ ItemF64 item_f64(int t, const FwdArgs& a, int BH) {
   const int p = t / BH;
   it.bh = t - p * BH;
   it.q0 = (a.n_pairs - 1 - p) * 256;
-  it.kv = a.N;
-  if (a.kv_len) it.kv = min(max(a.kv_len[it.bh / a.H], 0), a.N);
+  it.kv = a.Nk;
+  if (a.kv_len) it.kv = min(max(a.kv_len[it.bh / a.H], 0), a.Nk);
   const int nkt = (it.kv + 127) >> 7;
 #pragma unroll
-  for (int u = 0; u < 2; ++u) {
-    const int qs = it.q0 + u * 128;
-    it.n[u] = (qs >= a.N) ? 0 : (a.causal ? min(nkt, (qs >> 7) + 1) : nkt);
-  }
+  for (int u = 0; u < 2; ++u) it.n[u] = key_tiles(it.q0 + u * 128, a.N, nkt, a.causal, a.coff);
   it.nmax = max(it.n[0], it.n[1]);
   return it;
 }
@@ -803,9 +806,9 @@ __global__ void __launch_bounds__(352, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(s_free(t));
           const int k0 = j * 128;
-          const bool need_mask = (k0 + 127 >= kvv) || (a.causal && k0 + 127 > qs);
+          const bool need_mask = (k0 + 127 >= kvv) || (a.causal && k0 + 127 > qs + a.coff);
           if (need_mask) {
-            const int lim = a.causal ? min(kvv, grow + 1) : kvv;  // keys [0, lim) are valid
+            const int lim = a.causal ? min(kvv, grow + 1 + a.coff) : kvv;  // keys [0, lim) are valid
 #pragma unroll
             for (int c = 0; c < 128; ++c)
               if (k0 + c >= lim) sv[c] = -INFINITY;
@@ -939,11 +942,11 @@ static int launch_fwd_d(const void* q, const void* k, const void* v, void* o, co
                         cudaStream_t stream) {
   using C = FwdCfg<D>;
   CUtensorMap mq, mk, mv, mo;
-  const uint64_t N = (uint64_t)args.N;
+  const uint64_t N = (uint64_t)args.N, Nk = (uint64_t)args.Nk;
   const auto BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const auto SW = CU_TENSOR_MAP_SWIZZLE_128B;
-  if (!make_tmap_3d(&mq, q, BF, 2, D, N, BH, 64, 128, SW) || !make_tmap_3d(&mk, k, BF, 2, D, N, BH, 64, 128, SW) ||
-      !make_tmap_3d(&mv, v, BF, 2, D, N, BH, 64, 128, SW) || !make_tmap_3d(&mo, o, BF, 2, D, N, BH, 64, 128, SW))
+  if (!make_tmap_3d(&mq, q, BF, 2, D, N, BH, 64, 128, SW) || !make_tmap_3d(&mk, k, BF, 2, D, Nk, BH, 64, 128, SW) ||
+      !make_tmap_3d(&mv, v, BF, 2, D, Nk, BH, 64, 128, SW) || !make_tmap_3d(&mo, o, BF, 2, D, N, BH, 64, 128, SW))
     return cuda_fail("cuTensorMapEncodeTiled", 0, "tensor map rejected");
   static bool attr_set = false;  // benign race: idempotent
   if (!attr_set) {
@@ -961,11 +964,11 @@ static int launch_fwd_p64(const void* q, const void* k, const void* v, void* o, 
                           cudaStream_t stream) {
   using C = FwdP64;
   CUtensorMap mq, mk, mv, mo;
-  const uint64_t N = (uint64_t)args.N;
+  const uint64_t N = (uint64_t)args.N, Nk = (uint64_t)args.Nk;
   const auto BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const auto SW = CU_TENSOR_MAP_SWIZZLE_128B;
-  if (!make_tmap_3d(&mq, q, BF, 2, 64, N, BH, 64, 128, SW) || !make_tmap_3d(&mk, k, BF, 2, 64, N, BH, 64, 128, SW) ||
-      !make_tmap_3d(&mv, v, BF, 2, 64, N, BH, 64, 128, SW) || !make_tmap_3d(&mo, o, BF, 2, 64, N, BH, 64, 128, SW))
+  if (!make_tmap_3d(&mq, q, BF, 2, 64, N, BH, 64, 128, SW) || !make_tmap_3d(&mk, k, BF, 2, 64, Nk, BH, 64, 128, SW) ||
+      !make_tmap_3d(&mv, v, BF, 2, 64, Nk, BH, 64, 128, SW) || !make_tmap_3d(&mo, o, BF, 2, 64, N, BH, 64, 128, SW))
     return cuda_fail("cuTensorMapEncodeTiled", 0, "tensor map rejected");
   static bool attr_set = false;  // benign race: idempotent
   if (!attr_set) {
@@ -984,11 +987,11 @@ static int launch_fwd_p64(const void* q, const void* k, const void* v, void* o, 
 
 int launch_fwd(const void* q, const void* k, const void* v, void* o, const FwdArgs& args, int BH, int d,
                cudaStream_t stream) {
-  // Short rows (at most 4 query-tile pairs, N <= 1024): the persistent kernel, whose per-CTA
-  // setup and item epilogues overlap the next item's MMAs. Longer rows: one CTA per item,
-  // where the hardware's block dispatch balances the causal work at least as well as the
-  // static order and the per-item setup is amortised over many key tiles.
-  if (d == 64 && args.n_pairs <= 4) return launch_fwd_p64(q, k, v, o, args, BH, stream);
+  // Short rows (at most 4 query-tile pairs and 1024 keys): the persistent kernel, whose
+  // per-CTA setup and item epilogues overlap the next item's MMAs. Longer rows: one CTA per
+  // item, where the hardware's block dispatch balances the causal work at least as well as
+  // the static order and the per-item setup is amortised over many key tiles.
+  if (d == 64 && args.n_pairs <= 4 && args.Nk <= 1024) return launch_fwd_p64(q, k, v, o, args, BH, stream);
   if (d == 64) return launch_fwd_d<64>(q, k, v, o, args, BH, stream);
   if (d == 128) return launch_fwd_d<128>(q, k, v, o, args, BH, stream);
   return FA_ERR_UNSUPPORTED;

@@ -7,8 +7,10 @@
 namespace fa {
 
 struct FwdArgs {
-  int H, N;            // heads per batch, sequence length
-  int n_pairs;         // ceil(N / 256): CTAs per head (two 128-row query tiles each)
+  int H, N;            // heads per batch, query rows N_q (rows of Q, O, LSE)
+  int Nk;              // key rows N_k (rows of K, V)
+  int coff;            // N_k - N_q: causal query row i keeps keys j <= i + coff
+  int n_pairs;         // ceil(N_q / 256): work items per head (two 128-row query tiles each)
   int causal;
   float scale_log2;    // scale * log2(e)
   const int* kv_len;   // [B] device, or null
@@ -18,7 +20,9 @@ struct FwdArgs {
 };
 
 struct BwdArgs {
-  int H, N, Npad;      // Npad = N rounded up to a multiple of 128
+  int H, N, Npad;      // query rows N_q (rows of Q, O, dO, LSE, dQ); Npad = N_q rounded up to 128
+  int Nk;              // key rows N_k (rows of K, V, dK, dV)
+  int coff;            // N_k - N_q: causal query row i keeps keys j <= i + coff
   int BH;              // B * H (set by the launcher of the persistent d = 64 kernel)
   int causal;
   float scale;         // softmax scale s

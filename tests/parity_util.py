@@ -49,9 +49,10 @@ def compare(name, got, want):
     return err, max(bound, ABS_FLOOR)
 
 
-def check_all_heads(B, H, N, d, causal, kv_len=None, seed=0, device=None, qk_scale=1.0):
+def check_all_heads(B, H, N, d, causal, kv_len=None, seed=0, device=None, qk_scale=1.0, Nk=None):
+    """Every head of a [B, H, N, d] problem (keys [B, H, Nk, d]) against the oracle."""
     x = workloads.draw(B, H, N, d, seed=seed, qk_scale=qk_scale,
-                       len_range=None)
+                       len_range=None, Nk=Nk)
     if kv_len is not None:
         x["kv_len"] = torch.tensor(kv_len, dtype=torch.int32)
     g = run_gpu(x, causal, device)

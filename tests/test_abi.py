@@ -90,6 +90,17 @@ def test_backward_argument_errors(lib):
     assert lib.fa_backward_stage(1, *[A] * 9, 1, 1, 128, 96, 0.125, 0, None, A, 1 << 30, None) == 2
 
 
+def test_unequal_length_argument_errors(lib):
+    # queries without keys or keys without queries: unsupported; both empty: nothing to do
+    assert lib.fa_forward_qk(*[A] * 5, 1, 1, 0, 5, 64, 0.125, 1, None, None) == 2
+    assert lib.fa_forward_qk(*[A] * 5, 1, 1, 5, 0, 64, 0.125, 1, None, None) == 2
+    assert lib.fa_forward_qk(*[None] * 5, 1, 1, 0, 0, 64, 0.125, 1, None, None) == 0
+    assert lib.fa_forward_qk(*[A] * 5, 1, 1, 5, -1, 64, 0.125, 1, None, None) == 1
+    assert lib.fa_backward_qk(*[A] * 9, 1, 1, 0, 7, 64, 0.125, 0, None, A, 1 << 30, None) == 2
+    assert lib.fa_backward_qk(*[A] * 9, 1, 1, 3, 7, 96, 0.125, 0, None, A, 1 << 30, None) == 2
+    assert lib.fa_backward_stage_qk(3, *[A] * 9, 1, 1, 3, 7, 64, 0.125, 0, None, A, 1 << 30, None) == 1
+
+
 def test_selftest_argument_errors(built):
     st = _lib.load("libfa_selftest.so")
     assert st.fa_selftest_mma(A, A, A, 96, 64, 0, A, None) == 2

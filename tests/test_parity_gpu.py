@@ -56,6 +56,31 @@ def test_many_tiles_per_cta_match_oracle(gpu, B, H, N, d, causal, kv_len):
     assert_within(check_all_heads(B, H, N, d, causal, kv_len, seed=7 * N + B, device=gpu))
 
 
+# Query and key lengths that differ. Causal rows are aligned with the last keys: row i keeps
+# keys j <= i + N_k - N_q. Offsets that are not multiples of the 64- or 128-row tiles, more
+# queries than keys (leading rows with no key), single queries, and both forward kernels
+# (persistent for N_q <= 1024 and N_k <= 1024 at d = 64, one CTA per item otherwise).
+UNEQUAL = [
+    # B, H, N_q, N_k, d, causal, kv_len
+    (2, 3, 128, 1024, 64, True, None),
+    (1, 2, 300, 700, 64, True, None),
+    (2, 2, 700, 300, 64, True, None),            # rows 0..399 keep no key
+    (2, 2, 200, 1500, 64, False, [1500, 37]),
+    (1, 3, 1, 513, 64, True, None),
+    (1, 2, 64, 3000, 64, True, None),
+    (2, 1, 333, 398, 64, True, [398, 100]),      # offset 65
+    (1, 2, 600, 129, 64, True, None),            # offset -471
+    (1, 2, 256, 640, 128, True, None),
+    (2, 1, 384, 200, 128, True, [200, 150]),
+    (1, 2, 100, 333, 128, False, None),
+]
+
+
+@pytest.mark.parametrize("B,H,Nq,Nk,d,causal,kv_len", UNEQUAL)
+def test_unequal_query_and_key_lengths_match_oracle(gpu, B, H, Nq, Nk, d, causal, kv_len):
+    assert_within(check_all_heads(B, H, Nq, d, causal, kv_len, seed=Nq + 3 * Nk + d, device=gpu, Nk=Nk))
+
+
 def test_tiny_workload(gpu):
     w = workloads.WORKLOADS["tiny"]
     x = workloads.make_inputs(w)

@@ -11,7 +11,9 @@ heads) of "FlashAttention Algorithm > Recomputation Strategy", In[17]/Out[18].
 No dataset or trained weight is involved: every tensor is i.i.d. Gaussian.
 
 Draw recipe (one CPU ``torch.Generator`` seeded with ``seed``):
-  1. q, k, v, dO drawn in that order as fp32 ``[B, H, N, d]`` standard normals;
+  1. q, k, v, dO drawn in that order as fp32 standard normals, q and dO
+     ``[B, H, N, d]``, k and v ``[B, H, N_k, d]`` (N_k = N for every named
+     workload; the tests of unequal lengths set it);
   2. q and k multiplied by ``qk_scale`` (0.5 for the head-dim-128 workload);
   3. for key-padded workloads, per-sequence valid key counts drawn from the
      same generator as integers uniform in ``[len_lo, len_hi]`` inclusive;
@@ -73,14 +75,16 @@ WORKLOADS: Dict[str, Workload] = {
 
 
 def draw(B: int, H: int, N: int, d: int, *, seed: int = 0, qk_scale: float = 1.0,
-         len_range: Optional[tuple] = None) -> Dict[str, Optional[torch.Tensor]]:
-    """Draw q, k, v, dO (bf16, CPU, ``[B,H,N,d]``) and optional kv_len (int32 ``[B]``)."""
+         len_range: Optional[tuple] = None, Nk: Optional[int] = None) -> Dict[str, Optional[torch.Tensor]]:
+    """Draw q, k, v, dO (bf16, CPU) and optional kv_len (int32 ``[B]``): q and dO are
+    ``[B,H,N,d]``, k and v ``[B,H,Nk,d]`` (Nk defaults to N)."""
     g = torch.Generator(device="cpu")
     g.manual_seed(seed)
     shape = (B, H, N, d)
+    kshape = (B, H, N if Nk is None else Nk, d)
     q = torch.randn(shape, generator=g, dtype=torch.float32)
-    k = torch.randn(shape, generator=g, dtype=torch.float32)
-    v = torch.randn(shape, generator=g, dtype=torch.float32)
+    k = torch.randn(kshape, generator=g, dtype=torch.float32)
+    v = torch.randn(kshape, generator=g, dtype=torch.float32)
     do = torch.randn(shape, generator=g, dtype=torch.float32)
     if qk_scale != 1.0:
         q = q * qk_scale
