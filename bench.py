@@ -150,14 +150,12 @@ def oracle_sample(w, x, budget_s: float, max_heads=None):
     kv = None if x["kv_len"] is None else x["kv_len"].numpy()
     heads = [(b, h) for b in range(B) for h in range(H)]
     done, flops = 0, 0.0
-    c = 0.5 if w.causal else 1.0
     t0 = time.perf_counter()
     for b, h in heads:
         q, k, v, do = (f64(x[n][b, h]) for n in ("q", "k", "v", "do"))
         kl = None if kv is None else int(kv[b])
         ref.head_backward(q, k, v, do, w.scale, w.causal, kl, row_block=2048 if w.N > 4096 else None)
-        nk = w.N if kl is None else kl
-        flops += 12 * c * w.N * nk * w.d
+        flops += 12 * w.d * workloads.visible_pairs(w.N, w.nk, w.causal, kl)
         done += 1
         if time.perf_counter() - t0 > budget_s or (max_heads and done >= max_heads):
             break
@@ -222,7 +220,7 @@ def run_reference(args, w):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / max(1, args.steps),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded N(0,1), bf16-rounded, upcast to fp64)",
-        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal},
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "N_k": w.nk, "d": w.d, "causal": w.causal},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -246,12 +244,12 @@ def run_gpu(args, w):
     peaks, peak_src = load_peaks()
 
     x = workloads.make_inputs(w, seed=0)
-    B, H, N, d = w.B, w.H, w.N, w.d
+    B, H, N, Nk, d = w.B, w.H, w.N, w.nk, w.d
     q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "do"))
     kv = None if x["kv_len"] is None else x["kv_len"].to(dev)
     o = torch.empty_like(q)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
-    dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(k)
     wsb = int(lib.fa_backward_workspace_size(B, H, N, d))
     work = torch.empty(wsb, dtype=torch.uint8, device=dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
@@ -261,11 +259,12 @@ def run_gpu(args, w):
     causal = int(w.causal)
 
     def fwd():
-        _lib.check(lib.fa_forward_ex(P(q), P(k), P(v), P(o), P(lse), B, H, N, d, w.scale, causal, P(kv), sp), "fwd")
+        _lib.check(lib.fa_forward_qk(P(q), P(k), P(v), P(o), P(lse), B, H, N, Nk, d, w.scale, causal, P(kv), sp),
+                   "fwd")
 
     def bwd_stage(s):
-        _lib.check(lib.fa_backward_stage(s, P(q), P(k), P(v), P(o), P(do), P(lse), P(dq), P(dk), P(dv), B, H, N,
-                                         d, w.scale, causal, P(kv), P(work), wsb, sp), "bwd")
+        _lib.check(lib.fa_backward_stage_qk(s, P(q), P(k), P(v), P(o), P(do), P(lse), P(dq), P(dk), P(dv), B, H,
+                                            N, Nk, d, w.scale, causal, P(kv), P(work), wsb, sp), "bwd")
 
     kernels = ["fwd_kernel", "bwd_pre_kernel", "bwd_kernel", "dq_convert_kernel"]
 
@@ -358,10 +357,11 @@ def run_gpu(args, w):
 
     # end to end through host buffers: H2D inputs, fwd+bwd, D2H outputs, every step
     hq, hk, hv, hdo = (x[n].pin_memory() for n in ("q", "k", "v", "do"))
-    ho, hdq, hdk, hdv = (torch.empty_like(hq).pin_memory() for _ in range(4))
+    ho, hdq = (torch.empty_like(hq).pin_memory() for _ in range(2))
+    hdk, hdv = (torch.empty_like(hk).pin_memory() for _ in range(2))
     hlse = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
-    h2d = 4 * hq.numel() * 2
-    d2h = 4 * hq.numel() * 2 + hlse.numel() * 4
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo))
+    d2h = sum(t.numel() * t.element_size() for t in (ho, hlse, hdq, hdk, hdv))
     e2e_steps = max(3, min(args.steps, 50))
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e2e_ms = 0.0
@@ -398,7 +398,7 @@ def run_gpu(args, w):
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) inputs, bf16)",
-        "config": {"workload": w.name, "B": B, "H": H, "N": N, "d": d, "causal": w.causal,
+        "config": {"workload": w.name, "B": B, "H": H, "N": N, "N_k": Nk, "d": d, "causal": w.causal,
                    "key_padding": w.padded, "l2": "flushed before every step (256 MiB write, untimed)",
                    "flops": "nominal fwd+bwd 12*c*N*Nk*d per head (c = 1/2 causal), recompute excluded",
                    "parallelism": f"replicas x{ws} (heads independent)"},

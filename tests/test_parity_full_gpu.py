@@ -17,7 +17,7 @@ from tests.parity_util import assert_within, compare, f64, run_gpu
 
 pytestmark = pytest.mark.gpu
 
-FULL = ["gpt2", "bert", "d128", "long2048", "long8192", "long16384", "long32768"]
+FULL = ["gpt2", "bert", "d128", "long2048", "long8192", "long16384", "long32768", "prefill1024_kv4096"]
 
 
 def _heads(w):
@@ -38,10 +38,10 @@ def test_full_size_sampled_parity_and_invariants(gpu, name):
         kl = None if kv is None else int(kv[b])
         if w.N <= 4096:
             r = ref.head_backward(q, k, v, do, w.scale, w.causal, kl)
-            rows = keys = np.arange(w.N)
+            rows, keys = np.arange(w.N), np.arange(w.nk)
         else:
             rows = np.unique(np.concatenate([[0, 1, 127, 128, w.N // 2, w.N - 1], rng.integers(0, w.N, 10)]))
-            keys = np.unique(np.concatenate([[0, 1, 127, 128, w.N // 2, w.N - 1], rng.integers(0, w.N, 10)]))
+            keys = np.unique(np.concatenate([[0, 1, 127, 128, w.nk // 2, w.nk - 1], rng.integers(0, w.nk, 10)]))
             smp = ref.head_sampled(q, k, v, do, w.scale, w.causal, kl, rows, keys)
             r = {"o": smp["o"], "lse": smp["lse"], "dq": smp["dq"], "dk": smp["dk"], "dv": smp["dv"]}
         errs = {}

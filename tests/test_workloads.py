@@ -39,3 +39,30 @@ def test_flop_counts():
     # 8*12 heads, 0.5 * 1024^2 * 64 per unit
     unit = 8 * 12 * 0.5 * 1024 * 1024 * 64
     assert f["fwd"] == 4 * unit and f["fwd_bwd_nominal"] == 12 * unit and f["fwd_bwd_executed"] == 14 * unit
+
+
+def test_visible_pairs_equals_a_half_diagonal_count():
+    # brute force: key j of query i counts 1 below the causal bound, 1/2 on it, 0 past it
+    import itertools
+
+    def brute(nq, nk, causal, kv):
+        tot = 0.0
+        for i, j in itertools.product(range(nq), range(min(nk, kv))):
+            lim = i + nk - nq
+            tot += 1.0 if (not causal or j < lim) else (0.5 if j == lim else 0.0)
+        return tot
+
+    for nq, nk, causal, kv in [(4, 4, True, 4), (2, 6, True, 6), (6, 2, True, 2), (4, 6, True, 3),
+                               (5, 9, False, 7), (1, 513, True, 513), (700, 300, True, 300),
+                               (300, 700, True, 650)]:
+        assert abs(workloads.visible_pairs(nq, nk, causal, kv) - brute(nq, nk, causal, kv)) < 1e-9, (nq, nk, kv)
+    assert workloads.visible_pairs(1024, 1024, True) == 0.5 * 1024 * 1024
+
+
+def test_unequal_length_workload_shapes():
+    w = workloads.WORKLOADS["prefill1024_kv4096"]
+    x = workloads.draw(2, 1, 16, 8, Nk=40)
+    assert x["q"].shape == (2, 1, 16, 8) and x["k"].shape == (2, 1, 40, 8) and x["do"].shape == (2, 1, 16, 8)
+    assert w.nk == 4096 and w.N == 1024
+    f = workloads.flop_counts(w)
+    assert f["fwd"] == 4 * 64 * 8 * 12 * (1024 * 4096 - 1024 * 1024 / 2)

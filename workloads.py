@@ -40,6 +40,7 @@ class Workload:
     qk_scale: float = 1.0
     len_lo: Optional[int] = None  # key padding: valid lengths uniform in [len_lo, len_hi]
     len_hi: Optional[int] = None
+    Nk: Optional[int] = None      # key rows when they differ from the N query rows
 
     @property
     def scale(self) -> float:
@@ -49,9 +50,15 @@ class Workload:
     def padded(self) -> bool:
         return self.len_lo is not None
 
+    @property
+    def nk(self) -> int:
+        return self.N if self.Nk is None else self.Nk
+
     def describe(self) -> str:
         s = f"{self.name}: B={self.B} H={self.H} N={self.N} d={self.d} " + (
             "causal" if self.causal else "non-causal")
+        if self.Nk is not None:
+            s += f", N_k={self.Nk} (causal queries aligned with the last keys)"
         if self.padded:
             s += f", key padding len~U[{self.len_lo},{self.len_hi}]"
         if self.qk_scale != 1.0:
@@ -70,6 +77,8 @@ WORKLOADS: Dict[str, Workload] = {
         Workload("long8192", 1, 12, 8192, 64, True),
         Workload("long16384", 1, 12, 16384, 64, True),
         Workload("long32768", 1, 12, 32768, 64, True),
+        # unequal lengths: 1024 new queries over 4096 keys (3072 earlier positions + themselves)
+        Workload("prefill1024_kv4096", 8, 12, 1024, 64, True, Nk=4096),
     ]
 }
 
@@ -105,21 +114,34 @@ def draw(B: int, H: int, N: int, d: int, *, seed: int = 0, qk_scale: float = 1.0
 
 def make_inputs(w: Workload, seed: int = 0) -> Dict[str, Optional[torch.Tensor]]:
     rng = (w.len_lo, w.len_hi) if w.padded else None
-    return draw(w.B, w.H, w.N, w.d, seed=seed, qk_scale=w.qk_scale, len_range=rng)
+    return draw(w.B, w.H, w.N, w.d, seed=seed, qk_scale=w.qk_scale, len_range=rng, Nk=w.Nk)
+
+
+def visible_pairs(nq: int, nk: int, causal: bool, kv: Optional[int] = None) -> float:
+    """Query-key pairs of one head as FLOP counts take them: N_q * kv without a causal
+    mask; with one (query i keeps keys j <= i + N_k - N_q and j < kv) the area under that
+    bound over the rows, so that the diagonal counts half, as in the usual c = 1/2."""
+    kv = nk if kv is None else kv
+    if not causal:
+        return float(nq * kv)
+    off = nk - nq
+    x0 = max(0.0, float(-off))                   # first row that keeps a key
+    x1 = min(max(float(kv - off), x0), float(nq))  # rows past x1 keep all kv keys
+    return ((x1 + off) ** 2 - (x0 + off) ** 2) / 2 + kv * (nq - x1)
 
 
 def flop_counts(w: Workload, kv_len: Optional[torch.Tensor] = None) -> Dict[str, float]:
     """Matmul FLOPs of one fwd+bwd over the workload.
 
-    Per head: fwd 4*c*N*Nk*d (QK^T and PV), bwd nominal 8*c*N*Nk*d (dV, dP, dK,
-    dQ) and recompute 2*c*N*Nk*d (QK^T again), with c = 1/2 for causal masks
-    (diagonal counted half, the usual convention) and Nk the valid key count.
+    Per head: fwd 4*P*d (QK^T and PV), bwd nominal 8*P*d (dV, dP, dK, dQ) and
+    recompute 2*P*d (QK^T again), with P = visible_pairs (c * N * N_k for square
+    causal masks, c = 1/2 with the diagonal counted half, the usual convention;
+    N_k the valid key count).
     """
-    c = 0.5 if w.causal else 1.0
     if kv_len is not None:
-        nk_total = float(kv_len.to(torch.float64).sum().item()) * w.H
+        pairs = sum(visible_pairs(w.N, w.nk, w.causal, int(x)) for x in kv_len.tolist()) * w.H
     else:
-        nk_total = float(w.N) * w.B * w.H
-    base = c * w.N * nk_total * w.d
+        pairs = visible_pairs(w.N, w.nk, w.causal) * w.B * w.H
+    base = pairs * w.d
     return {"fwd": 4 * base, "bwd_nominal": 8 * base, "bwd_recompute": 2 * base,
             "fwd_bwd_nominal": 12 * base, "fwd_bwd_executed": 14 * base}
