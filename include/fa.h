@@ -87,6 +87,34 @@ FA_API int fa_forward_ex(const void* q, const void* k, const void* v, void* o, f
 FA_API int fa_forward_qk(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq,
                          int Nk, int d, float scale, int causal, const int32_t* kv_len, fa_stream_t stream);
 
+/* Forward pass for inference shapes: few query rows over many keys, where one
+ * CTA per (head, query-tile pair) leaves most SMs idle (the pages: inference
+ * workloads are mostly memory-bound). The key tiles of each work item are cut
+ * into n_split near-equal shares run by separate CTAs. Each writes its share's O
+ * (divided by its own normaliser, fp32) and LSE into `workspace`. A second
+ * kernel joins the shares with the running-maximum rescaling that the tiled
+ * softmax applies between key blocks. Shapes, masks and results as
+ * fa_forward_qk.
+ *  - lse may be NULL: then no LSE is written.
+ *  - workspace: at least fa_forward_split_workspace_size(B, H, Nq, d, n_split)
+ *    bytes, 256-byte aligned; its contents on entry do not matter.
+ *  - n_split >= 1 (more than 1024 returns FA_ERR_UNSUPPORTED). With
+ *    n_split = 1 and lse non-NULL this is fa_forward_qk and the workspace is
+ *    not touched. */
+FA_API int fa_forward_split(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq,
+                            int Nk, int d, float scale, int causal, const int32_t* kv_len, int n_split,
+                            void* workspace, size_t workspace_bytes, fa_stream_t stream);
+
+/* Workspace bytes of fa_forward_split: n_split * B * H * Nq rows of d + 1 fp32.
+ * Returns 0 for invalid arguments. */
+FA_API size_t fa_forward_split_workspace_size(int B, int H, int Nq, int d, int n_split);
+
+/* The library's choice of n_split for a shape on the current device. It is 1
+ * when B * H * ceil(Nq / 256) work items already reach the SM count. Otherwise
+ * it is enough shares for about two CTAs per SM, capped at ceil(Nk / 128) / 4
+ * (four key tiles a share) and at 64. */
+FA_API int fa_forward_split_count(int B, int H, int Nq, int Nk, int d);
+
 /* Bytes of device workspace fa_backward needs: per (b, h), D and a base-2
  * copy of LSE for every query row and an fp32 dQ accumulator, each padded to
  * a multiple of 128 rows. Linear in N. Returns 0 for unsupported d. */

@@ -27,6 +27,9 @@ SIGNATURES = {
         "fa_forward": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp]),
         "fa_forward_ex": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp, _vp]),
         "fa_forward_qk": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _vp, _vp]),
+        "fa_forward_split": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _vp, _i, _vp, _sz, _vp]),
+        "fa_forward_split_workspace_size": (_sz, [_i, _i, _i, _i, _i]),
+        "fa_forward_split_count": (_i, [_i, _i, _i, _i, _i]),
         "fa_backward_workspace_size": (_sz, [_i, _i, _i, _i]),
         "fa_backward": (_i, [_vp] * 9 + [_i, _i, _i, _i, _f, _i, _vp, _sz, _vp]),
         "fa_backward_ex": (_i, [_vp] * 9 + [_i, _i, _i, _i, _f, _i, _vp, _vp, _sz, _vp]),

@@ -76,6 +76,34 @@ def forward(q, k, v, causal: bool = False, scale: Optional[float] = None, kv_len
     return o, lse
 
 
+def forward_split(q, k, v, causal: bool = False, scale: Optional[float] = None, kv_len=None,
+                  n_split: Optional[int] = None, with_lse: bool = False, out=None, workspace=None):
+    """Inference forward with split keys (include/fa.h: fa_forward_split): O, and LSE when
+    with_lse (else None). n_split defaults to the library's choice for the shape."""
+    _check_bhnd("q", q)
+    B, H, N, d = q.shape
+    kshape = _kv_shape(q, k)
+    _check_bhnd("v", v, kshape)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    lib = _lib_fa()
+    if n_split is None:
+        with torch.cuda.device(q.device):
+            n_split = int(lib.fa_forward_split_count(B, H, N, kshape[2], d))
+    o = torch.empty_like(q) if out is None else out
+    _check_bhnd("out", o, q.shape)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if with_lse else None
+    need = int(lib.fa_forward_split_workspace_size(B, H, N, d, n_split))
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    kv = _kv(kv_len, B, q.device)
+    with torch.cuda.device(q.device):
+        rc = lib.fa_forward_split(_p(q), _p(k), _p(v), _p(o), _p(lse), B, H, N, kshape[2], d, scale,
+                                  int(bool(causal)), _p(kv), int(n_split), _p(workspace), workspace.numel(),
+                                  _stream(q.device))
+    _lib.check(rc, "fa_forward_split")
+    return o, lse
+
+
 def workspace_bytes(B: int, H: int, N: int, d: int) -> int:
     return int(_lib_fa().fa_backward_workspace_size(B, H, N, d))
 

@@ -2,6 +2,7 @@
 // construction (in the launchers) and the per-device status word.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstdio>
@@ -152,8 +153,66 @@ int fa_forward_qk(const void* q, const void* k, const void* v, void* o, float* l
   a.kv_len = kv_len;
   a.lse = lse;
   a.o = static_cast<uint16_t*>(o);
+  a.n_split = 1;
+  a.part_o = nullptr;
+  a.part_lse = nullptr;
   a.status = status;
   return fa::launch_fwd(q, k, v, o, a, B * H, d, reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t fa_forward_split_workspace_size(int B, int H, int Nq, int d, int n_split) {
+  if (B < 0 || H < 0 || Nq < 0 || (d != 64 && d != 128) || n_split < 1) return 0;
+  const long long rows = (long long)n_split * B * H * Nq;
+  return (size_t)(round_up(rows * d * 4, 256) + round_up(rows * 4, 256));
+}
+
+int fa_forward_split_count(int B, int H, int Nq, int Nk, int d) {
+  if (B <= 0 || H <= 0 || Nq <= 0 || Nk <= 0 || (d != 64 && d != 128)) return 1;
+  int sms = 0;
+  if (!fa::sm_count(&sms)) return 1;
+  const long long items = (long long)B * H * ((Nq + 255) / 256);
+  if (items >= sms) return 1;
+  // about two CTAs per SM in all, each share at least four 128-key tiles, at most 64 shares
+  long long n = (2LL * sms + items - 1) / items;
+  n = std::min<long long>(n, std::max(1, ((Nk + 127) / 128) / 4));
+  return (int)std::max<long long>(1, std::min<long long>(n, 64));
+}
+
+int fa_forward_split(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq, int Nk,
+                     int d, float scale, int causal, const int32_t* kv_len, int n_split, void* workspace,
+                     size_t workspace_bytes, fa_stream_t stream) {
+  int rc = check_common(B, H, Nq, Nk, d, scale, causal);
+  if (rc != FA_OK) return rc;
+  if (n_split < 1) return FA_ERR_INVALID_ARG;
+  if (n_split > 1024) return FA_ERR_UNSUPPORTED;
+  // one share with an LSE to write: the plain forward (no workspace used)
+  if (n_split == 1 && lse) return fa_forward_qk(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, kv_len, stream);
+  if ((long long)B * H * Nq == 0) return FA_OK;
+  if (!q || !k || !v || !o || !workspace) return FA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || (lse && !aligned16(lse)))
+    return FA_ERR_MISALIGNED;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return FA_ERR_MISALIGNED;
+  if (workspace_bytes < fa_forward_split_workspace_size(B, H, Nq, d, n_split)) return FA_ERR_INVALID_ARG;
+  int err = FA_OK;
+  int* status = device_status(&err);
+  if (!status) return err;
+  const long long rows = (long long)n_split * B * H * Nq;
+  fa::FwdArgs a;
+  a.H = H;
+  a.N = Nq;
+  a.Nk = Nk;
+  a.coff = Nk - Nq;
+  a.n_pairs = (Nq + 255) / 256;
+  a.causal = causal;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.kv_len = kv_len;
+  a.lse = lse;
+  a.o = static_cast<uint16_t*>(o);
+  a.n_split = n_split;
+  a.part_o = static_cast<float*>(workspace);
+  a.part_lse = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + round_up(rows * d * 4, 256));
+  a.status = status;
+  return fa::launch_fwd_split(q, k, v, o, a, B * H, d, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int fa_forward_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,

@@ -67,7 +67,11 @@ __device__ __forceinline__ int key_tiles(int qs, int nq, int nkt, int causal, in
   return lim <= 0 ? 0 : min(nkt, (lim + 127) >> 7);
 }
 
-template <int D>
+// SPLIT: the CTA (head, query pair, share z) runs key tiles [jb, je) of its item, the
+// z-th of a.n_split near-equal shares, and writes that share's normalised O (fp32) and LSE
+// to a.part_o / a.part_lse for fwd_combine_kernel; the same running-maximum rescaling
+// that joins key tiles inside a CTA then joins the shares.
+template <int D, bool SPLIT>
 __global__ void __launch_bounds__(352, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o, FwdArgs a) {
@@ -109,6 +113,16 @@ __global__ void __launch_bounds__(352, 1)
   int n_t[2];
 #pragma unroll
   for (int t = 0; t < 2; ++t) n_t[t] = key_tiles(q0 + t * 128, a.N, nkt, a.causal, a.coff);
+  // key tiles run here: [jb, jb + nmax), all of them without a split; loops count from 0
+  int jb = 0;
+  if (SPLIT) {
+    const int nall = max(n_t[0], n_t[1]);
+    const int z = blockIdx.z;
+    jb = (int)((long long)z * nall / a.n_split);
+    const int je = (int)((long long)(z + 1) * nall / a.n_split);
+#pragma unroll
+    for (int t = 0; t < 2; ++t) n_t[t] = max(0, min(n_t[t], je) - jb);
+  }
   const int nmax = max(n_t[0], n_t[1]);
 
   // The producer warp initialises the barriers and starts the first copies (Q and the first
@@ -121,10 +135,10 @@ __global__ void __launch_bounds__(352, 1)
     const uint32_t kd = sbase + C::OFF_K + s * C::TILE_BYTES, vd = sbase + C::OFF_V + s * C::TILE_BYTES;
     if (elect_one()) mbar_arrive_expect_tx(kf, C::TILE_BYTES);
     for (int c = 0; c < C::NSUB; ++c)
-      if (elect_one()) tma_load_3d(kd + c * C::SUB_BYTES, &tm_k, c * 64, j * 128, bh, kf);
+      if (elect_one()) tma_load_3d(kd + c * C::SUB_BYTES, &tm_k, c * 64, (jb + j) * 128, bh, kf);
     if (elect_one()) mbar_arrive_expect_tx(vf, C::TILE_BYTES);
     for (int c = 0; c < C::NSUB; ++c)
-      if (elect_one()) tma_load_3d(vd + c * C::SUB_BYTES, &tm_v, c * 64, j * 128, bh, vf);
+      if (elect_one()) tma_load_3d(vd + c * C::SUB_BYTES, &tm_v, c * 64, (jb + j) * 128, bh, vf);
     __syncwarp();
   };
   if (warp == 8) {
@@ -294,12 +308,18 @@ __global__ void __launch_bounds__(352, 1)
     const uint32_t tO = tmem + lane_off + C::tm_o(t);
     const float sl2 = a.scale_log2;
     float* lse_row = a.lse + (size_t)bh * a.N;
+    // split: this share's rows in the partial results
+    const size_t prow = ((size_t)blockIdx.z * gridDim.x + bh) * a.N + grow;
     if (qs < a.N && n == 0) {
-      // no valid key for any row of this tile: O = 0, LSE = -inf
+      // no valid key for any row of this tile (in this share): O = 0, LSE = -inf
       if (grow < a.N) {
-        uint4* orow = reinterpret_cast<uint4*>(a.o + ((size_t)bh * a.N + grow) * D);
-        for (int c = 0; c < D / 8; ++c) orow[c] = make_uint4(0, 0, 0, 0);
-        lse_row[grow] = -INFINITY;
+        if (SPLIT) {
+          a.part_lse[prow] = -INFINITY;  // the combine skips this share's O
+        } else {
+          uint4* orow = reinterpret_cast<uint4*>(a.o + ((size_t)bh * a.N + grow) * D);
+          for (int c = 0; c < D / 8; ++c) orow[c] = make_uint4(0, 0, 0, 0);
+          lse_row[grow] = -INFINITY;
+        }
       }
     } else if (n > 0) {
       float m_run = -INFINITY;  // running maximum of s*S*log2(e)
@@ -325,7 +345,7 @@ __global__ void __launch_bounds__(352, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(s_free(t));
         }
-        const int k0 = j * 128;
+        const int k0 = (jb + j) * 128;
         const bool need_mask = (k0 + 127 >= kv) || (a.causal && k0 + 127 > qs + a.coff);
         if (need_mask) {
           const int lim = a.causal ? min(kv, grow + 1 + a.coff) : kv;  // keys [0, lim) are valid
@@ -408,7 +428,26 @@ __global__ void __launch_bounds__(352, 1)
       // every warp of the warpgroup reaches this vote, aborted or not, so the
       // named barrier of the epilogue below is entered by all four or by none
       ok = named_bar_and(1 + t, 128, ok);
-      if (ok) {
+      if (ok && SPLIT) {
+        tc_fence_after();
+        // this share's O / l (fp32) and LSE, one row per thread
+        const float inv = (l_run > 0.f) ? 1.f / l_run : 0.f;
+        float4* dst = reinterpret_cast<float4*>(a.part_o + prow * D);
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld32(tO + c * 32, r);
+          tmem_wait_ld();
+          if (grow < a.N) {
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              dst[c * 8 + q] = make_float4(__uint_as_float(r[4 * q]) * inv, __uint_as_float(r[4 * q + 1]) * inv,
+                                           __uint_as_float(r[4 * q + 2]) * inv, __uint_as_float(r[4 * q + 3]) * inv);
+          }
+        }
+        if (grow < a.N)
+          a.part_lse[prow] = (l_run > 0.f) ? (m_run + lg2_approx(l_run)) * 0.6931471805599453f : -INFINITY;
+      } else if (ok) {
         tc_fence_after();
         // epilogue: O / l -> bf16 -> swizzled smem (this tile's Q buffer) -> TMA store
         const float inv = (l_run > 0.f) ? 1.f / l_run : 0.f;
@@ -937,7 +976,50 @@ __global__ void __launch_bounds__(352, 1)
   }
 }
 
+// Joins the n_split shares of each query row. With L_z the shares' LSEs and M their
+// maximum: LSE = M + ln sum_z e^(L_z - M), O = sum_z e^(L_z - LSE) O_z, each O_z already
+// divided by its own normaliser; shares with no key (L_z = -inf) drop out. Grid (row blocks,
+// heads), one group of D/8 lanes per row, 8 outputs per lane.
 template <int D>
+__global__ void __launch_bounds__(256) fwd_combine_kernel(FwdArgs a) {
+  griddep_wait();
+  griddep_launch_dependents();
+  constexpr int LPR = D / 8;
+  constexpr int RPB = 256 / LPR;
+  const int part = threadIdx.x % LPR;
+  const int n = blockIdx.x * RPB + threadIdx.x / LPR;
+  const int bh = blockIdx.y;
+  if (n >= a.N) return;
+  const size_t row = (size_t)bh * a.N + n, plane = (size_t)gridDim.y * a.N;
+  float mx = -INFINITY;
+  for (int z = 0; z < a.n_split; ++z) mx = fmaxf(mx, a.part_lse[z * plane + row]);
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  float wsum = 0.f;
+  if (mx != -INFINITY) {
+    for (int z = 0; z < a.n_split; ++z) {
+      const float lz = a.part_lse[z * plane + row];
+      if (lz == -INFINITY) continue;
+      const float w = ex2_approx((lz - mx) * 1.4426950408889634f);
+      wsum += w;
+      const float4* src = reinterpret_cast<const float4*>(a.part_o + (z * plane + row) * D + part * 8);
+      const float4 x0 = src[0], x1 = src[1];
+      acc[0] = fmaf(w, x0.x, acc[0]), acc[1] = fmaf(w, x0.y, acc[1]);
+      acc[2] = fmaf(w, x0.z, acc[2]), acc[3] = fmaf(w, x0.w, acc[3]);
+      acc[4] = fmaf(w, x1.x, acc[4]), acc[5] = fmaf(w, x1.y, acc[5]);
+      acc[6] = fmaf(w, x1.z, acc[6]), acc[7] = fmaf(w, x1.w, acc[7]);
+    }
+  }
+  const float inv = (wsum > 0.f) ? 1.f / wsum : 0.f;
+  uint4 out;
+  out.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+  out.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+  out.z = pack_bf16x2(acc[4] * inv, acc[5] * inv);
+  out.w = pack_bf16x2(acc[6] * inv, acc[7] * inv);
+  *reinterpret_cast<uint4*>(a.o + row * D + part * 8) = out;
+  if (part == 0 && a.lse) a.lse[row] = (wsum > 0.f) ? mx + lg2_approx(wsum) * 0.6931471805599453f : -INFINITY;
+}
+
+template <int D, bool SPLIT = false>
 static int launch_fwd_d(const void* q, const void* k, const void* v, void* o, const FwdArgs& args, int BH,
                         cudaStream_t stream) {
   using C = FwdCfg<D>;
@@ -951,12 +1033,13 @@ static int launch_fwd_d(const void* q, const void* k, const void* v, void* o, co
   static bool attr_set = false;  // benign race: idempotent
   if (!attr_set) {
     const cudaError_t e =
-        cudaFuncSetAttribute(fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+        cudaFuncSetAttribute(fwd_kernel<D, SPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return cuda_fail("cudaFuncSetAttribute", (int)e, cudaGetErrorName(e));
     attr_set = true;
   }
-  dim3 grid(BH, args.n_pairs);
-  return launch_pdl(__func__, fwd_kernel<D>, grid, dim3(C::THREADS), C::SMEM_BYTES, stream, mq, mk, mv, mo, args);
+  dim3 grid(BH, args.n_pairs, SPLIT ? args.n_split : 1);
+  return launch_pdl(__func__, fwd_kernel<D, SPLIT>, grid, dim3(C::THREADS), C::SMEM_BYTES, stream, mq, mk, mv, mo,
+                    args);
 }
 
 // d = 64: the persistent kernel, one CTA per SM (at most one per work item)
@@ -995,6 +1078,18 @@ int launch_fwd(const void* q, const void* k, const void* v, void* o, const FwdAr
   if (d == 64) return launch_fwd_d<64>(q, k, v, o, args, BH, stream);
   if (d == 128) return launch_fwd_d<128>(q, k, v, o, args, BH, stream);
   return FA_ERR_UNSUPPORTED;
+}
+
+int launch_fwd_split(const void* q, const void* k, const void* v, void* o, const FwdArgs& args, int BH, int d,
+                     cudaStream_t stream) {
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  int rc = (d == 64) ? launch_fwd_d<64, true>(q, k, v, o, args, BH, stream)
+                     : launch_fwd_d<128, true>(q, k, v, o, args, BH, stream);
+  if (rc != FA_OK) return rc;
+  const int rpb = 256 / (d / 8);
+  const dim3 grid((unsigned)((args.N + rpb - 1) / rpb), (unsigned)BH);
+  return (d == 64) ? launch_pdl("fwd_combine_kernel", fwd_combine_kernel<64>, grid, dim3(256), 0, stream, args)
+                   : launch_pdl("fwd_combine_kernel", fwd_combine_kernel<128>, grid, dim3(256), 0, stream, args);
 }
 
 }  // namespace fa

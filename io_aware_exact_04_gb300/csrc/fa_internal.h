@@ -14,8 +14,11 @@ struct FwdArgs {
   int causal;
   float scale_log2;    // scale * log2(e)
   const int* kv_len;   // [B] device, or null
-  float* lse;          // [B*H, N]
+  float* lse;          // [B*H, N]; null only with a split (the combine then writes none)
   uint16_t* o;         // [B*H, N, d] bf16 (also written through the tensor map)
+  int n_split;         // split-KV forward: key-tile shares per work item (1 = no split)
+  float* part_o;       // split-KV: [n_split, B*H, N, d] fp32 O of each share, normalised by its l
+  float* part_lse;     // split-KV: [n_split, B*H, N] fp32 LSE of each share (-inf: no key)
   int* status;         // device status word (4 ints)
 };
 
@@ -74,6 +77,10 @@ int launch_pdl(const char* name, void (*kernel)(Params...), dim3 grid, dim3 bloc
 
 int launch_fwd(const void* q, const void* k, const void* v, void* o, const FwdArgs& args, int BH, int d,
                cudaStream_t stream);
+// Split-KV forward: fwd_kernel over (head, query pair, share) writing per-share partial
+// results to args.part_o / args.part_lse, then fwd_combine_kernel joining them into o (and lse).
+int launch_fwd_split(const void* q, const void* k, const void* v, void* o, const FwdArgs& args, int BH, int d,
+                     cudaStream_t stream);
 // stage 0: D, base-2 LSE, zeroed dQ accumulator; 1: main kernel (dK, dV, dQ accumulator);
 // 2: dQ accumulator -> bf16 dQ
 int launch_bwd_stage(int stage, const void* q, const void* k, const void* v, const BwdArgs& args, int BH, int d,

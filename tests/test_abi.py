@@ -108,3 +108,18 @@ def test_selftest_argument_errors(built):
     assert st.fa_selftest_mma(None, A, A, 64, 64, 0, A, None) == 1
     assert st.fa_selftest_wait_timeout(None, 10, None) == 1
     assert st.fa_selftest_wait_timeout(A, 0, None) == 1
+
+
+def test_split_forward_argument_errors(lib):
+    need = lib.fa_forward_split_workspace_size(2, 3, 100, 64, 4)
+    assert need == ((4 * 6 * 100 * 64 * 4 + 255) // 256) * 256 + ((4 * 6 * 100 * 4 + 255) // 256) * 256
+    assert lib.fa_forward_split_workspace_size(2, 3, 100, 96, 4) == 0
+    assert lib.fa_forward_split_workspace_size(2, 3, 100, 64, 0) == 0
+    args = lambda n_split, ws, nbytes: (*[A] * 5, 2, 3, 100, 900, 64, 0.125, 1, None, n_split, ws, nbytes, None)  # noqa: E731
+    W = ctypes.c_void_p(0x10000)
+    assert lib.fa_forward_split(*args(0, W, need)) == 1        # no shares
+    assert lib.fa_forward_split(*args(2000, W, need)) == 2     # too many shares
+    assert lib.fa_forward_split(*args(4, W, need - 1)) == 1    # workspace too small
+    assert lib.fa_forward_split(*args(4, None, need)) == 1     # no workspace
+    assert lib.fa_forward_split(*args(4, ctypes.c_void_p(0x10010), need)) == 3  # 256-byte alignment
+    assert lib.fa_forward_split_count(0, 3, 100, 900, 64) == 1

@@ -126,3 +126,47 @@ def test_autograd_function(gpu):
     r = ref.attention(f64(x["q"]), f64(x["k"]), f64(x["v"]), f64(x["do"]), scale=1 / 8, causal=True)
     assert_within({"o": compare("o", f64(o), r["o"]), "dq": compare("dq", f64(q.grad), r["dq"]),
                    "dk": compare("dk", f64(k.grad), r["dk"]), "dv": compare("dv", f64(v.grad), r["dv"])})
+
+
+# Split-key forward (inference): shares of each item's key tiles joined by a second kernel.
+# Uneven shares, more shares than key tiles (empty shares), rows without keys, no LSE.
+SPLIT = [
+    # B, H, N_q, N_k, d, causal, kv_len, n_split, with_lse
+    (1, 2, 1, 4096, 64, True, None, 8, True),
+    (2, 3, 128, 3000, 64, True, None, 5, True),
+    (2, 2, 300, 2048, 128, False, [2048, 700], 4, True),
+    (1, 1, 256, 256, 64, True, None, 3, True),         # 2 key tiles, 3 shares: one is empty
+    (3, 1, 64, 1000, 64, False, [1000, 0, 17], 6, True),  # a batch without any valid key
+    (2, 2, 16, 5000, 128, True, None, 7, False),
+    (1, 2, 1, 700, 64, True, None, 1, False),          # one share, no LSE: still the split path
+]
+
+
+@pytest.mark.parametrize("B,H,Nq,Nk,d,causal,kv_len,n_split,with_lse", SPLIT)
+def test_split_key_forward_matches_oracle(gpu, B, H, Nq, Nk, d, causal, kv_len, n_split, with_lse):
+    from io_aware_exact_04_gb300 import api
+    x = workloads.draw(B, H, Nq, d, seed=Nq + Nk + n_split, Nk=Nk)
+    kv = None if kv_len is None else torch.tensor(kv_len, dtype=torch.int32)
+    q, k, v = (x[n].to(gpu) for n in ("q", "k", "v"))
+    o, lse = api.forward_split(q, k, v, causal=causal, kv_len=None if kv is None else kv.to(gpu),
+                               n_split=n_split, with_lse=with_lse)
+    torch.cuda.synchronize(gpu)
+    code, detail = api.device_status(gpu)
+    assert code == 0, f"device status {detail}"
+    r = ref.attention(f64(x["q"]), f64(x["k"]), f64(x["v"]), scale=1 / math.sqrt(d), causal=causal,
+                      kv_len=None if kv is None else kv.numpy(), backward=False)
+    errs = {"o": compare("o", f64(o), r["o"])}
+    if with_lse:
+        errs["lse"] = compare("lse", f64(lse), r["lse"])
+    assert_within(errs)
+
+
+def test_split_key_forward_default_count_matches_plain_forward(gpu):
+    from io_aware_exact_04_gb300 import api
+    x = workloads.draw(2, 4, 64, 64, seed=5, Nk=6000)
+    q, k, v = (x[n].to(gpu) for n in ("q", "k", "v"))
+    o1, lse1 = api.forward(q, k, v, causal=True)
+    o2, lse2 = api.forward_split(q, k, v, causal=True, with_lse=True)
+    torch.cuda.synchronize(gpu)
+    assert float((o1.float() - o2.float()).abs().max()) <= 2e-2 * float(o1.float().abs().max())
+    assert float((lse1 - lse2).abs().max()) <= 1e-3
