@@ -154,15 +154,20 @@ def oracle_sample(w, x, budget_s: float, max_heads=None):
     for b, h in heads:
         q, k, v, do = (f64(x[n][b, h]) for n in ("q", "k", "v", "do"))
         kl = None if kv is None else int(kv[b])
-        ref.head_backward(q, k, v, do, w.scale, w.causal, kl, row_block=2048 if w.N > 4096 else None)
-        flops += 12 * w.d * workloads.visible_pairs(w.N, w.nk, w.causal, kl)
+        if w.infer:  # forward only
+            ref.head_forward(q, k, v, w.scale, w.causal, kl)
+            flops += 4 * w.d * workloads.visible_pairs(w.N, w.nk, w.causal, kl)
+        else:
+            ref.head_backward(q, k, v, do, w.scale, w.causal, kl, row_block=2048 if w.N > 4096 else None)
+            flops += 12 * w.d * workloads.visible_pairs(w.N, w.nk, w.causal, kl)
         done += 1
         if time.perf_counter() - t0 > budget_s or (max_heads and done >= max_heads):
             break
     dt = time.perf_counter() - t0
     cores = len(os.sched_getaffinity(0))
     return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-            "sample": f"{done} of {B * H} heads of {w.name} (fp64 numpy, fwd+bwd, S and P materialised), "
+            "sample": f"{done} of {B * H} heads of {w.name} (fp64 numpy, {'fwd' if w.infer else 'fwd+bwd'}, "
+                      f"S and P materialised), "
                       f"{dt:.1f} s", "seconds": dt, "heads": done}
 
 
@@ -216,7 +221,7 @@ def run_reference(args, w):
     cores = len(os.sched_getaffinity(0))
     sample = f"each step: the fp64 oracle on as many heads of {w.name} as fit in {budget:.1f} s ({heads} heads over {args.steps} steps)"
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws,
+        "impl": "reference", "metric": INFER_METRIC if w.infer else METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / max(1, args.steps),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded N(0,1), bf16-rounded, upcast to fp64)",
@@ -426,6 +431,134 @@ def run_gpu(args, w):
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------------------ inference workloads
+INFER_METRIC = "attention forward-only TFLOP/s (inference, split keys; bf16, 1×GB300); roofline in GB/s"
+
+
+def infer_bytes(w, n_split):
+    """Algorithmic bytes of one split-key forward launch: Q, K, V read (bf16) and each
+    share's fp32 O and LSE written."""
+    rows_q = w.B * w.H * w.N
+    return 2 * rows_q * w.d + 2 * 2 * w.B * w.H * w.nk * w.d + n_split * rows_q * (w.d + 1) * 4
+
+
+def run_gpu_infer(args, w):
+    """Forward only through fa_forward_split: a step is one split-key forward and its combine."""
+    import ctypes
+
+    import torch
+
+    from io_aware_exact_04_gb300 import _lib
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    lib = _lib.load("libfa.so")
+    peaks, peak_src = load_peaks()
+    x = workloads.make_inputs(w, seed=0)
+    B, H, N, Nk, d = w.B, w.H, w.N, w.nk, w.d
+    q, k, v = (x[n].to(dev) for n in ("q", "k", "v"))
+    kv = None if x["kv_len"] is None else x["kv_len"].to(dev)
+    o = torch.empty_like(q)
+    n_split = int(lib.fa_forward_split_count(B, H, N, Nk, d))
+    wsb = int(lib.fa_forward_split_workspace_size(B, H, N, d, n_split))
+    work = torch.empty(max(wsb, 1), dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sp = ctypes.c_void_p(stream.cuda_stream)
+    P = lambda t: ctypes.c_void_p(t.data_ptr()) if t is not None else None  # noqa: E731
+
+    def step():
+        _lib.check(lib.fa_forward_split(P(q), P(k), P(v), P(o), None, B, H, N, Nk, d, w.scale, int(w.causal), P(kv),
+                                        n_split, P(work), wsb, sp), "fwd_split")
+
+    for _ in range(max(3, args.warmup)):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(dev)
+    detail = (ctypes.c_int * 4)()
+    if lib.fa_get_last_device_status(sp, detail) != 0:
+        raise RuntimeError(f"device status after warm-up: {list(detail)}")
+    step_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    sampler = ClockSampler(local if "CUDA_VISIBLE_DEVICES" not in os.environ else 0)
+    if rank == 0:
+        sampler.start()
+        time.sleep(0.3)
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    sampler.mark("t_start")
+    for i in range(args.steps):
+        flush.zero_()
+        step_ev[i][0].record(stream)
+        step()
+        step_ev[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    sampler.mark("t_stop")
+    if ws > 1:
+        torch.distributed.barrier()
+    total_ms = sum(e[0].elapsed_time(e[1]) for e in step_ev)
+    fwd_flops = 4.0 * d * workloads.visible_pairs(N, Nk, w.causal) * B * H
+    ms_step, rate = job_throughput(total_ms / args.steps, fwd_flops, device=dev)
+    value = rate / 1e12
+    # roofline of the step's two launches together (the combine reads back only the shares'
+    # small fp32 rows): algorithmic bytes over the event-timed step
+    bytes_alg = infer_bytes(w, n_split)
+    achieved = bytes_alg / (ms_step * 1e-3) / 1e9
+    peak = float(peaks["hbm_gbs"])
+    roof = {"bound": "hbm", "kernel": "fwd_split+combine (whole step)", "achieved": achieved, "peak": peak,
+            "unit": "GB/s", "frac": achieved / peak, "traffic": traffic_record("fwd_split", w.name),
+            "peak_source": f"{peak_src} hbm_gbs (copy)", "avg_launch_ms": ms_step,
+            "bytes_per_launch": bytes_alg}
+    # end to end through host buffers
+    hq, hk, hv = (x[n].pin_memory() for n in ("q", "k", "v"))
+    ho = torch.empty_like(hq).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
+    d2h = ho.numel() * ho.element_size()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_steps, e2e_ms = max(3, min(args.steps, 50)), 0.0
+    for i in range(e2e_steps + 2):
+        flush.zero_()
+        torch.cuda.synchronize(dev)
+        e0.record(stream)
+        q.copy_(hq, non_blocking=True)
+        k.copy_(hk, non_blocking=True)
+        v.copy_(hv, non_blocking=True)
+        step()
+        ho.copy_(o, non_blocking=True)
+        e1.record(stream)
+        e1.synchronize()
+        if i >= 2:
+            e2e_ms += e0.elapsed_time(e1)
+    e2e_ms, e2e_rate = job_throughput(e2e_ms / e2e_steps, fwd_flops, device=dev)
+    clocks = sampler.stop() if rank == 0 else None
+    if ws > 1:
+        torch.distributed.barrier()
+    if rank != 0:
+        return
+    cpu = oracle_sample(w, x, budget_s=args.cpu_budget) if not args.no_cpu_baseline else None
+    line = {
+        "metric": INFER_METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) inputs, bf16)",
+        "config": {"workload": w.name, "B": B, "H": H, "N": N, "N_k": Nk, "d": d, "causal": w.causal,
+                   "n_split": n_split, "lse": False,
+                   "l2": "flushed before every step (256 MiB write, untimed); K and V exceed L2",
+                   "flops": "nominal forward 4*P*d per head, P = visible query-key pairs",
+                   "parallelism": f"replicas x{ws} (heads independent)"},
+        "roofline": roof,
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_rate / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_ms, "steps": e2e_steps},
+        "gpu_launches": (2 if n_split > 1 else 1) * args.steps,
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -439,6 +572,8 @@ def main():
     w = workloads.WORKLOADS[args.workload]
     if args.impl == "reference":
         run_reference(args, w)
+    elif w.infer:
+        run_gpu_infer(args, w)
     else:
         run_gpu(args, w)
 

@@ -18,6 +18,7 @@ from tests.parity_util import assert_within, compare, f64, run_gpu
 pytestmark = pytest.mark.gpu
 
 FULL = ["gpt2", "bert", "d128", "long2048", "long8192", "long16384", "long32768", "prefill1024_kv4096"]
+INFER = [n for n, w in workloads.WORKLOADS.items() if w.infer]
 
 
 def _heads(w):
@@ -70,3 +71,19 @@ def test_full_size_sampled_parity_and_invariants(gpu, name):
             assert float((diff / dO[b].abs().sum(dim=1).amax(dim=-1)).max()) < 2e-3
     lse = g["lse"]
     assert torch.isfinite(lse).all()
+
+
+@pytest.mark.parametrize("name", INFER)
+def test_full_size_inference_forward(gpu, name):
+    """The inference workloads at full size, in the bench's launch configuration (the
+    library's share count, no LSE), every head against the oracle's forward."""
+    from io_aware_exact_04_gb300 import api
+    w = workloads.WORKLOADS[name]
+    x = workloads.make_inputs(w)
+    q, k, v = (x[n].to(gpu) for n in ("q", "k", "v"))
+    o, _ = api.forward_split(q, k, v, causal=w.causal)
+    o_lse, lse = api.forward_split(q, k, v, causal=w.causal, with_lse=True)
+    torch.cuda.synchronize(gpu)
+    assert torch.equal(o, o_lse)
+    r = ref.attention(f64(x["q"]), f64(x["k"]), f64(x["v"]), scale=w.scale, causal=w.causal, backward=False)
+    assert_within({"o": compare("o", f64(o), r["o"]), "lse": compare("lse", f64(lse), r["lse"])})

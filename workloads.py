@@ -41,6 +41,7 @@ class Workload:
     len_lo: Optional[int] = None  # key padding: valid lengths uniform in [len_lo, len_hi]
     len_hi: Optional[int] = None
     Nk: Optional[int] = None      # key rows when they differ from the N query rows
+    infer: bool = False           # forward only, split keys (inference): no backward, no LSE
 
     @property
     def scale(self) -> float:
@@ -59,6 +60,8 @@ class Workload:
             "causal" if self.causal else "non-causal")
         if self.Nk is not None:
             s += f", N_k={self.Nk} (causal queries aligned with the last keys)"
+        if self.infer:
+            s += ", forward only (inference, split keys)"
         if self.padded:
             s += f", key padding len~U[{self.len_lo},{self.len_hi}]"
         if self.qk_scale != 1.0:
@@ -79,6 +82,8 @@ WORKLOADS: Dict[str, Workload] = {
         Workload("long32768", 1, 12, 32768, 64, True),
         # unequal lengths: 1024 new queries over 4096 keys (3072 earlier positions + themselves)
         Workload("prefill1024_kv4096", 8, 12, 1024, 64, True, Nk=4096),
+        # inference: one new query per sequence over 8192 keys (forward only, split keys)
+        Workload("decode_kv8192", 8, 12, 1, 64, True, Nk=8192, infer=True),
     ]
 }
 
