@@ -105,14 +105,14 @@ FA_API int fa_forward_split(const void* q, const void* k, const void* v, void* o
                             int Nk, int d, float scale, int causal, const int32_t* kv_len, int n_split,
                             void* workspace, size_t workspace_bytes, fa_stream_t stream);
 
-/* Workspace bytes of fa_forward_split: n_split * B * H * Nq rows of d + 1 fp32.
+/* Workspace bytes of fa_forward_split: 2 * n_split * B * H * Nq rows of d + 1 fp32.
  * Returns 0 for invalid arguments. */
 FA_API size_t fa_forward_split_workspace_size(int B, int H, int Nq, int d, int n_split);
 
 /* The library's choice of n_split for a shape on the current device. It is 1
  * when B * H * ceil(Nq / 256) work items already reach the SM count. Otherwise
- * it is enough shares for about two CTAs per SM, capped at ceil(Nk / 128) / 4
- * (four key tiles a share) and at 64. */
+ * it is the largest count whose CTAs fit in two waves (floor(2 * SMs / items)),
+ * capped at ceil(Nk / 128) / 4 (four key tiles a share) and at 64. */
 FA_API int fa_forward_split_count(int B, int H, int Nq, int Nk, int d);
 
 /* Bytes of device workspace fa_backward needs: per (b, h), D and a base-2

@@ -162,7 +162,7 @@ int fa_forward_qk(const void* q, const void* k, const void* v, void* o, float* l
 
 size_t fa_forward_split_workspace_size(int B, int H, int Nq, int d, int n_split) {
   if (B < 0 || H < 0 || Nq < 0 || (d != 64 && d != 128) || n_split < 1) return 0;
-  const long long rows = (long long)n_split * B * H * Nq;
+  const long long rows = 2LL * n_split * B * H * Nq;  // two partial slots per share
   return (size_t)(round_up(rows * d * 4, 256) + round_up(rows * 4, 256));
 }
 
@@ -172,8 +172,9 @@ int fa_forward_split_count(int B, int H, int Nq, int Nk, int d) {
   if (!fa::sm_count(&sms)) return 1;
   const long long items = (long long)B * H * ((Nq + 255) / 256);
   if (items >= sms) return 1;
-  // about two CTAs per SM in all, each share at least four 128-key tiles, at most 64 shares
-  long long n = (2LL * sms + items - 1) / items;
+  // the most shares whose CTAs still fit in two waves (a partly filled last wave costs as
+  // much as a full one), each share at least four 128-key tiles, at most 64 shares
+  long long n = (2LL * sms) / items;
   n = std::min<long long>(n, std::max(1, ((Nk + 127) / 128) / 4));
   return (int)std::max<long long>(1, std::min<long long>(n, 64));
 }
@@ -196,7 +197,7 @@ int fa_forward_split(const void* q, const void* k, const void* v, void* o, float
   int err = FA_OK;
   int* status = device_status(&err);
   if (!status) return err;
-  const long long rows = (long long)n_split * B * H * Nq;
+  const long long rows = 2LL * n_split * B * H * Nq;
   fa::FwdArgs a;
   a.H = H;
   a.N = Nq;

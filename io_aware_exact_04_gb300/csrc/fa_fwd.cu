@@ -29,12 +29,14 @@
 
 namespace fa {
 
-template <int D>
+template <int D, bool SPLIT = false>
 struct FwdCfg {
   static constexpr int NSUB = D / 64;              // 128-byte column blocks per row
   static constexpr int SUB_BYTES = 128 * 128;      // one [128 rows][64 bf16] block
   static constexpr int TILE_BYTES = NSUB * SUB_BYTES;
-  static constexpr int NST = (D == 64) ? 3 : 2;    // K/V ring depth
+  // K/V ring depth. The split d = 64 kernel may give alternate ring tiles to its two query
+  // lanes (dual mode), so each lane sees only half of the ring ahead: six stages there.
+  static constexpr int NST = (D == 64) ? (SPLIT ? 6 : 3) : 2;
   static constexpr int OFF_Q = 0;                  // two query tiles
   static constexpr int OFF_K = OFF_Q + 2 * TILE_BYTES;
   static constexpr int OFF_V = OFF_K + NST * TILE_BYTES;
@@ -54,6 +56,9 @@ struct FwdCfg {
   static constexpr int NMMA = SEP_P ? 2 : 1;
 };
 
+static_assert(FwdCfg<64, true>::SMEM_BYTES <= 232448, "split d = 64 forward: shared memory above 227 KB");
+static_assert(8 * (1 + 3 * FwdCfg<64, true>::NST + 9) + 8 <= 256, "split d = 64 forward: barrier area");
+
 // Wait-site identifiers recorded with FA_ERR_TIMEOUT.
 enum { SITE_F_KV_EMPTY = 1, SITE_F_Q_FULL, SITE_F_K_FULL, SITE_F_V_FULL, SITE_F_P_READY, SITE_F_S_FULL,
        SITE_F_O_DONE, SITE_F_DRAIN, SITE_F_S_FREE };
@@ -68,16 +73,16 @@ __device__ __forceinline__ int key_tiles(int qs, int nq, int nkt, int causal, in
 }
 
 // SPLIT: the CTA (head, query pair, share z) runs key tiles [jb, je) of its item, the
-// z-th of a.n_split near-equal shares, and writes that share's normalised O (fp32) and LSE
-// to a.part_o / a.part_lse for fwd_combine_kernel; the same running-maximum rescaling
-// that joins key tiles inside a CTA then joins the shares.
+// z-th of a.n_split near-equal shares, and writes normalised partial O (fp32) and LSE to
+// slots 2z and 2z + 1 of a.part_o / a.part_lse for fwd_combine_kernel; the same
+// running-maximum rescaling that joins key tiles inside a CTA then joins the slots.
 template <int D, bool SPLIT>
 __global__ void __launch_bounds__(352, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o, FwdArgs a) {
   griddep_wait();  // before any access to global memory
   griddep_launch_dependents();
-  using C = FwdCfg<D>;
+  using C = FwdCfg<D, SPLIT>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1024(smem_raw);
   const uint32_t sbase = smem_u32(sm);
@@ -113,17 +118,29 @@ __global__ void __launch_bounds__(352, 1)
   int n_t[2];
 #pragma unroll
   for (int t = 0; t < 2; ++t) n_t[t] = key_tiles(q0 + t * 128, a.N, nkt, a.causal, a.coff);
-  // key tiles run here: [jb, jb + nmax), all of them without a split; loops count from 0
-  int jb = 0;
+  // key tiles run here: [jb, jb + nmax), all of them without a split; loops count from 0.
+  // dual (split only): the item's second query tile lies past N, so query lane 1 takes the
+  // same rows as lane 0 and the two lanes split the share's key tiles, even ones to lane 0
+  // and odd ones to lane 1; each lane's result is a partial of its own for the combine.
+  int jb = 0, nmax;
+  const bool dual = SPLIT && D == 64 && q0 + 128 >= a.N && n_t[0] > 0;
   if (SPLIT) {
     const int nall = max(n_t[0], n_t[1]);
     const int z = blockIdx.z;
     jb = (int)((long long)z * nall / a.n_split);
     const int je = (int)((long long)(z + 1) * nall / a.n_split);
+    if (dual) {
+      n_t[0] = (je - jb + 1) >> 1;
+      n_t[1] = (je - jb) >> 1;
+      nmax = je - jb;  // ring tiles of both lanes
+    } else {
 #pragma unroll
-    for (int t = 0; t < 2; ++t) n_t[t] = max(0, min(n_t[t], je) - jb);
+      for (int t = 0; t < 2; ++t) n_t[t] = max(0, min(n_t[t], je) - jb);
+      nmax = max(n_t[0], n_t[1]);
+    }
+  } else {
+    nmax = max(n_t[0], n_t[1]);
   }
-  const int nmax = max(n_t[0], n_t[1]);
 
   // The producer warp initialises the barriers and starts the first copies (Q and the first
   // NST K/V stages, whose slots are free) before the CTA-wide setup, hiding their latency. It
@@ -171,8 +188,8 @@ __global__ void __launch_bounds__(352, 1)
       for (int t = 0; t < nq; ++t)
         for (int s = 0; s < C::NSUB; ++s)
           if (elect_one())
-            tma_load_3d(sbase + C::OFF_Q + t * C::TILE_BYTES + s * C::SUB_BYTES, &tm_q, s * 64, q0 + t * 128, bh,
-                        q_full);
+            tma_load_3d(sbase + C::OFF_Q + t * C::TILE_BYTES + s * C::SUB_BYTES, &tm_q, s * 64,
+                        q0 + (dual ? 0 : t * 128), bh, q_full);
       for (int j = 0; j < n_pre; ++j) load_kv(j);
     }
   }
@@ -241,9 +258,15 @@ __global__ void __launch_bounds__(352, 1)
       const int t_lo = C::SEP_P ? warp - 9 : 0, t_hi = C::SEP_P ? warp - 9 : 1;  // query tiles served
       if (ok) {
         tc_fence_after();
-        for (int t = t_lo; t <= t_hi; ++t)
+        for (int t = t_lo; t <= t_hi && ok; ++t)
           if (n_t[t] > 0) {
-            issue_s(t, 0);
+            if (dual && t == 1) {  // lane 1 starts at ring tile 1
+              if (!C::SEP_P) continue;  // the single issuer starts it inside the loop
+              if (!(ok = wait_warp(k_full(1 % C::NST), (1 / C::NST) & 1, st, SITE_F_K_FULL))) break;
+              issue_s(1, 1 % C::NST);
+            } else {
+              issue_s(t, 0);
+            }
             commit(s_full(t));
           }
       }
@@ -252,6 +275,35 @@ __global__ void __launch_bounds__(352, 1)
         const int s2 = (s + 1 == C::NST) ? 0 : s + 1;
         const int ph2 = (s + 1 == C::NST) ? ph ^ 1 : ph;
         bool used = false;
+        if (dual) {
+          // ring tile j is lane (j & 1)'s tile j >> 1
+          if (!C::SEP_P && j + 1 < nmax) {
+            // one issuer for both lanes: the other lane's next S as soon as its K has landed
+            // (ring tile j + 1 is another stage than j: no wait on this tile's release)
+            if (!(ok = wait_warp(k_full(s2), ph2, st, SITE_F_K_FULL))) break;
+            issue_s((j + 1) & 1, s2);
+            commit(s_full((j + 1) & 1));
+          }
+          for (int t = t_lo; t <= t_hi && ok; ++t) {
+            if ((j & 1) != t) continue;
+            used = true;
+            const int kk = j >> 1;
+            if (C::SEP_P && kk + 1 < n_t[t]) {  // this lane's next tile is ring tile j + 2
+              const int sn = (j + 2) % C::NST;
+              const uint32_t phn = ((j + 2) / C::NST) & 1;
+              if (!(ok = wait_warp(k_full(sn), phn, st, SITE_F_K_FULL))) break;
+              if (!(ok = wait_warp(s_free(t), kk & 1, st, SITE_F_S_FREE))) break;
+              tc_fence_after();
+              issue_s(t, sn);
+              commit(s_full(t));
+            }
+            if (!(ok = wait_warp(v_full(s), ph, st, SITE_F_V_FULL))) break;
+            if (!(ok = wait_warp(p_ready(t), kk & 1, st, SITE_F_P_READY))) break;
+            tc_fence_after();
+            issue_pv(t, s, kk > 0);
+            commit(o_done(t));
+          }
+        } else
         for (int t = t_lo; t <= t_hi && ok; ++t) {
           const int n = n_t[t];
           if (j >= n) continue;
@@ -299,7 +351,7 @@ __global__ void __launch_bounds__(352, 1)
     const int t = warp >> 2;
     const int wq = warp & 3;
     const int row = wq * 32 + lane;  // TMEM lane == row within the query tile
-    const int qs = q0 + t * 128;
+    const int qs = q0 + (dual ? 0 : t * 128);
     const int grow = qs + row;
     const int n = n_t[t];
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
@@ -308,13 +360,16 @@ __global__ void __launch_bounds__(352, 1)
     const uint32_t tO = tmem + lane_off + C::tm_o(t);
     const float sl2 = a.scale_log2;
     float* lse_row = a.lse + (size_t)bh * a.N;
-    // split: this share's rows in the partial results
-    const size_t prow = ((size_t)blockIdx.z * gridDim.x + bh) * a.N + grow;
+    // split: this lane's partial slot (two per share: lanes of a dual CTA, or the tile's
+    // own result and an empty second slot)
+    const size_t plane = (size_t)gridDim.x * a.N;
+    const size_t prow = (size_t)(2 * blockIdx.z + (dual ? t : 0)) * plane + (size_t)bh * a.N + grow;
+    if (SPLIT && !dual && grow < a.N && qs < a.N) a.part_lse[prow + plane] = -INFINITY;
     if (qs < a.N && n == 0) {
       // no valid key for any row of this tile (in this share): O = 0, LSE = -inf
       if (grow < a.N) {
         if (SPLIT) {
-          a.part_lse[prow] = -INFINITY;  // the combine skips this share's O
+          a.part_lse[prow] = -INFINITY;  // the combine skips this slot's O
         } else {
           uint4* orow = reinterpret_cast<uint4*>(a.o + ((size_t)bh * a.N + grow) * D);
           for (int c = 0; c < D / 8; ++c) orow[c] = make_uint4(0, 0, 0, 0);
@@ -345,7 +400,7 @@ __global__ void __launch_bounds__(352, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(s_free(t));
         }
-        const int k0 = (jb + j) * 128;
+        const int k0 = (jb + (dual ? 2 * j + t : j)) * 128;
         const bool need_mask = (k0 + 127 >= kv) || (a.causal && k0 + 127 > qs + a.coff);
         if (need_mask) {
           const int lim = a.causal ? min(kv, grow + 1 + a.coff) : kv;  // keys [0, lim) are valid
@@ -976,9 +1031,9 @@ __global__ void __launch_bounds__(352, 1)
   }
 }
 
-// Joins the n_split shares of each query row. With L_z the shares' LSEs and M their
-// maximum: LSE = M + ln sum_z e^(L_z - M), O = sum_z e^(L_z - LSE) O_z, each O_z already
-// divided by its own normaliser; shares with no key (L_z = -inf) drop out. Grid (row blocks,
+// Joins the partial results of each query row (2 n_split slots: two per share). With L_z the
+// slots' LSEs and M their maximum: LSE = M + ln sum_z e^(L_z - M), O = sum_z e^(L_z - LSE) O_z,
+// each O_z already divided by its own normaliser; slots with no key (L_z = -inf) drop out. Grid (row blocks,
 // heads), one group of D/8 lanes per row, 8 outputs per lane.
 template <int D>
 __global__ void __launch_bounds__(256) fwd_combine_kernel(FwdArgs a) {
@@ -986,27 +1041,44 @@ __global__ void __launch_bounds__(256) fwd_combine_kernel(FwdArgs a) {
   griddep_launch_dependents();
   constexpr int LPR = D / 8;
   constexpr int RPB = 256 / LPR;
+  constexpr int G = 8;  // slots whose loads are issued together
   const int part = threadIdx.x % LPR;
   const int n = blockIdx.x * RPB + threadIdx.x / LPR;
   const int bh = blockIdx.y;
   if (n >= a.N) return;
   const size_t row = (size_t)bh * a.N + n, plane = (size_t)gridDim.y * a.N;
+  const int nz = 2 * a.n_split;
   float mx = -INFINITY;
-  for (int z = 0; z < a.n_split; ++z) mx = fmaxf(mx, a.part_lse[z * plane + row]);
+  for (int z0 = 0; z0 < nz; z0 += G) {
+    float l[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) l[g] = (z0 + g < nz) ? a.part_lse[(z0 + g) * plane + row] : -INFINITY;
+#pragma unroll
+    for (int g = 0; g < G; ++g) mx = fmaxf(mx, l[g]);
+  }
   float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
   float wsum = 0.f;
   if (mx != -INFINITY) {
-    for (int z = 0; z < a.n_split; ++z) {
-      const float lz = a.part_lse[z * plane + row];
-      if (lz == -INFINITY) continue;
-      const float w = ex2_approx((lz - mx) * 1.4426950408889634f);
-      wsum += w;
-      const float4* src = reinterpret_cast<const float4*>(a.part_o + (z * plane + row) * D + part * 8);
-      const float4 x0 = src[0], x1 = src[1];
-      acc[0] = fmaf(w, x0.x, acc[0]), acc[1] = fmaf(w, x0.y, acc[1]);
-      acc[2] = fmaf(w, x0.z, acc[2]), acc[3] = fmaf(w, x0.w, acc[3]);
-      acc[4] = fmaf(w, x1.x, acc[4]), acc[5] = fmaf(w, x1.y, acc[5]);
-      acc[6] = fmaf(w, x1.z, acc[6]), acc[7] = fmaf(w, x1.w, acc[7]);
+    for (int z0 = 0; z0 < nz; z0 += G) {
+      float w[G];
+      float4 x0[G], x1[G];
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        const float lz = (z0 + g < nz) ? a.part_lse[(z0 + g) * plane + row] : -INFINITY;
+        w[g] = (lz == -INFINITY) ? 0.f : ex2_approx((lz - mx) * 1.4426950408889634f);
+        const float4* src = reinterpret_cast<const float4*>(a.part_o + ((z0 + g) * plane + row) * D + part * 8);
+        // a slot without keys holds no O: read nothing there
+        x0[g] = (w[g] > 0.f) ? src[0] : make_float4(0.f, 0.f, 0.f, 0.f);
+        x1[g] = (w[g] > 0.f) ? src[1] : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        wsum += w[g];
+        acc[0] = fmaf(w[g], x0[g].x, acc[0]), acc[1] = fmaf(w[g], x0[g].y, acc[1]);
+        acc[2] = fmaf(w[g], x0[g].z, acc[2]), acc[3] = fmaf(w[g], x0[g].w, acc[3]);
+        acc[4] = fmaf(w[g], x1[g].x, acc[4]), acc[5] = fmaf(w[g], x1[g].y, acc[5]);
+        acc[6] = fmaf(w[g], x1[g].z, acc[6]), acc[7] = fmaf(w[g], x1[g].w, acc[7]);
+      }
     }
   }
   const float inv = (wsum > 0.f) ? 1.f / wsum : 0.f;
@@ -1022,7 +1094,7 @@ __global__ void __launch_bounds__(256) fwd_combine_kernel(FwdArgs a) {
 template <int D, bool SPLIT = false>
 static int launch_fwd_d(const void* q, const void* k, const void* v, void* o, const FwdArgs& args, int BH,
                         cudaStream_t stream) {
-  using C = FwdCfg<D>;
+  using C = FwdCfg<D, SPLIT>;
   CUtensorMap mq, mk, mv, mo;
   const uint64_t N = (uint64_t)args.N, Nk = (uint64_t)args.Nk;
   const auto BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;

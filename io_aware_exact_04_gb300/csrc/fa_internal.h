@@ -17,8 +17,9 @@ struct FwdArgs {
   float* lse;          // [B*H, N]; null only with a split (the combine then writes none)
   uint16_t* o;         // [B*H, N, d] bf16 (also written through the tensor map)
   int n_split;         // split-KV forward: key-tile shares per work item (1 = no split)
-  float* part_o;       // split-KV: [n_split, B*H, N, d] fp32 O of each share, normalised by its l
-  float* part_lse;     // split-KV: [n_split, B*H, N] fp32 LSE of each share (-inf: no key)
+  float* part_o;       // split-KV: [2 n_split, B*H, N, d] fp32 partial O (two slots per share),
+                       // each normalised by its own l
+  float* part_lse;     // split-KV: [2 n_split, B*H, N] fp32 LSE of each slot (-inf: no key)
   int* status;         // device status word (4 ints)
 };
 

@@ -112,7 +112,7 @@ def test_selftest_argument_errors(built):
 
 def test_split_forward_argument_errors(lib):
     need = lib.fa_forward_split_workspace_size(2, 3, 100, 64, 4)
-    assert need == ((4 * 6 * 100 * 64 * 4 + 255) // 256) * 256 + ((4 * 6 * 100 * 4 + 255) // 256) * 256
+    assert need == ((8 * 6 * 100 * 64 * 4 + 255) // 256) * 256 + ((8 * 6 * 100 * 4 + 255) // 256) * 256
     assert lib.fa_forward_split_workspace_size(2, 3, 100, 96, 4) == 0
     assert lib.fa_forward_split_workspace_size(2, 3, 100, 64, 0) == 0
     args = lambda n_split, ws, nbytes: (*[A] * 5, 2, 3, 100, 900, 64, 0.125, 1, None, n_split, ws, nbytes, None)  # noqa: E731
