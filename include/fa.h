@@ -87,6 +87,21 @@ FA_API int fa_forward_ex(const void* q, const void* k, const void* v, void* o, f
 FA_API int fa_forward_qk(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq,
                          int Nk, int d, float scale, int causal, const int32_t* kv_len, fa_stream_t stream);
 
+/* Forward pass over packed sequences of different lengths (variable-length
+ * batches with no padding): B sequences, each its own attention problem with
+ * N = len_b query and key rows (the pages' masks per sequence: causal j <= i).
+ *  - Layout: q, k, v, o are [H, T, d] bf16 with every head's rows of all
+ *    sequences packed back to back; lse is [H, T] fp32. Sequence b has rows
+ *    [cu_seqlens[b], cu_seqlens[b + 1]) of every head.
+ *  - cu_seqlens: device int32 [B + 1], non-decreasing, cu_seqlens[0] = 0,
+ *    cu_seqlens[B] = T. max_seqlen: host upper bound of every length; it sizes
+ *    the grid. A longer sequence is not fully computed and records
+ *    FA_ERR_DEVICE_CHECK in the device status word.
+ *  - A sequence of length 0 writes nothing. */
+FA_API int fa_forward_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                             const int32_t* cu_seqlens, int B, int H, int T, int max_seqlen, int d, float scale,
+                             int causal, fa_stream_t stream);
+
 /* Forward pass for inference shapes: few query rows over many keys, where one
  * CTA per (head, query-tile pair) leaves most SMs idle (the pages: inference
  * workloads are mostly memory-bound). The key tiles of each work item are cut

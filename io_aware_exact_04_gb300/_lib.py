@@ -27,6 +27,7 @@ SIGNATURES = {
         "fa_forward": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp]),
         "fa_forward_ex": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp, _vp]),
         "fa_forward_qk": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _vp, _vp]),
+        "fa_forward_varlen": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _vp]),
         "fa_forward_split": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _vp, _i, _vp, _sz, _vp]),
         "fa_forward_split_workspace_size": (_sz, [_i, _i, _i, _i, _i]),
         "fa_forward_split_count": (_i, [_i, _i, _i, _i, _i]),

@@ -76,6 +76,39 @@ def forward(q, k, v, causal: bool = False, scale: Optional[float] = None, kv_len
     return o, lse
 
 
+def _check_hTd(name: str, t: torch.Tensor, shape=None):
+    if not t.is_cuda or t.dtype != torch.bfloat16 or t.dim() != 3 or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous bfloat16 CUDA tensor [H, T, d]")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def _cu(cu_seqlens: torch.Tensor, device) -> torch.Tensor:
+    if cu_seqlens.dtype != torch.int32 or cu_seqlens.dim() != 1 or not cu_seqlens.is_contiguous():
+        raise ValueError("cu_seqlens must be a contiguous int32 tensor [B + 1]")
+    if cu_seqlens.device != device:
+        raise ValueError("cu_seqlens must live on the same device as q")
+    return cu_seqlens
+
+
+def forward_varlen(q, k, v, cu_seqlens, max_seqlen: int, causal: bool = False, scale: Optional[float] = None):
+    """O, LSE over packed sequences (include/fa.h: fa_forward_varlen): q, k, v [H, T, d], sequence
+    b at rows cu_seqlens[b] .. cu_seqlens[b + 1]; lse [H, T]."""
+    _check_hTd("q", q)
+    H, T, d = q.shape
+    _check_hTd("k", k, q.shape)
+    _check_hTd("v", v, q.shape)
+    cu = _cu(cu_seqlens, q.device)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    o = torch.empty_like(q)
+    lse = torch.empty((H, T), dtype=torch.float32, device=q.device)
+    with torch.cuda.device(q.device):
+        rc = _lib_fa().fa_forward_varlen(_p(q), _p(k), _p(v), _p(o), _p(lse), _p(cu), cu.numel() - 1, H, T,
+                                         int(max_seqlen), d, scale, int(bool(causal)), _stream(q.device))
+    _lib.check(rc, "fa_forward_varlen")
+    return o, lse
+
+
 def forward_split(q, k, v, causal: bool = False, scale: Optional[float] = None, kv_len=None,
                   n_split: Optional[int] = None, with_lse: bool = False, out=None, workspace=None):
     """Inference forward with split keys (include/fa.h: fa_forward_split): O, and LSE when

@@ -30,6 +30,16 @@ __device__ __forceinline__ void record_error(const DevStatus& st, int code, int 
   *(volatile int*)st.abort_smem = 1;
 }
 
+// A failed argument check inside a kernel, found before the CTA's pipeline exists: records
+// FA_ERR_DEVICE_CHECK (code 6) and the site once; the caller carries on or returns.
+__device__ __forceinline__ void record_check(int* word, int site) {
+  if (atomicCAS(word, 0, 6) == 0) {
+    word[1] = site;
+    word[2] = blockIdx.x;
+    word[3] = blockIdx.y;
+  }
+}
+
 // Single-thread bounded wait. Returns false if the CTA must abort.
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, DevStatus st, int site,
                                              uint64_t limit_ns = kWaitLimitNs) {

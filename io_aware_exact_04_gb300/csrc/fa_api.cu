@@ -153,11 +153,48 @@ int fa_forward_qk(const void* q, const void* k, const void* v, void* o, float* l
   a.kv_len = kv_len;
   a.lse = lse;
   a.o = static_cast<uint16_t*>(o);
+  a.cu_seqlens = nullptr;
+  a.T = 0;
+  a.max_seqlen = 0;
   a.n_split = 1;
   a.part_o = nullptr;
   a.part_lse = nullptr;
   a.status = status;
   return fa::launch_fwd(q, k, v, o, a, B * H, d, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int fa_forward_varlen(const void* q, const void* k, const void* v, void* o, float* lse, const int32_t* cu_seqlens,
+                      int B, int H, int T, int max_seqlen, int d, float scale, int causal, fa_stream_t stream) {
+  if (B < 0 || T < 0 || max_seqlen < 0) return FA_ERR_INVALID_ARG;
+  int rc = check_common(B, H, max_seqlen, max_seqlen, d, scale, causal);
+  if (rc != FA_OK) return rc;
+  if ((long long)B * H == 0 || T == 0 || max_seqlen == 0) return FA_OK;
+  if (!q || !k || !v || !o || !lse || !cu_seqlens) return FA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return FA_ERR_MISALIGNED;
+  if ((long long)H * T > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+  int err = FA_OK;
+  int* status = device_status(&err);
+  if (!status) return err;
+  fa::FwdArgs a;
+  a.H = H;
+  a.N = max_seqlen;
+  a.Nk = max_seqlen;
+  a.coff = 0;
+  a.n_pairs = (max_seqlen + 255) / 256;
+  a.causal = causal;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.kv_len = nullptr;
+  a.lse = lse;
+  a.o = static_cast<uint16_t*>(o);
+  a.cu_seqlens = cu_seqlens;
+  a.T = T;
+  a.max_seqlen = max_seqlen;
+  a.n_split = 1;
+  a.part_o = nullptr;
+  a.part_lse = nullptr;
+  a.status = status;
+  return fa::launch_fwd_varlen(q, k, v, o, a, B * H, d, reinterpret_cast<cudaStream_t>(stream));
 }
 
 size_t fa_forward_split_workspace_size(int B, int H, int Nq, int d, int n_split) {
@@ -209,6 +246,9 @@ int fa_forward_split(const void* q, const void* k, const void* v, void* o, float
   a.kv_len = kv_len;
   a.lse = lse;
   a.o = static_cast<uint16_t*>(o);
+  a.cu_seqlens = nullptr;
+  a.T = 0;
+  a.max_seqlen = 0;
   a.n_split = n_split;
   a.part_o = static_cast<float*>(workspace);
   a.part_lse = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + round_up(rows * d * 4, 256));

@@ -61,7 +61,7 @@ static_assert(8 * (1 + 3 * FwdCfg<64, true>::NST + 9) + 8 <= 256, "split d = 64 
 
 // Wait-site identifiers recorded with FA_ERR_TIMEOUT.
 enum { SITE_F_KV_EMPTY = 1, SITE_F_Q_FULL, SITE_F_K_FULL, SITE_F_V_FULL, SITE_F_P_READY, SITE_F_S_FULL,
-       SITE_F_O_DONE, SITE_F_DRAIN, SITE_F_S_FREE };
+       SITE_F_O_DONE, SITE_F_DRAIN, SITE_F_S_FREE, SITE_F_SEQLEN };
 
 // Key tiles that the query tile of rows [qs, qs + 128) needs: those below kv (the valid keys)
 // that some row of the tile may see. Causal row i sees keys j <= i + coff.
@@ -76,7 +76,7 @@ __device__ __forceinline__ int key_tiles(int qs, int nq, int nkt, int causal, in
 // z-th of a.n_split near-equal shares, and writes normalised partial O (fp32) and LSE to
 // slots 2z and 2z + 1 of a.part_o / a.part_lse for fwd_combine_kernel; the same
 // running-maximum rescaling that joins key tiles inside a CTA then joins the slots.
-template <int D, bool SPLIT>
+template <int D, bool SPLIT, bool VL = false>
 __global__ void __launch_bounds__(352, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o, FwdArgs a) {
@@ -111,19 +111,33 @@ __global__ void __launch_bounds__(352, 1)
   const int pair = a.n_pairs - 1 - (int)blockIdx.y;
   const int bh = blockIdx.x;
   const int b = bh / a.H;
-  int kv = a.Nk;
-  if (a.kv_len) kv = min(max(a.kv_len[b], 0), a.Nk);
+  // VL (packed sequences, layout [H, T, d]): this CTA's sequence b has rows [cu[b], cu[b+1])
+  // of head h; NQ is its query count, rbase the TMA row of its first row, zh the TMA head
+  // coordinate and obase the index of its row 0 among the O / LSE rows
+  int NQ = a.N, rbase = 0, zh = bh;
+  size_t obase = (size_t)bh * a.N;
+  if (VL) {
+    const int h = bh - b * a.H;
+    rbase = a.cu_seqlens[b];
+    NQ = a.cu_seqlens[b + 1] - rbase;
+    zh = h;
+    obase = (size_t)h * a.T + rbase;
+    if (NQ > a.max_seqlen && threadIdx.x == 0 && blockIdx.y == 0) record_check(a.status, SITE_F_SEQLEN);
+    if ((a.n_pairs - 1 - (int)blockIdx.y) * 256 >= NQ) return;  // this pair lies past the sequence
+  }
+  int kv = VL ? NQ : a.Nk;
+  if (!VL && a.kv_len) kv = min(max(a.kv_len[b], 0), a.Nk);
   const int nkt = (kv + 127) >> 7;
   const int q0 = pair * 256;
   int n_t[2];
 #pragma unroll
-  for (int t = 0; t < 2; ++t) n_t[t] = key_tiles(q0 + t * 128, a.N, nkt, a.causal, a.coff);
+  for (int t = 0; t < 2; ++t) n_t[t] = key_tiles(q0 + t * 128, NQ, nkt, a.causal, VL ? 0 : a.coff);
   // key tiles run here: [jb, jb + nmax), all of them without a split; loops count from 0.
   // dual (split only): the item's second query tile lies past N, so query lane 1 takes the
   // same rows as lane 0 and the two lanes split the share's key tiles, even ones to lane 0
   // and odd ones to lane 1; each lane's result is a partial of its own for the combine.
   int jb = 0, nmax;
-  const bool dual = SPLIT && D == 64 && q0 + 128 >= a.N && n_t[0] > 0;
+  const bool dual = SPLIT && D == 64 && q0 + 128 >= NQ && n_t[0] > 0;
   if (SPLIT) {
     const int nall = max(n_t[0], n_t[1]);
     const int z = blockIdx.z;
@@ -152,10 +166,10 @@ __global__ void __launch_bounds__(352, 1)
     const uint32_t kd = sbase + C::OFF_K + s * C::TILE_BYTES, vd = sbase + C::OFF_V + s * C::TILE_BYTES;
     if (elect_one()) mbar_arrive_expect_tx(kf, C::TILE_BYTES);
     for (int c = 0; c < C::NSUB; ++c)
-      if (elect_one()) tma_load_3d(kd + c * C::SUB_BYTES, &tm_k, c * 64, (jb + j) * 128, bh, kf);
+      if (elect_one()) tma_load_3d(kd + c * C::SUB_BYTES, &tm_k, c * 64, rbase + (jb + j) * 128, zh, kf);
     if (elect_one()) mbar_arrive_expect_tx(vf, C::TILE_BYTES);
     for (int c = 0; c < C::NSUB; ++c)
-      if (elect_one()) tma_load_3d(vd + c * C::SUB_BYTES, &tm_v, c * 64, (jb + j) * 128, bh, vf);
+      if (elect_one()) tma_load_3d(vd + c * C::SUB_BYTES, &tm_v, c * 64, rbase + (jb + j) * 128, zh, vf);
     __syncwarp();
   };
   if (warp == 8) {
@@ -189,7 +203,7 @@ __global__ void __launch_bounds__(352, 1)
         for (int s = 0; s < C::NSUB; ++s)
           if (elect_one())
             tma_load_3d(sbase + C::OFF_Q + t * C::TILE_BYTES + s * C::SUB_BYTES, &tm_q, s * 64,
-                        q0 + (dual ? 0 : t * 128), bh, q_full);
+                        rbase + q0 + (dual ? 0 : t * 128), zh, q_full);
       for (int j = 0; j < n_pre; ++j) load_kv(j);
     }
   }
@@ -359,19 +373,19 @@ __global__ void __launch_bounds__(352, 1)
     const uint32_t tP = tmem + lane_off + C::tm_p(t);
     const uint32_t tO = tmem + lane_off + C::tm_o(t);
     const float sl2 = a.scale_log2;
-    float* lse_row = a.lse + (size_t)bh * a.N;
+    float* lse_row = a.lse + obase;
     // split: this lane's partial slot (two per share: lanes of a dual CTA, or the tile's
     // own result and an empty second slot)
     const size_t plane = (size_t)gridDim.x * a.N;
-    const size_t prow = (size_t)(2 * blockIdx.z + (dual ? t : 0)) * plane + (size_t)bh * a.N + grow;
-    if (SPLIT && !dual && grow < a.N && qs < a.N) a.part_lse[prow + plane] = -INFINITY;
-    if (qs < a.N && n == 0) {
+    const size_t prow = (size_t)(2 * blockIdx.z + (dual ? t : 0)) * plane + obase + grow;
+    if (SPLIT && !dual && grow < NQ && qs < NQ) a.part_lse[prow + plane] = -INFINITY;
+    if (qs < NQ && n == 0) {
       // no valid key for any row of this tile (in this share): O = 0, LSE = -inf
-      if (grow < a.N) {
+      if (grow < NQ) {
         if (SPLIT) {
           a.part_lse[prow] = -INFINITY;  // the combine skips this slot's O
         } else {
-          uint4* orow = reinterpret_cast<uint4*>(a.o + ((size_t)bh * a.N + grow) * D);
+          uint4* orow = reinterpret_cast<uint4*>(a.o + (obase + grow) * D);
           for (int c = 0; c < D / 8; ++c) orow[c] = make_uint4(0, 0, 0, 0);
           lse_row[grow] = -INFINITY;
         }
@@ -504,9 +518,12 @@ __global__ void __launch_bounds__(352, 1)
           a.part_lse[prow] = (l_run > 0.f) ? (m_run + lg2_approx(l_run)) * 0.6931471805599453f : -INFINITY;
       } else if (ok) {
         tc_fence_after();
-        // epilogue: O / l -> bf16 -> swizzled smem (this tile's Q buffer) -> TMA store
+        // epilogue: O / l -> bf16 -> swizzled smem (this tile's Q buffer) -> TMA store; a VL
+        // tile that runs past its sequence writes its rows directly (the next sequence's
+        // rows follow in the same tensor)
         const float inv = (l_run > 0.f) ? 1.f / l_run : 0.f;
         uint8_t* stage = sm + C::OFF_Q + t * C::TILE_BYTES;
+        const bool direct = VL && qs + 128 > NQ;
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t r[32];
@@ -522,15 +539,19 @@ __global__ void __launch_bounds__(352, 1)
             v.y = pack_bf16x2(__uint_as_float(r[q * 8 + 2]) * inv, __uint_as_float(r[q * 8 + 3]) * inv);
             v.z = pack_bf16x2(__uint_as_float(r[q * 8 + 4]) * inv, __uint_as_float(r[q * 8 + 5]) * inv);
             v.w = pack_bf16x2(__uint_as_float(r[q * 8 + 6]) * inv, __uint_as_float(r[q * 8 + 7]) * inv);
-            *reinterpret_cast<uint4*>(stage + blk * C::SUB_BYTES + sw128_offset(row, chunk0 + q)) = v;
+            if (direct) {
+              if (grow < NQ) *reinterpret_cast<uint4*>(a.o + (obase + grow) * D + c * 32 + q * 8) = v;
+            } else {
+              *reinterpret_cast<uint4*>(stage + blk * C::SUB_BYTES + sw128_offset(row, chunk0 + q)) = v;
+            }
           }
         }
-        if (grow < a.N) lse_row[grow] = (l_run > 0.f) ? (m_run + lg2_approx(l_run)) * 0.6931471805599453f : -INFINITY;
+        if (grow < NQ) lse_row[grow] = (l_run > 0.f) ? (m_run + lg2_approx(l_run)) * 0.6931471805599453f : -INFINITY;
         fence_proxy_async_smem();
         named_bar_sync(1 + t, 128);
-        if (wq == 0 && lane == 0) {
+        if (wq == 0 && lane == 0 && !direct) {
           for (int c = 0; c < C::NSUB; ++c)
-            tma_store_3d(&tm_o, smem_u32(stage + c * C::SUB_BYTES), c * 64, qs, bh);
+            tma_store_3d(&tm_o, smem_u32(stage + c * C::SUB_BYTES), c * 64, rbase + qs, zh);
           bulk_commit();
           bulk_wait_read0();  // the staging tile must outlive the copy's reads
         }
@@ -1091,27 +1112,30 @@ __global__ void __launch_bounds__(256) fwd_combine_kernel(FwdArgs a) {
   if (part == 0 && a.lse) a.lse[row] = (wsum > 0.f) ? mx + lg2_approx(wsum) * 0.6931471805599453f : -INFINITY;
 }
 
-template <int D, bool SPLIT = false>
+// BH = B * H work items per query pair. VL: the tensors are [H, T, d] (rows of all sequences
+// packed per head), so the maps span T rows and H heads.
+template <int D, bool SPLIT = false, bool VL = false>
 static int launch_fwd_d(const void* q, const void* k, const void* v, void* o, const FwdArgs& args, int BH,
                         cudaStream_t stream) {
   using C = FwdCfg<D, SPLIT>;
   CUtensorMap mq, mk, mv, mo;
-  const uint64_t N = (uint64_t)args.N, Nk = (uint64_t)args.Nk;
+  const uint64_t N = (uint64_t)(VL ? args.T : args.N), Nk = (uint64_t)(VL ? args.T : args.Nk);
+  const uint64_t Z = (uint64_t)(VL ? args.H : BH);
   const auto BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const auto SW = CU_TENSOR_MAP_SWIZZLE_128B;
-  if (!make_tmap_3d(&mq, q, BF, 2, D, N, BH, 64, 128, SW) || !make_tmap_3d(&mk, k, BF, 2, D, Nk, BH, 64, 128, SW) ||
-      !make_tmap_3d(&mv, v, BF, 2, D, Nk, BH, 64, 128, SW) || !make_tmap_3d(&mo, o, BF, 2, D, N, BH, 64, 128, SW))
+  if (!make_tmap_3d(&mq, q, BF, 2, D, N, Z, 64, 128, SW) || !make_tmap_3d(&mk, k, BF, 2, D, Nk, Z, 64, 128, SW) ||
+      !make_tmap_3d(&mv, v, BF, 2, D, Nk, Z, 64, 128, SW) || !make_tmap_3d(&mo, o, BF, 2, D, N, Z, 64, 128, SW))
     return cuda_fail("cuTensorMapEncodeTiled", 0, "tensor map rejected");
   static bool attr_set = false;  // benign race: idempotent
   if (!attr_set) {
-    const cudaError_t e =
-        cudaFuncSetAttribute(fwd_kernel<D, SPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    const cudaError_t e = cudaFuncSetAttribute(fwd_kernel<D, SPLIT, VL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               C::SMEM_BYTES);
     if (e != cudaSuccess) return cuda_fail("cudaFuncSetAttribute", (int)e, cudaGetErrorName(e));
     attr_set = true;
   }
   dim3 grid(BH, args.n_pairs, SPLIT ? args.n_split : 1);
-  return launch_pdl(__func__, fwd_kernel<D, SPLIT>, grid, dim3(C::THREADS), C::SMEM_BYTES, stream, mq, mk, mv, mo,
-                    args);
+  return launch_pdl(__func__, fwd_kernel<D, SPLIT, VL>, grid, dim3(C::THREADS), C::SMEM_BYTES, stream, mq, mk, mv,
+                    mo, args);
 }
 
 // d = 64: the persistent kernel, one CTA per SM (at most one per work item)
@@ -1149,6 +1173,13 @@ int launch_fwd(const void* q, const void* k, const void* v, void* o, const FwdAr
   if (d == 64 && args.n_pairs <= 4 && args.Nk <= 1024) return launch_fwd_p64(q, k, v, o, args, BH, stream);
   if (d == 64) return launch_fwd_d<64>(q, k, v, o, args, BH, stream);
   if (d == 128) return launch_fwd_d<128>(q, k, v, o, args, BH, stream);
+  return FA_ERR_UNSUPPORTED;
+}
+
+int launch_fwd_varlen(const void* q, const void* k, const void* v, void* o, const FwdArgs& args, int BH, int d,
+                      cudaStream_t stream) {
+  if (d == 64) return launch_fwd_d<64, false, true>(q, k, v, o, args, BH, stream);
+  if (d == 128) return launch_fwd_d<128, false, true>(q, k, v, o, args, BH, stream);
   return FA_ERR_UNSUPPORTED;
 }
 

@@ -16,6 +16,8 @@ struct FwdArgs {
   const int* kv_len;   // [B] device, or null
   float* lse;          // [B*H, N]; null only with a split (the combine then writes none)
   uint16_t* o;         // [B*H, N, d] bf16 (also written through the tensor map)
+  const int* cu_seqlens;  // packed sequences: device [B + 1] row offsets, else null
+  int T, max_seqlen;   // packed sequences: rows per head, and an upper bound of every length
   int n_split;         // split-KV forward: key-tile shares per work item (1 = no split)
   float* part_o;       // split-KV: [2 n_split, B*H, N, d] fp32 partial O (two slots per share),
                        // each normalised by its own l
@@ -78,6 +80,9 @@ int launch_pdl(const char* name, void (*kernel)(Params...), dim3 grid, dim3 bloc
 
 int launch_fwd(const void* q, const void* k, const void* v, void* o, const FwdArgs& args, int BH, int d,
                cudaStream_t stream);
+// Packed sequences ([H, T, d], args.cu_seqlens): fwd_kernel over (sequence x head, query pair).
+int launch_fwd_varlen(const void* q, const void* k, const void* v, void* o, const FwdArgs& args, int BH, int d,
+                      cudaStream_t stream);
 // Split-KV forward: fwd_kernel over (head, query pair, share) writing per-share partial
 // results to args.part_o / args.part_lse, then fwd_combine_kernel joining them into o (and lse).
 int launch_fwd_split(const void* q, const void* k, const void* v, void* o, const FwdArgs& args, int BH, int d,

@@ -214,3 +214,29 @@ def attention(q, k, v, do=None, *, scale: float, causal: bool, kv_len=None,
     if heads is None:
         res = {key: val.reshape((B, H) + val.shape[1:]) for key, val in res.items()}
     return res
+
+
+def attention_varlen(q, k, v, do, cu_seqlens, *, scale: float, causal: bool,
+                     backward: bool = True) -> Dict[str, np.ndarray]:
+    """Packed sequences: q, k, v, do are [H, T, d] float64 arrays and sequence b holds rows
+    cu_seqlens[b] .. cu_seqlens[b + 1] of every head. Each sequence is its own attention
+    problem (no query of one sequence sees a key of another); outputs keep the packed
+    layout: o, dq, dk, dv [H, T, d]; lse, D [H, T]."""
+    q = np.asarray(q, dtype=np.float64)
+    H, T, d = q.shape
+    cu = [int(x) for x in cu_seqlens]
+    keys = ["o", "lse", "D", "dq", "dk", "dv"] if backward else ["o", "lse"]
+    out = {key: np.zeros((H, T, d) if key in ("o", "dq", "dk", "dv") else (H, T)) for key in keys}
+    for h in range(H):
+        for s0, s1 in zip(cu[:-1], cu[1:]):
+            if s1 <= s0:
+                continue
+            sl = slice(s0, s1)
+            if backward:
+                r = head_backward(q[h, sl], k[h, sl], v[h, sl], np.asarray(do[h, sl], dtype=np.float64), scale, causal)
+            else:
+                o, lse = head_forward(q[h, sl], k[h, sl], v[h, sl], scale, causal)
+                r = {"o": o, "lse": lse}
+            for key in keys:
+                out[key][h, sl] = r[key]
+    return out

@@ -403,3 +403,36 @@ def test_pins_catch_a_reversed_alignment():
     o_bad = p @ v
     o_loop, _ = _loops_forward_qk(q.tolist(), k.tolist(), v.tolist(), 0.5, True, None)
     assert np.abs(o_bad - o_loop).max() > 1e-3
+
+
+# ---- packed sequences (each sequence its own problem) ----
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_packed_sequences_equal_the_padded_batch_with_key_padding(causal):
+    # the same numbers through the mask route: a padded [B, H, Lmax, d] batch with key padding
+    # kv_len = len_b and dO zero on the padding rows (so they add nothing to dK, dV)
+    lens, H, d = [5, 9, 1, 0, 7], 2, 4
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    T, L = int(cu[-1]), max(lens)
+    r = np.random.default_rng(18)
+    q, k, v, do = (r.standard_normal((H, T, d)) for _ in range(4))
+    s = 0.45
+    got = ref.attention_varlen(q, k, v, do, cu, scale=s, causal=causal)
+    B = len(lens)
+    pad = lambda x: np.stack([np.pad(x[:, cu[b]:cu[b + 1]], ((0, 0), (0, L - lens[b]), (0, 0))) for b in range(B)])  # noqa: E731
+    want = ref.attention(pad(q), pad(k), pad(v), pad(do), scale=s, causal=causal, kv_len=np.array(lens))
+    for b in range(B):
+        for name in ("o", "dq", "dk", "dv"):
+            np.testing.assert_allclose(got[name][:, cu[b]:cu[b + 1]], want[name][b, :, :lens[b]], rtol=0, atol=1e-12)
+        np.testing.assert_allclose(got["lse"][:, cu[b]:cu[b + 1]], want["lse"][b, :, :lens[b]], rtol=0, atol=1e-12)
+
+
+def test_packed_sequences_do_not_see_each_other():
+    H, d = 1, 4
+    r = np.random.default_rng(19)
+    q, k, v, do = (r.standard_normal((H, 12, d)) for _ in range(4))
+    two = ref.attention_varlen(q, k, v, do, [0, 6, 12], scale=0.5, causal=False)
+    one = ref.attention_varlen(q, k, v, do, [0, 12], scale=0.5, causal=False)
+    assert np.abs(two["o"][:, 6:] - one["o"][:, 6:]).max() > 1e-3
+    solo = ref.head_forward(q[0, 6:], k[0, 6:], v[0, 6:], 0.5, False)[0]
+    np.testing.assert_allclose(two["o"][0, 6:], solo, rtol=0, atol=1e-12)

@@ -170,3 +170,44 @@ def test_split_key_forward_default_count_matches_plain_forward(gpu):
     torch.cuda.synchronize(gpu)
     assert float((o1.float() - o2.float()).abs().max()) <= 2e-2 * float(o1.float().abs().max())
     assert float((lse1 - lse2).abs().max()) <= 1e-3
+
+
+# Packed sequences ([H, T, d], cu_seqlens): ragged lengths, an empty sequence, a single row,
+# lengths past one tile pair, both head dims.
+VARLEN = [
+    # H, lengths, d, causal
+    (2, [100, 0, 257, 643], 64, True),
+    (3, [1, 384, 129, 7], 64, False),
+    (2, [300, 1000], 128, True),
+    (1, [64, 65, 200, 513], 128, False),
+]
+
+
+def _packed(H, lens, d, seed):
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    x = workloads.draw(1, H, int(cu[-1]), d, seed=seed)
+    return cu, {n: x[n][0] for n in ("q", "k", "v", "do")}
+
+
+@pytest.mark.parametrize("H,lens,d,causal", VARLEN)
+def test_packed_sequences_forward_matches_oracle(gpu, H, lens, d, causal):
+    from io_aware_exact_04_gb300 import api
+    cu, x = _packed(H, lens, d, seed=sum(lens) + d)
+    q, k, v = (x[n].to(gpu) for n in ("q", "k", "v"))
+    o, lse = api.forward_varlen(q, k, v, torch.tensor(cu, device=gpu), max(lens), causal=causal)
+    torch.cuda.synchronize(gpu)
+    code, detail = api.device_status(gpu)
+    assert code == 0, f"device status {detail}"
+    r = ref.attention_varlen(f64(x["q"]), f64(x["k"]), f64(x["v"]), f64(x["do"]), cu, scale=1 / math.sqrt(d),
+                             causal=causal, backward=False)
+    assert_within({"o": compare("o", f64(o), r["o"]), "lse": compare("lse", f64(lse), r["lse"])})
+
+
+def test_packed_sequences_longer_than_max_seqlen_are_reported(gpu):
+    from io_aware_exact_04_gb300 import api
+    cu, x = _packed(1, [100, 300], 64, seed=3)
+    q, k, v = (x[n].to(gpu) for n in ("q", "k", "v"))
+    api.forward_varlen(q, k, v, torch.tensor(cu, device=gpu), 256, causal=True)  # 300 > 256
+    torch.cuda.synchronize(gpu)
+    code, detail = api.device_status(gpu)
+    assert code == 6, detail  # FA_ERR_DEVICE_CHECK, recorded, no fault
