@@ -102,6 +102,21 @@ FA_API int fa_forward_varlen(const void* q, const void* k, const void* v, void* 
                              const int32_t* cu_seqlens, int B, int H, int T, int max_seqlen, int d, float scale,
                              int causal, fa_stream_t stream);
 
+/* Backward of fa_forward_varlen: q, k, v, o, dO, dq, dk, dv are [H, T, d] bf16,
+ * lse [H, T] fp32, sequences as in the forward call (same cu_seqlens,
+ * max_seqlen, scale and causal). workspace: fa_backward_varlen_workspace_size
+ * bytes, 256-byte aligned, contents on entry irrelevant. A sequence longer
+ * than max_seqlen records FA_ERR_DEVICE_CHECK. */
+FA_API int fa_backward_varlen(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                              const float* lse, void* dq, void* dk, void* dv, const int32_t* cu_seqlens, int B, int H,
+                              int T, int max_seqlen, int d, float scale, int causal, void* workspace,
+                              size_t workspace_bytes, fa_stream_t stream);
+
+/* Workspace bytes of fa_backward_varlen: per head, -D and a base-2 LSE for
+ * T + 4 B + 256 rows (each sequence's rows start on a 16-byte boundary) and
+ * an fp32 dQ accumulator of T rows rounded up to 128. 0 for invalid arguments. */
+FA_API size_t fa_backward_varlen_workspace_size(int B, int H, int T, int d);
+
 /* Forward pass for inference shapes: few query rows over many keys, where one
  * CTA per (head, query-tile pair) leaves most SMs idle (the pages: inference
  * workloads are mostly memory-bound). The key tiles of each work item are cut

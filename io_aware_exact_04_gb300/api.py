@@ -109,6 +109,30 @@ def forward_varlen(q, k, v, cu_seqlens, max_seqlen: int, causal: bool = False, s
     return o, lse
 
 
+def backward_varlen(q, k, v, o, do, lse, cu_seqlens, max_seqlen: int, causal: bool = False,
+                    scale: Optional[float] = None):
+    """dQ, dK, dV over packed sequences (include/fa.h: fa_backward_varlen); shapes as forward_varlen."""
+    _check_hTd("q", q)
+    H, T, d = q.shape
+    for name, t in (("k", k), ("v", v), ("o", o), ("do", do)):
+        _check_hTd(name, t, q.shape)
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (H, T) or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous float32 [H, T] tensor")
+    cu = _cu(cu_seqlens, q.device)
+    B = cu.numel() - 1
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+    lib = _lib_fa()
+    need = int(lib.fa_backward_varlen_workspace_size(B, H, T, d))
+    work = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    with torch.cuda.device(q.device):
+        rc = lib.fa_backward_varlen(_p(q), _p(k), _p(v), _p(o), _p(do), _p(lse), _p(dq), _p(dk), _p(dv), _p(cu), B, H,
+                                    T, int(max_seqlen), d, scale, int(bool(causal)), _p(work), work.numel(),
+                                    _stream(q.device))
+    _lib.check(rc, "fa_backward_varlen")
+    return dq, dk, dv
+
+
 def forward_split(q, k, v, causal: bool = False, scale: Optional[float] = None, kv_len=None,
                   n_split: Optional[int] = None, with_lse: bool = False, out=None, workspace=None):
     """Inference forward with split keys (include/fa.h: fa_forward_split): O, and LSE when

@@ -347,6 +347,61 @@ int fa_backward(const void* q, const void* k, const void* v, const void* o, cons
                         workspace_bytes, stream);
 }
 
+size_t fa_backward_varlen_workspace_size(int B, int H, int T, int d) {
+  if (B < 0 || H < 0 || T < 0 || (d != 64 && d != 128)) return 0;
+  const long long Lpad = round_up((long long)T + 4LL * B, 128) + 128, Tpad = round_up(T, 128);
+  const long long l2 = round_up((long long)H * Lpad * 4, 256);
+  return (size_t)(2 * l2 + round_up((long long)H * Tpad * d * 4, 256));
+}
+
+int fa_backward_varlen(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
+                       void* dq, void* dk, void* dv, const int32_t* cu_seqlens, int B, int H, int T, int max_seqlen,
+                       int d, float scale, int causal, void* workspace, size_t workspace_bytes, fa_stream_t stream) {
+  if (B < 0 || T < 0 || max_seqlen < 0) return FA_ERR_INVALID_ARG;
+  int rc = check_common(B, H, max_seqlen, max_seqlen, d, scale, causal);
+  if (rc != FA_OK) return rc;
+  if ((long long)B * H == 0 || T == 0 || max_seqlen == 0) return FA_OK;
+  if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv || !cu_seqlens || !workspace) return FA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dO) || !aligned16(lse) ||
+      !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+    return FA_ERR_MISALIGNED;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return FA_ERR_MISALIGNED;
+  if ((long long)H * (T + 4LL * B + 256) > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+  if (workspace_bytes < fa_backward_varlen_workspace_size(B, H, T, d)) return FA_ERR_INVALID_ARG;
+  int err = FA_OK;
+  int* status = device_status(&err);
+  if (!status) return err;
+  const long long Lpad = round_up((long long)T + 4LL * B, 128) + 128;
+  const long long l2 = round_up((long long)H * Lpad * 4, 256);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  fa::BwdArgs a;  // packed sequences: kv_len, N, Nk and coff carry cu_seqlens, max_seqlen, T, Lpad
+  a.H = H;
+  a.N = max_seqlen;
+  a.Npad = (int)round_up(T, 128);  // dQ accumulator rows per head
+  a.Nk = T;
+  a.coff = (int)Lpad;
+  a.kv_len = cu_seqlens;
+  a.BH = B * H;
+  a.causal = causal;
+  a.scale = scale;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.o = static_cast<const uint16_t*>(o);
+  a.dO = static_cast<const uint16_t*>(dO);
+  a.lse = lse;
+  a.lse2 = reinterpret_cast<float*>(ws);
+  a.dvec = reinterpret_cast<float*>(ws + l2);
+  a.dq_acc = reinterpret_cast<float*>(ws + 2 * l2);
+  a.dq = static_cast<uint16_t*>(dq);
+  a.dk = static_cast<uint16_t*>(dk);
+  a.dv = static_cast<uint16_t*>(dv);
+  a.status = status;
+  for (int stage = 0; stage < 3; ++stage) {
+    rc = fa::launch_bwd_varlen_stage(stage, q, k, v, a, B, H, d, reinterpret_cast<cudaStream_t>(stream));
+    if (rc != FA_OK) return rc;
+  }
+  return FA_OK;
+}
+
 int fa_get_last_device_status(fa_stream_t stream, int* detail) {
   int err = FA_OK;
   int* status = device_status(&err);

@@ -112,6 +112,58 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(BwdArgs a, int BH) {
   }
 }
 
+// Packed sequences ([H, T, d], cu_seqlens): -D and -LSE2 of sequence b of head h go to rows
+// [base_b, base_{b+1}) of the head's Lpad rows, base_b = (cu[b] + 4 b) rounded down to a multiple
+// of 4 (16-byte aligned for the main kernels' bulk copies; bases still increase past each
+// sequence's end). The rows between a sequence's end and the next base, and the last sequence's
+// rows up to Lpad, get -LSE2 = -inf and -D = 0, so a step that reads past a sequence finds
+// values that its mask turns into P = 0. Grid (row blocks, sequence x head); the dQ
+// accumulator rows of the packed tensor are zeroed as well.
+template <int D>
+__global__ void __launch_bounds__(256) bwd_pre_varlen_kernel(BwdArgs a, int B) {
+  griddep_wait();
+  griddep_launch_dependents();
+  constexpr int LPR = D / 8;
+  constexpr int RPB = 256 / LPR;
+  const int part = threadIdx.x % LPR;
+  const int n = blockIdx.x * RPB + threadIdx.x / LPR;  // row within the sequence's slots
+  const int b = blockIdx.y / a.H, h = blockIdx.y - b * a.H;
+  const int rb = vl_cu(a)[b];
+  const int len = vl_cu(a)[b + 1] - rb;
+  const int base = (rb + 4 * b) & ~3;
+  if (len > vl_maxlen(a) && blockIdx.x == 0 && threadIdx.x == 0) record_check(a.status, 40);  // grid too small
+  const int slots = (b + 1 < B) ? (((vl_cu(a)[b + 1] + 4 * (b + 1)) & ~3) - base) : (vl_Lpad(a) - base);
+  const bool valid = n < len;
+  float acc = 0.f;
+  if (valid) {
+    const size_t off = ((size_t)h * vl_T(a) + rb + n) * D + part * 8;
+    const uint4 ov = *reinterpret_cast<const uint4*>(a.o + off);
+    const uint4 gv = *reinterpret_cast<const uint4*>(a.dO + off);
+    const uint32_t ow[4] = {ov.x, ov.y, ov.z, ov.w};
+    const uint32_t gw4[4] = {gv.x, gv.y, gv.z, gv.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      acc = fmaf(__uint_as_float(ow[i] << 16), __uint_as_float(gw4[i] << 16), acc);
+      acc = fmaf(__uint_as_float(ow[i] & 0xFFFF0000u), __uint_as_float(gw4[i] & 0xFFFF0000u), acc);
+    }
+    float4* dq = reinterpret_cast<float4*>(a.dq_acc + ((size_t)h * a.Npad + rb + n) * D + part * 8);
+    dq[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+    dq[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+#pragma unroll
+  for (int m = LPR / 2; m > 0; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
+  if (part == 0 && n < slots) {
+    const size_t r = (size_t)h * vl_Lpad(a) + base + n;
+    a.dvec[r] = valid ? -acc : 0.f;
+    float l2 = -INFINITY;
+    if (valid) {
+      const float l = a.lse[(size_t)h * vl_T(a) + rb + n];
+      if (l != -INFINITY) l2 = l * -1.4426950408889634f;
+    }
+    a.lse2[r] = l2;
+  }
+}
+
 // ---------------------------------------------------------------------------------------------
 template <int D>
 struct BwdCfg {
@@ -149,7 +201,18 @@ struct BwdCfg {
 enum { SITE_B_KV_FULL = 20, SITE_B_QDO_EMPTY, SITE_B_QDO_FULL, SITE_B_S_FULL, SITE_B_DP_FULL, SITE_B_P_READY,
        SITE_B_DS_READY, SITE_B_DQ_EMPTY, SITE_B_DQ_FULL, SITE_B_FINAL };
 
-template <int D>
+// VL (packed sequences, [H, T, d]): the item is sequence b of head h. Each statement that
+// addresses rows has its packed form in an if-constexpr branch beside the plain [BH, N, d]
+// one, so the plain kernel compiles exactly as it does without packing.
+template <bool VL>
+struct SeqD128 {  // packed only: TMA row base and head, row count, -LSE2 / -D and dK / dV row bases
+  int rb, nq, zh;
+  size_t lrow, krow;
+};
+template <>
+struct SeqD128<false> {};
+
+template <int D, bool VL = false>
 __global__ void __launch_bounds__(448, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -182,27 +245,57 @@ __global__ void __launch_bounds__(448, 1)
   const int j = blockIdx.y;  // key tile
   const int bh = blockIdx.x;
   const int b = bh / a.H;
-  int kv = a.Nk;
-  if (a.kv_len) kv = min(max(a.kv_len[b], 0), a.Nk);
   const int k0 = j * 128;
-  const int n_qt = (a.N + BR - 1) / BR;
-  // causal: the first query row that sees key k0 is k0 - coff
-  const int i_start = a.causal ? max(0, k0 - a.coff) / BR : 0;
+  [[maybe_unused]] SeqD128<VL> sq;
+  int kv, n_qt, i_start;
+  if constexpr (VL) {
+    const int h = bh - b * a.H;
+    sq.rb = vl_cu(a)[b];
+    sq.nq = vl_cu(a)[b + 1] - sq.rb;
+    sq.zh = h;
+    sq.lrow = (size_t)h * vl_Lpad(a) + ((sq.rb + 4 * b) & ~3);  // 16-byte aligned for the bulk copies
+    sq.krow = (size_t)h * vl_T(a) + sq.rb;
+    if (k0 >= sq.nq) return;  // past the sequence: these rows are another sequence's
+    kv = sq.nq;
+    n_qt = (sq.nq + BR - 1) / BR;
+    i_start = a.causal ? k0 / BR : 0;
+  } else {
+    kv = a.Nk;
+    if (a.kv_len) kv = min(max(a.kv_len[b], 0), a.Nk);
+    n_qt = (a.N + BR - 1) / BR;
+    // causal: the first query row that sees key k0 is k0 - coff
+    i_start = a.causal ? max(0, k0 - a.coff) / BR : 0;
+  }
   const int n_it = (k0 >= kv || i_start >= n_qt) ? 0 : (n_qt - i_start);
 
   if (n_it == 0) {
     // no valid key in this tile, or no query sees it: its dK and dV rows are zero
-    const int rows = min(128, a.Nk - k0);
+    int rows;
+    size_t row0;
+    if constexpr (VL) {
+      rows = min(128, sq.nq - k0);
+      row0 = sq.krow + k0;
+    } else {
+      rows = min(128, a.Nk - k0);
+      row0 = (size_t)bh * a.Nk + k0;
+    }
     for (int idx = threadIdx.x; idx < rows * (D / 8); idx += blockDim.x) {
-      const size_t off = ((size_t)bh * a.Nk + k0 + idx / (D / 8)) * D + (idx % (D / 8)) * 8;
+      const size_t off = (row0 + idx / (D / 8)) * D + (idx % (D / 8)) * 8;
       *reinterpret_cast<uint4*>(a.dk + off) = make_uint4(0, 0, 0, 0);
       *reinterpret_cast<uint4*>(a.dv + off) = make_uint4(0, 0, 0, 0);
     }
     return;
   }
 
-  const float* lse2_h = a.lse2 + (size_t)bh * a.Npad;
-  const float* dvec_h = a.dvec + (size_t)bh * a.Npad;
+  const float* lse2_h;
+  const float* dvec_h;
+  if constexpr (VL) {
+    lse2_h = a.lse2 + sq.lrow;
+    dvec_h = a.dvec + sq.lrow;
+  } else {
+    lse2_h = a.lse2 + (size_t)bh * a.Npad;
+    dvec_h = a.dvec + (size_t)bh * a.Npad;
+  }
   // The producer warp initialises the barriers and starts the first copies (K, V and the first
   // two query steps, whose slots are free) before the CTA-wide setup, hiding their latency. It
   // runs its code with the whole warp and lets one elected lane issue each copy.
@@ -214,8 +307,15 @@ __global__ void __launch_bounds__(448, 1)
     const float* dsrc = dvec_h + (size_t)i * BR;
     if (elect_one()) mbar_arrive_expect_tx(bar, 2 * C::QTILE + 2 * BR * 4);
     for (int c = 0; c < C::NSUB; ++c) {
-      if (elect_one()) tma_load_3d(sbase + C::OFF_Q + s * C::QTILE + c * C::QSUB, &tm_q, c * 64, i * BR, bh, bar);
-      if (elect_one()) tma_load_3d(sbase + C::OFF_DO + s * C::QTILE + c * C::QSUB, &tm_do, c * 64, i * BR, bh, bar);
+      if constexpr (VL) {
+        if (elect_one())
+          tma_load_3d(sbase + C::OFF_Q + s * C::QTILE + c * C::QSUB, &tm_q, c * 64, sq.rb + i * BR, sq.zh, bar);
+        if (elect_one())
+          tma_load_3d(sbase + C::OFF_DO + s * C::QTILE + c * C::QSUB, &tm_do, c * 64, sq.rb + i * BR, sq.zh, bar);
+      } else {
+        if (elect_one()) tma_load_3d(sbase + C::OFF_Q + s * C::QTILE + c * C::QSUB, &tm_q, c * 64, i * BR, bh, bar);
+        if (elect_one()) tma_load_3d(sbase + C::OFF_DO + s * C::QTILE + c * C::QSUB, &tm_do, c * 64, i * BR, bh, bar);
+      }
     }
     if (elect_one()) bulk_load(sbase + C::OFF_LSE + s * BR * 4, lsrc, BR * 4, bar);
     if (elect_one()) bulk_load(sbase + C::OFF_DV + s * BR * 4, dsrc, BR * 4, bar);
@@ -245,8 +345,13 @@ __global__ void __launch_bounds__(448, 1)
     }
     if (elect_one()) mbar_arrive_expect_tx(kv_full, 2 * C::KTILE);
     for (int c = 0; c < C::NSUB; ++c) {
-      if (elect_one()) tma_load_3d(sbase + C::OFF_K + c * C::KSUB, &tm_k, c * 64, k0, bh, kv_full);
-      if (elect_one()) tma_load_3d(sbase + C::OFF_V + c * C::KSUB, &tm_v, c * 64, k0, bh, kv_full);
+      if constexpr (VL) {
+        if (elect_one()) tma_load_3d(sbase + C::OFF_K + c * C::KSUB, &tm_k, c * 64, sq.rb + k0, sq.zh, kv_full);
+        if (elect_one()) tma_load_3d(sbase + C::OFF_V + c * C::KSUB, &tm_v, c * 64, sq.rb + k0, sq.zh, kv_full);
+      } else {
+        if (elect_one()) tma_load_3d(sbase + C::OFF_K + c * C::KSUB, &tm_k, c * 64, k0, bh, kv_full);
+        if (elect_one()) tma_load_3d(sbase + C::OFF_V + c * C::KSUB, &tm_v, c * 64, k0, bh, kv_full);
+      }
     }
     for (int it = 0; it < n_pre; ++it) load_qdo(it);
   }
@@ -403,7 +508,10 @@ __global__ void __launch_bounds__(448, 1)
         constexpr int NBOX = D / 32;
         constexpr int BOX_BYTES = BR * 128;
         for (int x = 0; x < NBOX; ++x)
-          tma_reduce_add_3d(&tm_dqacc, smem_u32(stg + x * BOX_BYTES), x * 32, i * BR, bh);
+          if constexpr (VL)
+            tma_reduce_add_3d(&tm_dqacc, smem_u32(stg + x * BOX_BYTES), x * 32, sq.rb + i * BR, sq.zh);
+          else
+            tma_reduce_add_3d(&tm_dqacc, smem_u32(stg + x * BOX_BYTES), x * 32, i * BR, bh);
         bulk_commit();
       }
     }
@@ -429,7 +537,11 @@ __global__ void __launch_bounds__(448, 1)
       if (!(ok = wait_warp(qdo_full(s), (it >> 1) & 1, st, SITE_B_QDO_FULL))) break;
       if (!(ok = wait_warp(s_full, it & 1, st, SITE_B_S_FULL))) break;
       tc_fence_after();
-      const bool need_mask = (k0 + 127 >= kv) || (a.causal && k0 + 127 > q0 + a.coff);
+      bool need_mask;
+      if constexpr (VL)
+        need_mask = (k0 + 127 >= kv) || (a.causal && k0 + 127 > q0) || (q0 + BR > sq.nq);
+      else
+        need_mask = (k0 + 127 >= kv) || (a.causal && k0 + 127 > q0 + a.coff);
       // ---- P^T = exp2(S^T s log2e + lse2), bf16 into the S^T columns (lse2 = -LSE log2e)
 #pragma unroll
       for (int ch = 0; ch < NCH; ++ch) {
@@ -444,10 +556,18 @@ __global__ void __launch_bounds__(448, 1)
         }
         tmem_wait_ld();
         if (need_mask) {  // only steps on the diagonal or past kv_len: masked S -> -inf, so P = 0
-          const int lim = key >= kv ? 32 : (a.causal ? key - a.coff - q0 - cb : 0);  // columns [0, lim)
+          if constexpr (VL) {
+            const int lim = key >= kv ? 32 : (a.causal ? key - q0 - cb : 0);  // columns [0, lim)
+            const int hi = sq.nq - q0 - cb;  // columns [hi, 32) are past the sequence
 #pragma unroll
-          for (int c = 0; c < 32; ++c)
-            if (c < lim) sv[c] = 0xff800000u;
+            for (int c = 0; c < 32; ++c)
+              if (c < lim || c >= hi) sv[c] = 0xff800000u;
+          } else {
+            const int lim = key >= kv ? 32 : (a.causal ? key - a.coff - q0 - cb : 0);  // columns [0, lim)
+#pragma unroll
+            for (int c = 0; c < 32; ++c)
+              if (c < lim) sv[c] = 0xff800000u;
+          }
         }
         uint32_t pk[16];
         const uint64_t sl2x2 = f2_pack(sl2, sl2);
@@ -529,14 +649,27 @@ __global__ void __launch_bounds__(448, 1)
           v.y = pack_bf16x2(__uint_as_float(x[q * 8 + 2]) * mul, __uint_as_float(x[q * 8 + 3]) * mul);
           v.z = pack_bf16x2(__uint_as_float(x[q * 8 + 4]) * mul, __uint_as_float(x[q * 8 + 5]) * mul);
           v.w = pack_bf16x2(__uint_as_float(x[q * 8 + 6]) * mul, __uint_as_float(x[q * 8 + 7]) * mul);
+          if constexpr (VL) {
+            if (k0 + 128 > sq.nq) {  // the tile runs past its sequence: rows written directly
+              if (k0 + r < sq.nq)
+                *reinterpret_cast<uint4*>((wg == 0 ? a.dv : a.dk) + (sq.krow + k0 + r) * D + c * 32 + q * 8) = v;
+              continue;
+            }
+          }
           *reinterpret_cast<uint4*>(stage + blk * C::KSUB + sw128_offset(r, chunk0 + q)) = v;
         }
       }
       fence_proxy_async_smem();
       named_bar_sync(1 + wg, 128);
-      if (wq == 0 && lane == 0) {
-        for (int c = 0; c < C::NSUB; ++c)
-          tma_store_3d(wg == 0 ? &tm_dv : &tm_dk, smem_u32(stage + c * C::KSUB), c * 64, k0, bh);
+      bool tma_out = wq == 0 && lane == 0;
+      if constexpr (VL) tma_out = tma_out && k0 + 128 <= sq.nq;
+      if (tma_out) {
+        for (int c = 0; c < C::NSUB; ++c) {
+          if constexpr (VL)
+            tma_store_3d(wg == 0 ? &tm_dv : &tm_dk, smem_u32(stage + c * C::KSUB), c * 64, sq.rb + k0, sq.zh);
+          else
+            tma_store_3d(wg == 0 ? &tm_dv : &tm_dk, smem_u32(stage + c * C::KSUB), c * 64, k0, bh);
+        }
         bulk_commit();
         bulk_wait_read0();  // the staging tile must outlive the copy's reads
       }
@@ -596,19 +729,54 @@ static_assert(8 * (4 + 2 * Bwd64::NQS + 17) + 12 <= 256, "d = 64 backward: barri
 struct TileD64 {
   int bh, k0, kv, n_it, i_start;
 };
+// Where work item bh's rows live. VL (packed sequences, [H, T, d]): item bh is sequence
+// b = bh / H of head h, its rows start at TMA row rb of head zh and it has nq query (and key)
+// rows; its -LSE2 / -D rows start at lrow and its dK / dV rows at krow. Without VL these are
+// the plain [BH, N, d] offsets (rb = 0), so that code compiles as it did without packing.
+struct SeqD64 {
+  int rb, nq, zh;
+  size_t lrow, krow;
+};
+template <bool VL>
+__device__ __forceinline__ SeqD64 seq_d64(int bh, const BwdArgs& a) {
+  SeqD64 q;
+  if (VL) {
+    const int b = bh / a.H, h = bh - b * a.H;
+    q.rb = vl_cu(a)[b];
+    q.nq = vl_cu(a)[b + 1] - q.rb;
+    q.zh = h;
+    q.lrow = (size_t)h * vl_Lpad(a) + ((q.rb + 4 * b) & ~3);  // 16-byte aligned for the bulk copies
+    q.krow = (size_t)h * vl_T(a) + q.rb;
+  } else {
+    q.rb = 0;
+    q.nq = a.N;
+    q.zh = bh;
+    q.lrow = (size_t)bh * a.Npad;
+    q.krow = (size_t)bh * a.Nk;
+  }
+  return q;
+}
+template <bool VL>
 __device__ __forceinline__ TileD64 tile_d64(int t, const BwdArgs& a) {
   TileD64 r;
   const int j = t / a.BH;
   r.bh = t - j * a.BH;
-  r.kv = a.Nk;
-  if (a.kv_len) r.kv = min(max(a.kv_len[r.bh / a.H], 0), a.Nk);
   r.k0 = j * 128;
-  const int n_qt = (a.N + Bwd64::BR - 1) / Bwd64::BR;
+  int nq = a.N;
+  if (VL) {
+    nq = seq_d64<VL>(r.bh, a).nq;
+    r.kv = nq;  // a tile past its sequence gets no work (and writes nothing: see the epilogue)
+  } else {
+    r.kv = a.Nk;
+    if (a.kv_len) r.kv = min(max(a.kv_len[r.bh / a.H], 0), a.Nk);
+  }
+  const int n_qt = (nq + Bwd64::BR - 1) / Bwd64::BR;
   // causal: the first query row that sees key k0 is k0 - coff; steps start on a 128-row
   // boundary (even) so that dQ pairs cover whole 128-row blocks
-  r.i_start = a.causal ? (max(0, r.k0 - a.coff) >> 7) << 1 : 0;
+  r.i_start = a.causal ? (max(0, r.k0 - (VL ? 0 : a.coff)) >> 7) << 1 : 0;
   const int n = (r.k0 >= r.kv || r.i_start >= n_qt) ? 0 : (n_qt - r.i_start);
-  r.n_it = n + (n & 1);  // whole pairs: a trailing step past N reads zero Q/dO and -inf lse2, so adds nothing
+  // whole pairs: a trailing step past the last query reads masked (or zero) Q / dO rows and adds nothing
+  r.n_it = n + (n & 1);
   return r;
 }
 // Tile of round r for CTA c of G, or -1 past the end (later rounds are past it too).
@@ -617,16 +785,17 @@ __device__ __forceinline__ int sched_d64(int r, int c, int G, int T) {
   return t < T ? t : -1;
 }
 // First tile with work at or after round r; returns its round, or -1.
+template <bool VL>
 __device__ __forceinline__ int next_work_d64(int r, int c, int G, int T, const BwdArgs& a, TileD64& out) {
   for (;; ++r) {
     const int t = sched_d64(r, c, G, T);
     if (t < 0) return -1;
-    out = tile_d64(t, a);
+    out = tile_d64<VL>(t, a);
     if (out.n_it > 0) return r;
   }
 }
 
-template <int DUMMY>
+template <bool VL>
 __global__ void __launch_bounds__(480, 1)
     bwd_kernel_d64(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -665,26 +834,28 @@ __global__ void __launch_bounds__(480, 1)
   const uint32_t ds0_count = smem_u32(tmem_slot + 2);
   DevStatus st{a.status, abort_flag};
 
-  const int T = a.BH * ((a.Nk + 127) >> 7);
+  const int T = a.BH * (((VL ? vl_maxlen(a) : a.Nk) + 127) >> 7);
   const int G = gridDim.x, cta = blockIdx.x;
 
   // The producer warp initialises the barriers and starts the first copies (K, V and the first
   // NQS steps of this CTA's first tile, whose slots are free) before the CTA-wide setup, hiding
   // their latency. It runs its code with the whole warp and lets one elected lane issue each copy.
   auto load_kv = [&](int b, const TileD64& tl) {  // whole warp
+    const SeqD64 sq = seq_d64<VL>(tl.bh, a);
     if (elect_one()) mbar_arrive_expect_tx(kv_full(b), 2 * C::KTILE);
-    if (elect_one()) tma_load_3d(sbase + C::off_k(b), &tm_k, 0, tl.k0, tl.bh, kv_full(b));
-    if (elect_one()) tma_load_3d(sbase + C::off_v(b), &tm_v, 0, tl.k0, tl.bh, kv_full(b));
+    if (elect_one()) tma_load_3d(sbase + C::off_k(b), &tm_k, 0, sq.rb + tl.k0, sq.zh, kv_full(b));
+    if (elect_one()) tma_load_3d(sbase + C::off_v(b), &tm_v, 0, sq.rb + tl.k0, sq.zh, kv_full(b));
     __syncwarp();
   };
   auto load_qdo = [&](int gs, const TileD64& tl, int it) {  // whole warp
     const int s = gs % NQS, i = tl.i_start + it;
     const uint32_t bar = qdo_full(s);
-    const float* lsrc = a.lse2 + (size_t)tl.bh * a.Npad + (size_t)i * BR;
-    const float* dsrc = a.dvec + (size_t)tl.bh * a.Npad + (size_t)i * BR;
+    const SeqD64 sq = seq_d64<VL>(tl.bh, a);
+    const float* lsrc = a.lse2 + sq.lrow + (size_t)i * BR;
+    const float* dsrc = a.dvec + sq.lrow + (size_t)i * BR;
     if (elect_one()) mbar_arrive_expect_tx(bar, 2 * C::QTILE + 2 * BR * 4);
-    if (elect_one()) tma_load_3d(sbase + C::OFF_Q + s * C::QTILE, &tm_q, 0, i * BR, tl.bh, bar);
-    if (elect_one()) tma_load_3d(sbase + C::OFF_DO + s * C::QTILE, &tm_do, 0, i * BR, tl.bh, bar);
+    if (elect_one()) tma_load_3d(sbase + C::OFF_Q + s * C::QTILE, &tm_q, 0, sq.rb + i * BR, sq.zh, bar);
+    if (elect_one()) tma_load_3d(sbase + C::OFF_DO + s * C::QTILE, &tm_do, 0, sq.rb + i * BR, sq.zh, bar);
     if (elect_one()) bulk_load(sbase + C::OFF_LSE + s * BR * 4, lsrc, BR * 4, bar);
     if (elect_one()) bulk_load(sbase + C::OFF_DV + s * BR * 4, dsrc, BR * 4, bar);
     __syncwarp();
@@ -718,7 +889,7 @@ __global__ void __launch_bounds__(480, 1)
     }
     __syncwarp();
     TileD64 tl;
-    if (next_work_d64(0, cta, G, T, a, tl) >= 0) {
+    if (next_work_d64<VL>(0, cta, G, T, a, tl) >= 0) {
       if (elect_one()) {
         prefetch_tmap(&tm_q);
         prefetch_tmap(&tm_do);
@@ -756,7 +927,7 @@ __global__ void __launch_bounds__(480, 1)
     int gs0 = 0, tu = 0, issued = 0, kv_loads = 0;
     bool ok = true;
     TileD64 tl;
-    for (int r = next_work_d64(0, cta, G, T, a, tl); ok && r >= 0; r = next_work_d64(r + 1, cta, G, T, a, tl)) {
+    for (int r = next_work_d64<VL>(0, cta, G, T, a, tl); ok && r >= 0; r = next_work_d64<VL>(r + 1, cta, G, T, a, tl)) {
       const int b = tu & 1;
       if (tu > 0) {  // the first tile's K and V went out before the setup
         if (!(ok = wait_warp(kv_empty(b), ((tu >> 1) & 1) ^ 1, st, SITE_B_QDO_EMPTY))) break;
@@ -833,7 +1004,7 @@ __global__ void __launch_bounds__(480, 1)
     bool ok = true;
     int gs0 = 0, tu = 0;
     TileD64 cur, nxt;
-    int r = next_work_d64(0, cta, G, T, a, cur);
+    int r = next_work_d64<VL>(0, cta, G, T, a, cur);
     if (r >= 0) {
       ok = wait_warp(kv_full(0), 0, st, SITE_B_KV_FULL) && wait_warp(qdo_full(w), 0, st, SITE_B_QDO_FULL);
       if (ok) {
@@ -844,7 +1015,7 @@ __global__ void __launch_bounds__(480, 1)
     }
     while (ok && r >= 0) {
       const int b = tu & 1;
-      const int r2 = next_work_d64(r + 1, cta, G, T, a, nxt);
+      const int r2 = next_work_d64<VL>(r + 1, cta, G, T, a, nxt);
       for (int it = w; ok && it < cur.n_it; it += 2) {
         const int gs = gs0 + it;
         const uint32_t par = (gs >> 1) & 1;
@@ -938,11 +1109,13 @@ __global__ void __launch_bounds__(480, 1)
     for (int rr = 0; ok; ++rr) {
       const int t = sched_d64(rr, cta, G, T);
       if (t < 0) break;
-      const TileD64 tl = tile_d64(t, a);
+      const TileD64 tl = tile_d64<VL>(t, a);
+      const SeqD64 sq = seq_d64<VL>(tl.bh, a);
       if (tl.n_it == 0) {  // no valid key in this tile: its dK and dV rows are zero
-        const int rows = min(128, a.Nk - tl.k0);
+        if (VL && tl.k0 >= sq.nq) continue;  // past its sequence: those rows are another sequence's
+        const int rows = min(128, (VL ? sq.nq : a.Nk) - tl.k0);
         for (int idx = tid; idx < rows * (C::D / 8); idx += 128) {
-          const size_t off = ((size_t)tl.bh * a.Nk + tl.k0 + idx / (C::D / 8)) * C::D + (idx % (C::D / 8)) * 8;
+          const size_t off = (sq.krow + tl.k0 + idx / (C::D / 8)) * C::D + (idx % (C::D / 8)) * 8;
           *reinterpret_cast<uint4*>(a.dk + off) = make_uint4(0, 0, 0, 0);
           *reinterpret_cast<uint4*>(a.dv + off) = make_uint4(0, 0, 0, 0);
         }
@@ -971,7 +1144,7 @@ __global__ void __launch_bounds__(480, 1)
           fence_proxy_async_smem();
           named_bar_sync(3, 128);
           if (tid == 0) {
-            tma_reduce_add_3d(&tm_dqacc, smem_u32(stg), h * 32, (tl.i_start + 2 * p) * BR, tl.bh);
+            tma_reduce_add_3d(&tm_dqacc, smem_u32(stg), h * 32, sq.rb + (tl.i_start + 2 * p) * BR, sq.zh);
             bulk_commit();
           }
         }
@@ -993,7 +1166,15 @@ __global__ void __launch_bounds__(480, 1)
           out[e] = pack_bf16x2(__uint_as_float(x[e >> 4][(2 * e) & 31]) * mul,
                                __uint_as_float(x[e >> 4][(2 * e + 1) & 31]) * mul);
       };
-      auto stage_store = [&](const uint32_t (&pk)[32], const CUtensorMap* map) {
+      auto stage_store = [&](const uint32_t (&pk)[32], const CUtensorMap* map, uint16_t* gdst) {
+        if (VL && tl.k0 + 128 > sq.nq) {  // the tile runs past its sequence: rows written directly
+          if (tl.k0 + r < sq.nq) {
+            uint4* dst = reinterpret_cast<uint4*>(gdst + (sq.krow + tl.k0 + r) * C::D);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+          }
+          return;
+        }
         uint8_t* stg = stage_acquire();
 #pragma unroll
         for (int q = 0; q < 8; ++q)
@@ -1002,14 +1183,14 @@ __global__ void __launch_bounds__(480, 1)
         fence_proxy_async_smem();
         named_bar_sync(3, 128);
         if (tid == 0) {
-          tma_store_3d(map, smem_u32(stg), 0, tl.k0, tl.bh);
+          tma_store_3d(map, smem_u32(stg), 0, sq.rb + tl.k0, sq.zh);
           bulk_commit();
         }
       };
       {
         uint32_t pk[32];
         load_packed(C::TM_DV, 1.f, pk);
-        stage_store(pk, &tm_dv);
+        stage_store(pk, &tm_dv, a.dv);
       }
       {
         uint32_t pk[32];
@@ -1025,7 +1206,7 @@ __global__ void __launch_bounds__(480, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(acc_free);
-        stage_store(pk, &tm_dk);
+        stage_store(pk, &tm_dk, a.dk);
       }
       gs0 += tl.n_it;
       ++tu;
@@ -1043,8 +1224,9 @@ __global__ void __launch_bounds__(480, 1)
     bool ok = true;
     int gs0 = 0;
     TileD64 tl;
-    for (int rr = next_work_d64(0, cta, G, T, a, tl); ok && rr >= 0; rr = next_work_d64(rr + 1, cta, G, T, a, tl)) {
+    for (int rr = next_work_d64<VL>(0, cta, G, T, a, tl); ok && rr >= 0; rr = next_work_d64<VL>(rr + 1, cta, G, T, a, tl)) {
       const int key = tl.k0 + r;
+      const int nq = VL ? seq_d64<VL>(tl.bh, a).nq : 0;  // VL: query columns past it are masked
       for (int it = w; it < tl.n_it; it += 2) {
         const int gs = gs0 + it;
         const int s = gs % NQS;
@@ -1055,7 +1237,8 @@ __global__ void __launch_bounds__(480, 1)
         if (!(ok = wait_warp(qdo_full(s), (gs / NQS) & 1, st, SITE_B_QDO_FULL))) break;
         if (!(ok = wait_warp(s_full(w), par, st, SITE_B_S_FULL))) break;
         tc_fence_after();
-        const bool need_mask = (tl.k0 + 127 >= tl.kv) || (a.causal && tl.k0 + 127 > q0 + a.coff);
+        const bool need_mask = (tl.k0 + 127 >= tl.kv) || (a.causal && tl.k0 + 127 > q0 + (VL ? 0 : a.coff)) ||
+                               (VL && q0 + BR > nq);
         // ---- P^T = exp2(S^T s log2e + lse2) (lse2 = -LSE log2e) -> bf16 pairs in the first 32
         //      columns of this buffer, kept in registers too: S^T's columns are overwritten by
         //      the next step once P^T is out
@@ -1067,10 +1250,11 @@ __global__ void __launch_bounds__(480, 1)
           tmem_ld32(tST + 32, sv[1]);
           tmem_wait_ld();
           if (need_mask) {  // only steps on the diagonal or past kv_len: masked S -> -inf, so P = 0
-            const int lim = key >= tl.kv ? 64 : (a.causal ? key - a.coff - q0 : 0);  // columns [0, lim)
+            const int lim = key >= tl.kv ? 64 : (a.causal ? key - (VL ? 0 : a.coff) - q0 : 0);  // columns [0, lim)
+            const int hi = VL ? nq - q0 : 64;  // VL: columns [hi, 64) are past the sequence
 #pragma unroll
             for (int c = 0; c < 64; ++c)
-              if (c < lim) sv[c >> 5][c & 31] = 0xff800000u;
+              if (c < lim || c >= hi) sv[c >> 5][c & 31] = 0xff800000u;
           }
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
@@ -1152,26 +1336,30 @@ static int launch_bwd_pre_d(const BwdArgs& a, int BH, cudaStream_t stream) {
   return launch_pdl(__func__, bwd_pre_kernel<D>, grid, dim3(256), 0, stream, a, BH);
 }
 
-template <int D>
+// BH = B * H work items per key tile. VL: tensors are [H, T, d] (all sequences' rows packed
+// per head): the maps span T rows (the dQ accumulator Npad) and H heads.
+template <int D, bool VL = false>
 static int launch_bwd_main_d(const void* q, const void* k, const void* v, const BwdArgs& a, int BH,
                              cudaStream_t stream) {
   constexpr int BR = (D == 64) ? Bwd64::BR : BwdCfg<D>::BR;  // query rows per step
-  const uint64_t N = (uint64_t)a.N, Nk = (uint64_t)a.Nk;
+  const uint64_t N = (uint64_t)(VL ? vl_T(a) : a.N), Nk = (uint64_t)(VL ? vl_T(a) : a.Nk);
+  const uint64_t Z = (uint64_t)(VL ? a.H : BH);
   const auto BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const auto SW = CU_TENSOR_MAP_SWIZZLE_128B;
   CUtensorMap mq, mk, mv, mdo, mdk, mdv, mdq;
-  if (!make_tmap_3d(&mq, q, BF, 2, D, N, BH, 64, BR, SW) || !make_tmap_3d(&mdo, a.dO, BF, 2, D, N, BH, 64, BR, SW) ||
-      !make_tmap_3d(&mk, k, BF, 2, D, Nk, BH, 64, 128, SW) || !make_tmap_3d(&mv, v, BF, 2, D, Nk, BH, 64, 128, SW) ||
-      !make_tmap_3d(&mdk, a.dk, BF, 2, D, Nk, BH, 64, 128, SW) ||
-      !make_tmap_3d(&mdv, a.dv, BF, 2, D, Nk, BH, 64, 128, SW) ||
-      !make_tmap_3d(&mdq, a.dq_acc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, D, (uint64_t)a.Npad, BH, 32,
+  if (!make_tmap_3d(&mq, q, BF, 2, D, N, Z, 64, BR, SW) || !make_tmap_3d(&mdo, a.dO, BF, 2, D, N, Z, 64, BR, SW) ||
+      !make_tmap_3d(&mk, k, BF, 2, D, Nk, Z, 64, 128, SW) || !make_tmap_3d(&mv, v, BF, 2, D, Nk, Z, 64, 128, SW) ||
+      !make_tmap_3d(&mdk, a.dk, BF, 2, D, Nk, Z, 64, 128, SW) ||
+      !make_tmap_3d(&mdv, a.dv, BF, 2, D, Nk, Z, 64, 128, SW) ||
+      !make_tmap_3d(&mdq, a.dq_acc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, D, (uint64_t)a.Npad, Z, 32,
                     (D == 64) ? 128 : BR, SW))
     return cuda_fail("cuTensorMapEncodeTiled", 0, "tensor map rejected");
   static bool attr_set = false;  // benign race: idempotent
-  dim3 grid(BH, (a.Nk + 127) / 128);
+  const int n_kt = ((VL ? vl_maxlen(a) : a.Nk) + 127) / 128;
+  dim3 grid(BH, n_kt);
   if constexpr (D == 64) {
     if (!attr_set) {
-      const cudaError_t e = cudaFuncSetAttribute(bwd_kernel_d64<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      const cudaError_t e = cudaFuncSetAttribute(bwd_kernel_d64<VL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                  Bwd64::SMEM_BYTES);
       if (e != cudaSuccess) return cuda_fail("cudaFuncSetAttribute", (int)e, cudaGetErrorName(e));
       attr_set = true;
@@ -1179,21 +1367,21 @@ static int launch_bwd_main_d(const void* q, const void* k, const void* v, const 
     // persistent: one CTA per SM (at most one per key tile)
     int sms = 0;
     if (!sm_count(&sms)) return FA_ERR_CUDA;
-    const long long tiles = (long long)BH * ((a.Nk + 127) / 128);
+    const long long tiles = (long long)BH * n_kt;
     BwdArgs ap = a;
     ap.BH = BH;
-    return launch_pdl(__func__, bwd_kernel_d64<0>, dim3((unsigned)std::min<long long>(tiles, sms)),
+    return launch_pdl(__func__, bwd_kernel_d64<VL>, dim3((unsigned)std::min<long long>(tiles, sms)),
                       dim3(Bwd64::THREADS), Bwd64::SMEM_BYTES, stream, mq, mk, mv, mdo, mdk, mdv, mdq, ap);
   } else {
     using C = BwdCfg<D>;
     if (!attr_set) {
       const cudaError_t e =
-          cudaFuncSetAttribute(bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+          cudaFuncSetAttribute(bwd_kernel<D, VL>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
       if (e != cudaSuccess) return cuda_fail("cudaFuncSetAttribute", (int)e, cudaGetErrorName(e));
       attr_set = true;
     }
-    return launch_pdl(__func__, bwd_kernel<D>, grid, dim3(C::THREADS), C::SMEM_BYTES, stream, mq, mk, mv, mdo, mdk,
-                      mdv, mdq, a);
+    return launch_pdl(__func__, bwd_kernel<D, VL>, grid, dim3(C::THREADS), C::SMEM_BYTES, stream, mq, mk, mv, mdo,
+                      mdk, mdv, mdq, a);
   }
 }
 
@@ -1212,6 +1400,32 @@ int launch_bwd_stage(int stage, const void* q, const void* k, const void* v, con
     case 1:
       return d == 64 ? launch_bwd_main_d<64>(q, k, v, a, BH, stream) : launch_bwd_main_d<128>(q, k, v, a, BH, stream);
     case 2: return d == 64 ? launch_bwd_convert_d<64>(a, BH, stream) : launch_bwd_convert_d<128>(a, BH, stream);
+    default: return FA_ERR_INVALID_ARG;
+  }
+}
+
+// Packed sequences: stage 0 the -D / -LSE2 rows (aligned per sequence) and the zeroed dQ
+// accumulator, 1 the main kernel over (sequence x head, key tile), 2 the dQ rounding over
+// all H * T rows. args.BH = B * H.
+int launch_bwd_varlen_stage(int stage, const void* q, const void* k, const void* v, const BwdArgs& a, int B, int H,
+                            int d, cudaStream_t stream) {
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  switch (stage) {
+    case 0: {
+      const int rpb = 256 / (d / 8);
+      const dim3 grid((unsigned)((vl_maxlen(a) + 262 + rpb - 1) / rpb), (unsigned)(B * H));
+      return d == 64 ? launch_pdl("bwd_pre_varlen_kernel", bwd_pre_varlen_kernel<64>, grid, dim3(256), 0, stream, a, B)
+                     : launch_pdl("bwd_pre_varlen_kernel", bwd_pre_varlen_kernel<128>, grid, dim3(256), 0, stream, a,
+                                  B);
+    }
+    case 1:
+      return d == 64 ? launch_bwd_main_d<64, true>(q, k, v, a, B * H, stream)
+                     : launch_bwd_main_d<128, true>(q, k, v, a, B * H, stream);
+    case 2: {
+      BwdArgs c = a;  // rows of the packed tensor: H items of T rows
+      c.N = vl_T(a);
+      return d == 64 ? launch_bwd_convert_d<64>(c, H, stream) : launch_bwd_convert_d<128>(c, H, stream);
+    }
     default: return FA_ERR_INVALID_ARG;
   }
 }

@@ -123,3 +123,18 @@ def test_split_forward_argument_errors(lib):
     assert lib.fa_forward_split(*args(4, None, need)) == 1     # no workspace
     assert lib.fa_forward_split(*args(4, ctypes.c_void_p(0x10010), need)) == 3  # 256-byte alignment
     assert lib.fa_forward_split_count(0, 3, 100, 900, 64) == 1
+
+
+def test_varlen_argument_errors(lib):
+    assert lib.fa_backward_varlen_workspace_size(3, 2, 1000, 64) == (
+        2 * (((2 * ((1000 + 12 + 127) // 128 * 128 + 128) * 4) + 255) // 256 * 256) + 2 * 1024 * 64 * 4)
+    assert lib.fa_backward_varlen_workspace_size(3, 2, 1000, 96) == 0
+    # no cu_seqlens; negative sizes; unsupported head dim
+    assert lib.fa_forward_varlen(*[A] * 5, None, 2, 2, 100, 64, 64, 0.125, 0, None) == 1
+    assert lib.fa_forward_varlen(*[A] * 6, 2, 2, -1, 64, 64, 0.125, 0, None) == 1
+    assert lib.fa_forward_varlen(*[A] * 6, 2, 2, 100, 64, 96, 0.125, 0, None) == 2
+    assert lib.fa_forward_varlen(*[None] * 6, 2, 2, 0, 64, 64, 0.125, 0, None) == 0  # nothing to do
+    need = lib.fa_backward_varlen_workspace_size(2, 2, 100, 64)
+    W = ctypes.c_void_p(0x10000)
+    assert lib.fa_backward_varlen(*[A] * 10, 2, 2, 100, 64, 64, 0.125, 0, W, need - 1, None) == 1
+    assert lib.fa_backward_varlen(*[A] * 10, 2, 2, 100, 64, 64, 0.125, 0, ctypes.c_void_p(0x10010), need, None) == 3

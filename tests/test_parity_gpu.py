@@ -211,3 +211,20 @@ def test_packed_sequences_longer_than_max_seqlen_are_reported(gpu):
     torch.cuda.synchronize(gpu)
     code, detail = api.device_status(gpu)
     assert code == 6, detail  # FA_ERR_DEVICE_CHECK, recorded, no fault
+
+
+@pytest.mark.parametrize("H,lens,d,causal", VARLEN)
+def test_packed_sequences_backward_matches_oracle(gpu, H, lens, d, causal):
+    from io_aware_exact_04_gb300 import api
+    cu, x = _packed(H, lens, d, seed=2 * sum(lens) + d)
+    q, k, v, do = (x[n].to(gpu) for n in ("q", "k", "v", "do"))
+    cu_d = torch.tensor(cu, device=gpu)
+    o, lse = api.forward_varlen(q, k, v, cu_d, max(lens), causal=causal)
+    dq, dk, dv = api.backward_varlen(q, k, v, o, do, lse, cu_d, max(lens), causal=causal)
+    torch.cuda.synchronize(gpu)
+    code, detail = api.device_status(gpu)
+    assert code == 0, f"device status {detail}"
+    r = ref.attention_varlen(f64(x["q"]), f64(x["k"]), f64(x["v"]), f64(x["do"]), cu, scale=1 / math.sqrt(d),
+                             causal=causal)
+    assert_within({n: compare(n, f64(t), r[n]) for n, t in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk),
+                                                             ("dv", dv))})
