@@ -209,11 +209,12 @@ def run_reference(args, w):
         return
     x = workloads.make_inputs(w)
     budget = min(20.0, 150.0 / max(1, args.steps + args.warmup))  # whole run within a few minutes
+    sample = oracle_sample_packed if w.packed else oracle_sample
     for _ in range(args.warmup):
-        oracle_sample(w, x, budget, max_heads=1)
+        sample(w, x, budget, 1)
     vals, secs, heads = [], 0.0, 0
     for _ in range(args.steps):
-        r = oracle_sample(w, x, budget)
+        r = sample(w, x, budget)
         vals.append(r["value"])
         secs += r["seconds"]
         heads += r["heads"]
@@ -559,6 +560,156 @@ def run_gpu_infer(args, w):
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------------------ packed sequences
+def oracle_sample_packed(w, x, budget_s: float, max_problems=None):
+    """Time the fp64 oracle on as many (sequence, head) problems of a packed workload as fit."""
+    import torch
+
+    from oracle import ref
+    pk = workloads.pack(x)
+    lens = x["kv_len"].tolist()
+    f64 = lambda t: t.to(torch.float64).numpy()  # noqa: E731
+    cuh = pk["cu_seqlens"].tolist()
+    t0, done, flops = time.perf_counter(), 0, 0.0
+    for b in range(w.B):
+        for h in range(w.H):
+            sl = slice(cuh[b], cuh[b + 1])
+            ref.head_backward(f64(pk["q"][h, sl]), f64(pk["k"][h, sl]), f64(pk["v"][h, sl]), f64(pk["do"][h, sl]),
+                              w.scale, w.causal)
+            flops += 12.0 * w.d * workloads.visible_pairs(lens[b], lens[b], w.causal)
+            done += 1
+            if time.perf_counter() - t0 > budget_s or (max_problems and done >= max_problems):
+                break
+        if time.perf_counter() - t0 > budget_s or (max_problems and done >= max_problems):
+            break
+    dt = time.perf_counter() - t0
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
+            "sample": f"{done} of {w.B * w.H} (sequence, head) problems of {w.name} (fp64 numpy, fwd+bwd), {dt:.1f} s",
+            "seconds": dt, "heads": done}
+
+
+def run_gpu_packed(args, w):
+    """fwd+bwd over packed sequences through fa_forward_varlen / fa_backward_varlen."""
+    import ctypes
+
+    import torch
+
+    from io_aware_exact_04_gb300 import _lib
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    lib = _lib.load("libfa.so")
+    peaks, peak_src = load_peaks()
+    x = workloads.make_inputs(w, seed=0)
+    pk = workloads.pack(x)
+    lens = x["kv_len"].tolist()
+    H, d, B = w.H, w.d, w.B
+    T, maxlen = int(pk["cu_seqlens"][-1]), max(lens)
+    q, k, v, do = (pk[n].to(dev) for n in ("q", "k", "v", "do"))
+    cu = pk["cu_seqlens"].to(dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((H, T), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+    wsb = int(lib.fa_backward_varlen_workspace_size(B, H, T, d))
+    work = torch.empty(wsb, dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sp = ctypes.c_void_p(stream.cuda_stream)
+    P = lambda t: ctypes.c_void_p(t.data_ptr()) if t is not None else None  # noqa: E731
+    causal = int(w.causal)
+
+    def step():
+        _lib.check(lib.fa_forward_varlen(P(q), P(k), P(v), P(o), P(lse), P(cu), B, H, T, maxlen, d, w.scale, causal,
+                                         sp), "fwd_varlen")
+        _lib.check(lib.fa_backward_varlen(P(q), P(k), P(v), P(o), P(do), P(lse), P(dq), P(dk), P(dv), P(cu), B, H, T,
+                                          maxlen, d, w.scale, causal, P(work), wsb, sp), "bwd_varlen")
+
+    for _ in range(max(3, args.warmup)):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(dev)
+    detail = (ctypes.c_int * 4)()
+    if lib.fa_get_last_device_status(sp, detail) != 0:
+        raise RuntimeError(f"device status after warm-up: {list(detail)}")
+    step_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    sampler = ClockSampler(local if "CUDA_VISIBLE_DEVICES" not in os.environ else 0)
+    if rank == 0:
+        sampler.start()
+        time.sleep(0.3)
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    sampler.mark("t_start")
+    for i in range(args.steps):
+        flush.zero_()
+        step_ev[i][0].record(stream)
+        step()
+        step_ev[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    sampler.mark("t_stop")
+    if ws > 1:
+        torch.distributed.barrier()
+    pairs = sum(workloads.visible_pairs(n, n, w.causal) for n in lens) * H
+    fl = 12.0 * d * pairs
+    ms_step, rate = job_throughput(sum(e[0].elapsed_time(e[1]) for e in step_ev) / args.steps, fl, device=dev)
+    value = rate / 1e12
+    peak = float(peaks["bf16_tflops"])
+    # whole-step roofline (the packed calls launch their three backward stages inside one call)
+    roof = {"bound": "tensor", "kernel": "fwd+bwd step (packed calls)", "achieved": value * 14.0 / 12.0,
+            "peak": peak, "unit": "TFLOP/s", "frac": value * 14.0 / 12.0 / peak, "traffic": None,
+            "peak_source": f"{peak_src} MEASURED_PEAKS bf16_tflops", "avg_launch_ms": ms_step,
+            "flops": "executed 14*P*d per head (recompute included) over the event-timed step"}
+    hb = {n: pk[n].pin_memory() for n in ("q", "k", "v", "do")}
+    ho = [torch.empty_like(hb["q"]).pin_memory() for _ in range(4)]
+    hlse = torch.empty((H, T), dtype=torch.float32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in hb.values())
+    d2h = sum(t.numel() * t.element_size() for t in ho) + hlse.numel() * 4
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_steps, e2e_ms = max(3, min(args.steps, 50)), 0.0
+    for i in range(e2e_steps + 2):
+        flush.zero_()
+        torch.cuda.synchronize(dev)
+        e0.record(stream)
+        for n, t in (("q", q), ("k", k), ("v", v), ("do", do)):
+            t.copy_(hb[n], non_blocking=True)
+        step()
+        for h_, t in zip(ho, (o, dq, dk, dv)):
+            h_.copy_(t, non_blocking=True)
+        hlse.copy_(lse, non_blocking=True)
+        e1.record(stream)
+        e1.synchronize()
+        if i >= 2:
+            e2e_ms += e0.elapsed_time(e1)
+    e2e_ms, e2e_rate = job_throughput(e2e_ms / e2e_steps, fl, device=dev)
+    clocks = sampler.stop() if rank == 0 else None
+    if ws > 1:
+        torch.distributed.barrier()
+    if rank != 0:
+        return
+    cpu = oracle_sample_packed(w, x, args.cpu_budget) if not args.no_cpu_baseline else None
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) inputs, bf16), valid rows packed",
+        "config": {"workload": w.name, "B": B, "H": H, "T": T, "max_seqlen": maxlen, "d": d, "causal": w.causal,
+                   "lengths": f"U[{w.len_lo},{w.len_hi}] (the bert draw)",
+                   "l2": "flushed before every step (256 MiB write, untimed)",
+                   "flops": "nominal fwd+bwd 12*P*d per head, P = len^2 per sequence (non-causal)",
+                   "parallelism": f"replicas x{ws} (heads independent)"},
+        "roofline": roof,
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_rate / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_ms, "steps": e2e_steps},
+        "gpu_launches": 4 * args.steps,
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -574,6 +725,8 @@ def main():
         run_reference(args, w)
     elif w.infer:
         run_gpu_infer(args, w)
+    elif w.packed:
+        run_gpu_packed(args, w)
     else:
         run_gpu(args, w)
 

@@ -42,6 +42,7 @@ class Workload:
     len_hi: Optional[int] = None
     Nk: Optional[int] = None      # key rows when they differ from the N query rows
     infer: bool = False           # forward only, split keys (inference): no backward, no LSE
+    packed: bool = False          # the padded draw's valid rows packed per head: [H, T, d], cu_seqlens
 
     @property
     def scale(self) -> float:
@@ -62,6 +63,8 @@ class Workload:
             s += f", N_k={self.Nk} (causal queries aligned with the last keys)"
         if self.infer:
             s += ", forward only (inference, split keys)"
+        if self.packed:
+            s += ", sequences packed to their lengths ([H, T, d], cu_seqlens)"
         if self.padded:
             s += f", key padding len~U[{self.len_lo},{self.len_hi}]"
         if self.qk_scale != 1.0:
@@ -84,6 +87,8 @@ WORKLOADS: Dict[str, Workload] = {
         Workload("prefill1024_kv4096", 8, 12, 1024, 64, True, Nk=4096),
         # inference: one new query per sequence over 8192 keys (forward only, split keys)
         Workload("decode_kv8192", 8, 12, 1, 64, True, Nk=8192, infer=True),
+        # the bert draw with each sequence's valid rows packed (no padding rows computed)
+        Workload("bert_packed", 16, 16, 512, 64, False, len_lo=128, len_hi=512, packed=True),
     ]
 }
 
@@ -120,6 +125,19 @@ def draw(B: int, H: int, N: int, d: int, *, seed: int = 0, qk_scale: float = 1.0
 def make_inputs(w: Workload, seed: int = 0) -> Dict[str, Optional[torch.Tensor]]:
     rng = (w.len_lo, w.len_hi) if w.padded else None
     return draw(w.B, w.H, w.N, w.d, seed=seed, qk_scale=w.qk_scale, len_range=rng, Nk=w.Nk)
+
+
+def pack(x: Dict[str, Optional[torch.Tensor]]) -> Dict[str, torch.Tensor]:
+    """The valid rows of a key-padded draw, packed per head: q, k, v, dO [H, T, d] (sequence b's
+    first kv_len[b] rows, back to back) and cu_seqlens int32 [B + 1]."""
+    kv = x["kv_len"].to(torch.int64)
+    cu = torch.zeros(kv.numel() + 1, dtype=torch.int64)
+    cu[1:] = torch.cumsum(kv, 0)
+    out = {"cu_seqlens": cu.to(torch.int32)}
+    for n in ("q", "k", "v", "do"):
+        t = x[n]  # [B, H, N, d]
+        out[n] = torch.cat([t[b, :, :int(kv[b])] for b in range(t.shape[0])], dim=1).contiguous()
+    return out
 
 
 def visible_pairs(nq: int, nk: int, causal: bool, kv: Optional[int] = None) -> float:
