@@ -16,13 +16,15 @@
  * "FlashAttention Algorithm > Recomputation Strategy" (section "What Gets
  * Stored vs Recomputed"), folded here into one value LSE = m + ln l.
  *
- * Conventions shared by every entry point:
+ * Conventions shared by every entry point (the _qk, _varlen and _split entry
+ * points below state how their shapes differ):
  *  - Tensors Q, K, V, O, dO, dQ, dK, dV are contiguous [B, H, N, d] bf16 in
  *    device memory, d innermost; every base pointer 16-byte aligned.
  *    LSE is contiguous [B, H, N] fp32 (natural log). kv_len, when given, is
  *    a device int32 [B]: key j of batch b is valid iff j < kv_len[b].
  *  - d must be 64 or 128. N >= 0 (any value; N = 0 is a no-op). B, H >= 1.
- *    causal = 1 keeps key j for query i iff j <= i.
+ *    causal = 1 keeps key j for query i iff j <= i (with N_q query and N_k key
+ *    rows, fa_forward_qk: iff j <= i + N_k - N_q).
  *  - All memory is owned by the caller. The library allocates nothing and
  *    frees nothing; outputs are fully overwritten.
  *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
@@ -30,7 +32,9 @@
  *    after a failed launch.
  *  - Inside the kernels every wait is bounded; a wait that runs out records
  *    FA_ERR_TIMEOUT in a per-device status word that
- *    fa_get_last_device_status() reads.
+ *    fa_get_last_device_status() reads. An argument that only the kernels can
+ *    check (a packed sequence longer than max_seqlen) records
+ *    FA_ERR_DEVICE_CHECK there.
  *  - Entry points are reentrant; calls that share output buffers race.
  */
 #ifndef IO_AWARE_EXACT_FA_H
