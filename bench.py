@@ -194,6 +194,46 @@ def traffic_record(kernel: str, workload: str):
         return None
 
 
+def io_accounting(w, kv_len=None, measured=None):
+    """HBM bytes of one fwd+bwd step under the pages' access model, per workload.
+
+    compulsory: what any exact method must move (bf16 tensors, fp32 LSE): the forward
+    reads Q, K, V and writes O, LSE; the backward reads Q, K, V, O, dO, LSE, writes dQ,
+    dK, dV, and here also writes and reads -D, -LSE2 (fp32) and the fp32 dQ accumulator.
+    standard: the same plus the N x N matrices of standard attention in bf16, written
+    and read back (S written, S read, P written, P read in the forward; P read in the
+    backward: five passes of 2 bytes per entry, the IO analysis' N^2 term).
+    tiled_term: N^2 d^2 / M elements (bf16) per head for M = 116736 on-chip elements
+    (228 KB of shared memory in bf16): the order of the tiled method's HBM accesses.
+    measured: DRAM bytes of the two main kernels from the committed ncu records, if any;
+    step_bytes adds the modelled bytes of the two streaming backward kernels to them.
+    """
+    heads = w.B * w.H
+    N, Nk, d = w.N, w.nk, w.d
+    npad = (N + 127) // 128 * 128
+    fwd = heads * (2 * N * d + 2 * 2 * Nk * d + 2 * N * d + 4 * N)
+    bwd = heads * (2 * N * d + 2 * 2 * Nk * d + 2 * 2 * N * d + 4 * N + 2 * N * d + 2 * 2 * Nk * d
+                   + 2 * 8 * npad + 2 * 4 * npad * d)
+    if kv_len is not None:  # key padding: only valid keys' columns exist in the N x N matrix
+        cols = float(sum(int(x) for x in kv_len)) * w.H * N
+    else:
+        cols = float(heads) * N * Nk
+    standard = fwd + bwd + 5 * 2 * cols
+    tiled_term = heads * 2.0 * N * N * d * d / 116736
+    # the two streaming kernels of the backward move what they must: pre reads O, dO, LSE and
+    # writes -D, -LSE2 and the zeroed accumulator; the rounding reads the accumulator, writes dQ
+    small = heads * (2 * 2 * N * d + 4 * N + 8 * npad + 4 * npad * d) + heads * (4 * npad * d + 2 * N * d)
+    out = {"compulsory_bytes": fwd + bwd, "standard_attention_bytes": standard,
+           "tiled_order_term_bytes": tiled_term,
+           "model": "bf16 tensors, fp32 LSE / D / dQ accumulator; standard adds 5 passes over N x N bf16"}
+    if measured:
+        out["measured_main_kernels_bytes"] = measured
+        out["pre_and_rounding_bytes_model"] = small
+        out["step_bytes"] = measured + small
+        out["standard_over_step"] = standard / (measured + small)
+    return out
+
+
 def source_hash(files):
     h = hashlib.sha256()
     for fn in files:
@@ -421,6 +461,9 @@ def run_gpu(args, w):
         "peak_act_mem_bytes": act_bytes,
         "act_bytes_per_head_row": act_bytes / (B * H * N),
         "std_attention_matrix_bytes_bf16": B * 2 * N * N * H * 2,
+        "io": io_accounting(w, x["kv_len"], measured=(
+            (traffic_record("fwd_kernel", w.name) or 0) + (traffic_record("bwd_kernel", w.name) or 0)
+            if traffic_record("fwd_kernel", w.name) and traffic_record("bwd_kernel", w.name) else None)),
         "std_attention_memmodel_gb_per_layer_B1": std["standard_gb"],
         "roofline": roof,
         "cpu_baseline": cpu,
