@@ -66,3 +66,17 @@ def test_unequal_length_workload_shapes():
     assert w.nk == 4096 and w.N == 1024
     f = workloads.flop_counts(w)
     assert f["fwd"] == 4 * 64 * 8 * 12 * (1024 * 4096 - 1024 * 1024 / 2)
+
+
+def test_pack_keeps_each_sequence_valid_rows_in_order():
+    w = workloads.WORKLOADS["bert"]
+    x = workloads.draw(4, 3, 40, 8, seed=5, len_range=(3, 40))
+    pk = workloads.pack(x)
+    kv = x["kv_len"].tolist()
+    cu = pk["cu_seqlens"].tolist()
+    assert cu[0] == 0 and cu[-1] == sum(kv) and all(b - a == n for a, b, n in zip(cu, cu[1:], kv))
+    for name in ("q", "k", "v", "do"):
+        assert pk[name].shape == (3, sum(kv), 8) and pk[name].is_contiguous()
+        for b in range(4):
+            assert torch.equal(pk[name][:, cu[b]:cu[b + 1]], x[name][b, :, :kv[b]])
+    assert pk["cu_seqlens"].dtype == torch.int32 and w.packed is False
