@@ -32,7 +32,8 @@
  *    after a failed launch.
  *  - Inside the kernels every wait is bounded; a wait that runs out records
  *    FA_ERR_TIMEOUT in a per-device status word that
- *    fa_get_last_device_status() reads. An argument that only the kernels can
+ *    fa_get_last_device_status() reads (fa_get_last_device_status_detail()
+ *    also says where). An argument that only the kernels can
  *    check (a packed sequence longer than max_seqlen) records
  *    FA_ERR_DEVICE_CHECK there.
  *  - Entry points are reentrant; calls that share output buffers race.
@@ -209,13 +210,15 @@ FA_API int fa_backward_stage_qk(int stage, const void* q, const void* k, const v
  * uses one fixed scratch array compiled into the library, of
  * fa_backward_noalloc_max_bytes() bytes (32 MiB) on every GPU that loads the
  * library, held until the process exits.
- *  - Same arguments and results as fa_backward_ex without the workspace.
- *  - A shape whose workspace (fa_backward_workspace_size) exceeds the array
- *    returns FA_ERR_UNSUPPORTED before anything runs; fa_last_error_detail()
- *    then says how many bytes it needed.
- *  - Allocates nothing. The first call on each device looks up the array's
- *    device address (cudaGetSymbolAddress) with that device current; make that
- *    first call before any stream capture.
+ *  - Same arguments and results as fa_backward_ex without the workspace; the
+ *    same argument checks come first, in the same order.
+ *  - A valid shape whose workspace (fa_backward_workspace_size) exceeds the
+ *    array returns FA_ERR_UNSUPPORTED before anything runs;
+ *    fa_last_error_detail() then says how many bytes it needed.
+ *  - Allocates nothing. The first call on each device (and context) looks up
+ *    the array's device address (cudaGetSymbolAddress) with that device
+ *    current; make that first call before any stream capture. A device
+ *    ordinal of 64 or more returns FA_ERR_UNSUPPORTED.
  *  - All calls on a device share the one array: calls whose kernels overlap on
  *    the GPU (other streams, other host threads) race and corrupt each other's
  *    gradients. Serialise them. Each call re-initialises what it needs. */
@@ -230,9 +233,18 @@ FA_API size_t fa_backward_noalloc_max_bytes(void);
 FA_API const char* fa_status_string(int status);
 
 /* Synchronises `stream`, then returns and clears the current device's status
- * word (FA_OK if no kernel recorded an error). If detail is non-NULL it
- * receives 4 ints: code, wait site, blockIdx.x, blockIdx.y of the first error. */
-FA_API int fa_get_last_device_status(fa_stream_t stream, int* detail);
+ * word: FA_OK if no kernel recorded an error, else the first error a kernel
+ * recorded (FA_ERR_TIMEOUT or FA_ERR_DEVICE_CHECK). A failure of the CUDA
+ * calls this makes returns FA_ERR_CUDA (fa_last_error_detail names it); a
+ * device ordinal of 64 or more returns FA_ERR_UNSUPPORTED. The word's device
+ * address is looked up once per device and context; after cudaDeviceReset the
+ * next call looks it up again. */
+FA_API int fa_get_last_device_status(fa_stream_t stream);
+
+/* As fa_get_last_device_status; if detail is non-NULL it also receives 4 ints
+ * describing the first recorded error: code, site (which wait or check),
+ * blockIdx.x, blockIdx.y (all 0 when none was recorded). */
+FA_API int fa_get_last_device_status_detail(fa_stream_t stream, int* detail);
 
 /* For the calling host thread: text naming the CUDA call that made the last
  * FA_ERR_CUDA return and its error (or the reason for a size rejection by

@@ -42,7 +42,8 @@ SIGNATURES = {
         "fa_backward_noalloc": (_i, [_vp] * 9 + [_i, _i, _i, _i, _f, _i, _vp, _vp]),
         "fa_backward_noalloc_max_bytes": (_sz, []),
         "fa_status_string": (ctypes.c_char_p, [_i]),
-        "fa_get_last_device_status": (_i, [_vp, _vp]),
+        "fa_get_last_device_status": (_i, [_vp]),
+        "fa_get_last_device_status_detail": (_i, [_vp, _vp]),
         "fa_version": (_i, []),
         "fa_last_error_detail": (ctypes.c_char_p, []),
     },

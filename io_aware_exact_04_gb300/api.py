@@ -197,7 +197,7 @@ def device_status(device=None):
     dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
     detail = (ctypes.c_int * 4)()
     with torch.cuda.device(dev):
-        rc = _lib_fa().fa_get_last_device_status(_stream(dev), detail)
+        rc = _lib_fa().fa_get_last_device_status_detail(_stream(dev), detail)
     return rc, list(detail)
 
 

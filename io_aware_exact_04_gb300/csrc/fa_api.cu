@@ -1,5 +1,6 @@
 // C-ABI entry points: argument validation, workspace carving, tensor-map
 // construction (in the launchers) and the per-device status word.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -16,47 +17,33 @@ namespace {
 // Per-device word the kernels write when a bounded wait runs out or an
 // in-kernel check fails: code, wait site, blockIdx.x, blockIdx.y.
 __device__ int g_status[4];
-
-constexpr int kMaxDevices = 64;
-int* g_status_ptr[kMaxDevices] = {};
-std::mutex g_status_mu;
+fa::SymbolCache g_status_cache;
 
 int* device_status(int* err) {
-  int dev = 0;
-  const cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
-    *err = fa::cuda_fail("cudaGetDevice", (int)e, cudaGetErrorName(e));
-    return nullptr;
-  }
-  std::lock_guard<std::mutex> lk(g_status_mu);
-  if (!g_status_ptr[dev]) {
-    void* p = nullptr;
-    const cudaError_t e2 = cudaGetSymbolAddress(&p, g_status);
-    if (e2 != cudaSuccess) {
-      *err = fa::cuda_fail("cudaGetSymbolAddress", (int)e2, cudaGetErrorName(e2));
-      return nullptr;
-    }
-    g_status_ptr[dev] = static_cast<int*>(p);
-  }
-  return g_status_ptr[dev];
+  return static_cast<int*>(fa::symbol_on_current_device(g_status, g_status_cache, "status word", err));
 }
+
+// The current CUDA context (driver handle), through the driver entry point the runtime hands
+// out, so that the library needs no link-time dependency on libcuda.
+bool current_context(void** out) {
+  using Fn = CUresult (*)(CUcontext*);
+  static Fn fn = []() {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return (Fn) nullptr;
+    return reinterpret_cast<Fn>(p);
+  }();
+  CUcontext c = nullptr;
+  if (!fn || fn(&c) != CUDA_SUCCESS) return false;
+  *out = c;
+  return true;
+}
+
+std::mutex g_symbol_mu;
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
-int check_common(int B, int H, int Nq, int Nk, int d, float scale, int causal) {
-  if (B < 0 || H < 0 || Nq < 0 || Nk < 0) return FA_ERR_INVALID_ARG;
-  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
-  if (!(scale > 0.f) || !std::isfinite(scale)) return FA_ERR_INVALID_ARG;
-  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
-  const long long BH = (long long)B * H;
-  if (BH > 65535) return FA_ERR_UNSUPPORTED;  // documented limit on B*H
-  for (const int n : {Nq, Nk}) {
-    if ((long long)n + 255 > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
-    if ((n + 127) / 128 > 65535) return FA_ERR_UNSUPPORTED;  // key tiles / query pairs on the grid's y axis
-  }
-  if (BH > 0 && (Nq == 0) != (Nk == 0)) return FA_ERR_UNSUPPORTED;  // queries without keys or keys without queries
-  return FA_OK;
-}
 
 long long round_up(long long x, long long m) { return (x + m - 1) / m * m; }
 
@@ -80,6 +67,59 @@ thread_local char g_last_error[256] = "";
 }  // namespace
 
 namespace fa {
+int check_common(int B, int H, int Nq, int Nk, int d, float scale, int causal) {
+  if (B < 0 || H < 0 || Nq < 0 || Nk < 0) return FA_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  const long long BH = (long long)B * H;
+  if (BH > 65535) return FA_ERR_UNSUPPORTED;  // documented limit on B*H
+  for (const int n : {Nq, Nk}) {
+    if ((long long)n + 255 > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+    if ((n + 127) / 128 > 65535) return FA_ERR_UNSUPPORTED;  // key tiles / query pairs on the grid's y axis
+  }
+  if (BH > 0 && (Nq == 0) != (Nk == 0)) return FA_ERR_UNSUPPORTED;  // queries without keys or keys without queries
+  return FA_OK;
+}
+
+void* symbol_on_current_device(const void* symbol, SymbolCache& cache, const char* what, int* rc) {
+  int dev = 0;
+  const cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) {
+    *rc = cuda_fail("cudaGetDevice", (int)e, cudaGetErrorName(e));
+    return nullptr;
+  }
+  if (dev < 0 || dev >= SymbolCache::kMaxDevices) {
+    char msg[160];
+    std::snprintf(msg, sizeof(msg), "device ordinal %d: this library serves devices 0 .. %d", dev,
+                  SymbolCache::kMaxDevices - 1);
+    set_error_detail(msg);
+    *rc = FA_ERR_UNSUPPORTED;
+    return nullptr;
+  }
+  // the address belongs to the module loaded in the current context: a new context on the same
+  // device (after cudaDeviceReset, say) gets its own lookup
+  void* ctx = nullptr;
+  if (!current_context(&ctx)) {
+    *rc = cuda_fail("cuCtxGetCurrent", 0, "no current context");
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lk(g_symbol_mu);
+  if (cache.ptr[dev] == nullptr || cache.ctx[dev] != ctx) {
+    void* p = nullptr;
+    const cudaError_t e2 = cudaGetSymbolAddress(&p, symbol);
+    if (e2 != cudaSuccess || p == nullptr) {
+      char where[96];
+      std::snprintf(where, sizeof(where), "cudaGetSymbolAddress(%s)", what);
+      *rc = cuda_fail(where, (int)e2, cudaGetErrorName(e2));
+      return nullptr;
+    }
+    cache.ptr[dev] = p;
+    cache.ctx[dev] = ctx;
+  }
+  return cache.ptr[dev];
+}
+
 int cuda_fail(const char* where, int code, const char* what) {
   std::snprintf(g_last_error, sizeof(g_last_error), "%s failed: %s (code %d)", where, what ? what : "", code);
   return FA_ERR_CUDA;
@@ -133,7 +173,7 @@ const char* fa_status_string(int s) {
 
 int fa_forward_qk(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq, int Nk,
                   int d, float scale, int causal, const int32_t* kv_len, fa_stream_t stream) {
-  int rc = check_common(B, H, Nq, Nk, d, scale, causal);
+  int rc = fa::check_common(B, H, Nq, Nk, d, scale, causal);
   if (rc != FA_OK) return rc;
   if ((long long)B * H * Nq == 0) return FA_OK;
   if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
@@ -166,7 +206,7 @@ int fa_forward_qk(const void* q, const void* k, const void* v, void* o, float* l
 int fa_forward_varlen(const void* q, const void* k, const void* v, void* o, float* lse, const int32_t* cu_seqlens,
                       int B, int H, int T, int max_seqlen, int d, float scale, int causal, fa_stream_t stream) {
   if (B < 0 || T < 0 || max_seqlen < 0) return FA_ERR_INVALID_ARG;
-  int rc = check_common(B, H, max_seqlen, max_seqlen, d, scale, causal);
+  int rc = fa::check_common(B, H, max_seqlen, max_seqlen, d, scale, causal);
   if (rc != FA_OK) return rc;
   if ((long long)B * H == 0 || T == 0 || max_seqlen == 0) return FA_OK;
   if (!q || !k || !v || !o || !lse || !cu_seqlens) return FA_ERR_INVALID_ARG;
@@ -219,7 +259,7 @@ int fa_forward_split_count(int B, int H, int Nq, int Nk, int d) {
 int fa_forward_split(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq, int Nk,
                      int d, float scale, int causal, const int32_t* kv_len, int n_split, void* workspace,
                      size_t workspace_bytes, fa_stream_t stream) {
-  int rc = check_common(B, H, Nq, Nk, d, scale, causal);
+  int rc = fa::check_common(B, H, Nq, Nk, d, scale, causal);
   if (rc != FA_OK) return rc;
   if (n_split < 1) return FA_ERR_INVALID_ARG;
   if (n_split > 1024) return FA_ERR_UNSUPPORTED;
@@ -276,7 +316,7 @@ int fa_backward_stage_qk(int stage, const void* q, const void* k, const void* v,
                          float scale, int causal, const int32_t* kv_len, void* workspace, size_t workspace_bytes,
                          fa_stream_t stream) {
   if (stage < 0 || stage > 2) return FA_ERR_INVALID_ARG;
-  int rc = check_common(B, H, Nq, Nk, d, scale, causal);
+  int rc = fa::check_common(B, H, Nq, Nk, d, scale, causal);
   if (rc != FA_OK) return rc;
   if ((long long)B * H * Nq == 0) return FA_OK;
   const int N = Nq;
@@ -358,7 +398,7 @@ int fa_backward_varlen(const void* q, const void* k, const void* v, const void* 
                        void* dq, void* dk, void* dv, const int32_t* cu_seqlens, int B, int H, int T, int max_seqlen,
                        int d, float scale, int causal, void* workspace, size_t workspace_bytes, fa_stream_t stream) {
   if (B < 0 || T < 0 || max_seqlen < 0) return FA_ERR_INVALID_ARG;
-  int rc = check_common(B, H, max_seqlen, max_seqlen, d, scale, causal);
+  int rc = fa::check_common(B, H, max_seqlen, max_seqlen, d, scale, causal);
   if (rc != FA_OK) return rc;
   if ((long long)B * H == 0 || T == 0 || max_seqlen == 0) return FA_OK;
   if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv || !cu_seqlens || !workspace) return FA_ERR_INVALID_ARG;
@@ -402,20 +442,25 @@ int fa_backward_varlen(const void* q, const void* k, const void* v, const void* 
   return FA_OK;
 }
 
-int fa_get_last_device_status(fa_stream_t stream, int* detail) {
+int fa_get_last_device_status_detail(fa_stream_t stream, int* detail) {
   int err = FA_OK;
   int* status = device_status(&err);
   if (!status) return err;
-  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return FA_ERR_CUDA;
+  cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fa::cuda_fail("cudaStreamSynchronize", (int)e, cudaGetErrorName(e));
   int h[4] = {0, 0, 0, 0};
-  if (cudaMemcpy(h, status, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return FA_ERR_CUDA;
+  e = cudaMemcpy(h, status, sizeof(h), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return fa::cuda_fail("cudaMemcpy(status word)", (int)e, cudaGetErrorName(e));
   if (h[0] != 0) {
     const int zero[4] = {0, 0, 0, 0};
-    if (cudaMemcpy(status, zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return FA_ERR_CUDA;
+    e = cudaMemcpy(status, zero, sizeof(zero), cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return fa::cuda_fail("cudaMemcpy(status word)", (int)e, cudaGetErrorName(e));
   }
   if (detail)
     for (int i = 0; i < 4; ++i) detail[i] = h[i];
   return h[0];
 }
+
+int fa_get_last_device_status(fa_stream_t stream) { return fa_get_last_device_status_detail(stream, nullptr); }
 
 }  // extern "C"

@@ -55,6 +55,23 @@ __host__ __device__ inline int vl_T(const BwdArgs& a) { return a.Nk; }
 __host__ __device__ inline int vl_Lpad(const BwdArgs& a) { return a.coff; }
 
 
+// Argument checks shared by every entry point: sizes non-negative, causal 0 or 1, scale finite
+// and positive (FA_ERR_INVALID_ARG); d in {64, 128}, B * H <= 65535, lengths within 32-bit
+// indexing and the grid's y axis, and no queries without keys or the reverse
+// (FA_ERR_UNSUPPORTED). FA_OK otherwise.
+int check_common(int B, int H, int Nq, int Nk, int d, float scale, int causal);
+
+// Device address of a file-scope __device__ variable (`symbol`, its host-side stand-in) on the
+// current device, looked up with cudaGetSymbolAddress on the first call for each (device,
+// context) pair and cached in `cache`. Returns null with *rc set (FA_ERR_UNSUPPORTED for a
+// device ordinal of 64 or more, FA_ERR_CUDA for a failed CUDA call, detail recorded).
+struct SymbolCache {
+  static constexpr int kMaxDevices = 64;
+  void* ctx[kMaxDevices] = {};
+  void* ptr[kMaxDevices] = {};
+};
+void* symbol_on_current_device(const void* symbol, SymbolCache& cache, const char* what, int* rc);
+
 // Records, for this host thread, which CUDA call failed and why (read back by
 // fa_last_error_detail). Returns FA_ERR_CUDA for convenience.
 int cuda_fail(const char* where, int code, const char* what);

@@ -10,12 +10,11 @@
 // The array is a file-scope __device__ variable, so every GPU that loads the
 // library holds kScratchBytes of it until the process exits. In host code the
 // name g_scratch is only a host-side stand-in, not a device address; the
-// device address is obtained once per device with cudaGetSymbolAddress and
-// passed to the kernels as their workspace pointer.
+// device address is obtained once per device (and context) with
+// cudaGetSymbolAddress and passed to the kernels as their workspace pointer.
 #include <cuda_runtime.h>
 
 #include <cstdio>
-#include <mutex>
 
 #include "fa.h"
 #include "fa_internal.h"
@@ -24,32 +23,7 @@ namespace {
 
 constexpr size_t kScratchBytes = size_t(32) << 20;  // 32 MiB
 __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
-
-constexpr int kMaxDevices = 64;
-void* g_scratch_dev[kMaxDevices] = {};
-std::mutex g_scratch_mu;
-
-// Device address of the scratch array on the current device, looked up on the
-// first call for that device.
-void* scratch_on_current_device(int* rc) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
-    *rc = fa::cuda_fail("cudaGetDevice", (int)e, cudaGetErrorName(e));
-    return nullptr;
-  }
-  std::lock_guard<std::mutex> lk(g_scratch_mu);
-  if (!g_scratch_dev[dev]) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_scratch);
-    if (e != cudaSuccess || p == nullptr) {
-      *rc = fa::cuda_fail("cudaGetSymbolAddress(scratch)", (int)e, cudaGetErrorName(e));
-      return nullptr;
-    }
-    g_scratch_dev[dev] = p;
-  }
-  return g_scratch_dev[dev];
-}
+fa::SymbolCache g_scratch_cache;
 
 }  // namespace
 
@@ -60,11 +34,12 @@ size_t fa_backward_noalloc_max_bytes(void) { return kScratchBytes; }
 int fa_backward_noalloc(const void* q, const void* k, const void* v, const void* o, const void* dO,
                         const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale,
                         int causal, const int32_t* kv_len, fa_stream_t stream) {
-  if (B < 0 || H < 0 || N < 0) return FA_ERR_INVALID_ARG;
+  // the checks of fa_backward_ex, in its order, before the size of this entry point's array
+  const int rc0 = fa::check_common(B, H, N, N, d, scale, causal);
+  if (rc0 != FA_OK) return rc0;
   if ((long long)B * H * N == 0)  // nothing to compute; same result as fa_backward_ex
     return fa_backward_ex(q, k, v, o, dO, lse, dq, dk, dv, B, H, N, d, scale, causal, kv_len, nullptr, 0, stream);
   const size_t need = fa_backward_workspace_size(B, H, N, d);
-  if (need == 0) return FA_ERR_UNSUPPORTED;  // head dimension not supported
   if (need > kScratchBytes) {
     char msg[160];
     std::snprintf(msg, sizeof(msg), "fa_backward_noalloc: this shape needs %zu bytes of scratch, the fixed array has %zu",
@@ -73,7 +48,7 @@ int fa_backward_noalloc(const void* q, const void* k, const void* v, const void*
     return FA_ERR_UNSUPPORTED;
   }
   int rc = FA_OK;
-  void* scratch = scratch_on_current_device(&rc);
+  void* scratch = fa::symbol_on_current_device(g_scratch, g_scratch_cache, "scratch", &rc);
   if (!scratch) return rc;
   // The first stage overwrites D and LSE and zeroes the dQ accumulator, so
   // whatever an earlier call left in the array does not matter.
