@@ -139,34 +139,46 @@ def job_throughput(ms_local: float, units_local: float, device=None):
 
 
 # ------------------------------------------------------------------ oracle on host cores
-def oracle_sample(w, x, budget_s: float, max_heads=None):
-    """Time the fp64 oracle on as many heads of the workload as fit in budget_s."""
-    import numpy as np
+ORACLE_ROWS = 2048  # query rows per oracle unit on long rows
 
+
+def oracle_units(w):
+    """Units of oracle work over a workload, in order: whole heads up to 4096 rows; beyond
+    that the last ORACLE_ROWS query rows of each head (with all keys), the heaviest rows of a
+    causal head, computed by the oracle as a problem of ORACLE_ROWS queries over N_k keys
+    aligned with the last keys (exactly those rows' share of the head's work)."""
+    r = w.N if w.N <= 4096 else ORACLE_ROWS
+    return [(b, h, w.N - r) for b in range(w.B) for h in range(w.H)]
+
+
+def oracle_sample(w, x, budget_s: float, max_heads=None):
+    """Time the fp64 oracle on as many units of the workload as fit in budget_s."""
     from oracle import ref
 
-    B, H = w.B, w.H
     f64 = lambda t: t.to(dtype=__import__("torch").float64).numpy()  # noqa: E731
     kv = None if x["kv_len"] is None else x["kv_len"].numpy()
-    heads = [(b, h) for b in range(B) for h in range(H)]
+    units = oracle_units(w)
     done, flops = 0, 0.0
     t0 = time.perf_counter()
-    for b, h in heads:
-        q, k, v, do = (f64(x[n][b, h]) for n in ("q", "k", "v", "do"))
+    for b, h, r0 in units:
+        q, do = (f64(x[n][b, h, r0:]) for n in ("q", "do"))
+        k, v = (f64(x[n][b, h]) for n in ("k", "v"))
         kl = None if kv is None else int(kv[b])
+        nq = w.N - r0
         if w.infer:  # forward only
             ref.head_forward(q, k, v, w.scale, w.causal, kl)
-            flops += 4 * w.d * workloads.visible_pairs(w.N, w.nk, w.causal, kl)
+            flops += 4 * w.d * workloads.visible_pairs(nq, w.nk, w.causal, kl)
         else:
-            ref.head_backward(q, k, v, do, w.scale, w.causal, kl, row_block=2048 if w.N > 4096 else None)
-            flops += 12 * w.d * workloads.visible_pairs(w.N, w.nk, w.causal, kl)
+            ref.head_backward(q, k, v, do, w.scale, w.causal, kl)
+            flops += 12 * w.d * workloads.visible_pairs(nq, w.nk, w.causal, kl)
         done += 1
         if time.perf_counter() - t0 > budget_s or (max_heads and done >= max_heads):
             break
     dt = time.perf_counter() - t0
     cores = len(os.sched_getaffinity(0))
+    what = "heads" if units and units[0][2] == 0 else f"(head, last {w.N - units[0][2]} query rows) units"
     return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-            "sample": f"{done} of {B * H} heads of {w.name} (fp64 numpy, {'fwd' if w.infer else 'fwd+bwd'}, "
+            "sample": f"{done} of {len(units)} {what} of {w.name} (fp64 numpy, {'fwd' if w.infer else 'fwd+bwd'}, "
                       f"S and P materialised), "
                       f"{dt:.1f} s", "seconds": dt, "heads": done}
 
@@ -260,7 +272,9 @@ def run_reference(args, w):
         heads += r["heads"]
     value = statistics.median(vals)
     cores = len(os.sched_getaffinity(0))
-    sample = f"each step: the fp64 oracle on as many heads of {w.name} as fit in {budget:.1f} s ({heads} heads over {args.steps} steps)"
+    unit = "heads" if w.packed or oracle_units(w)[0][2] == 0 else f"(head, last {ORACLE_ROWS} query rows) units"
+    sample = (f"each step: the fp64 oracle on as many {unit} of {w.name} as fit in {budget:.1f} s "
+              f"({heads} over {args.steps} steps)")
     line = {
         "impl": "reference", "metric": INFER_METRIC if w.infer else METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / max(1, args.steps),
@@ -273,9 +287,177 @@ def run_reference(args, w):
     print(json.dumps(line), flush=True)
 
 
-def run_gpu(args, w):
-    import ctypes
+class TrainingSetup:
+    """One workload's tensors on the device and its fwd+bwd step through the C ABI."""
 
+    KERNELS = ["fwd_kernel", "bwd_pre_kernel", "bwd_kernel", "dq_convert_kernel"]
+
+    def __init__(self, w, dev, lib, flush):
+        import ctypes
+
+        import torch
+
+        from io_aware_exact_04_gb300 import _lib
+        self.w, self.dev, self.lib, self.flush = w, dev, lib, flush
+        self.x = x = workloads.make_inputs(w, seed=0)
+        B, H, N, Nk, d = w.B, w.H, w.N, w.nk, w.d
+        self.q, self.k, self.v, self.do = (x[n].to(dev) for n in ("q", "k", "v", "do"))
+        self.kv = None if x["kv_len"] is None else x["kv_len"].to(dev)
+        self.o = torch.empty_like(self.q)
+        self.lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+        self.dq, self.dk, self.dv = torch.empty_like(self.q), torch.empty_like(self.k), torch.empty_like(self.k)
+        self.wsb = int(lib.fa_backward_workspace_size(B, H, N, d))
+        self.work = torch.empty(self.wsb, dtype=torch.uint8, device=dev)
+        self.stream = torch.cuda.current_stream(dev)
+        self.sp = ctypes.c_void_p(self.stream.cuda_stream)
+        self._check = _lib.check
+        self.fl = workloads.flop_counts(w, x["kv_len"])
+
+    @staticmethod
+    def _p(t):
+        import ctypes
+        return ctypes.c_void_p(t.data_ptr()) if t is not None else None
+
+    def fwd(self):
+        w, P = self.w, self._p
+        self._check(self.lib.fa_forward_qk(P(self.q), P(self.k), P(self.v), P(self.o), P(self.lse), w.B, w.H, w.N,
+                                           w.nk, w.d, w.scale, int(w.causal), P(self.kv), self.sp), "fwd")
+
+    def bwd_stage(self, s):
+        w, P = self.w, self._p
+        self._check(self.lib.fa_backward_stage_qk(s, P(self.q), P(self.k), P(self.v), P(self.o), P(self.do),
+                                                  P(self.lse), P(self.dq), P(self.dk), P(self.dv), w.B, w.H, w.N,
+                                                  w.nk, w.d, w.scale, int(w.causal), P(self.kv), P(self.work),
+                                                  self.wsb, self.sp), "bwd")
+
+    def step(self, ev=None):
+        if ev is None:
+            self.fwd()
+            for s in range(3):
+                self.bwd_stage(s)
+            return
+        ev[0].record(self.stream)
+        self.fwd()
+        ev[1].record(self.stream)
+        for s in range(3):
+            self.bwd_stage(s)
+            ev[2 + s].record(self.stream)
+
+    def status(self, when):
+        import ctypes
+        detail = (ctypes.c_int * 4)()
+        if self.lib.fa_get_last_device_status_detail(self.sp, detail) != 0:
+            raise RuntimeError(f"device status {when}: {list(detail)}")
+
+    def warmup(self, n):
+        import torch
+        for _ in range(max(3, n)):
+            self.flush.zero_()
+            self.step()
+        torch.cuda.synchronize(self.dev)
+        self.status("after warm-up")
+
+    def time_steps(self, steps):
+        """(step ms total, per-kernel ms totals, step ms with an event after every kernel).
+
+        Step time: events at step boundaries only. The four kernels of a step are launched with
+        programmatic dependent launch, and an event recorded between two of them would serialise
+        that overlap, so the per-kernel breakdown comes from a second timed pass of the same
+        steps with an event after every kernel."""
+        import torch
+        step_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+        events = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(steps)]
+        for i in range(steps):
+            self.flush.zero_()
+            step_ev[i][0].record(self.stream)
+            self.step()
+            step_ev[i][1].record(self.stream)
+        torch.cuda.synchronize(self.dev)
+        for i in range(steps):
+            self.flush.zero_()
+            self.step(events[i])
+        torch.cuda.synchronize(self.dev)
+        per_kernel = {k: 0.0 for k in self.KERNELS}
+        total_ms = sum(ev[0].elapsed_time(ev[1]) for ev in step_ev)
+        for ev in events:
+            t = [ev[0].elapsed_time(ev[j]) for j in range(1, 5)]
+            per_kernel["fwd_kernel"] += t[0]
+            per_kernel["bwd_pre_kernel"] += t[1] - t[0]
+            per_kernel["bwd_kernel"] += t[2] - t[1]
+            per_kernel["dq_convert_kernel"] += t[3] - t[2]
+        with_events = sum(ev[0].elapsed_time(ev[4]) for ev in events)
+        return total_ms, per_kernel, with_events
+
+    def activation_memory(self):
+        """Peak device memory that one fwd+bwd through the public API holds beyond its inputs
+        (Q, K, V, dO) and its gradient outputs (dQ, dK, dV), as torch's allocator measures it:
+        O and LSE from the forward call, the backward call's workspace."""
+        import torch
+
+        from io_aware_exact_04_gb300 import api
+        w = self.w
+        torch.cuda.synchronize(self.dev)
+        base = torch.cuda.memory_allocated(self.dev)
+        torch.cuda.reset_peak_memory_stats(self.dev)
+        o, lse = api.forward(self.q, self.k, self.v, causal=w.causal, kv_len=self.kv)
+        api.backward(self.q, self.k, self.v, o, self.do, lse, causal=w.causal, kv_len=self.kv,
+                     dq=self.dq, dk=self.dk, dv=self.dv)
+        torch.cuda.synchronize(self.dev)
+        peak = torch.cuda.max_memory_allocated(self.dev) - base
+        del o, lse
+        self.status("after the memory measurement")
+        return int(peak)
+
+
+# the long-context sweep of the GPT-2 memory-table configuration (12 heads, d 64, causal)
+LONG_SWEEP = ["long2048", "long8192", "long16384", "long32768"]
+
+
+def sweep_entry(w, setup, peaks, steps):
+    """TFLOP/s and measured activation memory of one workload of the sweep."""
+    setup.warmup(3)
+    total, per_kernel, _ = setup.time_steps(steps)
+    ms = total / steps
+    fl = setup.fl
+    nominal = fl["fwd_bwd_nominal"] / (ms * 1e-3) / 1e12
+    executed = fl["fwd_bwd_executed"] / (ms * 1e-3) / 1e12
+    mem = setup.activation_memory()
+    peak = float(peaks["bf16_tflops"])
+    bwd_ms = (per_kernel["bwd_pre_kernel"] + per_kernel["bwd_kernel"] + per_kernel["dq_convert_kernel"]) / steps
+    return {"N": w.N, "ms_per_step": ms, "tflops_nominal": nominal, "tflops_executed": executed,
+            "pct_of_peak": 100 * nominal / peak, "pct_of_peak_executed": 100 * executed / peak,
+            "fwd_tflops": fl["fwd"] / (per_kernel["fwd_kernel"] / steps * 1e-3) / 1e12,
+            "bwd_tflops_nominal": fl["bwd_nominal"] / (bwd_ms * 1e-3) / 1e12,
+            "bwd_kernel_frac": (fl["bwd_nominal"] + fl["bwd_recompute"])
+            / (per_kernel["bwd_kernel"] / steps * 1e-3) / 1e12 / peak,
+            "peak_act_mem_bytes": mem, "act_bytes_per_head_row": mem / (w.B * w.H * w.N),
+            "std_attention_matrix_bytes_bf16": w.B * w.H * w.N * w.nk * 2}
+
+
+def standard_records():
+    """Measured DRAM bytes and times of standard (materialising) attention and of this
+    library's step on the same workloads, from the committed ncu records."""
+    out = {}
+    for wl in ("gpt2", "long8192"):
+        rec = {}
+        for kind in ("standard_attention", "flash_step"):
+            path = os.path.join(ROOT, "profiles", f"{kind}_{wl}_dram.txt")
+            try:
+                with open(path) as f:
+                    kv = dict(line.split(":", 1) for line in f if ":" in line and not line.startswith("#"))
+                files = [x.strip() for x in kv.get("source_files", "").split(",") if x.strip()]
+                if files and source_hash(files) != kv.get("source_sha256", "").strip():
+                    continue  # this library's kernels changed since the record was taken
+                rec[kind + "_dram_bytes"] = float(kv["dram_bytes_per_step"])
+            except (OSError, KeyError, ValueError):
+                pass
+        if len(rec) == 2:
+            rec["standard_over_flash"] = rec["standard_attention_dram_bytes"] / rec["flash_step_dram_bytes"]
+            out[wl] = rec
+    return out
+
+
+def run_gpu(args, w):
     import torch
 
     from io_aware_exact_04_gb300 import _lib, memmodel
@@ -289,61 +471,15 @@ def run_gpu(args, w):
     lib = _lib.load("libfa.so")
     peaks, peak_src = load_peaks()
 
-    x = workloads.make_inputs(w, seed=0)
-    B, H, N, Nk, d = w.B, w.H, w.N, w.nk, w.d
-    q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "do"))
-    kv = None if x["kv_len"] is None else x["kv_len"].to(dev)
-    o = torch.empty_like(q)
-    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
-    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(k)
-    wsb = int(lib.fa_backward_workspace_size(B, H, N, d))
-    work = torch.empty(wsb, dtype=torch.uint8, device=dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
-    stream = torch.cuda.current_stream(dev)
-    sp = ctypes.c_void_p(stream.cuda_stream)
-    P = lambda t: ctypes.c_void_p(t.data_ptr()) if t is not None else None  # noqa: E731
-    causal = int(w.causal)
+    S = TrainingSetup(w, dev, lib, flush)
+    x = S.x
+    B, H, N, Nk, d = w.B, w.H, w.N, w.nk, w.d
+    S.warmup(args.warmup)
+    # peak activation memory, measured: what one fwd+bwd holds besides inputs and gradients
+    act_bytes = S.activation_memory()
+    S.warmup(3)
 
-    def fwd():
-        _lib.check(lib.fa_forward_qk(P(q), P(k), P(v), P(o), P(lse), B, H, N, Nk, d, w.scale, causal, P(kv), sp),
-                   "fwd")
-
-    def bwd_stage(s):
-        _lib.check(lib.fa_backward_stage_qk(s, P(q), P(k), P(v), P(o), P(do), P(lse), P(dq), P(dk), P(dv), B, H,
-                                            N, Nk, d, w.scale, causal, P(kv), P(work), wsb, sp), "bwd")
-
-    kernels = ["fwd_kernel", "bwd_pre_kernel", "bwd_kernel", "dq_convert_kernel"]
-
-    def step(ev=None):
-        if ev is None:
-            fwd()
-            for s in range(3):
-                bwd_stage(s)
-            return
-        ev[0].record(stream)
-        fwd()
-        ev[1].record(stream)
-        for s in range(3):
-            bwd_stage(s)
-            ev[2 + s].record(stream)
-
-    for _ in range(max(3, args.warmup)):
-        flush.zero_()
-        step()
-    torch.cuda.synchronize(dev)
-    code, detail = ctypes.c_int(0), (ctypes.c_int * 4)()
-    if lib.fa_get_last_device_status(sp, detail) != 0:
-        raise RuntimeError(f"device status after warm-up: {list(detail)}")
-
-    # peak activation memory: what fwd+bwd holds besides inputs and gradients
-    act_bytes = o.numel() * 2 + lse.numel() * 4 + wsb
-
-    # Step time: events at step boundaries only. The four kernels of a step are launched with
-    # programmatic dependent launch, and an event recorded between two of them would serialise
-    # that overlap, so the per-kernel breakdown (and the roofline's kernel duration) comes from a
-    # second timed pass of the same steps with an event after every kernel.
-    step_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
-    events = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
     sampler = ClockSampler(local if "CUDA_VISIBLE_DEVICES" not in os.environ else 0)
     if rank == 0:
         sampler.start()
@@ -352,30 +488,12 @@ def run_gpu(args, w):
         torch.distributed.barrier()
     torch.cuda.synchronize(dev)
     sampler.mark("t_start")
-    for i in range(args.steps):
-        flush.zero_()
-        step_ev[i][0].record(stream)
-        step()
-        step_ev[i][1].record(stream)
-    torch.cuda.synchronize(dev)
-    for i in range(args.steps):
-        flush.zero_()
-        step(events[i])
-    torch.cuda.synchronize(dev)
+    total_ms, per_kernel, with_events = S.time_steps(args.steps)
     sampler.mark("t_stop")
     if ws > 1:
         torch.distributed.barrier()
-    per_kernel = {kname: 0.0 for kname in kernels}
-    total_ms = sum(ev[0].elapsed_time(ev[1]) for ev in step_ev)
-    for ev in events:
-        t = [ev[0].elapsed_time(ev[j]) for j in range(1, 5)]
-        per_kernel["fwd_kernel"] += t[0]
-        per_kernel["bwd_pre_kernel"] += t[1] - t[0]
-        per_kernel["bwd_kernel"] += t[2] - t[1]
-        per_kernel["dq_convert_kernel"] += t[3] - t[2]
-    if lib.fa_get_last_device_status(sp, detail) != 0:
-        raise RuntimeError(f"device status after timing: {list(detail)}")
-    fl = workloads.flop_counts(w, x["kv_len"])
+    S.status("after timing")
+    fl = S.fl
     ms_step, nominal_rate = job_throughput(total_ms / args.steps, fl["fwd_bwd_nominal"], device=dev)
     value = nominal_rate / 1e12
     executed = value * fl["fwd_bwd_executed"] / fl["fwd_bwd_nominal"]
@@ -383,7 +501,6 @@ def run_gpu(args, w):
     # dominant kernel and its roofline (tensor-bound: algorithmic flops per launch / event time)
     avg = {kname: t / args.steps for kname, t in per_kernel.items()}
     dom = max(avg, key=avg.get)
-    c = 0.5 if w.causal else 1.0
     alg_flops = {"fwd_kernel": fl["fwd"], "bwd_kernel": fl["bwd_nominal"] + fl["bwd_recompute"]}
     if dom in alg_flops:
         achieved = alg_flops[dom] / (avg[dom] * 1e-3) / 1e12
@@ -391,7 +508,8 @@ def run_gpu(args, w):
         traffic = traffic_record(dom, w.name)
         roof = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak, "traffic": traffic,
-                "peak_source": f"{peak_src} bf16 dense (burst)", "avg_launch_ms": avg[dom]}
+                "peak_source": f"{peak_src} bf16 dense (burst)", "avg_launch_ms": avg[dom],
+                "flops_per_launch": alg_flops[dom]}
     else:  # a memory-bound helper dominating would be reported against HBM
         nbytes = {"bwd_pre_kernel": B * H * N * d * 2 * 2 + B * H * (N + 127) // 128 * 128 * (8 + 4 * d),
                   "dq_convert_kernel": B * H * N * d * (4 + 2)}[dom]
@@ -411,20 +529,21 @@ def run_gpu(args, w):
     e2e_steps = max(3, min(args.steps, 50))
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e2e_ms = 0.0
+    stream = S.stream
     for i in range(e2e_steps + 2):
         flush.zero_()
         torch.cuda.synchronize(dev)
         e0.record(stream)
-        q.copy_(hq, non_blocking=True)
-        k.copy_(hk, non_blocking=True)
-        v.copy_(hv, non_blocking=True)
-        do.copy_(hdo, non_blocking=True)
-        step()
-        ho.copy_(o, non_blocking=True)
-        hlse.copy_(lse, non_blocking=True)
-        hdq.copy_(dq, non_blocking=True)
-        hdk.copy_(dk, non_blocking=True)
-        hdv.copy_(dv, non_blocking=True)
+        S.q.copy_(hq, non_blocking=True)
+        S.k.copy_(hk, non_blocking=True)
+        S.v.copy_(hv, non_blocking=True)
+        S.do.copy_(hdo, non_blocking=True)
+        S.step()
+        ho.copy_(S.o, non_blocking=True)
+        hlse.copy_(S.lse, non_blocking=True)
+        hdq.copy_(S.dq, non_blocking=True)
+        hdk.copy_(S.dk, non_blocking=True)
+        hdv.copy_(S.dv, non_blocking=True)
         e1.record(stream)
         e1.synchronize()
         if i >= 2:
@@ -434,12 +553,43 @@ def run_gpu(args, w):
     e2e_val = e2e_rate / 1e12
 
     clocks = sampler.stop() if rank == 0 else None
+
+    # the rest of the long-context sweep (same configuration, other N): TFLOP/s and measured
+    # activation memory at each N, so that linearity in N is observed, not assumed
+    sweep = None
+    if w.name in LONG_SWEEP and not args.no_sweep:
+        del S
+        torch.cuda.empty_cache()
+        sweep = []
+        for name in LONG_SWEEP:
+            ww = workloads.WORKLOADS[name]
+            if name == w.name:
+                sweep.append({"N": w.N, "ms_per_step": ms_step, "tflops_nominal": value, "tflops_executed": executed,
+                              "pct_of_peak": 100 * value / float(peaks["bf16_tflops"]),
+                              "pct_of_peak_executed": 100 * executed / float(peaks["bf16_tflops"]),
+                              "peak_act_mem_bytes": act_bytes, "act_bytes_per_head_row": act_bytes / (B * H * N),
+                              "std_attention_matrix_bytes_bf16": B * H * N * Nk * 2, "source": "main timing above"})
+                continue
+            st = TrainingSetup(ww, dev, lib, flush)
+            sweep.append(sweep_entry(ww, st, peaks, max(10, min(args.steps, 100))))
+            del st
+            torch.cuda.empty_cache()
+        per_row = [e["act_bytes_per_head_row"] for e in sweep]
+        sweep = {"workloads": LONG_SWEEP, "entries": sweep,
+                 "act_bytes_per_head_row_spread": (max(per_row) - min(per_row)) / min(per_row),
+                 "note": "each N: L2 flushed before every step; peak memory = torch max_memory_allocated over "
+                         "one fwd+bwd through the public API minus the resident inputs and gradient outputs"}
+
     if ws > 1:
         torch.distributed.barrier()
     if rank != 0:
         return
     cpu = oracle_sample(w, x, budget_s=args.cpu_budget) if not args.no_cpu_baseline else None
     std = memmodel.training_memory(N, d_model=H * d, heads=H, layers=1)
+    io = io_accounting(w, x["kv_len"], measured=(
+        (traffic_record("fwd_kernel", w.name) or 0) + (traffic_record("bwd_kernel", w.name) or 0)
+        if traffic_record("fwd_kernel", w.name) and traffic_record("bwd_kernel", w.name) else None))
+    io["standard_measured"] = standard_records()
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
@@ -457,14 +607,15 @@ def run_gpu(args, w):
         "bwd_tflops_nominal": fl["bwd_nominal"] / ((avg["bwd_pre_kernel"] + avg["bwd_kernel"] + avg["dq_convert_kernel"]) * 1e-3) / 1e12,
         "kernel_ms": avg,
         "kernel_ms_source": "second timed pass of the same steps, an event after every kernel",
-        "step_ms_with_kernel_events": sum(ev[0].elapsed_time(ev[4]) for ev in events) / args.steps,
+        "step_ms_with_kernel_events": with_events / args.steps,
         "peak_act_mem_bytes": act_bytes,
+        "peak_act_mem_source": "measured: torch max_memory_allocated over one fwd+bwd through the public API, "
+                               "minus the resident inputs and gradient outputs (O, LSE and the backward workspace)",
         "act_bytes_per_head_row": act_bytes / (B * H * N),
-        "std_attention_matrix_bytes_bf16": B * 2 * N * N * H * 2,
-        "io": io_accounting(w, x["kv_len"], measured=(
-            (traffic_record("fwd_kernel", w.name) or 0) + (traffic_record("bwd_kernel", w.name) or 0)
-            if traffic_record("fwd_kernel", w.name) and traffic_record("bwd_kernel", w.name) else None)),
+        "std_attention_matrix_bytes_bf16": B * H * N * Nk * 2,
+        "io": io,
         "std_attention_memmodel_gb_per_layer_B1": std["standard_gb"],
+        "long_sweep": sweep,
         "roofline": roof,
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
@@ -472,6 +623,86 @@ def run_gpu(args, w):
         "gpu_launches": 4 * args.steps,
         "clocks": clocks,
     }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ standard attention (comparison)
+def run_standard(args, w):
+    """Standard attention, forward and backward, with every N x N matrix in HBM: the
+    comparison the pages' IO analysis makes (the tiled method against the one that writes S
+    and P out and reads them back). PyTorch bf16 matmuls and softmax; not this library."""
+    import torch
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    peaks, peak_src = load_peaks()
+    x = workloads.make_inputs(w, seed=0)
+    B, H, N, Nk, d = w.B, w.H, w.N, w.nk, w.d
+    q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "do"))
+    scale = w.scale
+    keep = None
+    if w.causal:
+        i = torch.arange(N, device=dev)[:, None]
+        j = torch.arange(Nk, device=dev)[None, :]
+        keep = j <= i + (Nk - N)
+    if x["kv_len"] is not None:
+        kvm = torch.arange(Nk, device=dev)[None, :] < x["kv_len"].to(dev)[:, None]   # [B, Nk]
+        kvm = kvm[:, None, None, :]
+        keep = kvm if keep is None else (keep & kvm)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    drop = None if keep is None else ~keep
+    qs = (q * scale).to(torch.bfloat16)  # the scale folded into Q once (not an N x N pass)
+
+    # Every N x N matrix is a bf16 tensor in HBM; the elementwise steps run in place, so the
+    # N x N passes are: S written; S read and written (mask); S read, P written (softmax); P read
+    # twice (O, dV); dP written; dP read and written twice (- D, * P), giving dS; dS read twice.
+    def step():
+        s_ = torch.matmul(qs, k.transpose(-1, -2))                      # S = s Q K^T
+        if drop is not None:
+            s_.masked_fill_(drop, float("-inf"))
+        p_ = torch.softmax(s_, dim=-1)                                   # P
+        del s_
+        o_ = torch.matmul(p_, v)                                         # O = P V
+        dv_ = torch.matmul(p_.transpose(-1, -2), do)                     # dV = P^T dO
+        ds_ = torch.matmul(do, v.transpose(-1, -2))                      # dP = dO V^T
+        dd = (do.float() * o_.float()).sum(-1, keepdim=True).to(torch.bfloat16)  # D (per row)
+        ds_.sub_(dd).mul_(p_)                                            # dS = P (dP - D)
+        del p_
+        dq_ = torch.matmul(ds_, k).mul_(scale)                           # dQ = s dS K
+        dk_ = torch.matmul(ds_.transpose(-1, -2), q).mul_(scale)        # dK = s dS^T Q
+        return o_, dq_, dk_, dv_
+
+    for _ in range(max(3, args.warmup)):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(dev)
+    torch.cuda.reset_peak_memory_stats(dev)
+    base = torch.cuda.memory_allocated(dev)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush.zero_()
+        evs[i][0].record(stream)
+        out = step()
+        evs[i][1].record(stream)
+        del out
+    torch.cuda.synchronize(dev)
+    peak_mem = torch.cuda.max_memory_allocated(dev) - base
+    ms = sum(e[0].elapsed_time(e[1]) for e in evs) / args.steps
+    fl = workloads.flop_counts(w, x["kv_len"])
+    value = fl["fwd_bwd_nominal"] / (ms * 1e-3) / 1e12
+    rec = standard_records().get(w.name)
+    line = {"impl": "standard", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "dtype": "bf16", "data": "synthetic (seeded N(0,1) inputs, bf16)",
+            "config": {"workload": w.name, "B": B, "H": H, "N": N, "N_k": Nk, "d": d, "causal": w.causal,
+                       "method": "standard attention: S, P, dP, dS materialised in HBM (torch bf16 matmul, "
+                                 "softmax; comparison only, not this library)",
+                       "l2": "flushed before every step (256 MiB write, untimed)"},
+            "pct_of_peak": 100.0 * value / float(peaks["bf16_tflops"]),
+            "peak_mem_bytes_beyond_inputs": int(peak_mem),
+            "dram": rec, "peak_source": peak_src}
     print(json.dumps(line), flush=True)
 
 
@@ -524,7 +755,7 @@ def run_gpu_infer(args, w):
         step()
     torch.cuda.synchronize(dev)
     detail = (ctypes.c_int * 4)()
-    if lib.fa_get_last_device_status(sp, detail) != 0:
+    if lib.fa_get_last_device_status_detail(sp, detail) != 0:
         raise RuntimeError(f"device status after warm-up: {list(detail)}")
     step_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
     sampler = ClockSampler(local if "CUDA_VISIBLE_DEVICES" not in os.environ else 0)
@@ -676,7 +907,7 @@ def run_gpu_packed(args, w):
         step()
     torch.cuda.synchronize(dev)
     detail = (ctypes.c_int * 4)()
-    if lib.fa_get_last_device_status(sp, detail) != 0:
+    if lib.fa_get_last_device_status_detail(sp, detail) != 0:
         raise RuntimeError(f"device status after warm-up: {list(detail)}")
     step_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
     sampler = ClockSampler(local if "CUDA_VISIBLE_DEVICES" not in os.environ else 0)
@@ -756,16 +987,19 @@ def run_gpu_packed(args, w):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--workload", default="gpt2", choices=sorted(workloads.WORKLOADS))
-    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--workload", default="long32768", choices=sorted(workloads.WORKLOADS))
+    ap.add_argument("--impl", default="native", choices=["native", "reference", "standard"])
+    ap.add_argument("--no-sweep", action="store_true", help="skip the long-context sweep's other N")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     w = workloads.WORKLOADS[args.workload]
     if args.impl == "reference":
         run_reference(args, w)
+    elif args.impl == "standard":
+        run_standard(args, w)
     elif w.infer:
         run_gpu_infer(args, w)
     elif w.packed:

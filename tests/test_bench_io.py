@@ -29,3 +29,23 @@ def test_io_accounting_counts_only_valid_key_columns():
     part = bench.io_accounting(w, kv)
     assert full["standard_attention_bytes"] - part["standard_attention_bytes"] == 5 * 2 * (8 * 384) * 16 * 512
     assert "step_bytes" not in full  # nothing measured
+
+
+def test_oracle_units_cover_whole_heads_or_the_last_rows():
+    # up to 4096 rows a unit is a whole head; beyond, the last 2048 query rows of each head,
+    # whose share of a causal head's pairs is (N^2 - (N - 2048)^2) / 2
+    units = bench.oracle_units(workloads.WORKLOADS["gpt2"])
+    assert len(units) == 96 and all(r0 == 0 for _, _, r0 in units)
+    w = workloads.WORKLOADS["long32768"]
+    units = bench.oracle_units(w)
+    assert len(units) == 12 and all(r0 == w.N - bench.ORACLE_ROWS for _, _, r0 in units)
+    rows = w.N - units[0][2]
+    assert workloads.visible_pairs(rows, w.nk, True) == (w.N ** 2 - (w.N - rows) ** 2) / 2
+
+
+def test_standard_records_pair_the_two_measurements():
+    recs = bench.standard_records()
+    for wl, rec in recs.items():
+        assert rec["standard_attention_dram_bytes"] > rec["flash_step_dram_bytes"] > 0
+        assert abs(rec["standard_over_flash"] * rec["flash_step_dram_bytes"]
+                   - rec["standard_attention_dram_bytes"]) < 1.0

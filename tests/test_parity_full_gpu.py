@@ -1,6 +1,8 @@
 """Parity at the workloads' full sizes, in the launch configuration the
-benchmark times: selected heads compared with the fp64 oracle (whole heads up
-to N = 4096, sampled query rows and keys beyond), and on every head the
+benchmark times: two heads compared with the fp64 oracle (whole heads up to
+N = 4096; beyond that the first and last query row of every 128-row tile and
+the first and last key of every 128-key tile, plus random ones, so that every
+tile of the persistent kernels' schedule is checked), and on every head the
 invariants that hold at any size:
   sum_j dK_j = 0            (each row of dS sums to zero)
   sum_j dV_j = sum_i dO_i   (each row of P sums to one; rows with a valid key)
@@ -41,8 +43,12 @@ def test_full_size_sampled_parity_and_invariants(gpu, name):
             r = ref.head_backward(q, k, v, do, w.scale, w.causal, kl)
             rows, keys = np.arange(w.N), np.arange(w.nk)
         else:
-            rows = np.unique(np.concatenate([[0, 1, 127, 128, w.N // 2, w.N - 1], rng.integers(0, w.N, 10)]))
-            keys = np.unique(np.concatenate([[0, 1, 127, 128, w.nk // 2, w.nk - 1], rng.integers(0, w.nk, 10)]))
+            def per_tile(n):
+                ends = np.concatenate([np.arange(0, n, 128), np.minimum(np.arange(127, n + 127, 128), n - 1)])
+                return np.unique(np.concatenate([ends, [1, n // 2], rng.integers(0, n, 32)]))
+            rows, keys = per_tile(w.N), per_tile(w.nk)
+            assert len(np.unique(rows // 128)) == (w.N + 127) // 128
+            assert len(np.unique(keys // 128)) == (w.nk + 127) // 128
             smp = ref.head_sampled(q, k, v, do, w.scale, w.causal, kl, rows, keys)
             r = {"o": smp["o"], "lse": smp["lse"], "dq": smp["dq"], "dk": smp["dk"], "dv": smp["dv"]}
         errs = {}
