@@ -165,30 +165,36 @@ __global__ void __launch_bounds__(256) bwd_pre_varlen_kernel(BwdArgs a, int B) {
 }
 
 // ---------------------------------------------------------------------------------------------
+// d = 128 (the d = 64 kernel has its own layout, Bwd64 below). A step is 64 query rows; the
+// two warpgroups split its columns. S^T is double-buffered (the next step's S^T is formed while
+// the warpgroups still turn the current one into P^T and dS^T); the Q / dO ring has three
+// stages so that the copy for step i + 1 lands before its S^T is wanted.
 template <int D>
 struct BwdCfg {
-  static constexpr int BR = (D == 64) ? 128 : 64;  // query rows per step
+  static_assert(D == 128, "BwdCfg serves the d = 128 kernel");
+  static constexpr int BR = 64;                    // query rows per step
   static constexpr int NSUB = D / 64;
   static constexpr int KSUB = 128 * 128;           // [128 keys][64] bf16 block
   static constexpr int KTILE = NSUB * KSUB;        // K or V tile
   static constexpr int QSUB = BR * 128;            // [BR rows][64] bf16 block
   static constexpr int QTILE = NSUB * QSUB;        // Q_i or dO_i tile
-  static constexpr int NSTQ = 2;
+  static constexpr int NSTQ = 3;
   static constexpr int DS_BYTES = 128 * BR * 2;    // dS: [128 keys][BR queries] bf16, 64-query blocks
-  static constexpr int DQ_STAGE = BR * D * 4;      // fp32 dQ staging tile
+  static constexpr int DQ_STAGE = BR * D * 4;      // fp32 dQ staging tile (one)
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = OFF_K + KTILE;
   static constexpr int OFF_Q = OFF_V + KTILE;                 // NSTQ stages, contiguous
   static constexpr int OFF_DO = OFF_Q + NSTQ * QTILE;         // NSTQ stages, contiguous
   static constexpr int OFF_DS = OFF_DO + NSTQ * QTILE;
-  static constexpr int OFF_DQ = OFF_DS + DS_BYTES;            // 2 staging buffers
-  static constexpr int OFF_LSE = OFF_DQ + 2 * DQ_STAGE;       // NSTQ x BR floats
+  static constexpr int OFF_DQ = OFF_DS + DS_BYTES;            // one staging buffer
+  static constexpr int OFF_LSE = OFF_DQ + DQ_STAGE;           // NSTQ x BR floats
   static constexpr int OFF_DV = OFF_LSE + NSTQ * BR * 4;      // NSTQ x BR floats
   static constexpr int OFF_BAR = OFF_DV + NSTQ * BR * 4;
   static constexpr int SMEM_BYTES = OFF_BAR + 256 + 1024;
-  // TMEM columns
-  static constexpr uint32_t TM_ST = 0, TM_DPT = BR, TM_DV = 2 * BR, TM_DK = 2 * BR + D, TM_DQ = 2 * BR + 2 * D;
-  static constexpr uint32_t DQ_COLS = 64;  // d=64: 64 head dims; d=128: BR = 64 query columns
+  // TMEM columns: S^T buffer b at BR b (P^T packed into it), dP^T (dS^T packed into it), dV, dK
+  // and one dQ^T buffer (BR query columns of 128 head-dim lanes)
+  static constexpr uint32_t TM_ST = 0, TM_DPT = 2 * BR, TM_DV = 3 * BR, TM_DK = 3 * BR + D, TM_DQ = 3 * BR + 2 * D;
+  static constexpr uint32_t DQ_COLS = 64;
   static constexpr uint32_t TM_COLS = 512;
   static constexpr int THREADS = 448;
   // Each warpgroup owns BR/2 query columns of S^T (and dP^T) in TMEM and packs
@@ -197,6 +203,8 @@ struct BwdCfg {
   static constexpr int HC = BR / 2;
   __host__ __device__ static constexpr uint32_t pcol(int qc) { return (qc / HC) * HC + (qc % HC) / 2; }
 };
+static_assert(BwdCfg<128>::TM_DQ + BwdCfg<128>::DQ_COLS <= BwdCfg<128>::TM_COLS, "d = 128 backward: TMEM columns");
+static_assert(BwdCfg<128>::SMEM_BYTES <= 232448, "d = 128 backward: shared memory above the 227 KB per-CTA limit");
 
 enum { SITE_B_KV_FULL = 20, SITE_B_QDO_EMPTY, SITE_B_QDO_FULL, SITE_B_S_FULL, SITE_B_DP_FULL, SITE_B_P_READY,
        SITE_B_DS_READY, SITE_B_DQ_EMPTY, SITE_B_DQ_FULL, SITE_B_FINAL };
@@ -230,13 +238,14 @@ __global__ void __launch_bounds__(448, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::OFF_BAR);
   const uint32_t b0 = smem_u32(bars);
   auto BAR = [&](int i) { return b0 + 8u * i; };
+  constexpr int NSTQ = C::NSTQ;
   const uint32_t kv_full = BAR(0);
   auto qdo_full = [&](int s) { return BAR(1 + s); };
-  auto qdo_empty = [&](int s) { return BAR(3 + s); };
-  const uint32_t s_full = BAR(5), dp_full = BAR(6), p_ready = BAR(7), ds_ready = BAR(8);
-  auto dq_full = [&](int s) { return BAR(9 + s); };
-  auto dq_empty = [&](int s) { return BAR(11 + s); };
-  const uint32_t final_bar = BAR(13);
+  auto qdo_empty = [&](int s) { return BAR(1 + NSTQ + s); };
+  auto s_full = [&](int b) { return BAR(1 + 2 * NSTQ + b); };  // S^T buffer b
+  const uint32_t dp_full = BAR(3 + 2 * NSTQ), p_ready = BAR(4 + 2 * NSTQ), ds_ready = BAR(5 + 2 * NSTQ);
+  const uint32_t dq_full = BAR(6 + 2 * NSTQ), dq_empty = BAR(7 + 2 * NSTQ), final_bar = BAR(8 + 2 * NSTQ);
+  static_assert(9 + 2 * NSTQ <= 16, "d = 128 backward: barrier area");
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C::OFF_BAR + 8 * 16);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
   DevStatus st{a.status, abort_flag};
@@ -297,11 +306,11 @@ __global__ void __launch_bounds__(448, 1)
     dvec_h = a.dvec + (size_t)bh * a.Npad;
   }
   // The producer warp initialises the barriers and starts the first copies (K, V and the first
-  // two query steps, whose slots are free) before the CTA-wide setup, hiding their latency. It
+  // NSTQ query steps, whose slots are free) before the CTA-wide setup, hiding their latency. It
   // runs its code with the whole warp and lets one elected lane issue each copy.
-  const int n_pre = min(2, n_it);
+  const int n_pre = min(NSTQ, n_it);
   auto load_qdo = [&](int it) {  // whole warp
-    const int s = it & 1, i = i_start + it;
+    const int s = it % NSTQ, i = i_start + it;
     const uint32_t bar = qdo_full(s);
     const float* lsrc = lse2_h + (size_t)i * BR;
     const float* dsrc = dvec_h + (size_t)i * BR;
@@ -324,13 +333,14 @@ __global__ void __launch_bounds__(448, 1)
   if (warp == 12) {
     if (lane == 0) {
       mbar_init(kv_full, 1);
-      for (int s = 0; s < 2; ++s) {
+      for (int s = 0; s < NSTQ; ++s) {
         mbar_init(qdo_full(s), 1);
         mbar_init(qdo_empty(s), 1);
-        mbar_init(dq_full(s), 1);
-        mbar_init(dq_empty(s), 4);
       }
-      mbar_init(s_full, 1);
+      mbar_init(s_full(0), 1);
+      mbar_init(s_full(1), 1);
+      mbar_init(dq_full, 1);
+      mbar_init(dq_empty, 4);
       mbar_init(dp_full, 1);
       mbar_init(p_ready, 8);
       mbar_init(ds_ready, 8);
@@ -369,7 +379,7 @@ __global__ void __launch_bounds__(448, 1)
     {
       int issued = n_pre;
       for (int it = n_pre; it < n_it; ++it) {
-        if (!wait_warp(qdo_empty(it & 1), ((it >> 1) & 1) ^ 1, st, SITE_B_QDO_EMPTY)) break;
+        if (!wait_warp(qdo_empty(it % NSTQ), ((it / NSTQ) & 1) ^ 1, st, SITE_B_QDO_EMPTY)) break;
         load_qdo(it);
         issued = it + 1;
       }
@@ -378,8 +388,8 @@ __global__ void __launch_bounds__(448, 1)
         const uint64_t t0 = globaltimer_ns();
         while (!mbar_try_wait(kv_full, 0) && globaltimer_ns() - t0 < 100000000ull) {
         }
-        for (int it = max(0, issued - 2); it < issued; ++it)
-          while (!mbar_try_wait(qdo_full(it & 1), (it >> 1) & 1) && globaltimer_ns() - t0 < 100000000ull) {
+        for (int it = max(0, issued - NSTQ); it < issued; ++it)
+          while (!mbar_try_wait(qdo_full(it % NSTQ), (it / NSTQ) & 1) && globaltimer_ns() - t0 < 100000000ull) {
           }
       }
     }
@@ -428,28 +438,46 @@ __global__ void __launch_bounds__(448, 1)
                    IDESC_Q, k > 0);
         }
       };
-      bool ok = wait_warp(kv_full, 0, st, SITE_B_KV_FULL);
-      for (int it = 0; ok && it < n_it; ++it) {
-        const int s = it & 1;
-        const uint32_t so = s * QT16;
-        if (!(ok = wait_warp(qdo_full(s), (it >> 1) & 1, st, SITE_B_QDO_FULL))) break;
+      // Step i: S^T(i + 1) goes into the other S^T buffer as soon as its Q has landed (that
+      // buffer's P^T(i - 1) has been read by dV(i - 1), issued before, and by the warpgroups'
+      // dS^T(i - 1), waited for), so the warpgroups find it ready when they finish step i; then
+      // dV(i), dK(i), dQ^T(i) as P^T(i) and dS^T(i) arrive, and dP^T(i + 1) after dK(i) has read
+      // dS^T(i) out of the dP^T columns.
+      bool ok = wait_warp(kv_full, 0, st, SITE_B_KV_FULL) && wait_warp(qdo_full(0), 0, st, SITE_B_QDO_FULL);
+      if (ok) {
         tc_fence_after();
-        issue_kmajor(C::TM_ST, k_lo, q_lo + so);
-        commit(s_full);
-        issue_kmajor(C::TM_DPT, v_lo, do_lo + so);
+        issue_kmajor(C::TM_ST, k_lo, q_lo);
+        commit(s_full(0));
+        issue_kmajor(C::TM_DPT, v_lo, do_lo);
         commit(dp_full);
+      }
+      for (int it = 0; ok && it < n_it; ++it) {
+        const int s = it % NSTQ, sb = it & 1;
+        const uint32_t so = s * QT16;
+        const bool next = it + 1 < n_it;
+        const int s1 = (it + 1) % NSTQ;
+        if (next) {
+          if (!(ok = wait_warp(qdo_full(s1), ((it + 1) / NSTQ) & 1, st, SITE_B_QDO_FULL))) break;
+          tc_fence_after();
+          issue_kmajor(C::TM_ST + (sb ^ 1) * BR, k_lo, q_lo + s1 * QT16);
+          commit(s_full(sb ^ 1));
+        }
         if (!(ok = wait_warp(p_ready, it & 1, st, SITE_B_P_READY))) break;
         tc_fence_after();
-        issue_grad(C::TM_DV, C::TM_ST, domn_lo + so, it > 0);
+        issue_grad(C::TM_DV, C::TM_ST + sb * BR, domn_lo + so, it > 0);
         if (!(ok = wait_warp(ds_ready, it & 1, st, SITE_B_DS_READY))) break;
         tc_fence_after();
         issue_grad(C::TM_DK, C::TM_DPT, qmn_lo + so, it > 0);
-        const int qb = it & 1;
-        if (!(ok = wait_warp(dq_empty(qb), ((it >> 1) & 1) ^ 1, st, SITE_B_DQ_EMPTY))) break;
+        // one dQ^T buffer: the epilogue has read out the previous step's
+        if (!(ok = wait_warp(dq_empty, (it & 1) ^ 1, st, SITE_B_DQ_EMPTY))) break;
         tc_fence_after();
-        issue_dq(C::TM_DQ + qb * C::DQ_COLS);
-        commit(dq_full(qb));
-        commit(qdo_empty(s));
+        issue_dq(C::TM_DQ);
+        commit(dq_full);
+        commit(qdo_empty(s));  // last readers of Q_i and dO_i issued
+        if (next) {
+          issue_kmajor(C::TM_DPT, v_lo, do_lo + s1 * QT16);
+          commit(dp_full);
+        }
       }
       commit(final_bar);  // also the drain: completes after every MMA issued above
       const uint64_t t0 = globaltimer_ns();
@@ -463,22 +491,21 @@ __global__ void __launch_bounds__(448, 1)
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
     const int tid = threadIdx.x - 256;
     for (int it = 0; it < n_it; ++it) {
-      const int qb = it & 1;
       const int i = i_start + it;
       // the four warps leave the loop together, so the named barriers below never wait on a missing warp
-      if (!named_bar_and(3, 128, wait_warp(dq_full(qb), (it >> 1) & 1, st, SITE_B_DQ_FULL))) break;
+      if (!named_bar_and(3, 128, wait_warp(dq_full, it & 1, st, SITE_B_DQ_FULL))) break;
       tc_fence_after();
       uint32_t v[2][32];
-      tmem_ld32(tmem + lane_off + C::TM_DQ + qb * C::DQ_COLS, v[0]);
-      tmem_ld32(tmem + lane_off + C::TM_DQ + qb * C::DQ_COLS + 32, v[1]);
+      tmem_ld32(tmem + lane_off + C::TM_DQ, v[0]);
+      tmem_ld32(tmem + lane_off + C::TM_DQ + 32, v[1]);
       tmem_wait_ld();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(dq_empty(qb));
-      // the reduce issued two steps ago from this staging buffer has finished reading it
-      if (tid == 0) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+      if (lane == 0) mbar_arrive(dq_empty);
+      // the reduce issued from the staging buffer one step ago has finished reading it
+      if (tid == 0) bulk_wait_read0();
       named_bar_sync(3, 128);
-      uint8_t* stg = sm + C::OFF_DQ + qb * C::DQ_STAGE;
+      uint8_t* stg = sm + C::OFF_DQ;
       const float sc = a.scale;
       if (D == 64) {
         // row r of a [128 queries][64 dims] fp32 tile, two 32-column swizzled boxes
@@ -529,13 +556,14 @@ __global__ void __launch_bounds__(448, 1)
     const float sl2 = a.scale_log2;
     bool ok = true;
     for (int it = 0; it < n_it; ++it) {
-      const int s = it & 1;
+      const int s = it % NSTQ, sb = it & 1;
+      const uint32_t tST = C::TM_ST + sb * BR;  // this step's S^T buffer (P^T packed into it)
       const int i = i_start + it;
       const int q0 = i * BR;
       const float* lse_s = reinterpret_cast<const float*>(sm + C::OFF_LSE + s * BR * 4);
       const float* dv_s = reinterpret_cast<const float*>(sm + C::OFF_DV + s * BR * 4);
-      if (!(ok = wait_warp(qdo_full(s), (it >> 1) & 1, st, SITE_B_QDO_FULL))) break;
-      if (!(ok = wait_warp(s_full, it & 1, st, SITE_B_S_FULL))) break;
+      if (!(ok = wait_warp(qdo_full(s), (it / NSTQ) & 1, st, SITE_B_QDO_FULL))) break;
+      if (!(ok = wait_warp(s_full(sb), (it >> 1) & 1, st, SITE_B_S_FULL))) break;
       tc_fence_after();
       bool need_mask;
       if constexpr (VL)
@@ -547,7 +575,7 @@ __global__ void __launch_bounds__(448, 1)
       for (int ch = 0; ch < NCH; ++ch) {
         const int cb = c0 + ch * 32;  // query column base within the tile
         uint32_t sv[32];
-        tmem_ld32(tmem + lane_off + C::TM_ST + cb, sv);
+        tmem_ld32(tmem + lane_off + tST + cb, sv);
         float lz[32];  // LSE of the 32 queries, broadcast loads
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
@@ -579,7 +607,7 @@ __global__ void __launch_bounds__(448, 1)
                     x[0], x[1]);
           pk[e] = pack_bf16x2(ex2_approx(x[0]), ex2_approx(x[1]));
         }
-        tmem_st16(tmem + lane_off + C::TM_ST + C::pcol(cb), pk);
+        tmem_st16(tmem + lane_off + tST + C::pcol(cb), pk);
       }
       tmem_wait_st();
       tc_fence_before();
@@ -593,7 +621,7 @@ __global__ void __launch_bounds__(448, 1)
         const int cb = c0 + ch * 32;
         uint32_t dp[32], pp[16];
         tmem_ld32(tmem + lane_off + C::TM_DPT + cb, dp);
-        tmem_ld16(tmem + lane_off + C::TM_ST + C::pcol(cb), pp);
+        tmem_ld16(tmem + lane_off + tST + C::pcol(cb), pp);
         float dz[32];  // D of the 32 queries, broadcast loads
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
@@ -1341,7 +1369,8 @@ static int launch_bwd_pre_d(const BwdArgs& a, int BH, cudaStream_t stream) {
 template <int D, bool VL = false>
 static int launch_bwd_main_d(const void* q, const void* k, const void* v, const BwdArgs& a, int BH,
                              cudaStream_t stream) {
-  constexpr int BR = (D == 64) ? Bwd64::BR : BwdCfg<D>::BR;  // query rows per step
+  constexpr int BR = 64;  // query rows per step of both main kernels (Bwd64::BR, BwdCfg<128>::BR)
+  static_assert(Bwd64::BR == BR && BwdCfg<128>::BR == BR, "query rows per step");
   const uint64_t N = (uint64_t)(VL ? vl_T(a) : a.N), Nk = (uint64_t)(VL ? vl_T(a) : a.Nk);
   const uint64_t Z = (uint64_t)(VL ? a.H : BH);
   const auto BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
