@@ -207,7 +207,7 @@ static_assert(BwdCfg<128>::TM_DQ + BwdCfg<128>::DQ_COLS <= BwdCfg<128>::TM_COLS,
 static_assert(BwdCfg<128>::SMEM_BYTES <= 232448, "d = 128 backward: shared memory above the 227 KB per-CTA limit");
 
 enum { SITE_B_KV_FULL = 20, SITE_B_QDO_EMPTY, SITE_B_QDO_FULL, SITE_B_S_FULL, SITE_B_DP_FULL, SITE_B_P_READY,
-       SITE_B_DS_READY, SITE_B_DQ_EMPTY, SITE_B_DQ_FULL, SITE_B_FINAL };
+       SITE_B_DS_READY, SITE_B_DQ_EMPTY, SITE_B_DQ_FULL, SITE_B_FINAL, SITE_B_SMEM_ALIGN };
 
 // VL (packed sequences, [H, T, d]): the item is sequence b of head h. Each statement that
 // addresses rows has its packed form in an if-constexpr branch beside the plain [BH, N, d]
@@ -727,7 +727,7 @@ struct Bwd64 {
   static constexpr int D = 64, BR = 64;           // queries per step
   // Q/dO ring depth: four stages keep the copy of step g+2 clear of the readers of step g-1
   // (three measured 40 % slower); the epilogue warps need one staging buffer.
-  static constexpr int NQS = 4;
+  static constexpr int NQS = 5;
   static constexpr int NSTG = 1;
   static constexpr int KTILE = 128 * 128;          // K or V tile: [128 keys][64] bf16
   static constexpr int QTILE = BR * 128;           // Q_i or dO_i: [64 rows][64] bf16
@@ -741,7 +741,9 @@ struct Bwd64 {
   static constexpr int OFF_LSE = OFF_STG + NSTG * STG_BYTES; // NQS x BR floats
   static constexpr int OFF_DV = OFF_LSE + NQS * BR * 4;      // NQS x BR floats
   static constexpr int OFF_BAR = OFF_DV + NQS * BR * 4;
-  static constexpr int SMEM_BYTES = OFF_BAR + 256 + 1024;
+  // no alignment slack: the kernel checks that dynamic shared memory starts 1024-byte aligned
+  static constexpr int BAR_BYTES = 272;
+  static constexpr int SMEM_BYTES = OFF_BAR + BAR_BYTES;
   __host__ __device__ static constexpr int off_k(int b) { return OFF_KV + b * 2 * KTILE; }
   __host__ __device__ static constexpr int off_v(int b) { return OFF_KV + b * 2 * KTILE + KTILE; }
   // TMEM: S^T buffer w at 64 w (P^T packed in its first 32 columns), dP^T buffer w at
@@ -751,7 +753,7 @@ struct Bwd64 {
   static constexpr int THREADS = 480;
 };
 static_assert(Bwd64::SMEM_BYTES <= 232448, "d = 64 backward: shared memory above the 227 KB per-CTA limit");
-static_assert(8 * (4 + 2 * Bwd64::NQS + 17) + 12 <= 256, "d = 64 backward: barrier area");
+static_assert(8 * (4 + 2 * Bwd64::NQS + 17) + 12 <= Bwd64::BAR_BYTES, "d = 64 backward: barrier area");
 
 // One key tile of the persistent schedule.
 struct TileD64 {
@@ -834,7 +836,13 @@ __global__ void __launch_bounds__(480, 1)
   using C = Bwd64;
   constexpr int BR = C::BR, NQS = C::NQS;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = align1024(smem_raw);
+  // the layout has no room for alignment slack: dynamic shared memory must start on a 1024-byte
+  // boundary (the 128-byte swizzle atoms); otherwise record a device check and do nothing
+  if (smem_u32(smem_raw) & 1023u) {
+    if (threadIdx.x == 0) record_check(a.status, SITE_B_SMEM_ALIGN);
+    return;
+  }
+  uint8_t* sm = smem_raw;
   const uint32_t sbase = smem_u32(sm);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
