@@ -47,6 +47,7 @@ SIGNATURES = {
         "fa_version": (_i, []),
         "fa_last_error_detail": (ctypes.c_char_p, []),
     },
+    "libfa_withhold.so": None,  # the same C ABI as libfa.so (a test build of it)
     "libfa_selftest.so": {
         "fa_selftest_mma": (_i, [_vp, _vp, _vp, _i, _i, _i, _vp, _vp]),
         "fa_selftest_wait_timeout": (_i, [_vp, ctypes.c_uint, _vp]),
@@ -67,7 +68,8 @@ def load(name: str = "libfa.so") -> ctypes.CDLL:
     if not os.path.exists(path):
         raise ImportError(f"{path} is not built; run io_aware_exact_04_gb300.build.build()")
     lib = ctypes.CDLL(path)
-    for fn, (res, args) in SIGNATURES[name].items():
+    sigs = SIGNATURES[name] if SIGNATURES[name] is not None else SIGNATURES["libfa.so"]
+    for fn, (res, args) in sigs.items():
         f = getattr(lib, fn)
         f.restype = res
         f.argtypes = args

@@ -2,6 +2,9 @@
 
 libfa.so           the attention library (C ABI in include/fa.h)
 libfa_selftest.so  hardware self-checks (include/fa_selftest.h)
+libfa_withhold.so  test build of libfa.so: every CTA leaves out one of its TMA copies
+                   and waits give up after 20 ms, so that a test can check that the
+                   kernels report FA_ERR_TIMEOUT and stop cleanly (not for any other use)
 
 Each translation unit compiles in its own nvcc process, in parallel; objects
 go to _build/ at the repository root. A library is rebuilt when any source or
@@ -29,6 +32,11 @@ FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", 
 LIBS = {
     "libfa.so": ["fa_api.cu", "fa_fwd.cu", "fa_bwd.cu", "fa_noalloc.cu"],
     "libfa_selftest.so": ["selftest.cu"],
+    "libfa_withhold.so": ["fa_api.cu", "fa_fwd.cu", "fa_bwd.cu", "fa_noalloc.cu"],
+}
+# extra preprocessor definitions (and a separate object directory) per library
+DEFINES = {
+    "libfa_withhold.so": ["-DFA_TEST_WITHHOLD", "-DFA_WAIT_LIMIT_NS=20000000ull"],
 }
 
 
@@ -61,13 +69,16 @@ def build(verbose: bool = False, force: bool = False) -> dict:
     for lib, srcs in LIBS.items():
         target = os.path.join(PKG, lib)
         srcs = [os.path.join(CSRC, s) for s in srcs]
-        objs = [os.path.join(BUILD, os.path.basename(s) + ".o") for s in srcs]
+        defs = DEFINES.get(lib, [])
+        odir = os.path.join(BUILD, lib.replace(".so", "")) if defs else BUILD
+        os.makedirs(odir, exist_ok=True)
+        objs = [os.path.join(odir, os.path.basename(s) + ".o") for s in srcs]
         out[lib] = target
         if not force and not _stale(target, srcs + headers):
             continue
         for s, o in zip(srcs, objs):
             if force or _stale(o, [s] + headers):
-                cmd = [cc] + ARCH + FLAGS + ["-c", s, "-o", o]
+                cmd = [cc] + ARCH + FLAGS + defs + ["-c", s, "-o", o]
                 if verbose:
                     print(" ".join(cmd), flush=True)
                 jobs.append((cmd, subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT)))

@@ -12,8 +12,22 @@ namespace fa {
 
 // Upper bound for any single wait inside a kernel. Every wait in these kernels
 // normally completes within microseconds; after this long the CTA gives up,
-// records FA_ERR_TIMEOUT in the status word and exits cleanly.
-constexpr uint64_t kWaitLimitNs = 2000000000ull;
+// records FA_ERR_TIMEOUT in the status word and exits cleanly. A test build
+// may set a shorter limit (FA_WAIT_LIMIT_NS).
+#ifndef FA_WAIT_LIMIT_NS
+#define FA_WAIT_LIMIT_NS 2000000000ull
+#endif
+constexpr uint64_t kWaitLimitNs = FA_WAIT_LIMIT_NS;
+
+// Test build only (FA_TEST_WITHHOLD, never the library's own build): every CTA leaves out one
+// of its TMA copies (the forward's second K/V tile, the backward's second or third Q/dO step),
+// so that the wait for it runs out; the test then checks that the kernel reports
+// FA_ERR_TIMEOUT, stops cleanly and leaves the CUDA context usable.
+#ifdef FA_TEST_WITHHOLD
+constexpr bool kWithhold = true;
+#else
+constexpr bool kWithhold = false;
+#endif
 
 // status[0]: first error code, status[1]: wait site, status[2..3]: block index.
 struct DevStatus {

@@ -161,6 +161,7 @@ __global__ void __launch_bounds__(352, 1)
   // runs its code with the whole warp and lets one elected lane issue each copy.
   const int n_pre = min(C::NST, nmax);
   auto load_kv = [&](int j) {  // whole warp
+    if (kWithhold && j == 1) return;  // test build: this copy never arrives
     const int s = j % C::NST;
     const uint32_t kf = k_full(s), vf = v_full(s);
     const uint32_t kd = sbase + C::OFF_K + s * C::TILE_BYTES, vd = sbase + C::OFF_V + s * C::TILE_BYTES;
@@ -676,6 +677,7 @@ __global__ void __launch_bounds__(352, 1)
 
   // Producer warp: barriers, then the first item's Q and first K/V stages before the setup.
   auto load_kv = [&](int g, int j, int bh) {  // whole warp; ring index g, key tile j
+    if (kWithhold && g == 1) return;  // test build: this copy never arrives
     const int s = g % NST;
     const uint32_t kf = k_full(s), vf = v_full(s);
     if (elect_one()) mbar_arrive_expect_tx(kf, C::TILE_BYTES);
