@@ -598,16 +598,48 @@ static_assert(8 * (10 + 3 * FwdP64::NST + 1) + 8 <= 256, "persistent forward: ba
 struct ItemF64 {
   int bh, kv, q0, n[2], nmax;
 };
+// Where item bh's rows live. Plain [BH, N, d]: rows start at TMA row 0 of head bh, N query
+// rows, O / LSE row index base bh N. Packed sequences (VL, [H, T, d]): item bh is sequence
+// b = bh / H of head h, its rows start at TMA row cu[b] of head h, it has cu[b + 1] - cu[b]
+// rows, and its O / LSE rows start at h T + cu[b].
+struct RowsF64 {
+  int rb, nq, zh;
+  size_t obase;
+};
+template <bool VL>
+__device__ __forceinline__ RowsF64 rows_f64(int bh, const FwdArgs& a) {
+  RowsF64 r;
+  if (VL) {
+    const int b = bh / a.H, h = bh - b * a.H;
+    r.rb = a.cu_seqlens[b];
+    r.nq = a.cu_seqlens[b + 1] - r.rb;
+    r.zh = h;
+    r.obase = (size_t)h * a.T + r.rb;
+  } else {
+    r.rb = 0;
+    r.nq = a.N;
+    r.zh = bh;
+    r.obase = (size_t)bh * a.N;
+  }
+  return r;
+}
+template <bool VL>
 __device__ __forceinline__ ItemF64 item_f64(int t, const FwdArgs& a, int BH) {
   ItemF64 it;
   const int p = t / BH;
   it.bh = t - p * BH;
   it.q0 = (a.n_pairs - 1 - p) * 256;
-  it.kv = a.Nk;
-  if (a.kv_len) it.kv = min(max(a.kv_len[it.bh / a.H], 0), a.Nk);
+  int nq = a.N;
+  if (VL) {  // a pair past its sequence has no work (and writes nothing: the rows are another's)
+    nq = rows_f64<VL>(it.bh, a).nq;
+    it.kv = nq;
+  } else {
+    it.kv = a.Nk;
+    if (a.kv_len) it.kv = min(max(a.kv_len[it.bh / a.H], 0), a.Nk);
+  }
   const int nkt = (it.kv + 127) >> 7;
 #pragma unroll
-  for (int u = 0; u < 2; ++u) it.n[u] = key_tiles(it.q0 + u * 128, a.N, nkt, a.causal, a.coff);
+  for (int u = 0; u < 2; ++u) it.n[u] = key_tiles(it.q0 + u * 128, nq, nkt, a.causal, VL ? 0 : a.coff);
   it.nmax = max(it.n[0], it.n[1]);
   return it;
 }
@@ -631,6 +663,7 @@ __device__ __noinline__ void zero_rows_f64(uint16_t* o, float* lse, int N, int b
   }
 }
 
+template <bool VL>
 __global__ void __launch_bounds__(352, 1)
     fwd_kernel_p64(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o, FwdArgs a,
@@ -670,7 +703,7 @@ __global__ void __launch_bounds__(352, 1)
     for (;; ++r) {
       const int t = sched_f64(r, cta, G, T);
       if (t < 0) return -1;
-      out = item_f64(t, a, BH);
+      out = item_f64<VL>(t, a, BH);
       if (out.nmax > 0) return r;
     }
   };
@@ -680,17 +713,20 @@ __global__ void __launch_bounds__(352, 1)
     if (kWithhold && g == 1) return;  // test build: this copy never arrives
     const int s = g % NST;
     const uint32_t kf = k_full(s), vf = v_full(s);
+    const RowsF64 rw = rows_f64<VL>(bh, a);
     if (elect_one()) mbar_arrive_expect_tx(kf, C::TILE_BYTES);
-    if (elect_one()) tma_load_3d(sbase + C::OFF_K + s * C::TILE_BYTES, &tm_k, 0, j * 128, bh, kf);
+    if (elect_one()) tma_load_3d(sbase + C::OFF_K + s * C::TILE_BYTES, &tm_k, 0, rw.rb + j * 128, rw.zh, kf);
     if (elect_one()) mbar_arrive_expect_tx(vf, C::TILE_BYTES);
-    if (elect_one()) tma_load_3d(sbase + C::OFF_V + s * C::TILE_BYTES, &tm_v, 0, j * 128, bh, vf);
+    if (elect_one()) tma_load_3d(sbase + C::OFF_V + s * C::TILE_BYTES, &tm_v, 0, rw.rb + j * 128, rw.zh, vf);
     __syncwarp();
   };
   auto load_q = [&](int set, const ItemF64& it) {  // whole warp
     const int nq = (it.n[1] > 0) ? 2 : 1;
+    const RowsF64 rw = rows_f64<VL>(it.bh, a);
     if (elect_one()) mbar_arrive_expect_tx(q_full(set), nq * C::TILE_BYTES);
     for (int u = 0; u < nq; ++u)
-      if (elect_one()) tma_load_3d(sbase + C::off_q(set, u), &tm_q, 0, it.q0 + u * 128, it.bh, q_full(set));
+      if (elect_one())
+        tma_load_3d(sbase + C::off_q(set, u), &tm_q, 0, rw.rb + it.q0 + u * 128, rw.zh, q_full(set));
     __syncwarp();
   };
   int n_pre = 0;  // K/V stages of the first item issued before the setup (producer warp)
@@ -745,9 +781,11 @@ __global__ void __launch_bounds__(352, 1)
     for (int r = 0; ok; ++r) {
       const int tt = sched_f64(r, cta, G, T);
       if (tt < 0) break;
-      const ItemF64 it = item_f64(tt, a, BH);
+      const ItemF64 it = item_f64<VL>(tt, a, BH);
+      if (VL && lane == 0 && it.q0 == 0 && rows_f64<VL>(it.bh, a).nq > a.max_seqlen)
+        record_check(a.status, SITE_F_SEQLEN);  // the grid (sized by max_seqlen) misses rows of it
       if (it.nmax == 0) {
-        zero_rows_f64(a.o, a.lse, a.N, it.bh, it.q0, lane);
+        if (!VL) zero_rows_f64(a.o, a.lse, a.N, it.bh, it.q0, lane);
         continue;
       }
       const int set = iu & 1;
@@ -892,8 +930,9 @@ __global__ void __launch_bounds__(352, 1)
       const int kvv = it.kv;
       const int grow = qs + row;
       bool stored = false;
-      if (qs < a.N && n == 0) {
-        // no valid key for any row of this tile: O = 0, LSE = -inf
+      if (!VL && qs < a.N && n == 0) {
+        // no valid key for any row of this tile: O = 0, LSE = -inf (packed: no such tile, the
+        // rows past a sequence belong to the next one)
         if (grow < a.N) {
           uint4* orow = reinterpret_cast<uint4*>(a.o + ((size_t)it.bh * a.N + grow) * D);
           for (int c = 0; c < D / 8; ++c) orow[c] = make_uint4(0, 0, 0, 0);
@@ -1004,8 +1043,11 @@ __global__ void __launch_bounds__(352, 1)
         ok = named_bar_and(1 + t, 128, ok);
         if (!ok) break;
         tc_fence_after();
-        const int bh = item_f64(sched_f64(r, cta, G, T), a, BH).bh;
+        const RowsF64 rw = rows_f64<VL>(item_f64<VL>(sched_f64(r, cta, G, T), a, BH).bh, a);
         const int set = iu & 1;
+        // a packed sequence's partial last tile is written row by row: a TMA box would run into
+        // the next sequence's rows
+        const bool direct = VL && qs + 128 > rw.nq;
         // epilogue: O_t out of TMEM (then released to the next item's PV), O / l -> bf16 ->
         // swizzled smem (this item's Q_t buffer, which no MMA reads any more) -> TMA store
         uint32_t ov[2][32];
@@ -1025,17 +1067,22 @@ __global__ void __launch_bounds__(352, 1)
           v.y = pack_bf16x2(__uint_as_float(x[2]) * inv, __uint_as_float(x[3]) * inv);
           v.z = pack_bf16x2(__uint_as_float(x[4]) * inv, __uint_as_float(x[5]) * inv);
           v.w = pack_bf16x2(__uint_as_float(x[6]) * inv, __uint_as_float(x[7]) * inv);
-          *reinterpret_cast<uint4*>(stage + sw128_offset(row, q)) = v;
+          if (direct) {
+            if (grow < rw.nq) *reinterpret_cast<uint4*>(a.o + (rw.obase + grow) * D + q * 8) = v;
+          } else {
+            *reinterpret_cast<uint4*>(stage + sw128_offset(row, q)) = v;
+          }
         }
-        if (grow < a.N)
-          a.lse[(size_t)bh * a.N + grow] =
-              (l_run > 0.f) ? (m_run + lg2_approx(l_run)) * 0.6931471805599453f : -INFINITY;
+        if (grow < rw.nq)
+          a.lse[rw.obase + grow] = (l_run > 0.f) ? (m_run + lg2_approx(l_run)) * 0.6931471805599453f : -INFINITY;
         fence_proxy_async_smem();
         named_bar_sync(1 + t, 128);
         if (wq == 0 && lane == 0) {
-          tma_store_3d(&tm_o, smem_u32(stage), 0, qs, bh);
-          bulk_commit();
-          bulk_wait_read0();  // the Q_t buffer is free again once the store has read it
+          if (!direct) {
+            tma_store_3d(&tm_o, smem_u32(stage), 0, rw.rb + qs, rw.zh);
+            bulk_commit();
+            bulk_wait_read0();  // the Q_t buffer is free again once the store has read it
+          }
           mbar_arrive(q_empty(set));
         }
         stored = true;
@@ -1140,21 +1187,24 @@ static int launch_fwd_d(const void* q, const void* k, const void* v, void* o, co
                     mo, args);
 }
 
-// d = 64: the persistent kernel, one CTA per SM (at most one per work item)
+// d = 64: the persistent kernel, one CTA per SM (at most one per work item). VL: packed
+// sequences, [H, T, d] tensors; BH = B * H items per query pair.
+template <bool VL = false>
 static int launch_fwd_p64(const void* q, const void* k, const void* v, void* o, const FwdArgs& args, int BH,
                           cudaStream_t stream) {
   using C = FwdP64;
   CUtensorMap mq, mk, mv, mo;
-  const uint64_t N = (uint64_t)args.N, Nk = (uint64_t)args.Nk;
+  const uint64_t N = (uint64_t)(VL ? args.T : args.N), Nk = (uint64_t)(VL ? args.T : args.Nk);
+  const uint64_t Z = (uint64_t)(VL ? args.H : BH);
   const auto BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const auto SW = CU_TENSOR_MAP_SWIZZLE_128B;
-  if (!make_tmap_3d(&mq, q, BF, 2, 64, N, BH, 64, 128, SW) || !make_tmap_3d(&mk, k, BF, 2, 64, Nk, BH, 64, 128, SW) ||
-      !make_tmap_3d(&mv, v, BF, 2, 64, Nk, BH, 64, 128, SW) || !make_tmap_3d(&mo, o, BF, 2, 64, N, BH, 64, 128, SW))
+  if (!make_tmap_3d(&mq, q, BF, 2, 64, N, Z, 64, 128, SW) || !make_tmap_3d(&mk, k, BF, 2, 64, Nk, Z, 64, 128, SW) ||
+      !make_tmap_3d(&mv, v, BF, 2, 64, Nk, Z, 64, 128, SW) || !make_tmap_3d(&mo, o, BF, 2, 64, N, Z, 64, 128, SW))
     return cuda_fail("cuTensorMapEncodeTiled", 0, "tensor map rejected");
   static bool attr_set = false;  // benign race: idempotent
   if (!attr_set) {
     const cudaError_t e =
-        cudaFuncSetAttribute(fwd_kernel_p64, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+        cudaFuncSetAttribute(fwd_kernel_p64<VL>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return cuda_fail("cudaFuncSetAttribute", (int)e, cudaGetErrorName(e));
     attr_set = true;
   }
@@ -1162,8 +1212,8 @@ static int launch_fwd_p64(const void* q, const void* k, const void* v, void* o, 
   if (!sm_count(&sms)) return FA_ERR_CUDA;
   const long long items = (long long)BH * args.n_pairs;
   const dim3 grid((unsigned)std::min<long long>(items, sms));
-  return launch_pdl(__func__, fwd_kernel_p64, grid, dim3(C::THREADS), C::SMEM_BYTES, stream, mq, mk, mv, mo, args,
-                    BH);
+  return launch_pdl(__func__, fwd_kernel_p64<VL>, grid, dim3(C::THREADS), C::SMEM_BYTES, stream, mq, mk, mv, mo,
+                    args, BH);
 }
 
 int launch_fwd(const void* q, const void* k, const void* v, void* o, const FwdArgs& args, int BH, int d,
@@ -1172,7 +1222,7 @@ int launch_fwd(const void* q, const void* k, const void* v, void* o, const FwdAr
   // per-CTA setup and item epilogues overlap the next item's MMAs. Longer rows: one CTA per
   // item, where the hardware's block dispatch balances the causal work at least as well as
   // the static order and the per-item setup is amortised over many key tiles.
-  if (d == 64 && args.n_pairs <= 4 && args.Nk <= 1024) return launch_fwd_p64(q, k, v, o, args, BH, stream);
+  if (d == 64 && args.n_pairs <= 4 && args.Nk <= 1024) return launch_fwd_p64<false>(q, k, v, o, args, BH, stream);
   if (d == 64) return launch_fwd_d<64>(q, k, v, o, args, BH, stream);
   if (d == 128) return launch_fwd_d<128>(q, k, v, o, args, BH, stream);
   return FA_ERR_UNSUPPORTED;
@@ -1180,6 +1230,8 @@ int launch_fwd(const void* q, const void* k, const void* v, void* o, const FwdAr
 
 int launch_fwd_varlen(const void* q, const void* k, const void* v, void* o, const FwdArgs& args, int BH, int d,
                       cudaStream_t stream) {
+  // sequences of at most 1024 rows: the persistent kernel over (query pair, sequence x head)
+  if (d == 64 && args.n_pairs <= 4) return launch_fwd_p64<true>(q, k, v, o, args, BH, stream);
   if (d == 64) return launch_fwd_d<64, false, true>(q, k, v, o, args, BH, stream);
   if (d == 128) return launch_fwd_d<128, false, true>(q, k, v, o, args, BH, stream);
   return FA_ERR_UNSUPPORTED;

@@ -93,3 +93,24 @@ def test_full_size_inference_forward(gpu, name):
     assert torch.equal(o, o_lse)
     r = ref.attention(f64(x["q"]), f64(x["k"]), f64(x["v"]), scale=w.scale, causal=w.causal, backward=False)
     assert_within({"o": compare("o", f64(o), r["o"]), "lse": compare("lse", f64(lse), r["lse"])})
+
+
+def test_full_size_packed_sequences():
+    """The packed bert workload (16 sequences of 128..512 rows, 16 heads, d 64) at full size, in
+    the bench's launch configuration, every (sequence, head) problem against the oracle."""
+    from io_aware_exact_04_gb300 import api
+    w = workloads.WORKLOADS["bert_packed"]
+    x = workloads.make_inputs(w)
+    pk = workloads.pack(x)
+    lens = x["kv_len"].tolist()
+    gpu = torch.device("cuda", 0)
+    q, k, v, do = (pk[n].to(gpu) for n in ("q", "k", "v", "do"))
+    cu = pk["cu_seqlens"].to(gpu)
+    o, lse = api.forward_varlen(q, k, v, cu, max(lens), causal=w.causal)
+    dq, dk, dv = api.backward_varlen(q, k, v, o, do, lse, cu, max(lens), causal=w.causal)
+    torch.cuda.synchronize(gpu)
+    assert api.device_status(gpu)[0] == 0
+    r = ref.attention_varlen(f64(pk["q"]), f64(pk["k"]), f64(pk["v"]), f64(pk["do"]), pk["cu_seqlens"].numpy(),
+                             scale=w.scale, causal=w.causal)
+    assert_within({n: compare(n, f64(t), r[n]) for n, t in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk),
+                                                             ("dv", dv))})

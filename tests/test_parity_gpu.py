@@ -175,9 +175,12 @@ def test_split_key_forward_default_count_matches_plain_forward(gpu):
 # Packed sequences ([H, T, d], cu_seqlens): ragged lengths, an empty sequence, a single row,
 # lengths past one tile pair, both head dims.
 VARLEN = [
-    # H, lengths, d, causal
+    # H, lengths, d, causal (d = 64 with every sequence at most 1024 rows runs the persistent
+    # forward; longer ones, and d = 128, the one-CTA-per-item forward)
     (2, [100, 0, 257, 643], 64, True),
     (3, [1, 384, 129, 7], 64, False),
+    (4, [512, 128, 300, 1, 0, 1024, 77, 256, 640], 64, False),
+    (2, [1500, 37, 900], 64, True),
     (2, [300, 1000], 128, True),
     (1, [64, 65, 200, 513], 128, False),
 ]
