@@ -711,10 +711,11 @@ INFER_METRIC = "attention forward-only TFLOP/s (inference, split keys; bf16, 1×
 
 
 def infer_bytes(w, n_split):
-    """Algorithmic bytes of one split-key forward launch: Q, K, V read (bf16) and each
-    share's fp32 O and LSE written."""
+    """Algorithmic bytes of one split-key forward step: Q, K, V read (bf16), each partial
+    slot's fp32 O and LSE written (two slots a share) and read back by the combine, O written."""
     rows_q = w.B * w.H * w.N
-    return 2 * rows_q * w.d + 2 * 2 * w.B * w.H * w.nk * w.d + n_split * rows_q * (w.d + 1) * 4
+    return (2 * rows_q * w.d + 2 * 2 * w.B * w.H * w.nk * w.d + 2 * 2 * n_split * rows_q * (w.d + 1) * 4
+            + 2 * rows_q * w.d)
 
 
 def run_gpu_infer(args, w):

@@ -129,7 +129,9 @@ FA_API size_t fa_backward_varlen_workspace_size(int B, int H, int T, int d);
  * (divided by its own normaliser, fp32) and LSE into `workspace`. A second
  * kernel joins the shares with the running-maximum rescaling that the tiled
  * softmax applies between key blocks. Shapes, masks and results as
- * fa_forward_qk.
+ * fa_forward_qk. With Nq <= 8 (decode) the keys are cut into 2 * n_split
+ * chunks instead and a streaming kernel on the CUDA cores forms each chunk's
+ * partial result (one query row would waste a 128-row tensor-core tile).
  *  - lse may be NULL: then no LSE is written.
  *  - workspace: at least fa_forward_split_workspace_size(B, H, Nq, d, n_split)
  *    bytes, 256-byte aligned; its contents on entry do not matter.
@@ -144,10 +146,13 @@ FA_API int fa_forward_split(const void* q, const void* k, const void* v, void* o
  * Returns 0 for invalid arguments. */
 FA_API size_t fa_forward_split_workspace_size(int B, int H, int Nq, int d, int n_split);
 
-/* The library's choice of n_split for a shape on the current device. It is 1
- * when B * H * ceil(Nq / 256) work items already reach the SM count. Otherwise
- * it is the largest count whose CTAs fit in two waves (floor(2 * SMs / items)),
- * capped at ceil(Nk / 128) / 4 (four key tiles a share) and at 64. */
+/* The library's choice of n_split for a shape on the current device. For
+ * Nq <= 8 (the decode kernel): round(2 * SMs / (B * H)), capped at Nk / 256
+ * and at 64, at least 1 (about four (head, key chunk) units a persistent CTA,
+ * no chunk under 128 keys). Otherwise it is 1 when B * H * ceil(Nq / 256) work items
+ * already reach the SM count, else the largest count whose CTAs fit in two
+ * waves (floor(2 * SMs / items)), capped at ceil(Nk / 128) / 4 (four key tiles
+ * a share) and at 64. */
 FA_API int fa_forward_split_count(int B, int H, int Nq, int Nk, int d);
 
 /* Bytes of device workspace fa_backward needs: per (b, h), D and a base-2

@@ -247,6 +247,15 @@ int fa_forward_split_count(int B, int H, int Nq, int Nk, int d) {
   if (B <= 0 || H <= 0 || Nq <= 0 || Nk <= 0 || (d != 64 && d != 128)) return 1;
   int sms = 0;
   if (!fa::sm_count(&sms)) return 1;
+  if (Nq <= 8) {
+    // the streaming decode kernel (persistent, one CTA per SM, one chunk of keys per partial
+    // slot, two slots a share): about four work units per CTA (round(2 SMs / (B H)) shares),
+    // at most 64 shares and no chunk under 128 keys
+    const long long bh = (long long)B * H;
+    long long n = (2LL * sms + bh / 2) / bh;
+    n = std::min<long long>(n, std::max(1, Nk / 256));
+    return (int)std::max<long long>(1, std::min<long long>(n, 64));
+  }
   const long long items = (long long)B * H * ((Nq + 255) / 256);
   if (items >= sms) return 1;
   // the most shares whose CTAs still fit in two waves (a partly filled last wave costs as

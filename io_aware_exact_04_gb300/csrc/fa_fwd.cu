@@ -1111,7 +1111,7 @@ __global__ void __launch_bounds__(256) fwd_combine_kernel(FwdArgs a) {
   griddep_launch_dependents();
   constexpr int LPR = D / 8;
   constexpr int RPB = 256 / LPR;
-  constexpr int G = 8;  // slots whose loads are issued together
+  constexpr int G = 16;  // slots whose loads are issued together
   const int part = threadIdx.x % LPR;
   const int n = blockIdx.x * RPB + threadIdx.x / LPR;
   const int bh = blockIdx.y;
@@ -1159,6 +1159,252 @@ __global__ void __launch_bounds__(256) fwd_combine_kernel(FwdArgs a) {
   out.w = pack_bf16x2(acc[6] * inv, acc[7] * inv);
   *reinterpret_cast<uint4*>(a.o + row * D + part * 8) = out;
   if (part == 0 && a.lse) a.lse[row] = (wsum > 0.f) ? mx + lg2_approx(wsum) * 0.6931471805599453f : -INFINITY;
+}
+
+// Decode: few query rows (N_q <= 8) over many keys, the inference shape the pages call memory
+// bound. Such a problem has no dense contraction worth the tensor cores (one query row would
+// fill an M = 128 MMA with padding), so it streams K and V from HBM at copy speed and reduces
+// on the CUDA cores. Persistent: CTA c of G takes work units c, c + G, ... where unit
+// u = bh * n_chunks + z is keys [z chunk, (z + 1) chunk) of head bh. Warp 8 streams the units'
+// 128-key K and V tiles by TMA (128-byte swizzle) through an NS-stage ring, running ahead
+// across unit boundaries. Each of warps 0-7 owns 16 keys of every tile and keeps its own
+// running maximum, normaliser and O, so a tile needs no block-wide synchronisation: lane l
+// scores key l % 16 over half the head dimensions (the halves joined by one shuffle), the
+// warp's maximum and sum go through shuffles, and for P V lane l owns D / 32 dimensions of the
+// warp's 16 keys. The running maximum rescales O and the normaliser between tiles, as between
+// key blocks of the tiled forward. At a unit's end the eight warps' states are joined with the
+// same rescaling through shared memory, and the unit's O / l (fp32) and LSE go to partial slot
+// z, which fwd_combine_kernel joins. 288 threads; NQ >= N_q rows (1, 2, 4 or 8).
+constexpr int kDecodeMaxRows = 8;
+template <int D, int NQ>
+struct DecCfg {
+  static constexpr int NSUB = D / 64;
+  static constexpr int TILE = NSUB * 128 * 128;   // one 128-key tile of K (or V), bf16
+  // static shared memory of the kernel: the queries, the warps' states (m, l, O)
+  static constexpr int STATIC_BYTES = NQ * (D * 4 + 8 * (2 + D) * 4);
+  // ring stages (K and V each): as many as fit beside the static arrays, at most 5
+  static constexpr int NS_FIT = (232448 - STATIC_BYTES - 128 - 1024) / (2 * TILE);
+  static constexpr int NS = NS_FIT < 5 ? NS_FIT : 5;
+  static constexpr int OFF_K = 0, OFF_V = NS * TILE, OFF_BAR = 2 * NS * TILE;
+  static constexpr int SMEM_BYTES = OFF_BAR + 128 + 1024;
+  static_assert(NS >= 2, "decode: at least two ring stages");
+};
+enum { SITE_D_FULL = 11, SITE_D_EMPTY, SITE_D_SYNC };
+
+template <int D, int NQ>
+__global__ void __launch_bounds__(288, 1)
+    decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                  const uint16_t* __restrict__ q, FwdArgs a, int BH, int n_chunks, int chunk) {
+  griddep_wait();
+  griddep_launch_dependents();
+  using C = DecCfg<D, NQ>;
+  constexpr int NS = C::NS, DPL = D / 32, HD = D / 2;  // dims a lane takes in P V; half a row
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = align1024(smem_raw);
+  const uint32_t sbase = smem_u32(sm);
+  __shared__ float4 qs[NQ][D / 4];        // the unit's queries x s log2(e)
+  __shared__ float wm[8][NQ], wl[8][NQ];  // the warps' running maxima and normalisers
+  __shared__ float wo[8][NQ][D];          // ... and O
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::OFF_BAR);
+  const uint32_t b0 = smem_u32(bars);
+  auto full = [&](int s) { return b0 + 8u * s; };
+  auto empty = [&](int s) { return b0 + 8u * (NS + s); };
+  int* abort_flag = reinterpret_cast<int*>(sm + C::OFF_BAR + 8 * 2 * NS);
+  DevStatus st{a.status, abort_flag};
+  const int G = gridDim.x, cta = blockIdx.x;
+  const int nunits = BH * n_chunks;
+  // keys [j0, j1) of unit u and the number of 128-key tiles in it
+  auto unit_keys = [&](int u, int& bh, int& z, int& j0, int& j1) {
+    bh = u / n_chunks;
+    z = u - bh * n_chunks;
+    int kv = a.Nk;
+    if (a.kv_len) kv = min(max(a.kv_len[bh / a.H], 0), a.Nk);
+    j0 = z * chunk;
+    j1 = min(j0 + chunk, kv);
+    return j1 > j0 ? (j1 - j0 + 127) >> 7 : 0;
+  };
+  if (warp == 8) {
+    if (lane == 0) {
+      for (int s = 0; s < NS; ++s) {
+        mbar_init(full(s), 1);
+        mbar_init(empty(s), 8);  // one arrival per consumer warp
+      }
+      *abort_flag = 0;
+      fence_mbar_init();
+    }
+  }
+  __syncthreads();
+  if (warp == 8) {
+    // ------------------------------------------------------------ TMA producer
+    if (elect_one()) {
+      prefetch_tmap(&tm_k);
+      prefetch_tmap(&tm_v);
+    }
+    int g = 0;
+    bool ok = true;
+    for (int u = cta; ok && u < nunits; u += G) {
+      int bh, z, j0, j1;
+      const int nt = unit_keys(u, bh, z, j0, j1);
+      for (int t = 0; t < nt; ++t, ++g) {
+        const int s = g % NS;
+        if (!(ok = wait_warp(empty(s), ((g / NS) & 1) ^ 1, st, SITE_D_EMPTY))) break;
+        if (elect_one()) mbar_arrive_expect_tx(full(s), 2 * C::TILE);
+        for (int c = 0; c < C::NSUB; ++c) {
+          if (elect_one()) tma_load_3d(sbase + C::OFF_K + s * C::TILE + c * 16384, &tm_k, c * 64, j0 + t * 128, bh, full(s));
+          if (elect_one()) tma_load_3d(sbase + C::OFF_V + s * C::TILE + c * 16384, &tm_v, c * 64, j0 + t * 128, bh, full(s));
+        }
+        __syncwarp();
+      }
+    }
+    if (*(volatile int*)abort_flag) {
+      // let copies already in flight land before the CTA's smem is released
+      const uint64_t t0 = globaltimer_ns();
+      for (int gg = max(0, g - NS); gg < g; ++gg)
+        while (!mbar_try_wait(full(gg % NS), (gg / NS) & 1) && globaltimer_ns() - t0 < 100000000ull) {
+        }
+    }
+  } else {
+    // ------------------------------------------------------------ consumers (warps 0-7)
+    const int kl = lane & 15, half = lane >> 4;  // score phase: key of the warp, half of the row
+    const int key = 16 * warp + kl;              // ... within the tile
+    int g = 0;
+    bool ok = true;
+    for (int u = cta; ok && u < nunits; u += G) {
+      int bh, z, j0, j1;
+      const int nt = unit_keys(u, bh, z, j0, j1);
+      const int nq = a.N;
+      for (int idx = tid; idx < NQ * (D / 4); idx += 256) {
+        const int i = idx / (D / 4), c = idx % (D / 4);
+        float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (i < nq) {
+          const uint2 w = *reinterpret_cast<const uint2*>(q + ((size_t)bh * nq + i) * D + 4 * c);
+          f = make_float4(__uint_as_float(w.x << 16) * a.scale_log2, __uint_as_float(w.x & 0xFFFF0000u) * a.scale_log2,
+                          __uint_as_float(w.y << 16) * a.scale_log2, __uint_as_float(w.y & 0xFFFF0000u) * a.scale_log2);
+        }
+        qs[i][c] = f;
+      }
+      if (!(ok = named_bar_and(1, 256, ok))) break;
+      float m[NQ], l[NQ], o[NQ][DPL];
+#pragma unroll
+      for (int i = 0; i < NQ; ++i) {
+        m[i] = -INFINITY, l[i] = 0.f;
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) o[i][e] = 0.f;
+      }
+      bool wok = true;  // this warp's waits (voted at the unit's end)
+      for (int t = 0; t < nt; ++t, ++g) {
+        const int s = g % NS;
+        const int jb = j0 + t * 128;
+        if (!(wok = wait_warp(full(s), (g / NS) & 1, st, SITE_D_FULL))) break;
+        const uint8_t* kt = sm + C::OFF_K + s * C::TILE;
+        const uint8_t* vt = sm + C::OFF_V + s * C::TILE;
+        const int jj = jb + key;
+        const bool valid = jj < j1;
+        // ---- half-row partial scores of this lane's key, joined across the two halves
+        uint4 kr[HD / 8];
+#pragma unroll
+        for (int c = 0; c < HD / 8; ++c) {
+          const int cc = half * (HD / 8) + c;  // 16-byte chunk of the row
+          kr[c] = *reinterpret_cast<const uint4*>(kt + (cc >> 3) * 16384 + sw128_offset(key, cc & 7));
+        }
+        float sc[NQ];
+#pragma unroll
+        for (int i = 0; i < NQ; ++i) {
+          float acc = 0.f;
+          if (i < nq) {
+#pragma unroll
+            for (int c = 0; c < HD / 8; ++c) {
+              const float4 q0 = qs[i][half * (HD / 4) + 2 * c], q1 = qs[i][half * (HD / 4) + 2 * c + 1];
+              const uint32_t w[4] = {kr[c].x, kr[c].y, kr[c].z, kr[c].w};
+              acc = fmaf(q0.x, __uint_as_float(w[0] << 16), acc);
+              acc = fmaf(q0.y, __uint_as_float(w[0] & 0xFFFF0000u), acc);
+              acc = fmaf(q0.z, __uint_as_float(w[1] << 16), acc);
+              acc = fmaf(q0.w, __uint_as_float(w[1] & 0xFFFF0000u), acc);
+              acc = fmaf(q1.x, __uint_as_float(w[2] << 16), acc);
+              acc = fmaf(q1.y, __uint_as_float(w[2] & 0xFFFF0000u), acc);
+              acc = fmaf(q1.z, __uint_as_float(w[3] << 16), acc);
+              acc = fmaf(q1.w, __uint_as_float(w[3] & 0xFFFF0000u), acc);
+            }
+          }
+          acc += __shfl_xor_sync(0xffffffffu, acc, 16);
+          // causal: query i keeps keys j <= i + N_k - N_q; past the chunk's valid keys: none
+          sc[i] = (i < nq && valid && !(a.causal && jj > i + a.coff)) ? acc : -INFINITY;
+        }
+        // ---- the warp's maximum and sum over its 16 keys; rescale; O += P V
+        float p[NQ];
+#pragma unroll
+        for (int i = 0; i < NQ; ++i) {
+          float x = sc[i];
+#pragma unroll
+          for (int sh = 8; sh > 0; sh >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, sh));
+          const float mnew = fmaxf(m[i], x);
+          const float alpha = (mnew == -INFINITY) ? 1.f : ex2_approx(m[i] - mnew);
+          p[i] = (sc[i] == -INFINITY) ? 0.f : ex2_approx(sc[i] - mnew);
+          float y = p[i];
+#pragma unroll
+          for (int sh = 8; sh > 0; sh >>= 1) y += __shfl_xor_sync(0xffffffffu, y, sh);
+          l[i] = l[i] * alpha + y;
+          m[i] = mnew;
+#pragma unroll
+          for (int e = 0; e < DPL; ++e) o[i][e] *= alpha;
+        }
+#pragma unroll
+        for (int kk = 0; kk < 16; ++kk) {
+          const int r = 16 * warp + kk;           // V row
+          const int d0 = lane * DPL;              // this lane's first dimension
+          const int cc = d0 >> 3;                 // its 16-byte chunk
+          const uint8_t* src = vt + (cc >> 3) * 16384 + sw128_offset(r, cc & 7) + (d0 & 7) * 2;
+          uint32_t w[DPL / 2];
+          if (DPL == 2) {
+            w[0] = *reinterpret_cast<const uint32_t*>(src);
+          } else {
+            const uint2 t2 = *reinterpret_cast<const uint2*>(src);
+            w[0] = t2.x;
+            w[DPL / 2 - 1] = t2.y;
+          }
+#pragma unroll
+          for (int i = 0; i < NQ; ++i) {
+            const float pk = __shfl_sync(0xffffffffu, p[i], kk);
+#pragma unroll
+            for (int e = 0; e < DPL / 2; ++e) {
+              o[i][2 * e] = fmaf(pk, __uint_as_float(w[e] << 16), o[i][2 * e]);
+              o[i][2 * e + 1] = fmaf(pk, __uint_as_float(w[e] & 0xFFFF0000u), o[i][2 * e + 1]);
+            }
+          }
+        }
+        // this warp is done with the stage's K and V
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty(s));
+      }
+      // ---- join the eight warps' states and write slot z
+#pragma unroll
+      for (int i = 0; i < NQ; ++i) {
+        if (lane == 0) wm[warp][i] = m[i], wl[warp][i] = l[i];
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) wo[warp][i][lane * DPL + e] = o[i][e];
+      }
+      if (!(ok = named_bar_and(1, 256, wok))) break;
+      const size_t plane = (size_t)BH * nq;
+      for (int idx = tid; idx < nq * D; idx += 256) {
+        const int i = idx / D, d = idx % D;
+        float mx = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) mx = fmaxf(mx, wm[w][i]);
+        float lsum = 0.f, acc = 0.f;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) {
+          const float f = (wm[w][i] == -INFINITY) ? 0.f : ex2_approx(wm[w][i] - mx);
+          lsum = fmaf(wl[w][i], f, lsum);
+          acc = fmaf(wo[w][i][d], f, acc);
+        }
+        const size_t row = (size_t)z * plane + (size_t)bh * nq + i;
+        a.part_o[row * D + d] = (lsum > 0.f) ? acc / lsum : 0.f;
+        if (d == 0) a.part_lse[row] = (lsum > 0.f) ? (mx + lg2_approx(lsum)) * 0.6931471805599453f : -INFINITY;
+      }
+      if (!(ok = named_bar_and(1, 256, ok))) break;  // qs and the warps' states are rewritten next
+    }
+  }
 }
 
 // BH = B * H work items per query pair. VL: the tensors are [H, T, d] (rows of all sequences
@@ -1240,8 +1486,39 @@ int launch_fwd_varlen(const void* q, const void* k, const void* v, void* o, cons
 int launch_fwd_split(const void* q, const void* k, const void* v, void* o, const FwdArgs& args, int BH, int d,
                      cudaStream_t stream) {
   if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
-  int rc = (d == 64) ? launch_fwd_d<64, true>(q, k, v, o, args, BH, stream)
-                     : launch_fwd_d<128, true>(q, k, v, o, args, BH, stream);
+  int rc;
+  if (args.N <= kDecodeMaxRows) {
+    // decode: the streaming persistent kernel, one chunk of keys per partial slot
+    const int nz = 2 * args.n_split;
+    const int chunk = (args.Nk + nz - 1) / nz;
+    CUtensorMap mk, mv;
+    const auto BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const auto SW = CU_TENSOR_MAP_SWIZZLE_128B;
+    if (!make_tmap_3d(&mk, k, BF, 2, d, (uint64_t)args.Nk, BH, 64, 128, SW) ||
+        !make_tmap_3d(&mv, v, BF, 2, d, (uint64_t)args.Nk, BH, 64, 128, SW))
+      return cuda_fail("cuTensorMapEncodeTiled", 0, "tensor map rejected");
+    int sms = 0;
+    if (!sm_count(&sms)) return FA_ERR_CUDA;
+    const long long units = (long long)BH * nz;
+    const dim3 grid((unsigned)std::min<long long>(units, sms));
+    const auto* qq = static_cast<const uint16_t*>(q);
+    auto go = [&](auto kernel, int smem) {
+      const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      if (e != cudaSuccess) return cuda_fail("cudaFuncSetAttribute", (int)e, cudaGetErrorName(e));
+      return launch_pdl("decode_kernel", kernel, grid, dim3(288), (size_t)smem, stream, mk, mv, qq, args, BH, nz,
+                        chunk);
+    };
+    const int r = args.N;
+#define FA_DEC(DD, NN) go(decode_kernel<DD, NN>, DecCfg<DD, NN>::SMEM_BYTES)
+    if (d == 64)
+      rc = r <= 1 ? FA_DEC(64, 1) : r <= 2 ? FA_DEC(64, 2) : r <= 4 ? FA_DEC(64, 4) : FA_DEC(64, 8);
+    else
+      rc = r <= 1 ? FA_DEC(128, 1) : r <= 2 ? FA_DEC(128, 2) : r <= 4 ? FA_DEC(128, 4) : FA_DEC(128, 8);
+#undef FA_DEC
+  } else {
+    rc = (d == 64) ? launch_fwd_d<64, true>(q, k, v, o, args, BH, stream)
+                   : launch_fwd_d<128, true>(q, k, v, o, args, BH, stream);
+  }
   if (rc != FA_OK) return rc;
   const int rpb = 256 / (d / 8);
   const dim3 grid((unsigned)((args.N + rpb - 1) / rpb), (unsigned)BH);

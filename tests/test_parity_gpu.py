@@ -139,6 +139,12 @@ SPLIT = [
     (3, 1, 64, 1000, 64, False, [1000, 0, 17], 6, True),  # a batch without any valid key
     (2, 2, 16, 5000, 128, True, None, 7, False),
     (1, 2, 1, 700, 64, True, None, 1, False),          # one share, no LSE: still the split path
+    # N_q <= 8: the streaming decode kernel (2 n_split chunks of keys)
+    (4, 3, 1, 8192, 64, True, None, 8, True),
+    (2, 2, 4, 3000, 128, True, [3000, 1], 5, True),       # causal offset over 4 rows, a one-key batch
+    (2, 3, 8, 777, 64, False, [0, 500], 3, False),        # a batch without any valid key
+    (1, 1, 3, 100, 64, True, None, 64, True),             # more chunks than keys: empty chunks
+    (3, 2, 2, 1024, 128, False, None, 2, False),
 ]
 
 
