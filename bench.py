@@ -714,7 +714,8 @@ def infer_bytes(w, n_split):
     """Algorithmic bytes of one split-key forward step: Q, K, V read (bf16), each partial
     slot's fp32 O and LSE written (two slots a share) and read back by the combine, O written."""
     rows_q = w.B * w.H * w.N
-    return (2 * rows_q * w.d + 2 * 2 * w.B * w.H * w.nk * w.d + 2 * 2 * n_split * rows_q * (w.d + 1) * 4
+    slots = 0 if (w.N <= 8 and n_split == 1) else 2 * n_split  # decode with one chunk a head: none
+    return (2 * rows_q * w.d + 2 * 2 * w.B * w.H * w.nk * w.d + 2 * slots * rows_q * (w.d + 1) * 4
             + 2 * rows_q * w.d)
 
 

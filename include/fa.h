@@ -129,15 +129,17 @@ FA_API size_t fa_backward_varlen_workspace_size(int B, int H, int T, int d);
  * (divided by its own normaliser, fp32) and LSE into `workspace`. A second
  * kernel joins the shares with the running-maximum rescaling that the tiled
  * softmax applies between key blocks. Shapes, masks and results as
- * fa_forward_qk. With Nq <= 8 (decode) the keys are cut into 2 * n_split
- * chunks instead and a streaming kernel on the CUDA cores forms each chunk's
- * partial result (one query row would waste a 128-row tensor-core tile).
+ * fa_forward_qk. With Nq <= 8 (decode) a streaming kernel on the CUDA cores
+ * runs instead (one query row would waste a 128-row tensor-core tile): the keys
+ * are cut into 2 * n_split chunks whose partial results the second kernel
+ * joins, or, with n_split = 1, each head is one chunk and its O and LSE are
+ * written directly (no second kernel).
  *  - lse may be NULL: then no LSE is written.
  *  - workspace: at least fa_forward_split_workspace_size(B, H, Nq, d, n_split)
  *    bytes, 256-byte aligned; its contents on entry do not matter.
  *  - n_split >= 1 (more than 1024 returns FA_ERR_UNSUPPORTED). With
- *    n_split = 1 and lse non-NULL this is fa_forward_qk and the workspace is
- *    not touched. */
+ *    n_split = 1, Nq > 8 and lse non-NULL this is fa_forward_qk and the
+ *    workspace is not touched. */
 FA_API int fa_forward_split(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq,
                             int Nk, int d, float scale, int causal, const int32_t* kv_len, int n_split,
                             void* workspace, size_t workspace_bytes, fa_stream_t stream);
@@ -147,9 +149,10 @@ FA_API int fa_forward_split(const void* q, const void* k, const void* v, void* o
 FA_API size_t fa_forward_split_workspace_size(int B, int H, int Nq, int d, int n_split);
 
 /* The library's choice of n_split for a shape on the current device. For
- * Nq <= 8 (the decode kernel): round(2 * SMs / (B * H)), capped at Nk / 256
- * and at 64, at least 1 (about four (head, key chunk) units a persistent CTA,
- * no chunk under 128 keys). Otherwise it is 1 when B * H * ceil(Nq / 256) work items
+ * Nq <= 8 (the decode kernel): 1 when 2 * B * H >= SMs (one chunk a head,
+ * no second kernel), else round(2 * SMs / (B * H)), capped at Nk / 256 and at
+ * 64, at least 1 (about four (head, key chunk) units a persistent CTA, no
+ * chunk under 128 keys). Otherwise it is 1 when B * H * ceil(Nq / 256) work items
  * already reach the SM count, else the largest count whose CTAs fit in two
  * waves (floor(2 * SMs / items)), capped at ceil(Nk / 128) / 4 (four key tiles
  * a share) and at 64. */

@@ -248,10 +248,12 @@ int fa_forward_split_count(int B, int H, int Nq, int Nk, int d) {
   int sms = 0;
   if (!fa::sm_count(&sms)) return 1;
   if (Nq <= 8) {
-    // the streaming decode kernel (persistent, one CTA per SM, one chunk of keys per partial
-    // slot, two slots a share): about four work units per CTA (round(2 SMs / (B H)) shares),
-    // at most 64 shares and no chunk under 128 keys
+    // the streaming decode kernel (persistent, one CTA per SM): with at least half as many
+    // heads as SMs, one chunk a head (n_split = 1: no partial slots, no combine); otherwise one
+    // chunk of keys per partial slot, two slots a share, about four (head, chunk) units a CTA
+    // (round(2 SMs / (B H)) shares), at most 64 shares and no chunk under 128 keys
     const long long bh = (long long)B * H;
+    if (2 * bh >= sms) return 1;
     long long n = (2LL * sms + bh / 2) / bh;
     n = std::min<long long>(n, std::max(1, Nk / 256));
     return (int)std::max<long long>(1, std::min<long long>(n, 64));
@@ -272,8 +274,10 @@ int fa_forward_split(const void* q, const void* k, const void* v, void* o, float
   if (rc != FA_OK) return rc;
   if (n_split < 1) return FA_ERR_INVALID_ARG;
   if (n_split > 1024) return FA_ERR_UNSUPPORTED;
-  // one share with an LSE to write: the plain forward (no workspace used)
-  if (n_split == 1 && lse) return fa_forward_qk(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, kv_len, stream);
+  // one share with an LSE to write: the plain forward (no workspace used); decode rows (Nq <= 8)
+  // keep the streaming decode kernel, which then writes o and lse itself
+  if (n_split == 1 && lse && Nq > 8)
+    return fa_forward_qk(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, kv_len, stream);
   if ((long long)B * H * Nq == 0) return FA_OK;
   if (!q || !k || !v || !o || !workspace) return FA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || (lse && !aligned16(lse)))

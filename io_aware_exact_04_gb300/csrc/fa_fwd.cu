@@ -1174,7 +1174,8 @@ __global__ void __launch_bounds__(256) fwd_combine_kernel(FwdArgs a) {
 // warp's 16 keys. The running maximum rescales O and the normaliser between tiles, as between
 // key blocks of the tiled forward. At a unit's end the eight warps' states are joined with the
 // same rescaling through shared memory, and the unit's O / l (fp32) and LSE go to partial slot
-// z, which fwd_combine_kernel joins. 288 threads; NQ >= N_q rows (1, 2, 4 or 8).
+// z, which fwd_combine_kernel joins; with one chunk a head (n_chunks = 1) the unit's O (bf16)
+// and LSE are final and go straight to o and lse. 288 threads; NQ >= N_q rows (1, 2, 4 or 8).
 constexpr int kDecodeMaxRows = 8;
 template <int D, int NQ>
 struct DecCfg {
@@ -1398,9 +1399,17 @@ __global__ void __launch_bounds__(288, 1)
           lsum = fmaf(wl[w][i], f, lsum);
           acc = fmaf(wo[w][i][d], f, acc);
         }
-        const size_t row = (size_t)z * plane + (size_t)bh * nq + i;
-        a.part_o[row * D + d] = (lsum > 0.f) ? acc / lsum : 0.f;
-        if (d == 0) a.part_lse[row] = (lsum > 0.f) ? (mx + lg2_approx(lsum)) * 0.6931471805599453f : -INFINITY;
+        const float lse = (lsum > 0.f) ? (mx + lg2_approx(lsum)) * 0.6931471805599453f : -INFINITY;
+        const float ov = (lsum > 0.f) ? acc / lsum : 0.f;
+        if (n_chunks == 1) {  // the unit is the whole head: its result is final
+          const size_t row = (size_t)bh * nq + i;
+          a.o[row * D + d] = (uint16_t)(pack_bf16x2(ov, 0.f) & 0xFFFFu);
+          if (d == 0 && a.lse) a.lse[row] = lse;
+        } else {
+          const size_t row = (size_t)z * plane + (size_t)bh * nq + i;
+          a.part_o[row * D + d] = ov;
+          if (d == 0) a.part_lse[row] = lse;
+        }
       }
       if (!(ok = named_bar_and(1, 256, ok))) break;  // qs and the warps' states are rewritten next
     }
@@ -1488,8 +1497,9 @@ int launch_fwd_split(const void* q, const void* k, const void* v, void* o, const
   if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
   int rc;
   if (args.N <= kDecodeMaxRows) {
-    // decode: the streaming persistent kernel, one chunk of keys per partial slot
-    const int nz = 2 * args.n_split;
+    // decode: the streaming persistent kernel, one chunk of keys per partial slot (one chunk a
+    // head when n_split = 1: then no slots and no combine)
+    const int nz = args.n_split == 1 ? 1 : 2 * args.n_split;
     const int chunk = (args.Nk + nz - 1) / nz;
     CUtensorMap mk, mv;
     const auto BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
@@ -1520,6 +1530,7 @@ int launch_fwd_split(const void* q, const void* k, const void* v, void* o, const
                    : launch_fwd_d<128, true>(q, k, v, o, args, BH, stream);
   }
   if (rc != FA_OK) return rc;
+  if (args.N <= kDecodeMaxRows && args.n_split == 1) return FA_OK;  // decode wrote o and lse
   const int rpb = 256 / (d / 8);
   const dim3 grid((unsigned)((args.N + rpb - 1) / rpb), (unsigned)BH);
   return (d == 64) ? launch_pdl("fwd_combine_kernel", fwd_combine_kernel<64>, grid, dim3(256), 0, stream, args)

@@ -145,6 +145,8 @@ SPLIT = [
     (2, 3, 8, 777, 64, False, [0, 500], 3, False),        # a batch without any valid key
     (1, 1, 3, 100, 64, True, None, 64, True),             # more chunks than keys: empty chunks
     (3, 2, 2, 1024, 128, False, None, 2, False),
+    (2, 3, 2, 1500, 128, True, [1500, 900], 1, True),    # one chunk a head: O and LSE written directly
+    (3, 2, 1, 2000, 64, False, [0, 2000, 129], 1, False),
 ]
 
 
