@@ -446,29 +446,34 @@ __global__ void __launch_bounds__(352, 1)
             m_run = m_tile;
           }
         }
-        if (C::SEP_P && j > 0) {
-          // PV_t(j-1) has finished reading P_t(j-1) (and updating O_t) before both are touched
-          if (!(ok = wait_warp(o_done(t), (j - 1) & 1, st, SITE_F_O_DONE))) break;
-          tc_fence_after();
-        }
         const float base = (m_run == -INFINITY) ? 0.f : m_run;
         // P = exp2(S s log2e - base): the argument of two columns per fma.f32x2,
         // the row sum in two paired partial sums
         const uint64_t sl2x2 = f2_pack(sl2, sl2), nbase2 = f2_pack(-base, -base);
         uint64_t ps2[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
+        uint32_t pk[4][16];
 #pragma unroll
         for (int h = 0; h < 4; ++h) {  // 32 columns -> 16 packed bf16x2 words per store
-          uint32_t pk[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             float x0, x1;
             f2_unpack(f2_fma(f2_pack(sv[h * 32 + 2 * i], sv[h * 32 + 2 * i + 1]), sl2x2, nbase2), x0, x1);
             const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
             ps2[i & 1] = f2_add(ps2[i & 1], f2_pack(p0, p1));
-            pk[i] = pack_bf16x2(p0, p1);
+            pk[h][i] = pack_bf16x2(p0, p1);
           }
-          tmem_st16(tP + h * 16, pk);
+          if (C::SEP_P && h == 1) {
+            // separate P buffer: half of P is formed before PV_t(j-1) must be done with it
+            if (j > 0) {
+              if (!(ok = wait_warp(o_done(t), (j - 1) & 1, st, SITE_F_O_DONE))) break;
+              tc_fence_after();
+            }
+            tmem_st16(tP, pk[0]);
+            tmem_st16(tP + 16, pk[1]);
+          }
+          if (!C::SEP_P || h >= 2) tmem_st16(tP + h * 16, pk[h]);
         }
+        if (!ok) break;
         float ps[4];
         f2_unpack(ps2[0], ps[0], ps[1]);
         f2_unpack(ps2[1], ps[2], ps[3]);
@@ -993,29 +998,34 @@ __global__ void __launch_bounds__(352, 1)
               m_run = m_tile;
             }
           }
-          if (j > 0) {
-            // PV_t(j-1) has finished reading P_t(j-1) (and updating O_t) before both are touched
-            if (!(ok = wait_warp(o_done(t), par ^ 1, st, SITE_F_O_DONE))) break;
-            tc_fence_after();
-          }
           const float base = (m_run == -INFINITY) ? 0.f : m_run;
           // P = exp2(S s log2e - base): the argument of two columns per fma.f32x2,
           // the row sum in two paired partial sums
           const uint64_t sl2x2 = f2_pack(sl2, sl2), nbase2 = f2_pack(-base, -base);
           uint64_t ps2[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
+          uint32_t pk[4][16];
 #pragma unroll
           for (int h = 0; h < 4; ++h) {  // 32 columns -> 16 packed bf16x2 words per store
-            uint32_t pk[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
               float x0, x1;
               f2_unpack(f2_fma(f2_pack(sv[h * 32 + 2 * i], sv[h * 32 + 2 * i + 1]), sl2x2, nbase2), x0, x1);
               const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
               ps2[i & 1] = f2_add(ps2[i & 1], f2_pack(p0, p1));
-              pk[i] = pack_bf16x2(p0, p1);
+              pk[h][i] = pack_bf16x2(p0, p1);
             }
-            tmem_st16(tP + h * 16, pk);
+            if (h == 1) {
+              // half of P is formed before PV_t(j-1) must be done with P_t
+              if (j > 0) {
+                if (!(ok = wait_warp(o_done(t), par ^ 1, st, SITE_F_O_DONE))) break;
+                tc_fence_after();
+              }
+              tmem_st16(tP, pk[0]);
+              tmem_st16(tP + 16, pk[1]);
+            }
+            if (h >= 2) tmem_st16(tP + h * 16, pk[h]);
           }
+          if (!ok) break;
           float ps[4];
           f2_unpack(ps2[0], ps[0], ps[1]);
           f2_unpack(ps2[1], ps[2], ps[3]);
