@@ -715,13 +715,28 @@ INFER_METRIC = "attention forward-only TFLOP/s (inference, split keys; bf16, 1×
 INFER_ROTATE_BYTES = 800 << 20  # inference inputs rotated over copies of at least this much in all
 
 
-def infer_bytes(w, n_split):
-    """Algorithmic bytes of one split-key forward step: Q, K, V read (bf16), each partial
-    slot's fp32 O and LSE written (two slots a share) and read back by the combine, O written."""
+def infer_bytes(w):
+    """Algorithmic bytes of one inference forward step: Q, K and V read once (bf16), O written
+    (bf16). The partial results that a split head's CTAs exchange are not counted."""
     rows_q = w.B * w.H * w.N
-    slots = 0 if (w.N <= 8 and n_split == 1) else 2 * n_split  # decode with one chunk a head: none
-    return (2 * rows_q * w.d + 2 * 2 * w.B * w.H * w.nk * w.d + 2 * slots * rows_q * (w.d + 1) * 4
-            + 2 * rows_q * w.d)
+    return 2 * rows_q * w.d + 2 * 2 * w.B * w.H * w.nk * w.d + 2 * rows_q * w.d
+
+
+def infer_launches(w, n_split, sms, has_kv_len):
+    """Kernels one fa_forward_split call launches. Decode (N_q <= 8) with n_split = 1: whole
+    heads a CTA, one kernel. With n_split > 1: the stream-K kernel over G = min(SMs, 256,
+    n_split B H, T) CTAs, plus the join of split heads when key padding is given or some CTA's
+    run of key tiles starts inside a head. Otherwise: the split kernel and its combine
+    (n_split = 1 with an LSE is the plain forward, which the bench does not use)."""
+    if w.N > 8:
+        return 2
+    if n_split == 1:
+        return 1
+    bh, t_head = w.B * w.H, -(-w.nk // 128)
+    t_max = max(1, bh * t_head)
+    G = max(1, min(sms, 256, n_split * bh, t_max))
+    split = has_kv_len or any((c * t_max // G) % t_head for c in range(1, G))
+    return 2 if split else 1
 
 
 def run_gpu_infer(args, w):
@@ -769,6 +784,10 @@ def run_gpu_infer(args, w):
     detail = (ctypes.c_int * 4)()
     if lib.fa_get_last_device_status_detail(sp, detail) != 0:
         raise RuntimeError(f"device status after warm-up: {list(detail)}")
+    # The K steps run back to back between one pair of events, as a decode loop runs them (each
+    # launch may start while the previous one drains); a second pass times every step between
+    # events of its own (which serialises the launches) for comparison.
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     step_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
     sampler = ClockSampler(local if "CUDA_VISIBLE_DEVICES" not in os.environ else 0)
     if rank == 0:
@@ -778,27 +797,34 @@ def run_gpu_infer(args, w):
         torch.distributed.barrier()
     torch.cuda.synchronize(dev)
     sampler.mark("t_start")
+    ev0.record(stream)
+    for i in range(args.steps):
+        step(i)
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    sampler.mark("t_stop")
+    if ws > 1:
+        torch.distributed.barrier()
+    total_ms = ev0.elapsed_time(ev1)
     for i in range(args.steps):
         step_ev[i][0].record(stream)
         step(i)
         step_ev[i][1].record(stream)
     torch.cuda.synchronize(dev)
-    sampler.mark("t_stop")
-    if ws > 1:
-        torch.distributed.barrier()
-    total_ms = sum(e[0].elapsed_time(e[1]) for e in step_ev)
+    isolated_ms = sum(e[0].elapsed_time(e[1]) for e in step_ev) / args.steps
     fwd_flops = 4.0 * d * workloads.visible_pairs(N, Nk, w.causal) * B * H
     ms_step, rate = job_throughput(total_ms / args.steps, fwd_flops, device=dev)
     value = rate / 1e12
     # roofline of the step's two launches together (the combine reads back only the shares'
     # small fp32 rows): algorithmic bytes over the event-timed step
-    bytes_alg = infer_bytes(w, n_split)
+    bytes_alg = infer_bytes(w)
     achieved = bytes_alg / (ms_step * 1e-3) / 1e9
     peak = float(peaks["hbm_gbs"])
-    roof = {"bound": "hbm", "kernel": "fwd_split+combine (whole step)", "achieved": achieved, "peak": peak,
+    roof = {"bound": "hbm", "kernel": "decode_kernel (+ join of split heads): whole step", "achieved": achieved, "peak": peak,
             "unit": "GB/s", "frac": achieved / peak, "traffic": traffic_record("fwd_split", w.name),
             "peak_source": f"{peak_src} hbm_gbs (copy)", "avg_launch_ms": ms_step,
-            "bytes_per_launch": bytes_alg}
+            "bytes_per_launch": bytes_alg,
+            "isolated_step_ms": isolated_ms, "isolated_frac": bytes_alg / (isolated_ms * 1e-3) / 1e9 / peak}
     # end to end through host buffers
     hq, hk, hv = (x[n].pin_memory() for n in ("q", "k", "v"))
     ho = torch.empty_like(hq).pin_memory()
@@ -833,13 +859,16 @@ def run_gpu_infer(args, w):
                    "n_split": n_split, "lse": False,
                    "l2": f"no flush: inputs larger than L2, rotated over {R} copies ({R * in_bytes / 1e6:.0f} MB), "
                          "so a step's inputs were last read R - 1 steps earlier",
+                   "timing": "K steps back to back between one event pair (isolated_step_ms: an event pair "
+                             "around every step)",
                    "flops": "nominal forward 4*P*d per head, P = visible query-key pairs",
                    "parallelism": f"replicas x{ws} (heads independent)"},
         "roofline": roof,
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_rate / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_ms, "steps": e2e_steps},
-        "gpu_launches": (2 if n_split > 1 else 1) * args.steps,
+        "gpu_launches": infer_launches(w, n_split, torch.cuda.get_device_properties(dev).multi_processor_count,
+                                       kv is not None) * args.steps,
         "clocks": clocks,
     }
     print(json.dumps(line), flush=True)

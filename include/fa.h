@@ -130,10 +130,15 @@ FA_API size_t fa_backward_varlen_workspace_size(int B, int H, int T, int d);
  * kernel joins the shares with the running-maximum rescaling that the tiled
  * softmax applies between key blocks. Shapes, masks and results as
  * fa_forward_qk. With Nq <= 8 (decode) a streaming kernel on the CUDA cores
- * runs instead (one query row would waste a 128-row tensor-core tile): the keys
- * are cut into 2 * n_split chunks whose partial results the second kernel
- * joins, or, with n_split = 1, each head is one chunk and its O and LSE are
- * written directly (no second kernel).
+ * runs instead (one query row would waste a 128-row tensor-core tile). It
+ * takes the 128-key tiles of all heads as one sequence. With n_split = 1 each
+ * CTA takes ceil(B * H / min(#SMs, 256)) whole heads and writes their O and LSE
+ * directly (no second kernel, the workspace is not touched). With n_split > 1
+ * each of G = min(#SMs, 256, n_split * B * H) CTAs takes an equal run of the
+ * sequence; a head whose tiles all fall to one CTA is written directly, the
+ * partial results of a head split between CTAs go to the workspace and a
+ * second kernel joins them. That second kernel runs whenever kv_len is given
+ * (the tile counts are on the device) or some CTA's run starts inside a head.
  *  - lse may be NULL: then no LSE is written.
  *  - workspace: at least fa_forward_split_workspace_size(B, H, Nq, d, n_split)
  *    bytes, 256-byte aligned; its contents on entry do not matter.
@@ -144,15 +149,15 @@ FA_API int fa_forward_split(const void* q, const void* k, const void* v, void* o
                             int Nk, int d, float scale, int causal, const int32_t* kv_len, int n_split,
                             void* workspace, size_t workspace_bytes, fa_stream_t stream);
 
-/* Workspace bytes of fa_forward_split: 2 * n_split * B * H * Nq rows of d + 1 fp32.
+/* Workspace bytes of fa_forward_split: 2 * n_split * B * H * Nq rows of d + 1 fp32
+ * (the decode kernel uses 2 G * Nq of them, G <= n_split * B * H).
  * Returns 0 for invalid arguments. */
 FA_API size_t fa_forward_split_workspace_size(int B, int H, int Nq, int d, int n_split);
 
 /* The library's choice of n_split for a shape on the current device. For
- * Nq <= 8 (the decode kernel): 1 when 2 * B * H >= SMs (one chunk a head,
- * no second kernel), else round(2 * SMs / (B * H)), capped at Nk / 256 and at
- * 64, at least 1 (about four (head, key chunk) units a persistent CTA, no
- * chunk under 128 keys). Otherwise it is 1 when B * H * ceil(Nq / 256) work items
+ * Nq <= 8 (the decode kernel): 1 (whole heads a CTA) when 2 * B * H >= SMs, else
+ * ceil(SMs / (B * H)), at most 64, so that the decode kernel runs one CTA per SM.
+ * Otherwise it is 1 when B * H * ceil(Nq / 256) work items
  * already reach the SM count, else the largest count whose CTAs fit in two
  * waves (floor(2 * SMs / items)), capped at ceil(Nk / 128) / 4 (four key tiles
  * a share) and at 64. */

@@ -248,15 +248,12 @@ int fa_forward_split_count(int B, int H, int Nq, int Nk, int d) {
   int sms = 0;
   if (!fa::sm_count(&sms)) return 1;
   if (Nq <= 8) {
-    // the streaming decode kernel (persistent, one CTA per SM): with at least half as many
-    // heads as SMs, one chunk a head (n_split = 1: no partial slots, no combine); otherwise one
-    // chunk of keys per partial slot, two slots a share, about four (head, chunk) units a CTA
-    // (round(2 SMs / (B H)) shares), at most 64 shares and no chunk under 128 keys
+    // the streaming decode kernel: with heads for at least half the SMs, whole heads a CTA
+    // (n_split = 1, no join: the stream is memory-bound there already); fewer heads are cut
+    // between min(#SMs, n_split B H) CTAs, enough shares for one CTA per SM
     const long long bh = (long long)B * H;
     if (2 * bh >= sms) return 1;
-    long long n = (2LL * sms + bh / 2) / bh;
-    n = std::min<long long>(n, std::max(1, Nk / 256));
-    return (int)std::max<long long>(1, std::min<long long>(n, 64));
+    return (int)std::max<long long>(1, std::min<long long>((sms + bh - 1) / bh, 64));
   }
   const long long items = (long long)B * H * ((Nq + 255) / 256);
   if (items >= sms) return 1;

@@ -23,6 +23,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
+
 #include "common.cuh"
 #include "fa_internal.h"
 #include "tmap.h"
@@ -1174,19 +1176,29 @@ __global__ void __launch_bounds__(256) fwd_combine_kernel(FwdArgs a) {
 // Decode: few query rows (N_q <= 8) over many keys, the inference shape the pages call memory
 // bound. Such a problem has no dense contraction worth the tensor cores (one query row would
 // fill an M = 128 MMA with padding), so it streams K and V from HBM at copy speed and reduces
-// on the CUDA cores. Persistent: CTA c of G takes work units c, c + G, ... where unit
-// u = bh * n_chunks + z is keys [z chunk, (z + 1) chunk) of head bh. Warp 8 streams the units'
-// 128-key K and V tiles by TMA (128-byte swizzle) through an NS-stage ring, running ahead
-// across unit boundaries. Each of warps 0-7 owns 16 keys of every tile and keeps its own
-// running maximum, normaliser and O, so a tile needs no block-wide synchronisation: lane l
-// scores key l % 16 over half the head dimensions (the halves joined by one shuffle), the
-// warp's maximum and sum go through shuffles, and for P V lane l owns D / 32 dimensions of the
-// warp's 16 keys. The running maximum rescales O and the normaliser between tiles, as between
-// key blocks of the tiled forward. At a unit's end the eight warps' states are joined with the
-// same rescaling through shared memory, and the unit's O / l (fp32) and LSE go to partial slot
-// z, which fwd_combine_kernel joins; with one chunk a head (n_chunks = 1) the unit's O (bf16)
-// and LSE are final and go straight to o and lse. 288 threads; NQ >= N_q rows (1, 2, 4 or 8).
+// on the CUDA cores.
+//
+// Work decomposition: the 128-key tiles of all heads, head after head, form one sequence of T
+// tiles, of which each CTA takes a contiguous run. With hpc > 0, CTA c takes the hpc whole
+// heads [hpc c, hpc (c + 1)). With hpc = 0 (stream-K), CTA c of G takes tiles
+// [c T / G, (c + 1) T / G), so every SM gets the same number of tiles whatever the head count.
+// The tiles of one head inside a CTA's run form a segment. A segment that covers its whole head
+// writes the head's O (bf16) and LSE directly; otherwise it is a partial result (O / l in fp32
+// and its LSE) in partial slot 2c (the CTA's first segment) or 2c + 1 (its last), and
+// decode_combine_kernel joins the segments of each such head. Heads with no valid key are
+// written O = 0, LSE = -inf here.
+//
+// Within a CTA, warp 8 streams the segments' 128-key K and V tiles by TMA (128-byte swizzle)
+// through an NS-stage ring, running ahead across segment boundaries. Each of warps 0-7 owns
+// 16 keys of every tile and keeps its own running maximum, normaliser and O, so a tile needs
+// no block-wide synchronisation: lane l scores key l % 16 over half the head dimensions (the
+// halves joined by one shuffle), the warp's maximum and sum go through shuffles, and for P V
+// lane l owns D / 32 dimensions of the warp's 16 keys. The running maximum rescales O and the
+// normaliser between tiles, as between key blocks of the tiled forward. At a segment's end
+// the eight warps' states are joined with the same rescaling through shared memory. 288
+// threads; NQ >= N_q rows (1, 2, 4 or 8).
 constexpr int kDecodeMaxRows = 8;
+constexpr int kDecodeMaxCtas = 256;  // CTAs of the decode kernel at most (the join's slot list)
 template <int D, int NQ>
 struct DecCfg {
   static constexpr int NSUB = D / 64;
@@ -1202,18 +1214,79 @@ struct DecCfg {
 };
 enum { SITE_D_FULL = 11, SITE_D_EMPTY, SITE_D_SYNC };
 
+// 128-key tiles of each head of batch b: its valid keys, rounded up.
+__device__ __forceinline__ int dec_tiles(const FwdArgs& a, int b) {
+  int kv = a.Nk;
+  if (a.kv_len) kv = min(max(a.kv_len[b], 0), a.Nk);
+  return (kv + 127) >> 7;
+}
+
+// Position in the tile sequence of all heads: head h of batch b has tb tiles, its tile 0 is
+// global tile gbase. b == B: past the last head.
+struct DecCursor {
+  int b, h, tb;
+  long long gbase;
+};
+
+// The head that holds global tile g (g < T).
+__device__ DecCursor dec_seek(const FwdArgs& a, int B, long long g) {
+  DecCursor c{0, 0, 0, 0};
+  for (; c.b < B; ++c.b) {
+    c.tb = dec_tiles(a, c.b);
+    const long long span = (long long)a.H * c.tb;
+    if (g < c.gbase + span) {
+      c.h = (int)((g - c.gbase) / c.tb);
+      c.gbase += (long long)c.h * c.tb;
+      return c;
+    }
+    c.gbase += span;
+  }
+  c.tb = 0;
+  return c;
+}
+
+// The next head that has tiles.
+__device__ void dec_next_head(const FwdArgs& a, int B, DecCursor& c) {
+  c.gbase += c.tb;
+  if (++c.h < a.H) return;
+  c.h = 0;
+  do {
+    ++c.b;
+    c.tb = (c.b < B) ? dec_tiles(a, c.b) : 0;
+  } while (c.b < B && c.tb == 0);
+}
+
+// T, the tiles of all heads.
+__device__ long long dec_total(const FwdArgs& a, int B) {
+  if (!a.kv_len) return (long long)B * a.H * ((a.Nk + 127) >> 7);
+  long long t = 0;
+  for (int b = 0; b < B; ++b) t += dec_tiles(a, b);
+  return t * a.H;
+}
+
+// Global index of the first tile of head bh (bh = B H: T).
+__device__ long long dec_head_base(const FwdArgs& a, int B, int bh) {
+  const int b = bh / a.H, h = bh - b * a.H;
+  if (!a.kv_len) return (long long)bh * ((a.Nk + 127) >> 7);
+  long long t = 0;
+  for (int bb = 0; bb < b; ++bb) t += dec_tiles(a, bb);
+  return t * a.H + (b < B ? (long long)h * dec_tiles(a, b) : 0);
+}
+
 template <int D, int NQ>
 __global__ void __launch_bounds__(288, 1)
     decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                  const uint16_t* __restrict__ q, FwdArgs a, int BH, int n_chunks, int chunk) {
+                  const uint16_t* __restrict__ q, FwdArgs a, int B, int hpc) {
   griddep_wait();
   griddep_launch_dependents();
   using C = DecCfg<D, NQ>;
   constexpr int NS = C::NS, DPL = D / 32, HD = D / 2;  // dims a lane takes in P V; half a row
+  // key-major lanes (each lane its own key's O half-row) while NQ half-rows of O fit in registers
+  constexpr bool KM = NQ * D <= 128;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1024(smem_raw);
   const uint32_t sbase = smem_u32(sm);
-  __shared__ float4 qs[NQ][D / 4];        // the unit's queries x s log2(e)
+  __shared__ float4 qs[NQ][D / 4];        // the segment's queries x s log2(e)
   __shared__ float wm[8][NQ], wl[8][NQ];  // the warps' running maxima and normalisers
   __shared__ float wo[8][NQ][D];          // ... and O
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -1224,17 +1297,17 @@ __global__ void __launch_bounds__(288, 1)
   int* abort_flag = reinterpret_cast<int*>(sm + C::OFF_BAR + 8 * 2 * NS);
   DevStatus st{a.status, abort_flag};
   const int G = gridDim.x, cta = blockIdx.x;
-  const int nunits = BH * n_chunks;
-  // keys [j0, j1) of unit u and the number of 128-key tiles in it
-  auto unit_keys = [&](int u, int& bh, int& z, int& j0, int& j1) {
-    bh = u / n_chunks;
-    z = u - bh * n_chunks;
-    int kv = a.Nk;
-    if (a.kv_len) kv = min(max(a.kv_len[bh / a.H], 0), a.Nk);
-    j0 = z * chunk;
-    j1 = min(j0 + chunk, kv);
-    return j1 > j0 ? (j1 - j0 + 127) >> 7 : 0;
-  };
+  const int BH = B * a.H, nq = a.N;
+  // this CTA's tiles [g0, g1) of the sequence of all heads' tiles: heads [hpc c, hpc (c + 1))
+  // whole, or (hpc = 0) the c-th of G equal runs
+  long long g0, g1;
+  if (hpc > 0) {
+    g0 = dec_head_base(a, B, min(cta * hpc, BH));
+    g1 = dec_head_base(a, B, min((cta + 1) * hpc, BH));
+  } else {
+    const long long T = dec_total(a, B);
+    g0 = (long long)cta * T / G, g1 = (long long)(cta + 1) * T / G;
+  }
   if (warp == 8) {
     if (lane == 0) {
       for (int s = 0; s < NS; ++s) {
@@ -1252,20 +1325,25 @@ __global__ void __launch_bounds__(288, 1)
       prefetch_tmap(&tm_k);
       prefetch_tmap(&tm_v);
     }
-    int g = 0;
+    int g = 0;  // ring tiles issued
     bool ok = true;
-    for (int u = cta; ok && u < nunits; u += G) {
-      int bh, z, j0, j1;
-      const int nt = unit_keys(u, bh, z, j0, j1);
-      for (int t = 0; t < nt; ++t, ++g) {
-        const int s = g % NS;
-        if (!(ok = wait_warp(empty(s), ((g / NS) & 1) ^ 1, st, SITE_D_EMPTY))) break;
-        if (elect_one()) mbar_arrive_expect_tx(full(s), 2 * C::TILE);
-        for (int c = 0; c < C::NSUB; ++c) {
-          if (elect_one()) tma_load_3d(sbase + C::OFF_K + s * C::TILE + c * 16384, &tm_k, c * 64, j0 + t * 128, bh, full(s));
-          if (elect_one()) tma_load_3d(sbase + C::OFF_V + s * C::TILE + c * 16384, &tm_v, c * 64, j0 + t * 128, bh, full(s));
+    if (g0 < g1) {
+      DecCursor cur = dec_seek(a, B, g0);
+      for (long long gt = g0; ok && gt < g1;) {
+        const int bh = cur.b * a.H + cur.h;
+        const int ta = (int)(gt - cur.gbase), te = (int)min(g1 - cur.gbase, (long long)cur.tb);
+        for (int t = ta; t < te; ++t, ++g) {
+          const int s = g % NS;
+          if (!(ok = wait_warp(empty(s), ((g / NS) & 1) ^ 1, st, SITE_D_EMPTY))) break;
+          if (elect_one()) mbar_arrive_expect_tx(full(s), 2 * C::TILE);
+          for (int c = 0; c < C::NSUB; ++c) {
+            if (elect_one()) tma_load_3d(sbase + C::OFF_K + s * C::TILE + c * 16384, &tm_k, c * 64, t * 128, bh, full(s));
+            if (elect_one()) tma_load_3d(sbase + C::OFF_V + s * C::TILE + c * 16384, &tm_v, c * 64, t * 128, bh, full(s));
+          }
+          __syncwarp();
         }
-        __syncwarp();
+        gt = cur.gbase + te;
+        if (te == cur.tb) dec_next_head(a, B, cur);
       }
     }
     if (*(volatile int*)abort_flag) {
@@ -1277,14 +1355,26 @@ __global__ void __launch_bounds__(288, 1)
     }
   } else {
     // ------------------------------------------------------------ consumers (warps 0-7)
+    // heads without a valid key: O = 0, LSE = -inf (heads cta, cta + G, ...)
+    for (int bh = cta; bh < BH; bh += G) {
+      if (dec_tiles(a, bh / a.H) > 0) continue;
+      for (int idx = tid; idx < nq * D; idx += 256) {
+        const size_t row = (size_t)bh * nq + idx / D;
+        a.o[row * D + idx % D] = 0;
+        if (idx % D == 0 && a.lse) a.lse[row] = -INFINITY;
+      }
+    }
     const int kl = lane & 15, half = lane >> 4;  // score phase: key of the warp, half of the row
     const int key = 16 * warp + kl;              // ... within the tile
     int g = 0;
     bool ok = true;
-    for (int u = cta; ok && u < nunits; u += G) {
-      int bh, z, j0, j1;
-      const int nt = unit_keys(u, bh, z, j0, j1);
-      const int nq = a.N;
+    DecCursor cur{};
+    if (g0 < g1) cur = dec_seek(a, B, g0);
+    for (long long gt = g0, seg = 0; ok && gt < g1; ++seg) {
+      const int bh = cur.b * a.H + cur.h;
+      const int ta = (int)(gt - cur.gbase), te = (int)min(g1 - cur.gbase, (long long)cur.tb);
+      const int kv = a.kv_len ? min(max(a.kv_len[cur.b], 0), a.Nk) : a.Nk;
+      const int j1 = min(te * 128, kv);  // the segment's keys end here
       for (int idx = tid; idx < NQ * (D / 4); idx += 256) {
         const int i = idx / (D / 4), c = idx % (D / 4);
         float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -1296,107 +1386,203 @@ __global__ void __launch_bounds__(288, 1)
         qs[i][c] = f;
       }
       if (!(ok = named_bar_and(1, 256, ok))) break;
-      float m[NQ], l[NQ], o[NQ][DPL];
-#pragma unroll
-      for (int i = 0; i < NQ; ++i) {
-        m[i] = -INFINITY, l[i] = 0.f;
-#pragma unroll
-        for (int e = 0; e < DPL; ++e) o[i][e] = 0.f;
-      }
-      bool wok = true;  // this warp's waits (voted at the unit's end)
-      for (int t = 0; t < nt; ++t, ++g) {
-        const int s = g % NS;
-        const int jb = j0 + t * 128;
-        if (!(wok = wait_warp(full(s), (g / NS) & 1, st, SITE_D_FULL))) break;
-        const uint8_t* kt = sm + C::OFF_K + s * C::TILE;
-        const uint8_t* vt = sm + C::OFF_V + s * C::TILE;
-        const int jj = jb + key;
-        const bool valid = jj < j1;
-        // ---- half-row partial scores of this lane's key, joined across the two halves
-        uint4 kr[HD / 8];
-#pragma unroll
-        for (int c = 0; c < HD / 8; ++c) {
-          const int cc = half * (HD / 8) + c;  // 16-byte chunk of the row
-          kr[c] = *reinterpret_cast<const uint4*>(kt + (cc >> 3) * 16384 + sw128_offset(key, cc & 7));
-        }
-        float sc[NQ];
+      bool wok = true;  // this warp's waits (voted at the segment's end)
+      if constexpr (KM) {
+        // ---- key-major: lane (kl, half) owns key kl of the warp's 16 in every tile and the
+        //      head dimensions [half HD, half HD + HD) of its O. Each lane keeps its own
+        //      reference maximum, normaliser and O (lazily rescaled: the reference moves only when
+        //      a score exceeds it by more than 8, i.e. a factor 256), so a tile needs no reduction
+        //      across lanes; the 16 lanes of each half are joined once, at the segment's end.
+        float m[NQ], l[NQ], o[NQ][HD];
 #pragma unroll
         for (int i = 0; i < NQ; ++i) {
-          float acc = 0.f;
-          if (i < nq) {
+          m[i] = -INFINITY, l[i] = 0.f;
 #pragma unroll
-            for (int c = 0; c < HD / 8; ++c) {
-              const float4 q0 = qs[i][half * (HD / 4) + 2 * c], q1 = qs[i][half * (HD / 4) + 2 * c + 1];
-              const uint32_t w[4] = {kr[c].x, kr[c].y, kr[c].z, kr[c].w};
-              acc = fmaf(q0.x, __uint_as_float(w[0] << 16), acc);
-              acc = fmaf(q0.y, __uint_as_float(w[0] & 0xFFFF0000u), acc);
-              acc = fmaf(q0.z, __uint_as_float(w[1] << 16), acc);
-              acc = fmaf(q0.w, __uint_as_float(w[1] & 0xFFFF0000u), acc);
-              acc = fmaf(q1.x, __uint_as_float(w[2] << 16), acc);
-              acc = fmaf(q1.y, __uint_as_float(w[2] & 0xFFFF0000u), acc);
-              acc = fmaf(q1.z, __uint_as_float(w[3] << 16), acc);
-              acc = fmaf(q1.w, __uint_as_float(w[3] & 0xFFFF0000u), acc);
-            }
-          }
-          acc += __shfl_xor_sync(0xffffffffu, acc, 16);
-          // causal: query i keeps keys j <= i + N_k - N_q; past the chunk's valid keys: none
-          sc[i] = (i < nq && valid && !(a.causal && jj > i + a.coff)) ? acc : -INFINITY;
+          for (int e = 0; e < HD; ++e) o[i][e] = 0.f;
         }
-        // ---- the warp's maximum and sum over its 16 keys; rescale; O += P V
-        float p[NQ];
+        for (int t = ta; t < te; ++t, ++g) {
+          const int s = g % NS;
+          if (!(wok = wait_warp(full(s), (g / NS) & 1, st, SITE_D_FULL))) break;
+          const uint8_t* kt = sm + C::OFF_K + s * C::TILE;
+          const uint8_t* vt = sm + C::OFF_V + s * C::TILE;
+          const int jj = t * 128 + key;
+          const bool valid = jj < j1;
+          uint4 kr[HD / 8], vr[HD / 8];
 #pragma unroll
-        for (int i = 0; i < NQ; ++i) {
-          float x = sc[i];
-#pragma unroll
-          for (int sh = 8; sh > 0; sh >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, sh));
-          const float mnew = fmaxf(m[i], x);
-          const float alpha = (mnew == -INFINITY) ? 1.f : ex2_approx(m[i] - mnew);
-          p[i] = (sc[i] == -INFINITY) ? 0.f : ex2_approx(sc[i] - mnew);
-          float y = p[i];
-#pragma unroll
-          for (int sh = 8; sh > 0; sh >>= 1) y += __shfl_xor_sync(0xffffffffu, y, sh);
-          l[i] = l[i] * alpha + y;
-          m[i] = mnew;
-#pragma unroll
-          for (int e = 0; e < DPL; ++e) o[i][e] *= alpha;
-        }
-#pragma unroll
-        for (int kk = 0; kk < 16; ++kk) {
-          const int r = 16 * warp + kk;           // V row
-          const int d0 = lane * DPL;              // this lane's first dimension
-          const int cc = d0 >> 3;                 // its 16-byte chunk
-          const uint8_t* src = vt + (cc >> 3) * 16384 + sw128_offset(r, cc & 7) + (d0 & 7) * 2;
-          uint32_t w[DPL / 2];
-          if (DPL == 2) {
-            w[0] = *reinterpret_cast<const uint32_t*>(src);
-          } else {
-            const uint2 t2 = *reinterpret_cast<const uint2*>(src);
-            w[0] = t2.x;
-            w[DPL / 2 - 1] = t2.y;
+          for (int c = 0; c < HD / 8; ++c) {
+            const int cc = half * (HD / 8) + c;  // 16-byte chunk of the row
+            const int off = (cc >> 3) * 16384 + sw128_offset(key, cc & 7);
+            kr[c] = *reinterpret_cast<const uint4*>(kt + off);
+            vr[c] = *reinterpret_cast<const uint4*>(vt + off);
           }
+          // this lane's K and V rows are in registers: the stage may be refilled
+          __syncwarp();
+          if (lane == 0) mbar_arrive(empty(s));
 #pragma unroll
           for (int i = 0; i < NQ; ++i) {
-            const float pk = __shfl_sync(0xffffffffu, p[i], kk);
+            uint64_t acc2 = f2_pack(0.f, 0.f);
+            if (i < nq) {
 #pragma unroll
-            for (int e = 0; e < DPL / 2; ++e) {
-              o[i][2 * e] = fmaf(pk, __uint_as_float(w[e] << 16), o[i][2 * e]);
-              o[i][2 * e + 1] = fmaf(pk, __uint_as_float(w[e] & 0xFFFF0000u), o[i][2 * e + 1]);
+              for (int c = 0; c < HD / 8; ++c) {
+                const float4 q0 = qs[i][half * (HD / 4) + 2 * c], q1 = qs[i][half * (HD / 4) + 2 * c + 1];
+                const uint32_t w[4] = {kr[c].x, kr[c].y, kr[c].z, kr[c].w};
+                acc2 = f2_fma(f2_pack(q0.x, q0.y), f2_pack(__uint_as_float(w[0] << 16), __uint_as_float(w[0] & 0xFFFF0000u)), acc2);
+                acc2 = f2_fma(f2_pack(q0.z, q0.w), f2_pack(__uint_as_float(w[1] << 16), __uint_as_float(w[1] & 0xFFFF0000u)), acc2);
+                acc2 = f2_fma(f2_pack(q1.x, q1.y), f2_pack(__uint_as_float(w[2] << 16), __uint_as_float(w[2] & 0xFFFF0000u)), acc2);
+                acc2 = f2_fma(f2_pack(q1.z, q1.w), f2_pack(__uint_as_float(w[3] << 16), __uint_as_float(w[3] & 0xFFFF0000u)), acc2);
+              }
+            }
+            float a0, a1;
+            f2_unpack(acc2, a0, a1);
+            float acc = a0 + a1;
+            acc += __shfl_xor_sync(0xffffffffu, acc, 16);
+            // causal: query i keeps keys j <= i + N_k - N_q; past the head's valid keys: none
+            const float sc = (i < nq && valid && !(a.causal && jj > i + a.coff)) ? acc : -INFINITY;
+            if (sc > m[i] + 8.f) {  // both lanes of a key take the same branch
+              const float alpha = (m[i] == -INFINITY) ? 0.f : ex2_approx(m[i] - sc);
+              l[i] *= alpha;
+#pragma unroll
+              for (int e = 0; e < HD; ++e) o[i][e] *= alpha;
+              m[i] = sc;
+            }
+            const float p = (sc == -INFINITY) ? 0.f : ex2_approx(sc - m[i]);
+            l[i] += p;
+            const uint64_t p2 = f2_pack(p, p);
+#pragma unroll
+            for (int c = 0; c < HD / 8; ++c) {
+              const uint32_t w[4] = {vr[c].x, vr[c].y, vr[c].z, vr[c].w};
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                const uint64_t r2 = f2_fma(p2, f2_pack(__uint_as_float(w[u] << 16), __uint_as_float(w[u] & 0xFFFF0000u)),
+                                           f2_pack(o[i][8 * c + 2 * u], o[i][8 * c + 2 * u + 1]));
+                f2_unpack(r2, o[i][8 * c + 2 * u], o[i][8 * c + 2 * u + 1]);
+              }
             }
           }
         }
-        // this warp is done with the stage's K and V
-        __syncwarp();
-        if (lane == 0) mbar_arrive(empty(s));
-      }
-      // ---- join the eight warps' states and write slot z
+        // ---- join the 16 lanes of each half (same dimensions, different keys), then publish
+        //      the warp's state: lane 0 the maximum and normaliser, lanes 0 and 16 their halves of O
 #pragma unroll
-      for (int i = 0; i < NQ; ++i) {
-        if (lane == 0) wm[warp][i] = m[i], wl[warp][i] = l[i];
+        for (int i = 0; i < NQ; ++i) {
+          float mx = m[i];
 #pragma unroll
-        for (int e = 0; e < DPL; ++e) wo[warp][i][lane * DPL + e] = o[i][e];
+          for (int sh = 1; sh < 16; sh <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, sh));
+          const float f = (m[i] == -INFINITY) ? 0.f : ex2_approx(m[i] - mx);
+          float ls = l[i] * f;
+#pragma unroll
+          for (int sh = 1; sh < 16; sh <<= 1) ls += __shfl_xor_sync(0xffffffffu, ls, sh);
+#pragma unroll
+          for (int e = 0; e < HD; ++e) {
+            float x = o[i][e] * f;
+#pragma unroll
+            for (int sh = 1; sh < 16; sh <<= 1) x += __shfl_xor_sync(0xffffffffu, x, sh);
+            if (kl == 0) wo[warp][i][half * HD + e] = x;
+          }
+          if (lane == 0) wm[warp][i] = mx, wl[warp][i] = ls;
+        }
+      } else {
+        float m[NQ], l[NQ], o[NQ][DPL];
+#pragma unroll
+        for (int i = 0; i < NQ; ++i) {
+          m[i] = -INFINITY, l[i] = 0.f;
+#pragma unroll
+          for (int e = 0; e < DPL; ++e) o[i][e] = 0.f;
+        }
+        for (int t = ta; t < te; ++t, ++g) {
+          const int s = g % NS;
+          const int jb = t * 128;
+          if (!(wok = wait_warp(full(s), (g / NS) & 1, st, SITE_D_FULL))) break;
+          const uint8_t* kt = sm + C::OFF_K + s * C::TILE;
+          const uint8_t* vt = sm + C::OFF_V + s * C::TILE;
+          const int jj = jb + key;
+          const bool valid = jj < j1;
+          // ---- half-row partial scores of this lane's key, joined across the two halves
+          uint4 kr[HD / 8];
+#pragma unroll
+          for (int c = 0; c < HD / 8; ++c) {
+            const int cc = half * (HD / 8) + c;  // 16-byte chunk of the row
+            kr[c] = *reinterpret_cast<const uint4*>(kt + (cc >> 3) * 16384 + sw128_offset(key, cc & 7));
+          }
+          float sc[NQ];
+#pragma unroll
+          for (int i = 0; i < NQ; ++i) {
+            float acc = 0.f;
+            if (i < nq) {
+#pragma unroll
+              for (int c = 0; c < HD / 8; ++c) {
+                const float4 q0 = qs[i][half * (HD / 4) + 2 * c], q1 = qs[i][half * (HD / 4) + 2 * c + 1];
+                const uint32_t w[4] = {kr[c].x, kr[c].y, kr[c].z, kr[c].w};
+                acc = fmaf(q0.x, __uint_as_float(w[0] << 16), acc);
+                acc = fmaf(q0.y, __uint_as_float(w[0] & 0xFFFF0000u), acc);
+                acc = fmaf(q0.z, __uint_as_float(w[1] << 16), acc);
+                acc = fmaf(q0.w, __uint_as_float(w[1] & 0xFFFF0000u), acc);
+                acc = fmaf(q1.x, __uint_as_float(w[2] << 16), acc);
+                acc = fmaf(q1.y, __uint_as_float(w[2] & 0xFFFF0000u), acc);
+                acc = fmaf(q1.z, __uint_as_float(w[3] << 16), acc);
+                acc = fmaf(q1.w, __uint_as_float(w[3] & 0xFFFF0000u), acc);
+              }
+            }
+            acc += __shfl_xor_sync(0xffffffffu, acc, 16);
+            // causal: query i keeps keys j <= i + N_k - N_q; past the head's valid keys: none
+            sc[i] = (i < nq && valid && !(a.causal && jj > i + a.coff)) ? acc : -INFINITY;
+          }
+          // ---- the warp's maximum and sum over its 16 keys; rescale; O += P V
+          float p[NQ];
+#pragma unroll
+          for (int i = 0; i < NQ; ++i) {
+            float x = sc[i];
+#pragma unroll
+            for (int sh = 8; sh > 0; sh >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, sh));
+            const float mnew = fmaxf(m[i], x);
+            const float alpha = (mnew == -INFINITY) ? 1.f : ex2_approx(m[i] - mnew);
+            p[i] = (sc[i] == -INFINITY) ? 0.f : ex2_approx(sc[i] - mnew);
+            float y = p[i];
+#pragma unroll
+            for (int sh = 8; sh > 0; sh >>= 1) y += __shfl_xor_sync(0xffffffffu, y, sh);
+            l[i] = l[i] * alpha + y;
+            m[i] = mnew;
+#pragma unroll
+            for (int e = 0; e < DPL; ++e) o[i][e] *= alpha;
+          }
+#pragma unroll
+          for (int kk = 0; kk < 16; ++kk) {
+            const int r = 16 * warp + kk;           // V row
+            const int d0 = lane * DPL;              // this lane's first dimension
+            const int cc = d0 >> 3;                 // its 16-byte chunk
+            const uint8_t* src = vt + (cc >> 3) * 16384 + sw128_offset(r, cc & 7) + (d0 & 7) * 2;
+            uint32_t w[DPL / 2];
+            if (DPL == 2) {
+              w[0] = *reinterpret_cast<const uint32_t*>(src);
+            } else {
+              const uint2 t2 = *reinterpret_cast<const uint2*>(src);
+              w[0] = t2.x;
+              w[DPL / 2 - 1] = t2.y;
+            }
+#pragma unroll
+            for (int i = 0; i < NQ; ++i) {
+              const float pk = __shfl_sync(0xffffffffu, p[i], kk);
+#pragma unroll
+              for (int e = 0; e < DPL / 2; ++e) {
+                o[i][2 * e] = fmaf(pk, __uint_as_float(w[e] << 16), o[i][2 * e]);
+                o[i][2 * e + 1] = fmaf(pk, __uint_as_float(w[e] & 0xFFFF0000u), o[i][2 * e + 1]);
+              }
+            }
+          }
+          // this warp is done with the stage's K and V
+          __syncwarp();
+          if (lane == 0) mbar_arrive(empty(s));
+        }
+        // ---- join the eight warps' states; whole head: O and LSE, else partial slot 2c or 2c + 1
+#pragma unroll
+        for (int i = 0; i < NQ; ++i) {
+          if (lane == 0) wm[warp][i] = m[i], wl[warp][i] = l[i];
+#pragma unroll
+          for (int e = 0; e < DPL; ++e) wo[warp][i][lane * DPL + e] = o[i][e];
+        }
       }
       if (!(ok = named_bar_and(1, 256, wok))) break;
-      const size_t plane = (size_t)BH * nq;
+      const bool whole = (ta == 0 && te == cur.tb);
+      const int slot = 2 * cta + (seg == 0 ? 0 : 1);
       for (int idx = tid; idx < nq * D; idx += 256) {
         const int i = idx / D, d = idx % D;
         float mx = -INFINITY;
@@ -1411,18 +1597,105 @@ __global__ void __launch_bounds__(288, 1)
         }
         const float lse = (lsum > 0.f) ? (mx + lg2_approx(lsum)) * 0.6931471805599453f : -INFINITY;
         const float ov = (lsum > 0.f) ? acc / lsum : 0.f;
-        if (n_chunks == 1) {  // the unit is the whole head: its result is final
+        if (whole) {
           const size_t row = (size_t)bh * nq + i;
           a.o[row * D + d] = (uint16_t)(pack_bf16x2(ov, 0.f) & 0xFFFFu);
           if (d == 0 && a.lse) a.lse[row] = lse;
         } else {
-          const size_t row = (size_t)z * plane + (size_t)bh * nq + i;
+          const size_t row = (size_t)slot * nq + i;
           a.part_o[row * D + d] = ov;
           if (d == 0) a.part_lse[row] = lse;
         }
       }
       if (!(ok = named_bar_and(1, 256, ok))) break;  // qs and the warps' states are rewritten next
+      gt = cur.gbase + te;
+      if (te == cur.tb) dec_next_head(a, B, cur);
     }
+  }
+}
+
+// Joins the segments of each head that decode_kernel split between CTAs (grid: one block per
+// head). The head's tiles are global tiles [gs, ge); CTA c of G took [c T / G, (c + 1) T / G),
+// so the owner of tile g is ((g + 1) G - 1) / T. The first owner's segment is in its slot 2c
+// when its range starts at gs, else in 2c + 1 (its last segment); every later CTA with tiles up
+// to the owner of ge - 1 holds its first segment in slot 2c. With L_z the segments' LSEs and
+// M their maximum: LSE = M + ln sum_z e^(L_z - M), O = sum_z e^(L_z - LSE) O_z, each O_z
+// already divided by its own normaliser; segments with no visible key (L_z = -inf) drop out.
+// The slot list and the LSEs go through shared memory, so each thread's loads of O_z are
+// independent of one another (two memory round trips in all). G <= kDecodeMaxCtas.
+template <int D>
+__global__ void __launch_bounds__(256) decode_combine_kernel(FwdArgs a, int B, int G) {
+  griddep_wait();
+  griddep_launch_dependents();
+  const int bh = blockIdx.x, b = bh / a.H, h = bh - b * a.H, tid = threadIdx.x;
+  const int tb = dec_tiles(a, b);
+  if (tb == 0) return;
+  // T and the tiles of the batches before b, summed over the block
+  __shared__ long long part[2][8];
+  __shared__ int slots[kDecodeMaxCtas];
+  __shared__ float lses[kDecodeMaxCtas][kDecodeMaxRows];
+  __shared__ float wmax[kDecodeMaxRows];
+  long long sT = 0, sB = 0;
+  if (a.kv_len) {
+    for (int bb = tid; bb < B; bb += 256) {
+      const long long x = (long long)a.H * dec_tiles(a, bb);
+      sT += x;
+      if (bb < b) sB += x;
+    }
+  } else if (tid == 0) {
+    sT = (long long)B * a.H * tb;
+    sB = (long long)b * a.H * tb;
+  }
+#pragma unroll
+  for (int sh = 16; sh > 0; sh >>= 1) {
+    sT += __shfl_xor_sync(0xffffffffu, sT, sh);
+    sB += __shfl_xor_sync(0xffffffffu, sB, sh);
+  }
+  if ((tid & 31) == 0) part[0][tid >> 5] = sT, part[1][tid >> 5] = sB;
+  __syncthreads();
+  long long T = 0, gs = 0;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) T += part[0][w], gs += part[1][w];
+  gs += (long long)h * tb;
+  const long long ge = gs + tb;
+  const int clo = (int)(((gs + 1) * G - 1) / T), chi = (int)((ge * G - 1) / T);
+  if (clo == chi) return;  // one CTA held the whole head and wrote it
+  const int nseg = chi - clo + 1, nq = a.N;
+  // entry e: CTA clo + e, its slot (or -1: a CTA without tiles)
+  if (tid < nseg) {
+    const int c = clo + tid;
+    const long long st0 = (long long)c * T / G, st1 = (long long)(c + 1) * T / G;
+    slots[tid] = (tid > 0 && st0 == st1) ? -1 : (tid == 0 && st0 < gs) ? 2 * c + 1 : 2 * c;
+  }
+  __syncthreads();
+  for (int idx = tid; idx < nseg * nq; idx += 256) {
+    const int e = idx / nq, i = idx - e * nq;
+    lses[e][i] = slots[e] < 0 ? -INFINITY : a.part_lse[(size_t)slots[e] * nq + i];
+  }
+  __syncthreads();
+  if (tid < nq) {
+    float mx = -INFINITY;
+    for (int e = 0; e < nseg; ++e) mx = fmaxf(mx, lses[e][tid]);
+    wmax[tid] = mx;
+  }
+  __syncthreads();
+  for (int idx = tid; idx < nq * D; idx += 256) {
+    const int i = idx / D, d = idx - i * D;
+    const float mx = wmax[i];
+    float wsum = 0.f, acc = 0.f;
+    if (mx != -INFINITY) {
+#pragma unroll 4
+      for (int e = 0; e < nseg; ++e) {
+        const float lz = lses[e][i];
+        const float w = (lz == -INFINITY) ? 0.f : ex2_approx((lz - mx) * 1.4426950408889634f);
+        const float oz = (w > 0.f) ? a.part_o[((size_t)slots[e] * nq + i) * D + d] : 0.f;
+        wsum += w;
+        acc = fmaf(w, oz, acc);
+      }
+    }
+    const size_t row = (size_t)bh * nq + i;
+    a.o[row * D + d] = (uint16_t)(pack_bf16x2(wsum > 0.f ? acc / wsum : 0.f, 0.f) & 0xFFFFu);
+    if (d == 0 && a.lse) a.lse[row] = (wsum > 0.f) ? mx + lg2_approx(wsum) * 0.6931471805599453f : -INFINITY;
   }
 }
 
@@ -1502,15 +1775,35 @@ int launch_fwd_varlen(const void* q, const void* k, const void* v, void* o, cons
   return FA_ERR_UNSUPPORTED;
 }
 
+// The CTAs of the decode kernel. n_split = 1: whole heads, hpc = ceil(B H / min(#SMs, 256))
+// of them a CTA, never a join. n_split > 1: stream-K over G = min(#SMs, 256, n_split B H, T_max)
+// CTAs (T_max: the tiles of all heads at N_k keys each), so that the 2 G partial slots fit the
+// workspace of n_split shares; whether some head may be split between CTAs is written to
+// *split (always, with key padding: the tile counts are on the device).
+static int decode_grid(const FwdArgs& args, int BH, int sms, int* hpc, bool* split) {
+  const long long cap = std::min(sms, kDecodeMaxCtas);
+  if (args.n_split == 1) {
+    *hpc = (int)((BH + cap - 1) / cap);
+    *split = false;
+    return (BH + *hpc - 1) / *hpc;
+  }
+  *hpc = 0;
+  const long long t_head = (args.Nk + 127) / 128;
+  const long long t_max = std::max<long long>(1, BH * t_head);
+  const int G = (int)std::max<long long>(1, std::min<long long>({cap, (long long)args.n_split * BH, t_max}));
+  *split = args.kv_len != nullptr;
+  for (int c = 1; c < G && !*split; ++c)  // without padding a head splits where a CTA starts inside it
+    if ((long long)c * t_max / G % t_head != 0) *split = true;
+  return G;
+}
+
 int launch_fwd_split(const void* q, const void* k, const void* v, void* o, const FwdArgs& args, int BH, int d,
                      cudaStream_t stream) {
   if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
   int rc;
   if (args.N <= kDecodeMaxRows) {
-    // decode: the streaming persistent kernel, one chunk of keys per partial slot (one chunk a
-    // head when n_split = 1: then no slots and no combine)
-    const int nz = args.n_split == 1 ? 1 : 2 * args.n_split;
-    const int chunk = (args.Nk + nz - 1) / nz;
+    // decode: the streaming stream-K kernel over all heads' key tiles, then (if a head was split
+    // between CTAs) the join of its segments
     CUtensorMap mk, mv;
     const auto BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     const auto SW = CU_TENSOR_MAP_SWIZZLE_128B;
@@ -1519,14 +1812,16 @@ int launch_fwd_split(const void* q, const void* k, const void* v, void* o, const
       return cuda_fail("cuTensorMapEncodeTiled", 0, "tensor map rejected");
     int sms = 0;
     if (!sm_count(&sms)) return FA_ERR_CUDA;
-    const long long units = (long long)BH * nz;
-    const dim3 grid((unsigned)std::min<long long>(units, sms));
+    bool split = false;
+    int hpc = 0;
+    const int G = decode_grid(args, BH, sms, &hpc, &split);
+    const int B = BH / args.H;
     const auto* qq = static_cast<const uint16_t*>(q);
     auto go = [&](auto kernel, int smem) {
       const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
       if (e != cudaSuccess) return cuda_fail("cudaFuncSetAttribute", (int)e, cudaGetErrorName(e));
-      return launch_pdl("decode_kernel", kernel, grid, dim3(288), (size_t)smem, stream, mk, mv, qq, args, BH, nz,
-                        chunk);
+      return launch_pdl("decode_kernel", kernel, dim3(G), dim3(288), (size_t)smem, stream, mk, mv, qq, args, B,
+                        hpc);
     };
     const int r = args.N;
 #define FA_DEC(DD, NN) go(decode_kernel<DD, NN>, DecCfg<DD, NN>::SMEM_BYTES)
@@ -1535,12 +1830,15 @@ int launch_fwd_split(const void* q, const void* k, const void* v, void* o, const
     else
       rc = r <= 1 ? FA_DEC(128, 1) : r <= 2 ? FA_DEC(128, 2) : r <= 4 ? FA_DEC(128, 4) : FA_DEC(128, 8);
 #undef FA_DEC
-  } else {
-    rc = (d == 64) ? launch_fwd_d<64, true>(q, k, v, o, args, BH, stream)
-                   : launch_fwd_d<128, true>(q, k, v, o, args, BH, stream);
+    if (rc != FA_OK || !split) return rc;
+    return (d == 64) ? launch_pdl("decode_combine_kernel", decode_combine_kernel<64>, dim3(BH), dim3(256), 0, stream,
+                                  args, B, G)
+                     : launch_pdl("decode_combine_kernel", decode_combine_kernel<128>, dim3(BH), dim3(256), 0, stream,
+                                  args, B, G);
   }
+  rc = (d == 64) ? launch_fwd_d<64, true>(q, k, v, o, args, BH, stream)
+                 : launch_fwd_d<128, true>(q, k, v, o, args, BH, stream);
   if (rc != FA_OK) return rc;
-  if (args.N <= kDecodeMaxRows && args.n_split == 1) return FA_OK;  // decode wrote o and lse
   const int rpb = 256 / (d / 8);
   const dim3 grid((unsigned)((args.N + rpb - 1) / rpb), (unsigned)BH);
   return (d == 64) ? launch_pdl("fwd_combine_kernel", fwd_combine_kernel<64>, grid, dim3(256), 0, stream, args)

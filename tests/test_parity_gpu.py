@@ -139,14 +139,21 @@ SPLIT = [
     (3, 1, 64, 1000, 64, False, [1000, 0, 17], 6, True),  # a batch without any valid key
     (2, 2, 16, 5000, 128, True, None, 7, False),
     (1, 2, 1, 700, 64, True, None, 1, False),          # one share, no LSE: still the split path
-    # N_q <= 8: the streaming decode kernel (2 n_split chunks of keys)
-    (4, 3, 1, 8192, 64, True, None, 8, True),
+    # N_q <= 8: the streaming decode kernel. n_split = 1: whole heads a CTA; n_split > 1:
+    # min(SMs, 256, n_split B H) CTAs over all heads' key tiles, split heads joined
+    (4, 3, 1, 8192, 64, True, None, 8, True),             # heads split between CTAs
     (2, 2, 4, 3000, 128, True, [3000, 1], 5, True),       # causal offset over 4 rows, a one-key batch
     (2, 3, 8, 777, 64, False, [0, 500], 3, False),        # a batch without any valid key
-    (1, 1, 3, 100, 64, True, None, 64, True),             # more chunks than keys: empty chunks
+    (1, 1, 3, 100, 64, True, None, 64, True),             # one tile, one CTA
     (3, 2, 2, 1024, 128, False, None, 2, False),
-    (2, 3, 2, 1500, 128, True, [1500, 900], 1, True),    # one chunk a head: O and LSE written directly
+    (2, 3, 2, 1500, 128, True, [1500, 900], 1, True),    # whole heads, padded
     (3, 2, 1, 2000, 64, False, [0, 2000, 129], 1, False),
+    (2, 4, 1, 1024, 64, False, None, 1, True),            # one CTA a whole head
+    (20, 10, 1, 300, 64, True, None, 1, True),            # more heads than SMs: two whole heads a CTA
+    (20, 10, 2, 300, 64, True, [300, 1, 0, 257] * 5, 2, True),  # ... stream-K runs across heads, padded
+    (1, 1, 2, 20000, 64, True, None, 64, True),           # one head cut into 64 segments
+    (2, 2, 1, 640, 128, False, [0, 0], 2, True),          # no valid key anywhere
+    (1, 3, 1, 9000, 128, False, None, 1, True),           # whole heads, d = 128, one query row
 ]
 
 
