@@ -821,7 +821,7 @@ def run_gpu_infer(args, w):
     achieved = bytes_alg / (ms_step * 1e-3) / 1e9
     peak = float(peaks["hbm_gbs"])
     roof = {"bound": "hbm", "kernel": "decode_kernel (+ join of split heads): whole step", "achieved": achieved, "peak": peak,
-            "unit": "GB/s", "frac": achieved / peak, "traffic": traffic_record("fwd_split", w.name),
+            "unit": "GB/s", "frac": achieved / peak, "traffic": traffic_record("decode_kernel", w.name),
             "peak_source": f"{peak_src} hbm_gbs (copy)", "avg_launch_ms": ms_step,
             "bytes_per_launch": bytes_alg,
             "isolated_step_ms": isolated_ms, "isolated_frac": bytes_alg / (isolated_ms * 1e-3) / 1e9 / peak}
