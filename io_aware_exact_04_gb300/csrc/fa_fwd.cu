@@ -224,7 +224,7 @@ __global__ void __launch_bounds__(352, 1)
     if (nmax > 0) {
       int issued = n_pre;
       for (int j = n_pre; j < nmax; ++j) {
-        if (!wait_warp(kv_empty(j % C::NST), ((j / C::NST) & 1) ^ 1, st, SITE_F_KV_EMPTY)) break;
+        if (!wait_warp_sleep(kv_empty(j % C::NST), ((j / C::NST) & 1) ^ 1, st, SITE_F_KV_EMPTY)) break;
         load_kv(j);
         issued = j + 1;
       }
@@ -271,7 +271,7 @@ __global__ void __launch_bounds__(352, 1)
         if (elect_one()) mma_commit(bar);
         __syncwarp();
       };
-      bool ok = wait_warp(q_full, 0, st, SITE_F_Q_FULL) && wait_warp(k_full(0), 0, st, SITE_F_K_FULL);
+      bool ok = wait_warp_sleep(q_full, 0, st, SITE_F_Q_FULL) && wait_warp_sleep(k_full(0), 0, st, SITE_F_K_FULL);
       const int t_lo = C::SEP_P ? warp - 9 : 0, t_hi = C::SEP_P ? warp - 9 : 1;  // query tiles served
       if (ok) {
         tc_fence_after();
@@ -279,7 +279,7 @@ __global__ void __launch_bounds__(352, 1)
           if (n_t[t] > 0) {
             if (dual && t == 1) {  // lane 1 starts at ring tile 1
               if (!C::SEP_P) continue;  // the single issuer starts it inside the loop
-              if (!(ok = wait_warp(k_full(1 % C::NST), (1 / C::NST) & 1, st, SITE_F_K_FULL))) break;
+              if (!(ok = wait_warp_sleep(k_full(1 % C::NST), (1 / C::NST) & 1, st, SITE_F_K_FULL))) break;
               issue_s(1, 1 % C::NST);
             } else {
               issue_s(t, 0);
@@ -297,7 +297,7 @@ __global__ void __launch_bounds__(352, 1)
           if (!C::SEP_P && j + 1 < nmax) {
             // one issuer for both lanes: the other lane's next S as soon as its K has landed
             // (ring tile j + 1 is another stage than j: no wait on this tile's release)
-            if (!(ok = wait_warp(k_full(s2), ph2, st, SITE_F_K_FULL))) break;
+            if (!(ok = wait_warp_sleep(k_full(s2), ph2, st, SITE_F_K_FULL))) break;
             issue_s((j + 1) & 1, s2);
             commit(s_full((j + 1) & 1));
           }
@@ -308,14 +308,14 @@ __global__ void __launch_bounds__(352, 1)
             if (C::SEP_P && kk + 1 < n_t[t]) {  // this lane's next tile is ring tile j + 2
               const int sn = (j + 2) % C::NST;
               const uint32_t phn = ((j + 2) / C::NST) & 1;
-              if (!(ok = wait_warp(k_full(sn), phn, st, SITE_F_K_FULL))) break;
-              if (!(ok = wait_warp(s_free(t), kk & 1, st, SITE_F_S_FREE))) break;
+              if (!(ok = wait_warp_sleep(k_full(sn), phn, st, SITE_F_K_FULL))) break;
+              if (!(ok = wait_warp_sleep(s_free(t), kk & 1, st, SITE_F_S_FREE))) break;
               tc_fence_after();
               issue_s(t, sn);
               commit(s_full(t));
             }
-            if (!(ok = wait_warp(v_full(s), ph, st, SITE_F_V_FULL))) break;
-            if (!(ok = wait_warp(p_ready(t), kk & 1, st, SITE_F_P_READY))) break;
+            if (!(ok = wait_warp_sleep(v_full(s), ph, st, SITE_F_V_FULL))) break;
+            if (!(ok = wait_warp_sleep(p_ready(t), kk & 1, st, SITE_F_P_READY))) break;
             tc_fence_after();
             issue_pv(t, s, kk > 0);
             commit(o_done(t));
@@ -327,19 +327,19 @@ __global__ void __launch_bounds__(352, 1)
           used = true;
           if (C::SEP_P && j + 1 < n) {
             // S_t(j+1) as soon as the warpgroup has S_t(j) in registers
-            if (!(ok = wait_warp(k_full(s2), ph2, st, SITE_F_K_FULL))) break;
-            if (!(ok = wait_warp(s_free(t), j & 1, st, SITE_F_S_FREE))) break;
+            if (!(ok = wait_warp_sleep(k_full(s2), ph2, st, SITE_F_K_FULL))) break;
+            if (!(ok = wait_warp_sleep(s_free(t), j & 1, st, SITE_F_S_FREE))) break;
             tc_fence_after();
             issue_s(t, s2);
             commit(s_full(t));
           }
-          if (!(ok = wait_warp(v_full(s), ph, st, SITE_F_V_FULL))) break;
-          if (!(ok = wait_warp(p_ready(t), j & 1, st, SITE_F_P_READY))) break;
+          if (!(ok = wait_warp_sleep(v_full(s), ph, st, SITE_F_V_FULL))) break;
+          if (!(ok = wait_warp_sleep(p_ready(t), j & 1, st, SITE_F_P_READY))) break;
           tc_fence_after();
           issue_pv(t, s, j > 0);
           commit(o_done(t));
           if (!C::SEP_P && j + 1 < n) {  // P_t(j) lives over S_t(j): S_t(j+1) follows PV_t(j)
-            if (!(ok = wait_warp(k_full(s2), ph2, st, SITE_F_K_FULL))) break;
+            if (!(ok = wait_warp_sleep(k_full(s2), ph2, st, SITE_F_K_FULL))) break;
             issue_s(t, s2);
             commit(s_full(t));
           }
@@ -350,7 +350,7 @@ __global__ void __launch_bounds__(352, 1)
         } else {
           // tile j is not this warp's: once it has landed (so its stage's previous use
           // is released), add this warp's arrival without waiting for anything else
-          if (!(ok = wait_warp(v_full(s), ph, st, SITE_F_V_FULL))) break;
+          if (!(ok = wait_warp_sleep(v_full(s), ph, st, SITE_F_V_FULL))) break;
           if (elect_one()) mbar_arrive(kv_empty(s));
           __syncwarp();
         }
@@ -398,7 +398,7 @@ __global__ void __launch_bounds__(352, 1)
       float l_run = 0.f;        // running normaliser
       bool ok = true;
       for (int j = 0; j < n; ++j) {
-        ok = wait_warp(s_full(t), j & 1, st, SITE_F_S_FULL);
+        ok = wait_warp_sleep(s_full(t), j & 1, st, SITE_F_S_FULL);
         if (!ok) break;
         tc_fence_after();
         float sv[128];
@@ -467,7 +467,7 @@ __global__ void __launch_bounds__(352, 1)
           if (C::SEP_P && h == 1) {
             // separate P buffer: half of P is formed before PV_t(j-1) must be done with it
             if (j > 0) {
-              if (!(ok = wait_warp(o_done(t), (j - 1) & 1, st, SITE_F_O_DONE))) break;
+              if (!(ok = wait_warp_sleep(o_done(t), (j - 1) & 1, st, SITE_F_O_DONE))) break;
               tc_fence_after();
             }
             tmem_st16(tP, pk[0]);
@@ -483,7 +483,7 @@ __global__ void __launch_bounds__(352, 1)
         l_run = l_run * f + lsum;
         if (rescale_warp) {
           if (!C::SEP_P) {  // PV_{j-1} must have landed in O before it is rescaled
-            if (!(ok = wait_warp(o_done(t), (j - 1) & 1, st, SITE_F_O_DONE))) break;
+            if (!(ok = wait_warp_sleep(o_done(t), (j - 1) & 1, st, SITE_F_O_DONE))) break;
             tc_fence_after();
           }
           uint32_t r[32];
@@ -501,7 +501,7 @@ __global__ void __launch_bounds__(352, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(p_ready(t));
       }
-      if (ok) ok = wait_warp(o_done(t), (n - 1) & 1, st, SITE_F_O_DONE);
+      if (ok) ok = wait_warp_sleep(o_done(t), (n - 1) & 1, st, SITE_F_O_DONE);
       // every warp of the warpgroup reaches this vote, aborted or not, so the
       // named barrier of the epilogue below is entered by all four or by none
       ok = named_bar_and(1 + t, 128, ok);
@@ -797,13 +797,13 @@ __global__ void __launch_bounds__(352, 1)
       }
       const int set = iu & 1;
       if (iu > 0) {
-        if (!(ok = wait_warp(q_empty(set), ((iu >> 1) & 1) ^ 1, st, SITE_F_Q_FULL))) break;
+        if (!(ok = wait_warp_sleep(q_empty(set), ((iu >> 1) & 1) ^ 1, st, SITE_F_Q_FULL))) break;
         load_q(set, it);
         ++q_loads;
       }
       for (int j = (iu == 0 ? n_pre : 0); j < it.nmax; ++j) {
         const int g = g0 + j;
-        if (!(ok = wait_warp(kv_empty(g % NST), ((g / NST) & 1) ^ 1, st, SITE_F_KV_EMPTY))) break;
+        if (!(ok = wait_warp_sleep(kv_empty(g % NST), ((g / NST) & 1) ^ 1, st, SITE_F_KV_EMPTY))) break;
         load_kv(g, j, it.bh);
         issued = g + 1;
       }
@@ -856,9 +856,9 @@ __global__ void __launch_bounds__(352, 1)
       const int n = (t == 0 ? it.n[0] : it.n[1]);
       const int r2 = next_item(r + 1, nx);
       if (n > 0 && !s0_issued) {  // S_t(0) of this item (S_t is free once its last one was read)
-        if (!(ok = wait_warp(q_full(set), (iu >> 1) & 1, st, SITE_F_Q_FULL))) break;
-        if (!(ok = wait_warp(k_full(g0 % NST), (g0 / NST) & 1, st, SITE_F_K_FULL))) break;
-        if (gj > 0 && !(ok = wait_warp(s_free(t), (gj - 1) & 1, st, SITE_F_S_FREE))) break;
+        if (!(ok = wait_warp_sleep(q_full(set), (iu >> 1) & 1, st, SITE_F_Q_FULL))) break;
+        if (!(ok = wait_warp_sleep(k_full(g0 % NST), (g0 / NST) & 1, st, SITE_F_K_FULL))) break;
+        if (gj > 0 && !(ok = wait_warp_sleep(s_free(t), (gj - 1) & 1, st, SITE_F_S_FREE))) break;
         tc_fence_after();
         issue_s(set, g0 % NST);
         commit(s_full(t));
@@ -869,8 +869,8 @@ __global__ void __launch_bounds__(352, 1)
         const uint32_t ph = (g / NST) & 1;
         if (j < n) {
           if (j + 1 < n) {  // S_t(j+1) as soon as the warpgroup has S_t(j) in registers
-            if (!(ok = wait_warp(k_full((g + 1) % NST), ((g + 1) / NST) & 1, st, SITE_F_K_FULL))) break;
-            if (!(ok = wait_warp(s_free(t), (gj + j) & 1, st, SITE_F_S_FREE))) break;
+            if (!(ok = wait_warp_sleep(k_full((g + 1) % NST), ((g + 1) / NST) & 1, st, SITE_F_K_FULL))) break;
+            if (!(ok = wait_warp_sleep(s_free(t), (gj + j) & 1, st, SITE_F_S_FREE))) break;
             tc_fence_after();
             issue_s(set, (g + 1) % NST);
             commit(s_full(t));
@@ -879,18 +879,18 @@ __global__ void __launch_bounds__(352, 1)
             // which waits for this warp's release of ring slot g0 + nmax - 1 - NST: processed
             // already when nmax - n <= NST (always for causal and full tiles).
             const int g2 = g0 + it.nmax;
-            if (!(ok = wait_warp(q_full(set ^ 1), ((iu + 1) >> 1) & 1, st, SITE_F_Q_FULL))) break;
-            if (!(ok = wait_warp(k_full(g2 % NST), (g2 / NST) & 1, st, SITE_F_K_FULL))) break;
-            if (!(ok = wait_warp(s_free(t), (gj + j) & 1, st, SITE_F_S_FREE))) break;
+            if (!(ok = wait_warp_sleep(q_full(set ^ 1), ((iu + 1) >> 1) & 1, st, SITE_F_Q_FULL))) break;
+            if (!(ok = wait_warp_sleep(k_full(g2 % NST), (g2 / NST) & 1, st, SITE_F_K_FULL))) break;
+            if (!(ok = wait_warp_sleep(s_free(t), (gj + j) & 1, st, SITE_F_S_FREE))) break;
             tc_fence_after();
             issue_s(set ^ 1, g2 % NST);
             commit(s_full(t));
             s0_issued = true;
           }
-          if (!(ok = wait_warp(v_full(s), ph, st, SITE_F_V_FULL))) break;
-          if (!(ok = wait_warp(p_ready(t), (gj + j) & 1, st, SITE_F_P_READY))) break;
+          if (!(ok = wait_warp_sleep(v_full(s), ph, st, SITE_F_V_FULL))) break;
+          if (!(ok = wait_warp_sleep(p_ready(t), (gj + j) & 1, st, SITE_F_P_READY))) break;
           if (j == 0 && ep > 0) {  // the epilogue has read O_t of the previous item
-            if (!(ok = wait_warp(o_free(t), (ep - 1) & 1, st, SITE_F_O_DONE))) break;
+            if (!(ok = wait_warp_sleep(o_free(t), (ep - 1) & 1, st, SITE_F_O_DONE))) break;
           }
           tc_fence_after();
           issue_pv(s, j > 0);
@@ -899,7 +899,7 @@ __global__ void __launch_bounds__(352, 1)
         } else {
           // tile j is not this warp's: once it has landed (so its stage's previous use is
           // released), add this warp's arrival without waiting for anything else
-          if (!(ok = wait_warp(v_full(s), ph, st, SITE_F_V_FULL))) break;
+          if (!(ok = wait_warp_sleep(v_full(s), ph, st, SITE_F_V_FULL))) break;
           if (elect_one()) mbar_arrive(kv_empty(s));
           __syncwarp();
         }
@@ -950,7 +950,7 @@ __global__ void __launch_bounds__(352, 1)
         float l_run = 0.f;        // running normaliser
         for (int j = 0; j < n; ++j) {
           const uint32_t par = (gj + j) & 1;
-          ok = wait_warp(s_full(t), par, st, SITE_F_S_FULL);
+          ok = wait_warp_sleep(s_full(t), par, st, SITE_F_S_FULL);
           if (!ok) break;
           tc_fence_after();
           float sv[128];
@@ -1019,7 +1019,7 @@ __global__ void __launch_bounds__(352, 1)
             if (h == 1) {
               // half of P is formed before PV_t(j-1) must be done with P_t
               if (j > 0) {
-                if (!(ok = wait_warp(o_done(t), par ^ 1, st, SITE_F_O_DONE))) break;
+                if (!(ok = wait_warp_sleep(o_done(t), par ^ 1, st, SITE_F_O_DONE))) break;
                 tc_fence_after();
               }
               tmem_st16(tP, pk[0]);
@@ -1049,7 +1049,7 @@ __global__ void __launch_bounds__(352, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(p_ready(t));
         }
-        if (ok) ok = wait_warp(o_done(t), (gj + n - 1) & 1, st, SITE_F_O_DONE);
+        if (ok) ok = wait_warp_sleep(o_done(t), (gj + n - 1) & 1, st, SITE_F_O_DONE);
         // every warp of the warpgroup reaches this vote, aborted or not, so the
         // named barrier of the epilogue below is entered by all four or by none
         ok = named_bar_and(1 + t, 128, ok);
@@ -1334,7 +1334,7 @@ __global__ void __launch_bounds__(288, 1)
         const int ta = (int)(gt - cur.gbase), te = (int)min(g1 - cur.gbase, (long long)cur.tb);
         for (int t = ta; t < te; ++t, ++g) {
           const int s = g % NS;
-          if (!(ok = wait_warp(empty(s), ((g / NS) & 1) ^ 1, st, SITE_D_EMPTY))) break;
+          if (!(ok = wait_warp_sleep(empty(s), ((g / NS) & 1) ^ 1, st, SITE_D_EMPTY))) break;
           if (elect_one()) mbar_arrive_expect_tx(full(s), 2 * C::TILE);
           for (int c = 0; c < C::NSUB; ++c) {
             if (elect_one()) tma_load_3d(sbase + C::OFF_K + s * C::TILE + c * 16384, &tm_k, c * 64, t * 128, bh, full(s));
@@ -1402,7 +1402,7 @@ __global__ void __launch_bounds__(288, 1)
         }
         for (int t = ta; t < te; ++t, ++g) {
           const int s = g % NS;
-          if (!(wok = wait_warp(full(s), (g / NS) & 1, st, SITE_D_FULL))) break;
+          if (!(wok = wait_warp_sleep(full(s), (g / NS) & 1, st, SITE_D_FULL))) break;
           const uint8_t* kt = sm + C::OFF_K + s * C::TILE;
           const uint8_t* vt = sm + C::OFF_V + s * C::TILE;
           const int jj = t * 128 + key;
@@ -1491,7 +1491,7 @@ __global__ void __launch_bounds__(288, 1)
         for (int t = ta; t < te; ++t, ++g) {
           const int s = g % NS;
           const int jb = t * 128;
-          if (!(wok = wait_warp(full(s), (g / NS) & 1, st, SITE_D_FULL))) break;
+          if (!(wok = wait_warp_sleep(full(s), (g / NS) & 1, st, SITE_D_FULL))) break;
           const uint8_t* kt = sm + C::OFF_K + s * C::TILE;
           const uint8_t* vt = sm + C::OFF_V + s * C::TILE;
           const int jj = jb + key;
