@@ -154,6 +154,7 @@ SPLIT = [
     (1, 1, 2, 20000, 64, True, None, 64, True),           # one head cut into 64 segments
     (2, 2, 1, 640, 128, False, [0, 0], 2, True),          # no valid key anywhere
     (1, 3, 1, 9000, 128, False, None, 1, True),           # whole heads, d = 128, one query row
+    (3, 5, 1, 4000, 128, True, [4000, 2, 3999], 4, True),  # d = 128 key-major lanes, cut heads, padding
 ]
 
 
