@@ -35,7 +35,8 @@
  *    fa_get_last_device_status() reads (fa_get_last_device_status_detail()
  *    also says where). An argument that only the kernels can
  *    check (a packed sequence longer than max_seqlen) records
- *    FA_ERR_DEVICE_CHECK there.
+ *    FA_ERR_DEVICE_CHECK there; so does a failed bounds check in the
+ *    bounds-checked build of this library (fa_debug.h).
  *  - Entry points are reentrant; calls that share output buffers race.
  */
 #ifndef IO_AWARE_EXACT_FA_H

@@ -47,12 +47,17 @@ SIGNATURES = {
         "fa_version": (_i, []),
         "fa_last_error_detail": (ctypes.c_char_p, []),
     },
-    "libfa_withhold.so": None,  # the same C ABI as libfa.so (a test build of it)
+    # builds of the same sources: libfa.so's C ABI plus the entry points listed here
+    "libfa_withhold.so": {},  # test build (a withheld copy per CTA)
+    "libfa_debug.so": {"fa_debug_set_check_slack": (_i, [_i])},  # include/fa_debug.h
     "libfa_selftest.so": {
         "fa_selftest_mma": (_i, [_vp, _vp, _vp, _i, _i, _i, _vp, _vp]),
         "fa_selftest_wait_timeout": (_i, [_vp, ctypes.c_uint, _vp]),
     },
 }
+
+# libraries compiled from the attention sources with other flags
+BUILDS_OF_LIBFA = ("libfa_withhold.so", "libfa_debug.so")
 
 _loaded = {}
 
@@ -68,7 +73,8 @@ def load(name: str = "libfa.so") -> ctypes.CDLL:
     if not os.path.exists(path):
         raise ImportError(f"{path} is not built; run io_aware_exact_04_gb300.build.build()")
     lib = ctypes.CDLL(path)
-    sigs = SIGNATURES[name] if SIGNATURES[name] is not None else SIGNATURES["libfa.so"]
+    sigs = dict(SIGNATURES["libfa.so"]) if name in BUILDS_OF_LIBFA else {}
+    sigs.update(SIGNATURES[name])
     for fn, (res, args) in sigs.items():
         f = getattr(lib, fn)
         f.restype = res

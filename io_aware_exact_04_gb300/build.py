@@ -5,6 +5,8 @@ libfa_selftest.so  hardware self-checks (include/fa_selftest.h)
 libfa_withhold.so  test build of libfa.so: every CTA leaves out one of its TMA copies
                    and waits give up after 20 ms, so that a test can check that the
                    kernels report FA_ERR_TIMEOUT and stop cleanly (not for any other use)
+libfa_debug.so     libfa.so with bounds checks on every global, shared-memory and TMEM
+                   access and TMA coordinate (include/fa_debug.h); slower, for tests
 
 Each translation unit compiles in its own nvcc process, in parallel; objects
 go to _build/ at the repository root. A library is rebuilt when any source or
@@ -33,10 +35,12 @@ LIBS = {
     "libfa.so": ["fa_api.cu", "fa_fwd.cu", "fa_bwd.cu", "fa_noalloc.cu"],
     "libfa_selftest.so": ["selftest.cu"],
     "libfa_withhold.so": ["fa_api.cu", "fa_fwd.cu", "fa_bwd.cu", "fa_noalloc.cu"],
+    "libfa_debug.so": ["fa_api.cu", "fa_fwd.cu", "fa_bwd.cu", "fa_noalloc.cu"],
 }
 # extra preprocessor definitions (and a separate object directory) per library
 DEFINES = {
     "libfa_withhold.so": ["-DFA_TEST_WITHHOLD", "-DFA_WAIT_LIMIT_NS=20000000ull"],
+    "libfa_debug.so": ["-DFA_DEBUG"],
 }
 
 

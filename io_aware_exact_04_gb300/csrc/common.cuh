@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 
 #include "fa.h"
+#include "fa_debug.h"
 #include "ptx.cuh"
 
 namespace fa {
@@ -52,6 +53,74 @@ __device__ __forceinline__ void record_check(int* word, int site) {
     word[2] = blockIdx.x;
     word[3] = blockIdx.y;
   }
+}
+
+// ---------------------------------------------------------------------------------------------
+// Debug build (FA_DEBUG: libfa_debug.so, never the library's own build). Before use, the kernels
+// check the indices of their direct global loads and stores and of the metadata they read
+// (kv_len, cu_seqlens). They also check the coordinates and the shared-memory range of every TMA
+// or bulk copy, the shared-memory operands of their MMAs, and the TMEM lanes and columns of each
+// warp's accumulators. A failed check records FA_ERR_DEVICE_CHECK with its site (fa_debug.h) in
+// the status word and raises the CTA's abort flag where the CTA has one, so that the CTA's
+// waits give up and it leaves through the same path as after a timeout. The access is skipped.
+// In every other build FA_CHECK is the literal `true` and its condition is not compiled.
+// FA_SLACK(args) is the debug-only shrink of the row extents the checks compare against (0 in
+// every other build); a test sets it so that a check fails on memory that is really there.
+#ifdef FA_DEBUG
+constexpr bool kDebugChecks = true;
+#define FA_CHECK(cond, st, site) ::fa::dbg_check((cond), (st), (site))
+#define FA_SLACK(args) ((args).dbg_slack)
+#else
+constexpr bool kDebugChecks = false;
+#define FA_CHECK(cond, st, site) true
+#define FA_SLACK(args) 0
+#endif
+
+// Check sites recorded with FA_ERR_DEVICE_CHECK.
+enum { DBG_META = FA_DBG_META, DBG_TMA_LOAD = FA_DBG_TMA_LOAD, DBG_TMA_STORE = FA_DBG_TMA_STORE,
+       DBG_BULK = FA_DBG_BULK, DBG_GLOBAL_LOAD = FA_DBG_GLOBAL_LOAD, DBG_GLOBAL_STORE = FA_DBG_GLOBAL_STORE,
+       DBG_SMEM = FA_DBG_SMEM, DBG_TMEM = FA_DBG_TMEM };
+
+__device__ __forceinline__ bool dbg_check(bool ok, const DevStatus& st, int site) {
+  if (!ok) {
+    if (atomicCAS(st.word, 0, FA_ERR_DEVICE_CHECK) == 0) {
+      st.word[1] = site;
+      st.word[2] = blockIdx.x;
+      st.word[3] = blockIdx.y;
+    }
+    *(volatile int*)st.abort_smem = 1;
+  }
+  return ok;
+}
+__device__ __forceinline__ bool dbg_check(bool ok, int* word, int site) {
+  if (!ok) record_check(word, site);
+  return ok;
+}
+
+// Index idx of a buffer of n elements.
+__device__ __forceinline__ bool in_range(long long idx, long long n) { return idx >= 0 && idx < n; }
+// The elements [idx, idx + len) of a buffer of n elements.
+__device__ __forceinline__ bool span_in(long long idx, long long len, long long n) {
+  return idx >= 0 && len >= 0 && idx + len <= n;
+}
+// A tiled TMA copy at (x, row, z) of a 3-D tensor [outer][rows][inner], box_rows rows high:
+// x inside the row on a 16-byte boundary, z inside [0, outer), and the box overlapping rows
+// [0, rows). A load may start above row 0 (the rows there read as zero); a store or a
+// reduce-add must start at a row of the tensor.
+__device__ __forceinline__ bool tma_coords_ok(int x, int row, int z, int inner, int rows, int outer, int elem_bytes,
+                                              int box_rows, bool store) {
+  if (x < 0 || x >= inner || (x * elem_bytes) % 16 != 0 || z < 0 || z >= outer) return false;
+  return store ? (row >= 0 && row < rows) : (row > -box_rows && row < rows);
+}
+// The shared-memory bytes [addr, addr + bytes) inside [lo, hi).
+__device__ __forceinline__ bool smem_in(uint32_t addr, uint32_t bytes, uint32_t lo, uint32_t hi) {
+  return addr >= lo && addr + bytes <= hi;
+}
+// An access of `cols` TMEM columns at taddr by a warp: its lane quarter, and the columns inside
+// the allocation of ncols columns at base.
+__device__ __forceinline__ bool tmem_in(uint32_t taddr, uint32_t cols, uint32_t base, uint32_t ncols) {
+  const uint32_t lane = taddr >> 16, col = taddr & 0xFFFFu, c0 = base & 0xFFFFu;
+  return lane < 128 && (lane & 31) == 0 && col >= c0 && col + cols <= c0 + ncols;
 }
 
 // Single-thread bounded wait. Returns false if the CTA must abort. SLEEP: after the first

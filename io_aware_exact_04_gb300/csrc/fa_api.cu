@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cstdio>
@@ -11,6 +12,9 @@
 
 #include "fa.h"
 #include "fa_internal.h"
+#ifdef FA_DEBUG
+#include "fa_debug.h"
+#endif
 
 namespace {
 
@@ -150,11 +154,25 @@ int check_launch(const char* kernel) {
   if (e == cudaSuccess) return FA_OK;
   return cuda_fail(kernel, (int)e, cudaGetErrorName(e));
 }
+#ifdef FA_DEBUG
+namespace {
+std::atomic<int> g_check_slack{0};
+}
+int debug_check_slack() { return g_check_slack.load(std::memory_order_relaxed); }
+#endif
 }  // namespace fa
 
 extern "C" {
 
 const char* fa_last_error_detail(void) { return g_last_error; }
+
+#ifdef FA_DEBUG
+int fa_debug_set_check_slack(int rows) {
+  if (rows < 0) return FA_ERR_INVALID_ARG;
+  fa::g_check_slack.store(rows, std::memory_order_relaxed);
+  return FA_OK;
+}
+#endif
 
 int fa_version(void) { return 100; }
 
@@ -200,6 +218,7 @@ int fa_forward_qk(const void* q, const void* k, const void* v, void* o, float* l
   a.part_o = nullptr;
   a.part_lse = nullptr;
   a.status = status;
+  FA_DEBUG_ARGS(a, B);
   return fa::launch_fwd(q, k, v, o, a, B * H, d, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -234,6 +253,7 @@ int fa_forward_varlen(const void* q, const void* k, const void* v, void* o, floa
   a.part_o = nullptr;
   a.part_lse = nullptr;
   a.status = status;
+  FA_DEBUG_ARGS(a, B);
   return fa::launch_fwd_varlen(q, k, v, o, a, B * H, d, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -303,6 +323,7 @@ int fa_forward_split(const void* q, const void* k, const void* v, void* o, float
   a.part_o = static_cast<float*>(workspace);
   a.part_lse = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + round_up(rows * d * 4, 256));
   a.status = status;
+  FA_DEBUG_ARGS(a, B);
   return fa::launch_fwd_split(q, k, v, o, a, B * H, d, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -361,6 +382,7 @@ int fa_backward_stage_qk(int stage, const void* q, const void* k, const void* v,
   a.dk = static_cast<uint16_t*>(dk);
   a.dv = static_cast<uint16_t*>(dv);
   a.status = status;
+  FA_DEBUG_ARGS(a, B);
   return fa::launch_bwd_stage(stage, q, k, v, a, B * H, d, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -445,6 +467,7 @@ int fa_backward_varlen(const void* q, const void* k, const void* v, const void* 
   a.dk = static_cast<uint16_t*>(dk);
   a.dv = static_cast<uint16_t*>(dv);
   a.status = status;
+  FA_DEBUG_ARGS(a, B);
   for (int stage = 0; stage < 3; ++stage) {
     rc = fa::launch_bwd_varlen_stage(stage, q, k, v, a, B, H, d, reinterpret_cast<cudaStream_t>(stream));
     if (rc != FA_OK) return rc;

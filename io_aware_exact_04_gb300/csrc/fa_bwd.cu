@@ -32,6 +32,31 @@
 
 namespace fa {
 
+#ifdef FA_DEBUG
+// Extents that the debug build checks the backward's accesses against, each less the check
+// slack. Per tensor-map head: rows of Q / O / dO / dQ, of K / V / dK / dV and of the dQ
+// accumulator, and the maps' outer extent. In all: those rows, and the -LSE2 / -D rows. Plain
+// [B H, N, d] or packed [H, T, d] (vl) tensors.
+struct BwdExt {
+  int rows_q, rows_k, rows_acc, heads;
+  long long q_rows, k_rows, acc_rows, stat_rows;
+};
+__device__ __forceinline__ BwdExt bwd_ext(const BwdArgs& a, bool vl) {
+  const long long bh = (long long)a.dbg_B * a.H;
+  const int sl = a.dbg_slack;
+  BwdExt e;
+  e.rows_q = (vl ? vl_T(a) : a.N) - sl;
+  e.rows_k = (vl ? vl_T(a) : a.Nk) - sl;
+  e.rows_acc = a.Npad - sl;
+  e.heads = vl ? a.H : (int)bh;
+  e.q_rows = (vl ? (long long)a.H * vl_T(a) : bh * a.N) - sl;
+  e.k_rows = (vl ? (long long)a.H * vl_T(a) : bh * a.Nk) - sl;
+  e.acc_rows = (vl ? (long long)a.H : bh) * a.Npad - sl;
+  e.stat_rows = (vl ? (long long)a.H * vl_Lpad(a) : bh * a.Npad) - sl;
+  return e;
+}
+#endif
+
 // ---------------------------------------------------------------------------------------------
 // Stored negated, so that the main kernels add them with no extra instruction:
 // dvec_i = -D_i = -sum_k dO_ik O_ik; lse2_i = -LSE_i * log2(e) (-inf where no row or
@@ -48,7 +73,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(BwdArgs a, int BH) {
   const int bh = blockIdx.y;
   if (n >= a.Npad) return;  // whole row groups leave together: RPB divides the 128-row padding
   float acc = 0.f;
-  if (n < a.N) {
+  if (n < a.N && FA_CHECK(in_range((long long)bh * a.N + n, bwd_ext(a, false).q_rows), a.status, DBG_GLOBAL_LOAD)) {
     const size_t off = ((size_t)bh * a.N + n) * D + part * 8;
     const uint4 ov = *reinterpret_cast<const uint4*>(a.o + off);
     const uint4 gv = *reinterpret_cast<const uint4*>(a.dO + off);
@@ -63,6 +88,9 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(BwdArgs a, int BH) {
 #pragma unroll
   for (int m = LPR / 2; m > 0; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
   const size_t r = (size_t)bh * a.Npad + n;
+  if (!FA_CHECK(in_range(r, bwd_ext(a, false).acc_rows) && in_range(r, bwd_ext(a, false).stat_rows), a.status,
+                DBG_GLOBAL_STORE))
+    return;
   float4* dq = reinterpret_cast<float4*>(a.dq_acc + r * D + part * 8);
   dq[0] = make_float4(0.f, 0.f, 0.f, 0.f);
   dq[1] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -92,7 +120,8 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(BwdArgs a, int BH) {
 #pragma unroll
   for (int u = 0; u < 2; ++u) {
     const int n = n0 + u * RPB;
-    if (n < a.N) {
+    if (n < a.N &&
+        FA_CHECK(in_range((long long)bh * a.Npad + n, bwd_ext(a, false).acc_rows), a.status, DBG_GLOBAL_LOAD)) {
       const float4* src = reinterpret_cast<const float4*>(a.dq_acc + ((size_t)bh * a.Npad + n) * D + part * 8);
       x[u][0] = src[0];
       x[u][1] = src[1];
@@ -101,7 +130,7 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(BwdArgs a, int BH) {
 #pragma unroll
   for (int u = 0; u < 2; ++u) {
     const int n = n0 + u * RPB;
-    if (n < a.N) {
+    if (n < a.N && FA_CHECK(in_range((long long)bh * a.N + n, bwd_ext(a, false).q_rows), a.status, DBG_GLOBAL_STORE)) {
       uint4 o;
       o.x = pack_bf16x2(x[u][0].x, x[u][0].y);
       o.y = pack_bf16x2(x[u][0].z, x[u][0].w);
@@ -128,6 +157,7 @@ __global__ void __launch_bounds__(256) bwd_pre_varlen_kernel(BwdArgs a, int B) {
   const int part = threadIdx.x % LPR;
   const int n = blockIdx.x * RPB + threadIdx.x / LPR;  // row within the sequence's slots
   const int b = blockIdx.y / a.H, h = blockIdx.y - b * a.H;
+  if (!FA_CHECK(in_range(b + 1, a.dbg_B + 1LL), a.status, DBG_META)) return;
   const int rb = vl_cu(a)[b];
   const int len = vl_cu(a)[b + 1] - rb;
   const int base = (rb + 4 * b) & ~3;
@@ -135,7 +165,9 @@ __global__ void __launch_bounds__(256) bwd_pre_varlen_kernel(BwdArgs a, int B) {
   const int slots = (b + 1 < B) ? (((vl_cu(a)[b + 1] + 4 * (b + 1)) & ~3) - base) : (vl_Lpad(a) - base);
   const bool valid = n < len;
   float acc = 0.f;
-  if (valid) {
+  if (valid && FA_CHECK(in_range((long long)h * vl_T(a) + rb + n, bwd_ext(a, true).q_rows) &&
+                            in_range((long long)h * a.Npad + rb + n, bwd_ext(a, true).acc_rows),
+                        a.status, DBG_GLOBAL_LOAD)) {
     const size_t off = ((size_t)h * vl_T(a) + rb + n) * D + part * 8;
     const uint4 ov = *reinterpret_cast<const uint4*>(a.o + off);
     const uint4 gv = *reinterpret_cast<const uint4*>(a.dO + off);
@@ -152,11 +184,12 @@ __global__ void __launch_bounds__(256) bwd_pre_varlen_kernel(BwdArgs a, int B) {
   }
 #pragma unroll
   for (int m = LPR / 2; m > 0; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
-  if (part == 0 && n < slots) {
+  if (part == 0 && n < slots &&
+      FA_CHECK(in_range((long long)h * vl_Lpad(a) + base + n, bwd_ext(a, true).stat_rows), a.status, DBG_GLOBAL_STORE)) {
     const size_t r = (size_t)h * vl_Lpad(a) + base + n;
     a.dvec[r] = valid ? -acc : 0.f;
     float l2 = -INFINITY;
-    if (valid) {
+    if (valid && FA_CHECK(in_range((long long)h * vl_T(a) + rb + n, bwd_ext(a, true).q_rows), a.status, DBG_GLOBAL_LOAD)) {
       const float l = a.lse[(size_t)h * vl_T(a) + rb + n];
       if (l != -INFINITY) l2 = l * -1.4426950408889634f;
     }
@@ -259,6 +292,7 @@ __global__ void __launch_bounds__(448, 1)
   int kv, n_qt, i_start;
   if constexpr (VL) {
     const int h = bh - b * a.H;
+    if (!FA_CHECK(in_range(b + 1, a.dbg_B + 1LL), a.status, DBG_META)) return;
     sq.rb = vl_cu(a)[b];
     sq.nq = vl_cu(a)[b + 1] - sq.rb;
     sq.zh = h;
@@ -270,7 +304,7 @@ __global__ void __launch_bounds__(448, 1)
     i_start = a.causal ? k0 / BR : 0;
   } else {
     kv = a.Nk;
-    if (a.kv_len) kv = min(max(a.kv_len[b], 0), a.Nk);
+    if (a.kv_len && FA_CHECK(in_range(b, a.dbg_B), a.status, DBG_META)) kv = min(max(a.kv_len[b], 0), a.Nk);
     n_qt = (a.N + BR - 1) / BR;
     // causal: the first query row that sees key k0 is k0 - coff
     i_start = a.causal ? max(0, k0 - a.coff) / BR : 0;
@@ -288,6 +322,7 @@ __global__ void __launch_bounds__(448, 1)
       rows = min(128, a.Nk - k0);
       row0 = (size_t)bh * a.Nk + k0;
     }
+    if (!FA_CHECK(span_in(row0, rows, bwd_ext(a, VL).k_rows), a.status, DBG_GLOBAL_STORE)) return;
     for (int idx = threadIdx.x; idx < rows * (D / 8); idx += blockDim.x) {
       const size_t off = (row0 + idx / (D / 8)) * D + (idx % (D / 8)) * 8;
       *reinterpret_cast<uint4*>(a.dk + off) = make_uint4(0, 0, 0, 0);
@@ -317,18 +352,35 @@ __global__ void __launch_bounds__(448, 1)
     const float* dsrc = dvec_h + (size_t)i * BR;
     if (elect_one()) mbar_arrive_expect_tx(bar, 2 * C::QTILE + 2 * BR * 4);
     for (int c = 0; c < C::NSUB; ++c) {
+      const bool in =
+          FA_CHECK(tma_coords_ok(c * 64, VL ? i * BR + vl_cu(a)[b] : i * BR, VL ? bh - b * a.H : bh, D,
+                                 bwd_ext(a, VL).rows_q, bwd_ext(a, VL).heads, 2, BR, false) &&
+                       smem_in(sbase + C::OFF_Q + s * C::QTILE + c * C::QSUB, C::QSUB, sbase + C::OFF_Q,
+                               sbase + C::OFF_DO) &&
+                       smem_in(sbase + C::OFF_DO + s * C::QTILE + c * C::QSUB, C::QSUB, sbase + C::OFF_DO,
+                               sbase + C::OFF_DS),
+                   st, DBG_TMA_LOAD);
       if constexpr (VL) {
-        if (elect_one())
+        if (in && elect_one())
           tma_load_3d(sbase + C::OFF_Q + s * C::QTILE + c * C::QSUB, &tm_q, c * 64, sq.rb + i * BR, sq.zh, bar);
-        if (elect_one())
+        if (in && elect_one())
           tma_load_3d(sbase + C::OFF_DO + s * C::QTILE + c * C::QSUB, &tm_do, c * 64, sq.rb + i * BR, sq.zh, bar);
       } else {
-        if (elect_one()) tma_load_3d(sbase + C::OFF_Q + s * C::QTILE + c * C::QSUB, &tm_q, c * 64, i * BR, bh, bar);
-        if (elect_one()) tma_load_3d(sbase + C::OFF_DO + s * C::QTILE + c * C::QSUB, &tm_do, c * 64, i * BR, bh, bar);
+        if (in && elect_one())
+          tma_load_3d(sbase + C::OFF_Q + s * C::QTILE + c * C::QSUB, &tm_q, c * 64, i * BR, bh, bar);
+        if (in && elect_one())
+          tma_load_3d(sbase + C::OFF_DO + s * C::QTILE + c * C::QSUB, &tm_do, c * 64, i * BR, bh, bar);
       }
     }
-    if (elect_one()) bulk_load(sbase + C::OFF_LSE + s * BR * 4, lsrc, BR * 4, bar);
-    if (elect_one()) bulk_load(sbase + C::OFF_DV + s * BR * 4, dsrc, BR * 4, bar);
+    // the -LSE2 and -D rows of the step: inside the workspace, 16-byte aligned
+    const bool rows_in = FA_CHECK(
+        span_in(lsrc - a.lse2, BR, bwd_ext(a, VL).stat_rows) && span_in(dsrc - a.dvec, BR, bwd_ext(a, VL).stat_rows) &&
+            ((reinterpret_cast<uintptr_t>(lsrc) | reinterpret_cast<uintptr_t>(dsrc)) & 15) == 0 &&
+            smem_in(sbase + C::OFF_LSE + s * BR * 4, BR * 4, sbase + C::OFF_LSE, sbase + C::OFF_DV) &&
+            smem_in(sbase + C::OFF_DV + s * BR * 4, BR * 4, sbase + C::OFF_DV, sbase + C::OFF_BAR),
+        st, DBG_BULK);
+    if (rows_in && elect_one()) bulk_load(sbase + C::OFF_LSE + s * BR * 4, lsrc, BR * 4, bar);
+    if (rows_in && elect_one()) bulk_load(sbase + C::OFF_DV + s * BR * 4, dsrc, BR * 4, bar);
     __syncwarp();
   };
   if (warp == 12) {
@@ -356,12 +408,17 @@ __global__ void __launch_bounds__(448, 1)
     }
     if (elect_one()) mbar_arrive_expect_tx(kv_full, 2 * C::KTILE);
     for (int c = 0; c < C::NSUB; ++c) {
+      const bool in = FA_CHECK(tma_coords_ok(c * 64, VL ? k0 + vl_cu(a)[b] : k0, VL ? bh - b * a.H : bh, D,
+                                             bwd_ext(a, VL).rows_k, bwd_ext(a, VL).heads, 2, 128, false) &&
+                                   smem_in(sbase + C::OFF_K + c * C::KSUB, C::KSUB, sbase + C::OFF_K, sbase + C::OFF_V) &&
+                                   smem_in(sbase + C::OFF_V + c * C::KSUB, C::KSUB, sbase + C::OFF_V, sbase + C::OFF_Q),
+                               st, DBG_TMA_LOAD);
       if constexpr (VL) {
-        if (elect_one()) tma_load_3d(sbase + C::OFF_K + c * C::KSUB, &tm_k, c * 64, sq.rb + k0, sq.zh, kv_full);
-        if (elect_one()) tma_load_3d(sbase + C::OFF_V + c * C::KSUB, &tm_v, c * 64, sq.rb + k0, sq.zh, kv_full);
+        if (in && elect_one()) tma_load_3d(sbase + C::OFF_K + c * C::KSUB, &tm_k, c * 64, sq.rb + k0, sq.zh, kv_full);
+        if (in && elect_one()) tma_load_3d(sbase + C::OFF_V + c * C::KSUB, &tm_v, c * 64, sq.rb + k0, sq.zh, kv_full);
       } else {
-        if (elect_one()) tma_load_3d(sbase + C::OFF_K + c * C::KSUB, &tm_k, c * 64, k0, bh, kv_full);
-        if (elect_one()) tma_load_3d(sbase + C::OFF_V + c * C::KSUB, &tm_v, c * 64, k0, bh, kv_full);
+        if (in && elect_one()) tma_load_3d(sbase + C::OFF_K + c * C::KSUB, &tm_k, c * 64, k0, bh, kv_full);
+        if (in && elect_one()) tma_load_3d(sbase + C::OFF_V + c * C::KSUB, &tm_v, c * 64, k0, bh, kv_full);
       }
     }
     for (int it = 0; it < n_pre; ++it) load_qdo(it);
@@ -444,7 +501,14 @@ __global__ void __launch_bounds__(448, 1)
       // dS^T(i - 1), waited for), so the warpgroups find it ready when they finish step i; then
       // dV(i), dK(i), dQ^T(i) as P^T(i) and dS^T(i) arrive, and dP^T(i + 1) after dK(i) has read
       // dS^T(i) out of the dP^T columns.
-      bool ok = wait_warp(kv_full, 0, st, SITE_B_KV_FULL) && wait_warp(qdo_full(0), 0, st, SITE_B_QDO_FULL);
+      // the TMEM layout inside this CTA's allocation
+      bool ok = FA_CHECK(tmem_in(tmem + C::TM_ST, 2 * BR, tmem, C::TM_COLS) &&
+                             tmem_in(tmem + C::TM_DPT, BR, tmem, C::TM_COLS) &&
+                             tmem_in(tmem + C::TM_DV, D, tmem, C::TM_COLS) &&
+                             tmem_in(tmem + C::TM_DK, D, tmem, C::TM_COLS) &&
+                             tmem_in(tmem + C::TM_DQ, C::DQ_COLS, tmem, C::TM_COLS),
+                         st, DBG_TMEM) &&
+                wait_warp(kv_full, 0, st, SITE_B_KV_FULL) && wait_warp(qdo_full(0), 0, st, SITE_B_QDO_FULL);
       if (ok) {
         tc_fence_after();
         issue_kmajor(C::TM_ST, k_lo, q_lo);
@@ -535,11 +599,17 @@ __global__ void __launch_bounds__(448, 1)
       if (tid == 0) {
         constexpr int NBOX = D / 32;
         constexpr int BOX_BYTES = BR * 128;
-        for (int x = 0; x < NBOX; ++x)
+        for (int x = 0; x < NBOX; ++x) {
+          if (!FA_CHECK(tma_coords_ok(x * 32, VL ? i * BR + vl_cu(a)[b] : i * BR, VL ? bh - b * a.H : bh, D,
+                                      bwd_ext(a, VL).rows_acc, bwd_ext(a, VL).heads, 4, BR, true) &&
+                            smem_in(smem_u32(stg + x * BOX_BYTES), BOX_BYTES, sbase + C::OFF_DQ, sbase + C::OFF_LSE),
+                        st, DBG_TMA_STORE))
+            continue;
           if constexpr (VL)
             tma_reduce_add_3d(&tm_dqacc, smem_u32(stg + x * BOX_BYTES), x * 32, sq.rb + i * BR, sq.zh);
           else
             tma_reduce_add_3d(&tm_dqacc, smem_u32(stg + x * BOX_BYTES), x * 32, i * BR, bh);
+        }
         bulk_commit();
       }
     }
@@ -680,7 +750,8 @@ __global__ void __launch_bounds__(448, 1)
           v.w = pack_bf16x2(__uint_as_float(x[q * 8 + 6]) * mul, __uint_as_float(x[q * 8 + 7]) * mul);
           if constexpr (VL) {
             if (k0 + 128 > sq.nq) {  // the tile runs past its sequence: rows written directly
-              if (k0 + r < sq.nq)
+              if (k0 + r < sq.nq &&
+                  FA_CHECK(in_range(sq.krow + k0 + r, bwd_ext(a, VL).k_rows), st, DBG_GLOBAL_STORE))
                 *reinterpret_cast<uint4*>((wg == 0 ? a.dv : a.dk) + (sq.krow + k0 + r) * D + c * 32 + q * 8) = v;
               continue;
             }
@@ -694,6 +765,11 @@ __global__ void __launch_bounds__(448, 1)
       if constexpr (VL) tma_out = tma_out && k0 + 128 <= sq.nq;
       if (tma_out) {
         for (int c = 0; c < C::NSUB; ++c) {
+          if (!FA_CHECK(tma_coords_ok(c * 64, VL ? k0 + vl_cu(a)[b] : k0, VL ? bh - b * a.H : bh, D,
+                                      bwd_ext(a, VL).rows_k, bwd_ext(a, VL).heads, 2, 128, true) &&
+                            smem_in(smem_u32(stage + c * C::KSUB), C::KSUB, sbase + C::OFF_Q, sbase + C::OFF_DS),
+                        st, DBG_TMA_STORE))
+            continue;
           if constexpr (VL)
             tma_store_3d(wg == 0 ? &tm_dv : &tm_dk, smem_u32(stage + c * C::KSUB), c * 64, sq.rb + k0, sq.zh);
           else
@@ -773,8 +849,13 @@ __device__ __forceinline__ SeqD64 seq_d64(int bh, const BwdArgs& a) {
   SeqD64 q;
   if (VL) {
     const int b = bh / a.H, h = bh - b * a.H;
-    q.rb = vl_cu(a)[b];
-    q.nq = vl_cu(a)[b + 1] - q.rb;
+    if (FA_CHECK(in_range(b + 1, a.dbg_B + 1LL), a.status, DBG_META)) {
+      q.rb = vl_cu(a)[b];
+      q.nq = vl_cu(a)[b + 1] - q.rb;
+    } else {
+      q.rb = 0;
+      q.nq = 0;
+    }
     q.zh = h;
     q.lrow = (size_t)h * vl_Lpad(a) + ((q.rb + 4 * b) & ~3);  // 16-byte aligned for the bulk copies
     q.krow = (size_t)h * vl_T(a) + q.rb;
@@ -799,7 +880,8 @@ __device__ __forceinline__ TileD64 tile_d64(int t, const BwdArgs& a) {
     r.kv = nq;  // a tile past its sequence gets no work (and writes nothing: see the epilogue)
   } else {
     r.kv = a.Nk;
-    if (a.kv_len) r.kv = min(max(a.kv_len[r.bh / a.H], 0), a.Nk);
+    if (a.kv_len && FA_CHECK(in_range(r.bh / a.H, a.dbg_B), a.status, DBG_META))
+      r.kv = min(max(a.kv_len[r.bh / a.H], 0), a.Nk);
   }
   const int n_qt = (nq + Bwd64::BR - 1) / Bwd64::BR;
   // causal: the first query row that sees key k0 is k0 - coff; steps start on a 128-row
@@ -879,9 +961,14 @@ __global__ void __launch_bounds__(480, 1)
   // their latency. It runs its code with the whole warp and lets one elected lane issue each copy.
   auto load_kv = [&](int b, const TileD64& tl) {  // whole warp
     const SeqD64 sq = seq_d64<VL>(tl.bh, a);
+    const bool in = FA_CHECK(tma_coords_ok(0, sq.rb + tl.k0, sq.zh, C::D, bwd_ext(a, VL).rows_k, bwd_ext(a, VL).heads,
+                                           2, 128, false) &&
+                                 smem_in(sbase + C::off_k(b), C::KTILE, sbase + C::OFF_KV, sbase + C::OFF_Q) &&
+                                 smem_in(sbase + C::off_v(b), C::KTILE, sbase + C::OFF_KV, sbase + C::OFF_Q),
+                             st, DBG_TMA_LOAD);
     if (elect_one()) mbar_arrive_expect_tx(kv_full(b), 2 * C::KTILE);
-    if (elect_one()) tma_load_3d(sbase + C::off_k(b), &tm_k, 0, sq.rb + tl.k0, sq.zh, kv_full(b));
-    if (elect_one()) tma_load_3d(sbase + C::off_v(b), &tm_v, 0, sq.rb + tl.k0, sq.zh, kv_full(b));
+    if (in && elect_one()) tma_load_3d(sbase + C::off_k(b), &tm_k, 0, sq.rb + tl.k0, sq.zh, kv_full(b));
+    if (in && elect_one()) tma_load_3d(sbase + C::off_v(b), &tm_v, 0, sq.rb + tl.k0, sq.zh, kv_full(b));
     __syncwarp();
   };
   auto load_qdo = [&](int gs, const TileD64& tl, int it) {  // whole warp
@@ -891,11 +978,25 @@ __global__ void __launch_bounds__(480, 1)
     const SeqD64 sq = seq_d64<VL>(tl.bh, a);
     const float* lsrc = a.lse2 + sq.lrow + (size_t)i * BR;
     const float* dsrc = a.dvec + sq.lrow + (size_t)i * BR;
+    // (a step that completes the tile's last pair may start up to one step past the last row:
+    // TMA reads zeros there, and its columns are masked)
+    const bool in = FA_CHECK(tma_coords_ok(0, sq.rb + i * BR, sq.zh, C::D, bwd_ext(a, VL).rows_q + BR,
+                                           bwd_ext(a, VL).heads, 2, BR, false) &&
+                                 smem_in(sbase + C::OFF_Q + s * C::QTILE, C::QTILE, sbase + C::OFF_Q, sbase + C::OFF_DO) &&
+                                 smem_in(sbase + C::OFF_DO + s * C::QTILE, C::QTILE, sbase + C::OFF_DO, sbase + C::OFF_DS),
+                             st, DBG_TMA_LOAD);
+    // the -LSE2 and -D rows of the step: inside the workspace, 16-byte aligned
+    const bool rows_in = FA_CHECK(
+        span_in(lsrc - a.lse2, BR, bwd_ext(a, VL).stat_rows) && span_in(dsrc - a.dvec, BR, bwd_ext(a, VL).stat_rows) &&
+            ((reinterpret_cast<uintptr_t>(lsrc) | reinterpret_cast<uintptr_t>(dsrc)) & 15) == 0 &&
+            smem_in(sbase + C::OFF_LSE + s * BR * 4, BR * 4, sbase + C::OFF_LSE, sbase + C::OFF_DV) &&
+            smem_in(sbase + C::OFF_DV + s * BR * 4, BR * 4, sbase + C::OFF_DV, sbase + C::OFF_BAR),
+        st, DBG_BULK);
     if (elect_one()) mbar_arrive_expect_tx(bar, 2 * C::QTILE + 2 * BR * 4);
-    if (elect_one()) tma_load_3d(sbase + C::OFF_Q + s * C::QTILE, &tm_q, 0, sq.rb + i * BR, sq.zh, bar);
-    if (elect_one()) tma_load_3d(sbase + C::OFF_DO + s * C::QTILE, &tm_do, 0, sq.rb + i * BR, sq.zh, bar);
-    if (elect_one()) bulk_load(sbase + C::OFF_LSE + s * BR * 4, lsrc, BR * 4, bar);
-    if (elect_one()) bulk_load(sbase + C::OFF_DV + s * BR * 4, dsrc, BR * 4, bar);
+    if (in && elect_one()) tma_load_3d(sbase + C::OFF_Q + s * C::QTILE, &tm_q, 0, sq.rb + i * BR, sq.zh, bar);
+    if (in && elect_one()) tma_load_3d(sbase + C::OFF_DO + s * C::QTILE, &tm_do, 0, sq.rb + i * BR, sq.zh, bar);
+    if (rows_in && elect_one()) bulk_load(sbase + C::OFF_LSE + s * BR * 4, lsrc, BR * 4, bar);
+    if (rows_in && elect_one()) bulk_load(sbase + C::OFF_DV + s * BR * 4, dsrc, BR * 4, bar);
     __syncwarp();
   };
   int pre_steps = 0;  // steps of the first tile issued before the setup
@@ -1044,7 +1145,13 @@ __global__ void __launch_bounds__(480, 1)
     TileD64 cur, nxt;
     int r = next_work_d64<VL>(0, cta, G, T, a, cur);
     if (r >= 0) {
-      ok = wait_warp(kv_full(0), 0, st, SITE_B_KV_FULL) && wait_warp(qdo_full(w), 0, st, SITE_B_QDO_FULL);
+      // the TMEM layout inside this CTA's allocation, then the first copies
+      ok = FA_CHECK(tmem_in(tmem + C::TM_ST, 128, tmem, C::TM_COLS) && tmem_in(tmem + C::TM_DPT, 128, tmem, C::TM_COLS) &&
+                        tmem_in(tmem + C::TM_DV, C::D, tmem, C::TM_COLS) &&
+                        tmem_in(tmem + C::TM_DK, C::D, tmem, C::TM_COLS) &&
+                        tmem_in(tmem + C::TM_DQ, 128, tmem, C::TM_COLS),
+                    st, DBG_TMEM) &&
+           wait_warp(kv_full(0), 0, st, SITE_B_KV_FULL) && wait_warp(qdo_full(w), 0, st, SITE_B_QDO_FULL);
       if (ok) {
         tc_fence_after();
         issue_s(w, 0);
@@ -1152,6 +1259,7 @@ __global__ void __launch_bounds__(480, 1)
       if (tl.n_it == 0) {  // no valid key in this tile: its dK and dV rows are zero
         if (VL && tl.k0 >= sq.nq) continue;  // past its sequence: those rows are another sequence's
         const int rows = min(128, (VL ? sq.nq : a.Nk) - tl.k0);
+        if (!FA_CHECK(span_in(sq.krow + tl.k0, rows, bwd_ext(a, VL).k_rows), st, DBG_GLOBAL_STORE)) continue;
         for (int idx = tid; idx < rows * (C::D / 8); idx += 128) {
           const size_t off = (sq.krow + tl.k0 + idx / (C::D / 8)) * C::D + (idx % (C::D / 8)) * 8;
           *reinterpret_cast<uint4*>(a.dk + off) = make_uint4(0, 0, 0, 0);
@@ -1182,7 +1290,11 @@ __global__ void __launch_bounds__(480, 1)
           fence_proxy_async_smem();
           named_bar_sync(3, 128);
           if (tid == 0) {
-            tma_reduce_add_3d(&tm_dqacc, smem_u32(stg), h * 32, sq.rb + (tl.i_start + 2 * p) * BR, sq.zh);
+            if (FA_CHECK(tma_coords_ok(h * 32, sq.rb + (tl.i_start + 2 * p) * BR, sq.zh, C::D, bwd_ext(a, VL).rows_acc,
+                                       bwd_ext(a, VL).heads, 4, 128, true) &&
+                             smem_in(smem_u32(stg), C::STG_BYTES, sbase + C::OFF_STG, sbase + C::OFF_LSE),
+                         st, DBG_TMA_STORE))
+              tma_reduce_add_3d(&tm_dqacc, smem_u32(stg), h * 32, sq.rb + (tl.i_start + 2 * p) * BR, sq.zh);
             bulk_commit();
           }
         }
@@ -1206,7 +1318,8 @@ __global__ void __launch_bounds__(480, 1)
       };
       auto stage_store = [&](const uint32_t (&pk)[32], const CUtensorMap* map, uint16_t* gdst) {
         if (VL && tl.k0 + 128 > sq.nq) {  // the tile runs past its sequence: rows written directly
-          if (tl.k0 + r < sq.nq) {
+          if (tl.k0 + r < sq.nq &&
+              FA_CHECK(in_range(sq.krow + tl.k0 + r, bwd_ext(a, VL).k_rows), st, DBG_GLOBAL_STORE)) {
             uint4* dst = reinterpret_cast<uint4*>(gdst + (sq.krow + tl.k0 + r) * C::D);
 #pragma unroll
             for (int q = 0; q < 8; ++q) dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
@@ -1221,7 +1334,11 @@ __global__ void __launch_bounds__(480, 1)
         fence_proxy_async_smem();
         named_bar_sync(3, 128);
         if (tid == 0) {
-          tma_store_3d(map, smem_u32(stg), 0, sq.rb + tl.k0, sq.zh);
+          if (FA_CHECK(tma_coords_ok(0, sq.rb + tl.k0, sq.zh, C::D, bwd_ext(a, VL).rows_k, bwd_ext(a, VL).heads, 2, 128,
+                                     true) &&
+                           smem_in(smem_u32(stg), C::STG_BYTES, sbase + C::OFF_STG, sbase + C::OFF_LSE),
+                       st, DBG_TMA_STORE))
+            tma_store_3d(map, smem_u32(stg), 0, sq.rb + tl.k0, sq.zh);
           bulk_commit();
         }
       };

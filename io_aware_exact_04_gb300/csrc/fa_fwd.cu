@@ -74,6 +74,26 @@ __device__ __forceinline__ int key_tiles(int qs, int nq, int nkt, int causal, in
   return lim <= 0 ? 0 : min(nkt, (lim + 127) >> 7);
 }
 
+#ifdef FA_DEBUG
+// Extents that the debug build checks the forward's accesses against, each less the check slack:
+// rows per tensor-map head of Q / O and of K / V, the maps' outer extent, and the rows of O and
+// LSE and of the split partials in all; plain [B H, N, d] or packed [H, T, d] (vl) tensors.
+struct FwdExt {
+  int rows_q, rows_k, heads;
+  long long o_rows, part_rows;
+};
+__device__ __forceinline__ FwdExt fwd_ext(const FwdArgs& a, bool vl) {
+  const long long bh = (long long)a.dbg_B * a.H;
+  FwdExt e;
+  e.rows_q = (vl ? a.T : a.N) - a.dbg_slack;
+  e.rows_k = (vl ? a.T : a.Nk) - a.dbg_slack;
+  e.heads = vl ? a.H : (int)bh;
+  e.o_rows = (vl ? (long long)a.H * a.T : bh * a.N) - a.dbg_slack;
+  e.part_rows = 2LL * a.n_split * bh * a.N - a.dbg_slack;
+  return e;
+}
+#endif
+
 // SPLIT: the CTA (head, query pair, share z) runs key tiles [jb, je) of its item, the
 // z-th of a.n_split near-equal shares, and writes normalised partial O (fp32) and LSE to
 // slots 2z and 2z + 1 of a.part_o / a.part_lse for fwd_combine_kernel; the same
@@ -120,15 +140,19 @@ __global__ void __launch_bounds__(352, 1)
   size_t obase = (size_t)bh * a.N;
   if (VL) {
     const int h = bh - b * a.H;
-    rbase = a.cu_seqlens[b];
-    NQ = a.cu_seqlens[b + 1] - rbase;
+    if (FA_CHECK(in_range(b + 1, a.dbg_B + 1LL), a.status, DBG_META)) {
+      rbase = a.cu_seqlens[b];
+      NQ = a.cu_seqlens[b + 1] - rbase;
+    } else {
+      NQ = 0;
+    }
     zh = h;
     obase = (size_t)h * a.T + rbase;
     if (NQ > a.max_seqlen && threadIdx.x == 0 && blockIdx.y == 0) record_check(a.status, SITE_F_SEQLEN);
     if ((a.n_pairs - 1 - (int)blockIdx.y) * 256 >= NQ) return;  // this pair lies past the sequence
   }
   int kv = VL ? NQ : a.Nk;
-  if (!VL && a.kv_len) kv = min(max(a.kv_len[b], 0), a.Nk);
+  if (!VL && a.kv_len && FA_CHECK(in_range(b, a.dbg_B), a.status, DBG_META)) kv = min(max(a.kv_len[b], 0), a.Nk);
   const int nkt = (kv + 127) >> 7;
   const int q0 = pair * 256;
   int n_t[2];
@@ -169,10 +193,20 @@ __global__ void __launch_bounds__(352, 1)
     const uint32_t kd = sbase + C::OFF_K + s * C::TILE_BYTES, vd = sbase + C::OFF_V + s * C::TILE_BYTES;
     if (elect_one()) mbar_arrive_expect_tx(kf, C::TILE_BYTES);
     for (int c = 0; c < C::NSUB; ++c)
-      if (elect_one()) tma_load_3d(kd + c * C::SUB_BYTES, &tm_k, c * 64, rbase + (jb + j) * 128, zh, kf);
+      if (FA_CHECK(tma_coords_ok(c * 64, rbase + (jb + j) * 128, zh, D, fwd_ext(a, VL).rows_k, fwd_ext(a, VL).heads, 2,
+                                 128, false) &&
+                       smem_in(kd + c * C::SUB_BYTES, C::SUB_BYTES, sbase + C::OFF_K, sbase + C::OFF_V),
+                   st, DBG_TMA_LOAD) &&
+          elect_one())
+        tma_load_3d(kd + c * C::SUB_BYTES, &tm_k, c * 64, rbase + (jb + j) * 128, zh, kf);
     if (elect_one()) mbar_arrive_expect_tx(vf, C::TILE_BYTES);
     for (int c = 0; c < C::NSUB; ++c)
-      if (elect_one()) tma_load_3d(vd + c * C::SUB_BYTES, &tm_v, c * 64, rbase + (jb + j) * 128, zh, vf);
+      if (FA_CHECK(tma_coords_ok(c * 64, rbase + (jb + j) * 128, zh, D, fwd_ext(a, VL).rows_k, fwd_ext(a, VL).heads, 2,
+                                 128, false) &&
+                       smem_in(vd + c * C::SUB_BYTES, C::SUB_BYTES, sbase + C::OFF_V, sbase + C::OFF_BAR),
+                   st, DBG_TMA_LOAD) &&
+          elect_one())
+        tma_load_3d(vd + c * C::SUB_BYTES, &tm_v, c * 64, rbase + (jb + j) * 128, zh, vf);
     __syncwarp();
   };
   if (warp == 8) {
@@ -203,10 +237,15 @@ __global__ void __launch_bounds__(352, 1)
       const int nq = (n_t[1] > 0) ? 2 : 1;
       if (elect_one()) mbar_arrive_expect_tx(q_full, nq * C::TILE_BYTES);
       for (int t = 0; t < nq; ++t)
-        for (int s = 0; s < C::NSUB; ++s)
-          if (elect_one())
-            tma_load_3d(sbase + C::OFF_Q + t * C::TILE_BYTES + s * C::SUB_BYTES, &tm_q, s * 64,
-                        rbase + q0 + (dual ? 0 : t * 128), zh, q_full);
+        for (int s = 0; s < C::NSUB; ++s) {
+          const uint32_t dst = sbase + C::OFF_Q + t * C::TILE_BYTES + s * C::SUB_BYTES;
+          const int row = rbase + q0 + (dual ? 0 : t * 128);
+          if (FA_CHECK(tma_coords_ok(s * 64, row, zh, D, fwd_ext(a, VL).rows_q, fwd_ext(a, VL).heads, 2, 128, false) &&
+                           smem_in(dst, C::SUB_BYTES, sbase, sbase + C::OFF_K),
+                       st, DBG_TMA_LOAD) &&
+              elect_one())
+            tma_load_3d(dst, &tm_q, s * 64, row, zh, q_full);
+        }
       for (int j = 0; j < n_pre; ++j) load_kv(j);
     }
   }
@@ -255,6 +294,12 @@ __global__ void __launch_bounds__(352, 1)
       constexpr uint32_t TILE16 = C::TILE_BYTES >> 4;
       auto issue_s = [&](int t, int kst) {  // S_t = Q_t K^T (K from stage kst)
         const uint32_t qa = q_lo + t * TILE16, ka = k_lo + kst * TILE16, d = tmem + C::tm_s(t);
+        if (!FA_CHECK(smem_in(sbase + C::OFF_Q + t * C::TILE_BYTES, C::TILE_BYTES, sbase, sbase + C::OFF_K) &&
+                          smem_in(sbase + C::OFF_K + kst * C::TILE_BYTES, C::TILE_BYTES, sbase + C::OFF_K,
+                                  sbase + C::OFF_V),
+                      st, DBG_SMEM) ||
+            !FA_CHECK(tmem_in(d, 128, tmem, C::TM_COLS), st, DBG_TMEM))
+          return;
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
           const uint32_t off = ((k >> 2) * C::SUB_BYTES + (k & 3) * 32) >> 4;
@@ -263,6 +308,11 @@ __global__ void __launch_bounds__(352, 1)
       };
       auto issue_pv = [&](int t, int vst, uint32_t acc) {  // O_t += P_t V (V from stage vst)
         const uint32_t va = v_lo + vst * TILE16, d = tmem + C::tm_o(t), pa = tmem + C::tm_p(t);
+        if (!FA_CHECK(smem_in(sbase + C::OFF_V + vst * C::TILE_BYTES, C::TILE_BYTES, sbase + C::OFF_V,
+                              sbase + C::OFF_BAR),
+                      st, DBG_SMEM) ||
+            !FA_CHECK(tmem_in(d, D, tmem, C::TM_COLS) && tmem_in(pa, 64, tmem, C::TM_COLS), st, DBG_TMEM))
+          return;
 #pragma unroll
         for (int k = 0; k < 8; ++k)  // 128 keys, 16 per MMA
           if (elect_one()) mma_ts(d, pa + k * 8, sdesc_join(va + k * (2048 >> 4), HI), IDESC_O, (acc | k) != 0);
@@ -381,19 +431,25 @@ __global__ void __launch_bounds__(352, 1)
     // own result and an empty second slot)
     const size_t plane = (size_t)gridDim.x * a.N;
     const size_t prow = (size_t)(2 * blockIdx.z + (dual ? t : 0)) * plane + obase + grow;
-    if (SPLIT && !dual && grow < NQ && qs < NQ) a.part_lse[prow + plane] = -INFINITY;
+    if (SPLIT && !dual && grow < NQ && qs < NQ &&
+        FA_CHECK(in_range(prow + plane, fwd_ext(a, VL).part_rows), st, DBG_GLOBAL_STORE))
+      a.part_lse[prow + plane] = -INFINITY;
     if (qs < NQ && n == 0) {
       // no valid key for any row of this tile (in this share): O = 0, LSE = -inf
       if (grow < NQ) {
         if (SPLIT) {
-          a.part_lse[prow] = -INFINITY;  // the combine skips this slot's O
-        } else {
+          if (FA_CHECK(in_range(prow, fwd_ext(a, VL).part_rows), st, DBG_GLOBAL_STORE))
+            a.part_lse[prow] = -INFINITY;  // the combine skips this slot's O
+        } else if (FA_CHECK(in_range(obase + grow, fwd_ext(a, VL).o_rows), st, DBG_GLOBAL_STORE)) {
           uint4* orow = reinterpret_cast<uint4*>(a.o + (obase + grow) * D);
           for (int c = 0; c < D / 8; ++c) orow[c] = make_uint4(0, 0, 0, 0);
           lse_row[grow] = -INFINITY;
         }
       }
-    } else if (n > 0) {
+    } else if (n > 0 && FA_CHECK(tmem_in(tmem + C::tm_s(t), 128, tmem, C::TM_COLS) &&
+                                     tmem_in(tmem + C::tm_p(t), 64, tmem, C::TM_COLS) &&
+                                     tmem_in(tmem + C::tm_o(t), D, tmem, C::TM_COLS),
+                                 st, DBG_TMEM)) {
       float m_run = -INFINITY;  // running maximum of s*S*log2(e)
       float l_run = 0.f;        // running normaliser
       bool ok = true;
@@ -515,14 +571,14 @@ __global__ void __launch_bounds__(352, 1)
           uint32_t r[32];
           tmem_ld32(tO + c * 32, r);
           tmem_wait_ld();
-          if (grow < a.N) {
+          if (grow < a.N && FA_CHECK(in_range(prow, fwd_ext(a, VL).part_rows), st, DBG_GLOBAL_STORE)) {
 #pragma unroll
             for (int q = 0; q < 8; ++q)
               dst[c * 8 + q] = make_float4(__uint_as_float(r[4 * q]) * inv, __uint_as_float(r[4 * q + 1]) * inv,
                                            __uint_as_float(r[4 * q + 2]) * inv, __uint_as_float(r[4 * q + 3]) * inv);
           }
         }
-        if (grow < a.N)
+        if (grow < a.N && FA_CHECK(in_range(prow, fwd_ext(a, VL).part_rows), st, DBG_GLOBAL_STORE))
           a.part_lse[prow] = (l_run > 0.f) ? (m_run + lg2_approx(l_run)) * 0.6931471805599453f : -INFINITY;
       } else if (ok) {
         tc_fence_after();
@@ -548,18 +604,27 @@ __global__ void __launch_bounds__(352, 1)
             v.z = pack_bf16x2(__uint_as_float(r[q * 8 + 4]) * inv, __uint_as_float(r[q * 8 + 5]) * inv);
             v.w = pack_bf16x2(__uint_as_float(r[q * 8 + 6]) * inv, __uint_as_float(r[q * 8 + 7]) * inv);
             if (direct) {
-              if (grow < NQ) *reinterpret_cast<uint4*>(a.o + (obase + grow) * D + c * 32 + q * 8) = v;
-            } else {
+              if (grow < NQ && FA_CHECK(in_range(obase + grow, fwd_ext(a, VL).o_rows), st, DBG_GLOBAL_STORE))
+                *reinterpret_cast<uint4*>(a.o + (obase + grow) * D + c * 32 + q * 8) = v;
+            } else if (FA_CHECK(smem_in(smem_u32(stage + blk * C::SUB_BYTES + sw128_offset(row, chunk0 + q)), 16,
+                                        sbase + C::OFF_Q, sbase + C::OFF_K),
+                                st, DBG_SMEM)) {
               *reinterpret_cast<uint4*>(stage + blk * C::SUB_BYTES + sw128_offset(row, chunk0 + q)) = v;
             }
           }
         }
-        if (grow < NQ) lse_row[grow] = (l_run > 0.f) ? (m_run + lg2_approx(l_run)) * 0.6931471805599453f : -INFINITY;
+        if (grow < NQ && FA_CHECK(in_range(obase + grow, fwd_ext(a, VL).o_rows), st, DBG_GLOBAL_STORE))
+          lse_row[grow] = (l_run > 0.f) ? (m_run + lg2_approx(l_run)) * 0.6931471805599453f : -INFINITY;
         fence_proxy_async_smem();
         named_bar_sync(1 + t, 128);
         if (wq == 0 && lane == 0 && !direct) {
           for (int c = 0; c < C::NSUB; ++c)
-            tma_store_3d(&tm_o, smem_u32(stage + c * C::SUB_BYTES), c * 64, rbase + qs, zh);
+            if (FA_CHECK(tma_coords_ok(c * 64, rbase + qs, zh, D, fwd_ext(a, VL).rows_q, fwd_ext(a, VL).heads, 2, 128,
+                                       true) &&
+                             smem_in(smem_u32(stage + c * C::SUB_BYTES), C::SUB_BYTES, sbase + C::OFF_Q,
+                                     sbase + C::OFF_K),
+                         st, DBG_TMA_STORE))
+              tma_store_3d(&tm_o, smem_u32(stage + c * C::SUB_BYTES), c * 64, rbase + qs, zh);
           bulk_commit();
           bulk_wait_read0();  // the staging tile must outlive the copy's reads
         }
@@ -618,8 +683,13 @@ __device__ __forceinline__ RowsF64 rows_f64(int bh, const FwdArgs& a) {
   RowsF64 r;
   if (VL) {
     const int b = bh / a.H, h = bh - b * a.H;
-    r.rb = a.cu_seqlens[b];
-    r.nq = a.cu_seqlens[b + 1] - r.rb;
+    if (FA_CHECK(in_range(b + 1, a.dbg_B + 1LL), a.status, DBG_META)) {
+      r.rb = a.cu_seqlens[b];
+      r.nq = a.cu_seqlens[b + 1] - r.rb;
+    } else {
+      r.rb = 0;
+      r.nq = 0;
+    }
     r.zh = h;
     r.obase = (size_t)h * a.T + r.rb;
   } else {
@@ -642,7 +712,8 @@ __device__ __forceinline__ ItemF64 item_f64(int t, const FwdArgs& a, int BH) {
     it.kv = nq;
   } else {
     it.kv = a.Nk;
-    if (a.kv_len) it.kv = min(max(a.kv_len[it.bh / a.H], 0), a.Nk);
+    if (a.kv_len && FA_CHECK(in_range(it.bh / a.H, a.dbg_B), a.status, DBG_META))
+      it.kv = min(max(a.kv_len[it.bh / a.H], 0), a.Nk);
   }
   const int nkt = (it.kv + 127) >> 7;
 #pragma unroll
@@ -722,9 +793,20 @@ __global__ void __launch_bounds__(352, 1)
     const uint32_t kf = k_full(s), vf = v_full(s);
     const RowsF64 rw = rows_f64<VL>(bh, a);
     if (elect_one()) mbar_arrive_expect_tx(kf, C::TILE_BYTES);
-    if (elect_one()) tma_load_3d(sbase + C::OFF_K + s * C::TILE_BYTES, &tm_k, 0, rw.rb + j * 128, rw.zh, kf);
+    if (FA_CHECK(tma_coords_ok(0, rw.rb + j * 128, rw.zh, D, fwd_ext(a, VL).rows_k, fwd_ext(a, VL).heads, 2, 128,
+                               false) &&
+                     smem_in(sbase + C::OFF_K + s * C::TILE_BYTES, C::TILE_BYTES, sbase + C::OFF_K, sbase + C::OFF_V),
+                 st, DBG_TMA_LOAD) &&
+        elect_one())
+      tma_load_3d(sbase + C::OFF_K + s * C::TILE_BYTES, &tm_k, 0, rw.rb + j * 128, rw.zh, kf);
     if (elect_one()) mbar_arrive_expect_tx(vf, C::TILE_BYTES);
-    if (elect_one()) tma_load_3d(sbase + C::OFF_V + s * C::TILE_BYTES, &tm_v, 0, rw.rb + j * 128, rw.zh, vf);
+    if (FA_CHECK(tma_coords_ok(0, rw.rb + j * 128, rw.zh, D, fwd_ext(a, VL).rows_k, fwd_ext(a, VL).heads, 2, 128,
+                               false) &&
+                     smem_in(sbase + C::OFF_V + s * C::TILE_BYTES, C::TILE_BYTES, sbase + C::OFF_V,
+                             sbase + C::OFF_BAR),
+                 st, DBG_TMA_LOAD) &&
+        elect_one())
+      tma_load_3d(sbase + C::OFF_V + s * C::TILE_BYTES, &tm_v, 0, rw.rb + j * 128, rw.zh, vf);
     __syncwarp();
   };
   auto load_q = [&](int set, const ItemF64& it) {  // whole warp
@@ -732,7 +814,11 @@ __global__ void __launch_bounds__(352, 1)
     const RowsF64 rw = rows_f64<VL>(it.bh, a);
     if (elect_one()) mbar_arrive_expect_tx(q_full(set), nq * C::TILE_BYTES);
     for (int u = 0; u < nq; ++u)
-      if (elect_one())
+      if (FA_CHECK(tma_coords_ok(0, rw.rb + it.q0 + u * 128, rw.zh, D, fwd_ext(a, VL).rows_q, fwd_ext(a, VL).heads, 2,
+                                 128, false) &&
+                       smem_in(sbase + C::off_q(set, u), C::TILE_BYTES, sbase + C::OFF_Q, sbase + C::OFF_K),
+                   st, DBG_TMA_LOAD) &&
+          elect_one())
         tma_load_3d(sbase + C::off_q(set, u), &tm_q, 0, rw.rb + it.q0 + u * 128, rw.zh, q_full(set));
     __syncwarp();
   };
@@ -792,7 +878,9 @@ __global__ void __launch_bounds__(352, 1)
       if (VL && lane == 0 && it.q0 == 0 && rows_f64<VL>(it.bh, a).nq > a.max_seqlen)
         record_check(a.status, SITE_F_SEQLEN);  // the grid (sized by max_seqlen) misses rows of it
       if (it.nmax == 0) {
-        if (!VL) zero_rows_f64(a.o, a.lse, a.N, it.bh, it.q0, lane);
+        if (!VL && FA_CHECK(span_in((long long)it.bh * a.N + it.q0, min(256, a.N - it.q0), fwd_ext(a, VL).o_rows), st,
+                            DBG_GLOBAL_STORE))
+          zero_rows_f64(a.o, a.lse, a.N, it.bh, it.q0, lane);
         continue;
       }
       const int set = iu & 1;
@@ -833,12 +921,23 @@ __global__ void __launch_bounds__(352, 1)
     const uint32_t v_lo = sdesc_lo(sbase + C::OFF_V, C::TILE_BYTES);
     auto issue_s = [&](int set, int kst) {  // S_t = Q_t K^T (Q from set, K from stage kst)
       const uint32_t qa = sdesc_lo(sbase + C::off_q(set, t), 16), ka = k_lo + kst * TILE16, d = tmem + C::tm_s(t);
+      if (!FA_CHECK(smem_in(sbase + C::off_q(set, t), C::TILE_BYTES, sbase + C::OFF_Q, sbase + C::OFF_K) &&
+                        smem_in(sbase + C::OFF_K + kst * C::TILE_BYTES, C::TILE_BYTES, sbase + C::OFF_K,
+                                sbase + C::OFF_V),
+                    st, DBG_SMEM) ||
+          !FA_CHECK(tmem_in(d, 128, tmem, C::TM_COLS), st, DBG_TMEM))
+        return;
 #pragma unroll
       for (int k = 0; k < D / 16; ++k)
         if (elect_one()) mma_ss(d, sdesc_join(qa + 2 * k, HI), sdesc_join(ka + 2 * k, HI), IDESC_S, k > 0);
     };
     auto issue_pv = [&](int vst, uint32_t acc) {  // O_t += P_t V (V from stage vst)
       const uint32_t va = v_lo + vst * TILE16, d = tmem + C::tm_o(t), pa = tmem + C::tm_p(t);
+      if (!FA_CHECK(smem_in(sbase + C::OFF_V + vst * C::TILE_BYTES, C::TILE_BYTES, sbase + C::OFF_V,
+                            sbase + C::OFF_BAR),
+                    st, DBG_SMEM) ||
+          !FA_CHECK(tmem_in(d, D, tmem, C::TM_COLS) && tmem_in(pa, 64, tmem, C::TM_COLS), st, DBG_TMEM))
+        return;
 #pragma unroll
       for (int k = 0; k < 8; ++k)  // 128 keys, 16 per MMA
         if (elect_one()) mma_ts(d, pa + k * 8, sdesc_join(va + k * (2048 >> 4), HI), IDESC_O, (acc | k) != 0);
@@ -926,7 +1025,10 @@ __global__ void __launch_bounds__(352, 1)
     const uint32_t tP = tmem + lane_off + C::tm_p(t);
     const uint32_t tO = tmem + lane_off + C::tm_o(t);
     const float sl2 = a.scale_log2;
-    bool ok = true;
+    bool ok = FA_CHECK(tmem_in(tmem + C::tm_s(t), 128, tmem, C::TM_COLS) &&
+                           tmem_in(tmem + C::tm_p(t), 64, tmem, C::TM_COLS) &&
+                           tmem_in(tmem + C::tm_o(t), D, tmem, C::TM_COLS),
+                       st, DBG_TMEM);
     int iu = 0, gj = 0;
     ItemF64 it;
     for (int r = next_item(0, it); ok && r >= 0; r = next_item(r + 1, it)) {
@@ -940,7 +1042,8 @@ __global__ void __launch_bounds__(352, 1)
       if (!VL && qs < a.N && n == 0) {
         // no valid key for any row of this tile: O = 0, LSE = -inf (packed: no such tile, the
         // rows past a sequence belong to the next one)
-        if (grow < a.N) {
+        if (grow < a.N &&
+            FA_CHECK(in_range((long long)it.bh * a.N + grow, fwd_ext(a, VL).o_rows), st, DBG_GLOBAL_STORE)) {
           uint4* orow = reinterpret_cast<uint4*>(a.o + ((size_t)it.bh * a.N + grow) * D);
           for (int c = 0; c < D / 8; ++c) orow[c] = make_uint4(0, 0, 0, 0);
           a.lse[(size_t)it.bh * a.N + grow] = -INFINITY;
@@ -1080,18 +1183,24 @@ __global__ void __launch_bounds__(352, 1)
           v.z = pack_bf16x2(__uint_as_float(x[4]) * inv, __uint_as_float(x[5]) * inv);
           v.w = pack_bf16x2(__uint_as_float(x[6]) * inv, __uint_as_float(x[7]) * inv);
           if (direct) {
-            if (grow < rw.nq) *reinterpret_cast<uint4*>(a.o + (rw.obase + grow) * D + q * 8) = v;
-          } else {
+            if (grow < rw.nq && FA_CHECK(in_range(rw.obase + grow, fwd_ext(a, VL).o_rows), st, DBG_GLOBAL_STORE))
+              *reinterpret_cast<uint4*>(a.o + (rw.obase + grow) * D + q * 8) = v;
+          } else if (FA_CHECK(smem_in(smem_u32(stage + sw128_offset(row, q)), 16, sbase + C::OFF_Q, sbase + C::OFF_K),
+                              st, DBG_SMEM)) {
             *reinterpret_cast<uint4*>(stage + sw128_offset(row, q)) = v;
           }
         }
-        if (grow < rw.nq)
+        if (grow < rw.nq && FA_CHECK(in_range(rw.obase + grow, fwd_ext(a, VL).o_rows), st, DBG_GLOBAL_STORE))
           a.lse[rw.obase + grow] = (l_run > 0.f) ? (m_run + lg2_approx(l_run)) * 0.6931471805599453f : -INFINITY;
         fence_proxy_async_smem();
         named_bar_sync(1 + t, 128);
         if (wq == 0 && lane == 0) {
           if (!direct) {
-            tma_store_3d(&tm_o, smem_u32(stage), 0, rw.rb + qs, rw.zh);
+            if (FA_CHECK(tma_coords_ok(0, rw.rb + qs, rw.zh, D, fwd_ext(a, VL).rows_q, fwd_ext(a, VL).heads, 2, 128,
+                                       true) &&
+                             smem_in(smem_u32(stage), C::TILE_BYTES, sbase + C::OFF_Q, sbase + C::OFF_K),
+                         st, DBG_TMA_STORE))
+              tma_store_3d(&tm_o, smem_u32(stage), 0, rw.rb + qs, rw.zh);
             bulk_commit();
             bulk_wait_read0();  // the Q_t buffer is free again once the store has read it
           }
@@ -1134,7 +1243,11 @@ __global__ void __launch_bounds__(256) fwd_combine_kernel(FwdArgs a) {
   for (int z0 = 0; z0 < nz; z0 += G) {
     float l[G];
 #pragma unroll
-    for (int g = 0; g < G; ++g) l[g] = (z0 + g < nz) ? a.part_lse[(z0 + g) * plane + row] : -INFINITY;
+    for (int g = 0; g < G; ++g)
+      l[g] = (z0 + g < nz && FA_CHECK(in_range((z0 + g) * plane + row, fwd_ext(a, false).part_rows), a.status,
+                                      DBG_GLOBAL_LOAD))
+                 ? a.part_lse[(z0 + g) * plane + row]
+                 : -INFINITY;
 #pragma unroll
     for (int g = 0; g < G; ++g) mx = fmaxf(mx, l[g]);
   }
@@ -1146,7 +1259,11 @@ __global__ void __launch_bounds__(256) fwd_combine_kernel(FwdArgs a) {
       float4 x0[G], x1[G];
 #pragma unroll
       for (int g = 0; g < G; ++g) {
-        const float lz = (z0 + g < nz) ? a.part_lse[(z0 + g) * plane + row] : -INFINITY;
+        // a slot out of range reads as one without keys (its O is then not read either)
+        const float lz = (z0 + g < nz && FA_CHECK(in_range((z0 + g) * plane + row, fwd_ext(a, false).part_rows),
+                                                  a.status, DBG_GLOBAL_LOAD))
+                             ? a.part_lse[(z0 + g) * plane + row]
+                             : -INFINITY;
         w[g] = (lz == -INFINITY) ? 0.f : ex2_approx((lz - mx) * 1.4426950408889634f);
         const float4* src = reinterpret_cast<const float4*>(a.part_o + ((z0 + g) * plane + row) * D + part * 8);
         // a slot without keys holds no O: read nothing there
@@ -1169,6 +1286,7 @@ __global__ void __launch_bounds__(256) fwd_combine_kernel(FwdArgs a) {
   out.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
   out.z = pack_bf16x2(acc[4] * inv, acc[5] * inv);
   out.w = pack_bf16x2(acc[6] * inv, acc[7] * inv);
+  if (!FA_CHECK(in_range(row, fwd_ext(a, false).o_rows), a.status, DBG_GLOBAL_STORE)) return;
   *reinterpret_cast<uint4*>(a.o + row * D + part * 8) = out;
   if (part == 0 && a.lse) a.lse[row] = (wsum > 0.f) ? mx + lg2_approx(wsum) * 0.6931471805599453f : -INFINITY;
 }
@@ -1217,7 +1335,7 @@ enum { SITE_D_FULL = 11, SITE_D_EMPTY, SITE_D_SYNC };
 // 128-key tiles of each head of batch b: its valid keys, rounded up.
 __device__ __forceinline__ int dec_tiles(const FwdArgs& a, int b) {
   int kv = a.Nk;
-  if (a.kv_len) kv = min(max(a.kv_len[b], 0), a.Nk);
+  if (a.kv_len && FA_CHECK(in_range(b, a.dbg_B), a.status, DBG_META)) kv = min(max(a.kv_len[b], 0), a.Nk);
   return (kv + 127) >> 7;
 }
 
@@ -1337,8 +1455,13 @@ __global__ void __launch_bounds__(288, 1)
           if (!(ok = wait_warp_sleep(empty(s), ((g / NS) & 1) ^ 1, st, SITE_D_EMPTY))) break;
           if (elect_one()) mbar_arrive_expect_tx(full(s), 2 * C::TILE);
           for (int c = 0; c < C::NSUB; ++c) {
-            if (elect_one()) tma_load_3d(sbase + C::OFF_K + s * C::TILE + c * 16384, &tm_k, c * 64, t * 128, bh, full(s));
-            if (elect_one()) tma_load_3d(sbase + C::OFF_V + s * C::TILE + c * 16384, &tm_v, c * 64, t * 128, bh, full(s));
+            const bool in = FA_CHECK(
+                tma_coords_ok(c * 64, t * 128, bh, D, fwd_ext(a, false).rows_k, fwd_ext(a, false).heads, 2, 128, false) &&
+                    smem_in(sbase + C::OFF_K + s * C::TILE + c * 16384, 16384, sbase + C::OFF_K, sbase + C::OFF_V) &&
+                    smem_in(sbase + C::OFF_V + s * C::TILE + c * 16384, 16384, sbase + C::OFF_V, sbase + C::OFF_BAR),
+                st, DBG_TMA_LOAD);
+            if (in && elect_one()) tma_load_3d(sbase + C::OFF_K + s * C::TILE + c * 16384, &tm_k, c * 64, t * 128, bh, full(s));
+            if (in && elect_one()) tma_load_3d(sbase + C::OFF_V + s * C::TILE + c * 16384, &tm_v, c * 64, t * 128, bh, full(s));
           }
           __syncwarp();
         }
@@ -1360,6 +1483,7 @@ __global__ void __launch_bounds__(288, 1)
       if (dec_tiles(a, bh / a.H) > 0) continue;
       for (int idx = tid; idx < nq * D; idx += 256) {
         const size_t row = (size_t)bh * nq + idx / D;
+        if (!FA_CHECK(in_range(row, fwd_ext(a, false).o_rows), st, DBG_GLOBAL_STORE)) continue;
         a.o[row * D + idx % D] = 0;
         if (idx % D == 0 && a.lse) a.lse[row] = -INFINITY;
       }
@@ -1373,12 +1497,14 @@ __global__ void __launch_bounds__(288, 1)
     for (long long gt = g0, seg = 0; ok && gt < g1; ++seg) {
       const int bh = cur.b * a.H + cur.h;
       const int ta = (int)(gt - cur.gbase), te = (int)min(g1 - cur.gbase, (long long)cur.tb);
-      const int kv = a.kv_len ? min(max(a.kv_len[cur.b], 0), a.Nk) : a.Nk;
+      const int kv = (a.kv_len && FA_CHECK(in_range(cur.b, a.dbg_B), st, DBG_META))
+                         ? min(max(a.kv_len[cur.b], 0), a.Nk)
+                         : a.Nk;
       const int j1 = min(te * 128, kv);  // the segment's keys end here
       for (int idx = tid; idx < NQ * (D / 4); idx += 256) {
         const int i = idx / (D / 4), c = idx % (D / 4);
         float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (i < nq) {
+        if (i < nq && FA_CHECK(in_range((size_t)bh * nq + i, fwd_ext(a, false).o_rows), st, DBG_GLOBAL_LOAD)) {
           const uint2 w = *reinterpret_cast<const uint2*>(q + ((size_t)bh * nq + i) * D + 4 * c);
           f = make_float4(__uint_as_float(w.x << 16) * a.scale_log2, __uint_as_float(w.x & 0xFFFF0000u) * a.scale_log2,
                           __uint_as_float(w.y << 16) * a.scale_log2, __uint_as_float(w.y & 0xFFFF0000u) * a.scale_log2);
@@ -1403,6 +1529,10 @@ __global__ void __launch_bounds__(288, 1)
         for (int t = ta; t < te; ++t, ++g) {
           const int s = g % NS;
           if (!(wok = wait_warp_sleep(full(s), (g / NS) & 1, st, SITE_D_FULL))) break;
+          wok = FA_CHECK(smem_in(sbase + C::OFF_K + s * C::TILE, C::TILE, sbase + C::OFF_K, sbase + C::OFF_V) &&
+                             smem_in(sbase + C::OFF_V + s * C::TILE, C::TILE, sbase + C::OFF_V, sbase + C::OFF_BAR),
+                         st, DBG_SMEM);
+          if (!wok) break;
           const uint8_t* kt = sm + C::OFF_K + s * C::TILE;
           const uint8_t* vt = sm + C::OFF_V + s * C::TILE;
           const int jj = t * 128 + key;
@@ -1492,6 +1622,10 @@ __global__ void __launch_bounds__(288, 1)
           const int s = g % NS;
           const int jb = t * 128;
           if (!(wok = wait_warp_sleep(full(s), (g / NS) & 1, st, SITE_D_FULL))) break;
+          wok = FA_CHECK(smem_in(sbase + C::OFF_K + s * C::TILE, C::TILE, sbase + C::OFF_K, sbase + C::OFF_V) &&
+                             smem_in(sbase + C::OFF_V + s * C::TILE, C::TILE, sbase + C::OFF_V, sbase + C::OFF_BAR),
+                         st, DBG_SMEM);
+          if (!wok) break;
           const uint8_t* kt = sm + C::OFF_K + s * C::TILE;
           const uint8_t* vt = sm + C::OFF_V + s * C::TILE;
           const int jj = jb + key;
@@ -1599,10 +1733,12 @@ __global__ void __launch_bounds__(288, 1)
         const float ov = (lsum > 0.f) ? acc / lsum : 0.f;
         if (whole) {
           const size_t row = (size_t)bh * nq + i;
+          if (!FA_CHECK(in_range(row, fwd_ext(a, false).o_rows), st, DBG_GLOBAL_STORE)) continue;
           a.o[row * D + d] = (uint16_t)(pack_bf16x2(ov, 0.f) & 0xFFFFu);
           if (d == 0 && a.lse) a.lse[row] = lse;
         } else {
           const size_t row = (size_t)slot * nq + i;
+          if (!FA_CHECK(in_range(row, fwd_ext(a, false).part_rows), st, DBG_GLOBAL_STORE)) continue;
           a.part_o[row * D + d] = ov;
           if (d == 0) a.part_lse[row] = lse;
         }
@@ -1662,6 +1798,7 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(FwdArgs a, int B, i
   if (clo == chi) return;  // one CTA held the whole head and wrote it
   const int nseg = chi - clo + 1, nq = a.N;
   // entry e: CTA clo + e, its slot (or -1: a CTA without tiles)
+  if (!FA_CHECK(nseg <= kDecodeMaxCtas && nq <= kDecodeMaxRows, a.status, DBG_SMEM)) return;
   if (tid < nseg) {
     const int c = clo + tid;
     const long long st0 = (long long)c * T / G, st1 = (long long)(c + 1) * T / G;
@@ -1670,7 +1807,10 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(FwdArgs a, int B, i
   __syncthreads();
   for (int idx = tid; idx < nseg * nq; idx += 256) {
     const int e = idx / nq, i = idx - e * nq;
-    lses[e][i] = slots[e] < 0 ? -INFINITY : a.part_lse[(size_t)slots[e] * nq + i];
+    lses[e][i] = (slots[e] < 0 || !FA_CHECK(in_range((size_t)slots[e] * nq + i, fwd_ext(a, false).part_rows),
+                                            a.status, DBG_GLOBAL_LOAD))
+                     ? -INFINITY
+                     : a.part_lse[(size_t)slots[e] * nq + i];
   }
   __syncthreads();
   if (tid < nq) {
@@ -1694,6 +1834,7 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(FwdArgs a, int B, i
       }
     }
     const size_t row = (size_t)bh * nq + i;
+    if (!FA_CHECK(in_range(row, fwd_ext(a, false).o_rows), a.status, DBG_GLOBAL_STORE)) continue;
     a.o[row * D + d] = (uint16_t)(pack_bf16x2(wsum > 0.f ? acc / wsum : 0.f, 0.f) & 0xFFFFu);
     if (d == 0 && a.lse) a.lse[row] = (wsum > 0.f) ? mx + lg2_approx(wsum) * 0.6931471805599453f : -INFINITY;
   }

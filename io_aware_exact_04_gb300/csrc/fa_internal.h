@@ -23,6 +23,10 @@ struct FwdArgs {
                        // each normalised by its own l
   float* part_lse;     // split-KV: [2 n_split, B*H, N] fp32 LSE of each slot (-inf: no key)
   int* status;         // device status word (4 ints)
+#ifdef FA_DEBUG
+  int dbg_B;           // batch count B, for the extents the debug build checks against
+  int dbg_slack;       // rows taken off those extents (fa_debug_set_check_slack)
+#endif
 };
 
 // Packed sequences ([H, T, d], cu_seqlens) reuse four fields that mean nothing there (no key
@@ -48,12 +52,31 @@ struct BwdArgs {
   uint16_t* dk;        // [B*H, N, d] bf16
   uint16_t* dv;        // [B*H, N, d] bf16
   int* status;
+#ifdef FA_DEBUG
+  int dbg_B;           // batch count B, for the extents the debug build checks against
+  int dbg_slack;       // rows taken off those extents (fa_debug_set_check_slack)
+#endif
 };
 __host__ __device__ inline const int* vl_cu(const BwdArgs& a) { return a.kv_len; }
 __host__ __device__ inline int vl_maxlen(const BwdArgs& a) { return a.N; }
 __host__ __device__ inline int vl_T(const BwdArgs& a) { return a.Nk; }
 __host__ __device__ inline int vl_Lpad(const BwdArgs& a) { return a.coff; }
 
+
+// Debug build: the batch count and the current check slack into the kernels' arguments (no-op in
+// every other build).
+#ifdef FA_DEBUG
+int debug_check_slack();
+#define FA_DEBUG_ARGS(args, B)            \
+  do {                                    \
+    (args).dbg_B = (B);                   \
+    (args).dbg_slack = ::fa::debug_check_slack(); \
+  } while (0)
+#else
+#define FA_DEBUG_ARGS(args, B) \
+  do {                         \
+  } while (0)
+#endif
 
 // Argument checks shared by every entry point: sizes non-negative, causal 0 or 1, scale finite
 // and positive (FA_ERR_INVALID_ARG); d in {64, 128}, B * H <= 65535, lengths within 32-bit

@@ -23,6 +23,35 @@ def test_exports_every_declared_function(built, header, so):
     assert set(names) == set(_lib.SIGNATURES[so]), "binding signatures and header disagree"
 
 
+def test_debug_build_exports_the_abi_and_its_own_entry_point(built):
+    """libfa_debug.so (bounds-checked build) carries fa.h unchanged plus fa_debug.h; the
+    library's own build has no debug entry point."""
+    dbg = _lib.load("libfa_debug.so")
+    extra = _lib.declared_functions("fa_debug.h")
+    assert extra == ["fa_debug_set_check_slack"]
+    for name in _lib.declared_functions("fa.h") + extra:
+        assert hasattr(dbg, name), name
+    assert set(_lib.SIGNATURES["libfa_debug.so"]) == set(extra)
+    assert not hasattr(_lib.load("libfa.so"), "fa_debug_set_check_slack")
+    # host-side argument check, no CUDA call
+    assert dbg.fa_debug_set_check_slack(-1) == 1
+    assert dbg.fa_debug_set_check_slack(0) == 0
+
+
+def test_debug_sites_match_the_header():
+    """The site numbers the kernels record are the ones fa_debug.h publishes."""
+    import os
+    import re
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    with open(os.path.join(root, "include", "fa_debug.h")) as fh:
+        header = dict((k, int(v)) for k, v in re.findall(r"(FA_DBG_[A-Z_]+) = (\d+)", fh.read()))
+    assert header == {"FA_DBG_META": 100, "FA_DBG_TMA_LOAD": 101, "FA_DBG_TMA_STORE": 102, "FA_DBG_BULK": 103,
+                      "FA_DBG_GLOBAL_LOAD": 104, "FA_DBG_GLOBAL_STORE": 105, "FA_DBG_SMEM": 106, "FA_DBG_TMEM": 107}
+    with open(os.path.join(root, "io_aware_exact_04_gb300", "csrc", "common.cuh")) as fh:
+        aliases = re.findall(r"DBG_([A-Z_]+) = FA_DBG_([A-Z_]+)", fh.read())
+    assert len(aliases) == len(header) and all(a == b for a, b in aliases)
+
+
 def test_status_strings(lib):
     for code in range(7):
         assert lib.fa_status_string(code)
