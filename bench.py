@@ -9,7 +9,9 @@ workload, whose K/V cache alone exceeds L2, rotates over copies of its inputs
 instead, so no flush's dirty lines are written back inside its step). The JSON
 line reports nominal fwd+bwd TFLOP/s (12 c N^2 d per head, recompute FLOPs
 excluded and reported separately), the roofline of the dominant kernel, the
-end-to-end number through host buffers, the oracle on host cores, peak
+end-to-end number through host buffers (every step uploads its inputs and
+downloads its outputs; the copies overlap the neighbouring steps' compute, and
+the serial schedule is reported beside it), the oracle on host cores, peak
 activation memory and the SM clocks seen while timing.
 
 --impl reference times the fp64 CPU oracle instead (the only reference this
@@ -21,6 +23,7 @@ independent: weak scaling, no collective on the data path).
 from __future__ import annotations
 
 import argparse
+import copy
 import hashlib
 import json
 import math
@@ -254,6 +257,66 @@ def source_hash(files):
         with open(os.path.join(ROOT, fn), "rb") as f:
             h.update(f.read())
     return h.hexdigest()
+
+
+E2E_PIPELINED = ("pipelined: each step uploads its inputs (pinned host -> device, copy stream), runs fwd+bwd and "
+                 "downloads O, LSE, dQ, dK, dV (device -> pinned host, a second copy stream); uploads and downloads "
+                 "overlap the neighbouring steps' compute, two device buffer sets, L2 flushed before every step "
+                 "inside the timed region")
+E2E_SERIAL = ("upload, compute, download, synchronise, step after step; L2 flushed before each step, outside the "
+              "timed region")
+
+
+def pipelined_e2e(dev, sets, host_in, host_out, flush, steps):
+    """Milliseconds per step of `steps` end-to-end steps whose host copies overlap compute.
+
+    Each step uploads its inputs from pinned host memory, runs the whole path and downloads
+    its outputs, as in a training or serving loop that prefetches. Step i's upload (one
+    copy stream) runs while step i - 1 computes. Its download (another copy stream) runs
+    while step i + 1 computes. `sets` are two device buffer sets used in turn, each an
+    (inputs, outputs, step) triple. A set is reused only after the step two back has
+    finished with it: its compute for the inputs, its download for the outputs. L2 is
+    flushed on the compute stream before every step's kernels, inside the timed region.
+    The timed region runs from the first upload to the last download, between device
+    synchronisations."""
+    import torch
+    comp = torch.cuda.current_stream(dev)
+    up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+
+    def run(k):
+        ready = [torch.cuda.Event() for _ in range(k)]
+        done = [torch.cuda.Event() for _ in range(k)]
+        read = [torch.cuda.Event() for _ in range(k)]
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        t0.record(comp)
+        up.wait_event(t0)
+        for i in range(k):
+            ins, outs, step = sets[i % 2]
+            with torch.cuda.stream(up):
+                if i >= 2:
+                    up.wait_event(done[i - 2])  # the set's inputs are no longer read
+                for dst, src in zip(ins, host_in):
+                    dst.copy_(src, non_blocking=True)
+                ready[i].record(up)
+            comp.wait_event(ready[i])
+            if i >= 2:
+                comp.wait_event(read[i - 2])  # the set's outputs have been downloaded
+            flush.zero_()
+            step()
+            done[i].record(comp)
+            with torch.cuda.stream(down):
+                down.wait_event(done[i])
+                for dst, src in zip(host_out, outs):
+                    dst.copy_(src, non_blocking=True)
+                read[i].record(down)
+        comp.wait_event(read[k - 1])
+        t1.record(comp)
+        t1.synchronize()
+        return t0.elapsed_time(t1)
+
+    run(2)  # the streams, events and second buffer set warmed up
+    return run(steps) / steps
 
 
 # ------------------------------------------------------------------ main arms
@@ -551,8 +614,18 @@ def run_gpu(args, w):
         if i >= 2:
             e2e_ms += e0.elapsed_time(e1)
     e2e_ms /= e2e_steps
+    serial_ms, serial_rate = job_throughput(e2e_ms, fl["fwd_bwd_nominal"], device=dev)
+    # ... and pipelined: the same steps with their copies overlapping the neighbouring steps'
+    # compute (two device buffer sets; the workspace and the compute stream are shared)
+    T = copy.copy(S)
+    T.q, T.k, T.v, T.do = (torch.empty_like(t) for t in (S.q, S.k, S.v, S.do))
+    T.o, T.lse, T.dq, T.dk, T.dv = (torch.empty_like(t) for t in (S.o, S.lse, S.dq, S.dk, S.dv))
+    sets = [((b.q, b.k, b.v, b.do), (b.o, b.lse, b.dq, b.dk, b.dv), b.step) for b in (S, T)]
+    e2e_ms = pipelined_e2e(dev, sets, (hq, hk, hv, hdo), (ho, hlse, hdq, hdk, hdv), flush, e2e_steps)
+    S.status("after the end-to-end steps")
     e2e_ms, e2e_rate = job_throughput(e2e_ms, fl["fwd_bwd_nominal"], device=dev)
     e2e_val = e2e_rate / 1e12
+    del T, sets
 
     clocks = sampler.stop() if rank == 0 else None
 
@@ -621,7 +694,9 @@ def run_gpu(args, w):
         "roofline": roof,
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": e2e_ms, "steps": e2e_steps},
+                "ms_per_step": e2e_ms, "steps": e2e_steps,
+                "schedule": E2E_PIPELINED,
+                "serial": {"value": serial_rate / 1e12, "ms_per_step": serial_ms, "schedule": E2E_SERIAL}},
         "gpu_launches": 4 * args.steps,
         "clocks": clocks,
     }
@@ -936,11 +1011,15 @@ def run_gpu_packed(args, w):
     P = lambda t: ctypes.c_void_p(t.data_ptr()) if t is not None else None  # noqa: E731
     causal = int(w.causal)
 
-    def step():
-        _lib.check(lib.fa_forward_varlen(P(q), P(k), P(v), P(o), P(lse), P(cu), B, H, T, maxlen, d, w.scale, causal,
-                                         sp), "fwd_varlen")
-        _lib.check(lib.fa_backward_varlen(P(q), P(k), P(v), P(o), P(do), P(lse), P(dq), P(dk), P(dv), P(cu), B, H, T,
-                                          maxlen, d, w.scale, causal, P(work), wsb, sp), "bwd_varlen")
+    def make_step(q, k, v, do, o, lse, dq, dk, dv):
+        def step():
+            _lib.check(lib.fa_forward_varlen(P(q), P(k), P(v), P(o), P(lse), P(cu), B, H, T, maxlen, d, w.scale,
+                                             causal, sp), "fwd_varlen")
+            _lib.check(lib.fa_backward_varlen(P(q), P(k), P(v), P(o), P(do), P(lse), P(dq), P(dk), P(dv), P(cu), B, H,
+                                              T, maxlen, d, w.scale, causal, P(work), wsb, sp), "bwd_varlen")
+        return step
+
+    step = make_step(q, k, v, do, o, lse, dq, dk, dv)
 
     for _ in range(max(3, args.warmup)):
         flush.zero_()
@@ -998,7 +1077,16 @@ def run_gpu_packed(args, w):
         e1.synchronize()
         if i >= 2:
             e2e_ms += e0.elapsed_time(e1)
-    e2e_ms, e2e_rate = job_throughput(e2e_ms / e2e_steps, fl, device=dev)
+    serial_ms, serial_rate = job_throughput(e2e_ms / e2e_steps, fl, device=dev)
+    # ... and pipelined (two device buffer sets; the workspace and the compute stream are shared)
+    second = [torch.empty_like(t) for t in (q, k, v, do, o, lse, dq, dk, dv)]
+    sets = [((q, k, v, do), (o, dq, dk, dv, lse), step),
+            (tuple(second[:4]), (second[4], second[6], second[7], second[8], second[5]), make_step(*second))]
+    e2e_ms = pipelined_e2e(dev, sets, tuple(hb[n] for n in ("q", "k", "v", "do")), (*ho, hlse), flush, e2e_steps)
+    if lib.fa_get_last_device_status_detail(sp, detail) != 0:
+        raise RuntimeError(f"device status after the end-to-end steps: {list(detail)}")
+    e2e_ms, e2e_rate = job_throughput(e2e_ms, fl, device=dev)
+    del second, sets
     clocks = sampler.stop() if rank == 0 else None
     if ws > 1:
         torch.distributed.barrier()
@@ -1017,7 +1105,8 @@ def run_gpu_packed(args, w):
         "roofline": roof,
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_rate / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": e2e_ms, "steps": e2e_steps},
+                "ms_per_step": e2e_ms, "steps": e2e_steps, "schedule": E2E_PIPELINED,
+                "serial": {"value": serial_rate / 1e12, "ms_per_step": serial_ms, "schedule": E2E_SERIAL}},
         "gpu_launches": 4 * args.steps,
         "clocks": clocks,
     }
