@@ -973,18 +973,22 @@ __global__ void __launch_bounds__(352, 1)
             tc_fence_after();
             issue_s(set, (g + 1) % NST);
             commit(s_full(t));
-          } else if (r2 >= 0 && (t == 0 ? nx.n[0] : nx.n[1]) > 0 && it.nmax - n <= NST) {
-            // ... and S_t(0) of the next item. Its Q goes out after this item's last K/V copy,
-            // which waits for this warp's release of ring slot g0 + nmax - 1 - NST: processed
-            // already when nmax - n <= NST (always for causal and full tiles).
+          } else if (r2 >= 0 && (t == 0 ? nx.n[0] : nx.n[1]) > 0) {
+            // ... and S_t(0) of the next item, if its Q and first K tile have landed already.
+            // Waiting for them here would hold up PV_t(j), and with it this item's epilogue;
+            // otherwise S_t(0) is issued at the next item's start.
             const int g2 = g0 + it.nmax;
-            if (!(ok = wait_warp_sleep(q_full(set ^ 1), ((iu + 1) >> 1) & 1, st, SITE_F_Q_FULL))) break;
-            if (!(ok = wait_warp_sleep(k_full(g2 % NST), (g2 / NST) & 1, st, SITE_F_K_FULL))) break;
-            if (!(ok = wait_warp_sleep(s_free(t), (gj + j) & 1, st, SITE_F_S_FREE))) break;
-            tc_fence_after();
-            issue_s(set ^ 1, g2 % NST);
-            commit(s_full(t));
-            s0_issued = true;
+            bool rdy = false;
+            if (lane == 0)
+              rdy = mbar_test_wait(q_full(set ^ 1), ((iu + 1) >> 1) & 1) &&
+                    mbar_test_wait(k_full(g2 % NST), (g2 / NST) & 1);
+            if (__shfl_sync(0xffffffffu, rdy, 0)) {
+              if (!(ok = wait_warp_sleep(s_free(t), (gj + j) & 1, st, SITE_F_S_FREE))) break;
+              tc_fence_after();
+              issue_s(set ^ 1, g2 % NST);
+              commit(s_full(t));
+              s0_issued = true;
+            }
           }
           if (!(ok = wait_warp_sleep(v_full(s), ph, st, SITE_F_V_FULL))) break;
           if (!(ok = wait_warp_sleep(p_ready(t), (gj + j) & 1, st, SITE_F_P_READY))) break;
@@ -1030,6 +1034,18 @@ __global__ void __launch_bounds__(352, 1)
                            tmem_in(tmem + C::tm_o(t), D, tmem, C::TM_COLS),
                        st, DBG_TMEM);
     int iu = 0, gj = 0;
+    // Q_t set whose O store (issued by warp 0 of this warpgroup) may still be reading it: the
+    // wait for those reads, and the set's release to the producer, come after the warpgroup's
+    // next S wait, off the path from one item to the next
+    int pend = -1;
+    auto release_pending = [&]() {
+      if (pend >= 0 && wq == 0 && lane == 0) {
+        bulk_wait_read0();
+        mbar_arrive(q_empty(pend));
+      }
+      __syncwarp();
+      pend = -1;
+    };
     ItemF64 it;
     for (int r = next_item(0, it); ok && r >= 0; r = next_item(r + 1, it)) {
       // only n, qs and kv live through the key loop; the rest of the item is recomputed for
@@ -1055,6 +1071,7 @@ __global__ void __launch_bounds__(352, 1)
           const uint32_t par = (gj + j) & 1;
           ok = wait_warp_sleep(s_full(t), par, st, SITE_F_S_FULL);
           if (!ok) break;
+          if (pend >= 0) release_pending();
           tc_fence_after();
           float sv[128];
           {
@@ -1194,24 +1211,29 @@ __global__ void __launch_bounds__(352, 1)
           a.lse[rw.obase + grow] = (l_run > 0.f) ? (m_run + lg2_approx(l_run)) * 0.6931471805599453f : -INFINITY;
         fence_proxy_async_smem();
         named_bar_sync(1 + t, 128);
-        if (wq == 0 && lane == 0) {
-          if (!direct) {
+        if (!direct) {
+          if (wq == 0 && lane == 0) {
             if (FA_CHECK(tma_coords_ok(0, rw.rb + qs, rw.zh, D, fwd_ext(a, VL).rows_q, fwd_ext(a, VL).heads, 2, 128,
                                        true) &&
                              smem_in(smem_u32(stage), C::TILE_BYTES, sbase + C::OFF_Q, sbase + C::OFF_K),
                          st, DBG_TMA_STORE))
               tma_store_3d(&tm_o, smem_u32(stage), 0, rw.rb + qs, rw.zh);
             bulk_commit();
-            bulk_wait_read0();  // the Q_t buffer is free again once the store has read it
           }
+          pend = set;  // the Q_t buffer is free again once the store has read it
+        } else if (wq == 0 && lane == 0) {
           mbar_arrive(q_empty(set));
         }
         stored = true;
       }
-      if (!stored && wq == 0 && lane == 0) mbar_arrive(q_empty(iu & 1));  // nothing staged in Q_t
+      if (!stored) {  // nothing staged in Q_t; a pending set is released first (the producer may need it)
+        release_pending();
+        if (wq == 0 && lane == 0) mbar_arrive(q_empty(iu & 1));
+      }
       gj += n;
       ++iu;
     }
+    release_pending();
   }
 
   tc_fence_before();
