@@ -496,11 +496,14 @@ __global__ void __launch_bounds__(448, 1)
                    IDESC_Q, k > 0);
         }
       };
-      // Step i: S^T(i + 1) goes into the other S^T buffer as soon as its Q has landed (that
-      // buffer's P^T(i - 1) has been read by dV(i - 1), issued before, and by the warpgroups'
-      // dS^T(i - 1), waited for), so the warpgroups find it ready when they finish step i; then
+      // Step i: once P^T(i) is complete, S^T(i + 1) goes into the other S^T buffer (whose
+      // P^T(i - 1) has been read by dV(i - 1), issued before, and by the warpgroups' dS^T(i - 1),
+      // waited for), where it forms while the warpgroups turn dP^T(i) into dS^T(i); then
       // dV(i), dK(i), dQ^T(i) as P^T(i) and dS^T(i) arrive, and dP^T(i + 1) after dK(i) has read
-      // dS^T(i) out of the dP^T columns.
+      // dS^T(i) out of the dP^T columns. S^T(i + 1) must not start earlier: both warpgroups
+      // count into one p_ready barrier, and a warpgroup that reached P^T(i + 1) first would
+      // complete phase i with its second arrivals while the other's P^T(i) is still being
+      // stored (dV(i) then reads unfinished columns).
       // the TMEM layout inside this CTA's allocation
       bool ok = FA_CHECK(tmem_in(tmem + C::TM_ST, 2 * BR, tmem, C::TM_COLS) &&
                              tmem_in(tmem + C::TM_DPT, BR, tmem, C::TM_COLS) &&
@@ -521,13 +524,15 @@ __global__ void __launch_bounds__(448, 1)
         const uint32_t so = s * QT16;
         const bool next = it + 1 < n_it;
         const int s1 = (it + 1) % NSTQ;
+        if (!(ok = wait_warp(p_ready, it & 1, st, SITE_B_P_READY))) break;
+        // S^T(i + 1) only now: both warpgroups count into the one p_ready barrier, so neither
+        // may reach P^T(i + 1), and arrive again, before phase i has completed here
         if (next) {
           if (!(ok = wait_warp(qdo_full(s1), ((it + 1) / NSTQ) & 1, st, SITE_B_QDO_FULL))) break;
           tc_fence_after();
           issue_kmajor(C::TM_ST + (sb ^ 1) * BR, k_lo, q_lo + s1 * QT16);
           commit(s_full(sb ^ 1));
         }
-        if (!(ok = wait_warp(p_ready, it & 1, st, SITE_B_P_READY))) break;
         tc_fence_after();
         issue_grad(C::TM_DV, C::TM_ST + sb * BR, domn_lo + so, it > 0);
         if (!(ok = wait_warp(ds_ready, it & 1, st, SITE_B_DS_READY))) break;
