@@ -10,7 +10,7 @@ It stands in for a memory checker. The tests below show two things:
   - the split forward and its join;
   - the decode kernel in both decompositions, with its join.
 - With the check slack (row extents taken down by one row), checks near the end of a tensor
-  fail on memory that is really there. The call reports FA_ERR_DEVICE_CHECK with a site from
+  fail on memory that is really there (training at d = 64 and 128, packed sequences, decode). The call reports FA_ERR_DEVICE_CHECK with a site from
   fa_debug.h, and the CUDA context stays usable: the next call is clean and correct. Every
   access still stays inside the tensors, because a failed check only skips its access.
 """
@@ -134,6 +134,27 @@ def test_training_checks_fire_under_slack_and_context_survives(dbg, gpu, d):
 
     o, lse, dq, dk, dv = _reported_then_clean(gpu, run)
     r = ref.attention(f64(x["q"]), f64(x["k"]), f64(x["v"]), f64(x["do"]), scale=1 / math.sqrt(d), causal=True)
+    assert_within({n: compare(n, f64(t), r[n]) for n, t in
+                   (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv))})
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_packed_checks_fire_under_slack_and_context_survives(dbg, gpu, d):
+    # packed sequences: the last sequence's rows end at the last row of each head's T rows
+    H, lens = 2, [100, 257, 3, 130]
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    full = workloads.draw(1, H, int(cu[-1]), d, seed=5 + d)
+    x = {n: full[n][0] for n in ("q", "k", "v", "do")}
+    q, k, v, do = (x[n].to(gpu) for n in ("q", "k", "v", "do"))
+    cu_d = torch.tensor(cu, device=gpu)
+
+    def run():
+        o, lse = api.forward_varlen(q, k, v, cu_d, max(lens), causal=True)
+        return (o, lse) + tuple(api.backward_varlen(q, k, v, o, do, lse, cu_d, max(lens), causal=True))
+
+    o, lse, dq, dk, dv = _reported_then_clean(gpu, run)
+    r = ref.attention_varlen(f64(x["q"]), f64(x["k"]), f64(x["v"]), f64(x["do"]), cu, scale=1 / math.sqrt(d),
+                             causal=True)
     assert_within({n: compare(n, f64(t), r[n]) for n, t in
                    (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv))})
 
