@@ -155,6 +155,8 @@ SPLIT = [
     (2, 2, 1, 640, 128, False, [0, 0], 2, True),          # no valid key anywhere
     (1, 3, 1, 9000, 128, False, None, 1, True),           # whole heads, d = 128, one query row
     (3, 5, 1, 4000, 128, True, [4000, 2, 3999], 4, True),  # d = 128 key-major lanes, cut heads, padding
+    (2, 2, 6, 2500, 128, True, [2500, 1200], 3, True),    # d = 128, up to 8 query rows: cut heads
+    (1, 2, 7, 1800, 128, False, None, 1, True),           # ... whole heads
 ]
 
 
