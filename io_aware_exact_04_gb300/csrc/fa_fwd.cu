@@ -94,11 +94,14 @@ __device__ __forceinline__ FwdExt fwd_ext(const FwdArgs& a, bool vl) {
 }
 #endif
 
+// ONE (plain rows only): the CTA takes one 128-row query tile instead of a pair (a.n_pairs then
+// counts tiles), its second lane idle; for grids of pairs too small to fill the SMs, where
+// one lane alone runs a tile faster than two sharing an SM.
 // SPLIT: the CTA (head, query pair, share z) runs key tiles [jb, je) of its item, the
 // z-th of a.n_split near-equal shares, and writes normalised partial O (fp32) and LSE to
 // slots 2z and 2z + 1 of a.part_o / a.part_lse for fwd_combine_kernel; the same
 // running-maximum rescaling that joins key tiles inside a CTA then joins the slots.
-template <int D, bool SPLIT, bool VL = false>
+template <int D, bool SPLIT, bool VL = false, bool ONE = false>
 __global__ void __launch_bounds__(352, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o, FwdArgs a) {
@@ -154,10 +157,12 @@ __global__ void __launch_bounds__(352, 1)
   int kv = VL ? NQ : a.Nk;
   if (!VL && a.kv_len && FA_CHECK(in_range(b, a.dbg_B), a.status, DBG_META)) kv = min(max(a.kv_len[b], 0), a.Nk);
   const int nkt = (kv + 127) >> 7;
-  const int q0 = pair * 256;
+  static_assert(!ONE || (!SPLIT && !VL), "one query tile per CTA: plain rows only");
+  const int q0 = pair * (ONE ? 128 : 256);
   int n_t[2];
 #pragma unroll
-  for (int t = 0; t < 2; ++t) n_t[t] = key_tiles(q0 + t * 128, NQ, nkt, a.causal, VL ? 0 : a.coff);
+  for (int t = 0; t < 2; ++t)
+    n_t[t] = (ONE && t == 1) ? 0 : key_tiles(q0 + t * 128, NQ, nkt, a.causal, VL ? 0 : a.coff);
   // key tiles run here: [jb, jb + nmax), all of them without a split; loops count from 0.
   // dual (split only): the item's second query tile lies past N, so query lane 1 takes the
   // same rows as lane 0 and the two lanes split the share's key tiles, even ones to lane 0
@@ -434,7 +439,7 @@ __global__ void __launch_bounds__(352, 1)
     if (SPLIT && !dual && grow < NQ && qs < NQ &&
         FA_CHECK(in_range(prow + plane, fwd_ext(a, VL).part_rows), st, DBG_GLOBAL_STORE))
       a.part_lse[prow + plane] = -INFINITY;
-    if (qs < NQ && n == 0) {
+    if ((!ONE || t == 0) && qs < NQ && n == 0) {  // (ONE: lane 1's rows are another CTA's)
       // no valid key for any row of this tile (in this share): O = 0, LSE = -inf
       if (grow < NQ) {
         if (SPLIT) {
@@ -1864,7 +1869,7 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(FwdArgs a, int B, i
 
 // BH = B * H work items per query pair. VL: the tensors are [H, T, d] (rows of all sequences
 // packed per head), so the maps span T rows and H heads.
-template <int D, bool SPLIT = false, bool VL = false>
+template <int D, bool SPLIT = false, bool VL = false, bool ONE = false>
 static int launch_fwd_d(const void* q, const void* k, const void* v, void* o, const FwdArgs& args, int BH,
                         cudaStream_t stream) {
   using C = FwdCfg<D, SPLIT>;
@@ -1878,14 +1883,16 @@ static int launch_fwd_d(const void* q, const void* k, const void* v, void* o, co
     return cuda_fail("cuTensorMapEncodeTiled", 0, "tensor map rejected");
   static bool attr_set = false;  // benign race: idempotent
   if (!attr_set) {
-    const cudaError_t e = cudaFuncSetAttribute(fwd_kernel<D, SPLIT, VL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               C::SMEM_BYTES);
+    const cudaError_t e = cudaFuncSetAttribute(fwd_kernel<D, SPLIT, VL, ONE>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return cuda_fail("cudaFuncSetAttribute", (int)e, cudaGetErrorName(e));
     attr_set = true;
   }
-  dim3 grid(BH, args.n_pairs, SPLIT ? args.n_split : 1);
-  return launch_pdl(__func__, fwd_kernel<D, SPLIT, VL>, grid, dim3(C::THREADS), C::SMEM_BYTES, stream, mq, mk, mv,
-                    mo, args);
+  FwdArgs a = args;
+  if (ONE) a.n_pairs = (args.N + 127) / 128;  // query tiles along y
+  dim3 grid(BH, a.n_pairs, SPLIT ? args.n_split : 1);
+  return launch_pdl(__func__, fwd_kernel<D, SPLIT, VL, ONE>, grid, dim3(C::THREADS), C::SMEM_BYTES, stream, mq, mk,
+                    mv, mo, a);
 }
 
 // d = 64: the persistent kernel, one CTA per SM (at most one per work item). VL: packed
@@ -1924,8 +1931,14 @@ int launch_fwd(const void* q, const void* k, const void* v, void* o, const FwdAr
   // item, where the hardware's block dispatch balances the causal work at least as well as
   // the static order and the per-item setup is amortised over many key tiles.
   if (d == 64 && args.n_pairs <= 4 && args.Nk <= 1024) return launch_fwd_p64<false>(q, k, v, o, args, BH, stream);
-  if (d == 64) return launch_fwd_d<64>(q, k, v, o, args, BH, stream);
-  if (d == 128) return launch_fwd_d<128>(q, k, v, o, args, BH, stream);
+  // Fewer pairs than SMs: one query tile per CTA, so that more SMs work and each lane runs
+  // alone (a lane alone takes ~1700 cycles a key tile, two sharing an SM ~2175 each).
+  int sms = 0;
+  const bool one = sm_count(&sms) && (long long)BH * args.n_pairs < sms;
+  if (d == 64) return one ? launch_fwd_d<64, false, false, true>(q, k, v, o, args, BH, stream)
+                          : launch_fwd_d<64>(q, k, v, o, args, BH, stream);
+  if (d == 128) return one ? launch_fwd_d<128, false, false, true>(q, k, v, o, args, BH, stream)
+                           : launch_fwd_d<128>(q, k, v, o, args, BH, stream);
   return FA_ERR_UNSUPPORTED;
 }
 
