@@ -48,6 +48,8 @@ MANY_TILES = [
     (8, 24, 256, 64, True, None),                              # 384 tiles
     (6, 20, 300, 64, False, [0, 50, 300, 129, 257, 1]),        # 360 tiles, empty ones included
     (4, 30, 384, 64, True, [384, 200, 10, 384]),               # 360 tiles, causal with padding
+    (4, 20, 384, 128, True, [384, 200, 10, 384]),              # d = 128: 240 CTAs, forward in pairs
+    (3, 30, 1100, 64, True, [1100, 700, 3]),                   # rows past 1024, forward in pairs, padded
 ]
 
 
