@@ -191,6 +191,32 @@ def test_matches_torch_fp64_autograd(causal, kv_len):
         assert np.abs(a - b).max() <= 1e-12 * max(1.0, np.abs(b).max()), name
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_large_growing_scores_stay_exact(causal):
+    """Scores of several hundred (the regime of the GPU test whose keys' norms ramp up along the
+    sequence): the oracle, which subtracts each row's maximum, still matches torch's fp64
+    softmax and autograd, and stays finite."""
+    n, d = 60, 16
+    q, k, v, do = _rand(n, d, 9)
+    q = q * 6.0
+    k = k * (1.0 + 20.0 * np.arange(n) / n)[:, None]
+    s = 1 / math.sqrt(d)
+    g = ref.head_backward(q, k, v, do, s, causal)
+    assert all(np.isfinite(g[name]).all() for name in ("o", "lse", "dq", "dk", "dv"))
+    tq, tk, tv = (torch.tensor(x, dtype=torch.float64, requires_grad=True) for x in (q, k, v))
+    logits = (tq @ tk.T) * s
+    assert float(logits.detach().abs().max()) > 200.0  # the regime this pins
+    if causal:
+        logits = logits.masked_fill(torch.ones(n, n, dtype=torch.bool).triu(1), float("-inf"))
+    o = torch.softmax(logits, dim=-1) @ tv
+    lse = torch.logsumexp(logits, dim=-1)
+    o.backward(torch.tensor(do))
+    for name, a, b in (("o", g["o"], o.detach().numpy()), ("lse", g["lse"], lse.detach().numpy()),
+                       ("dq", g["dq"], tq.grad.numpy()), ("dk", g["dk"], tk.grad.numpy()),
+                       ("dv", g["dv"], tv.grad.numpy())):
+        assert np.abs(a - b).max() <= 1e-11 * max(1.0, np.abs(b).max()), name
+
+
 def test_row_groups_do_not_change_results():
     n, d = 300, 16
     q, k, v, do = _rand(n, d, 9)
